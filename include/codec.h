@@ -1,0 +1,213 @@
+/*
+ * codec.h - C ABI of the GB300 (sm_103a) streaming codec-to-waveform decoder.
+ *
+ * The decoder turns residual-VQ code frames (12.5 Hz, Q codebooks) into 24 kHz
+ * audio, 1920 samples per frame, through: codebook embedding sum -> causal
+ * Conv1d -> sliding-window causal transformer -> 2x2 latent upsampling ->
+ * BigVGAN stages (Snake -> transposed conv -> multi-receptive-field residual
+ * blocks) -> Snake -> conv -> tanh (vllm-omni "Edge TTS design", section 1.3).
+ * It decodes chunk by chunk and carries each stream's state between calls:
+ * every causal conv's left context and the attention window's keys/values
+ * (section 1.3 "Cross-chunk state"; blixt/phonon "Speed" item 7), so decoding
+ * a stream in chunks of any sizes gives the same audio as one full decode.
+ *
+ * Conventions
+ *   - Every entry point returns a codec_status; nothing aborts the process.
+ *   - Pointers documented "device" are CUDA device pointers on the device that
+ *     was current at codec_create; "host" pointers are ordinary host memory.
+ *   - stream arguments are cudaStream_t values passed as void*; NULL means the
+ *     legacy default stream.
+ *   - Argument checks happen before anything is enqueued: a call that returns
+ *     an error status other than CODEC_ERR_CUDA has enqueued no GPU work.
+ *   - codec_t is immutable after creation and may be shared by threads.  A
+ *     codec_state_t must be used by one host thread at a time.
+ *   - All device memory is allocated in codec_create / codec_state_create
+ *     (blixt/phonon "Speed" item 4: nothing is allocated per request).
+ */
+#ifndef GB300_CODEC_H
+#define GB300_CODEC_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define CODEC_API __attribute__((visibility("default")))
+#else
+#define CODEC_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum codec_status {
+    CODEC_OK = 0,
+    CODEC_ERR_NULL = 1,        /* a required pointer argument is NULL */
+    CODEC_ERR_CONFIG = 2,      /* configuration invalid or unsupported */
+    CODEC_ERR_WEIGHTS = 3,     /* weight blob length does not match the config */
+    CODEC_ERR_ARG = 4,         /* an argument is out of range, or stream ids repeat */
+    CODEC_ERR_CAPACITY = 5,    /* request exceeds max_streams, max_chunk_frames or max_batch_frames */
+    CODEC_ERR_OOM = 6,         /* a device allocation failed (create calls only) */
+    CODEC_ERR_CUDA = 7,        /* a CUDA runtime/driver call failed */
+    CODEC_ERR_NO_DEVICE = 8    /* no usable sm_103 device */
+} codec_status;
+
+/* Sticky per-stream device error bits, read with codec_state_query. */
+#define CODEC_STREAM_ERR_BAD_CODE 1u   /* a code outside [0, V): that frame's embedding was zeroed */
+
+typedef enum codec_precision {
+    /* fp32 operands on CUDA cores for every stage. */
+    CODEC_PRECISION_FP32 = 0,
+    /* Dense contractions (conv, transposed conv, linear with >= 64 channels) on
+     * tcgen05 tensor cores with both operands split into fp16 hi + lo parts and
+     * three MMAs (hi*hi + hi*lo + lo*hi) accumulated in fp32 in TMEM; the rest
+     * on CUDA cores in fp32. */
+    CODEC_PRECISION_FP16X3 = 1
+} codec_precision;
+
+/*
+ * Decoder shape and capacity.  The layer list is fixed by the stage order
+ * above; these fields size it.
+ */
+typedef struct codec_config {
+    int32_t Q, V, E;          /* codebooks, entries per codebook, codebook width */
+    int32_t pre_k;            /* kernel of the causal Conv1d E -> d */
+    int32_t d, heads, ffn;    /* transformer width, heads (d % heads == 0), MLP width */
+    int32_t layers, window;   /* transformer layers; keys per query (itself included) */
+    int32_t n_up, up_k, up_s; /* latent transposed convs: count (1..4), kernel, stride; up_k == 2*up_s */
+    int32_t up_ch[4];         /* their output channels; up_ch[n_up-1] = C_0 */
+    int32_t n_stages;         /* BigVGAN stages (1..8) */
+    int32_t strides[8];       /* stage strides s_i; the stage's ConvT kernel is 2*s_i */
+    int32_t ch[8];            /* stage output channels C_1..C_n */
+    int32_t n_rb;             /* resblocks per stage (1..3), averaged when > 1 */
+    int32_t rb_k[4];          /* their kernels (odd) */
+    int32_t n_dil;            /* dilations per resblock (1..4) */
+    int32_t dil[4];
+    int32_t final_k;          /* kernel of the final conv C_n -> 1 */
+    float rms_eps;
+    int32_t max_streams;      /* default stream slots for codec_state_create(n_streams = 0) */
+    int32_t max_chunk_frames; /* largest n_frames[b] accepted in one call (>= 1) */
+    int32_t max_batch_frames; /* largest sum of n_frames over one call (>= max_chunk_frames) */
+    int32_t precision;        /* codec_precision */
+} codec_config;
+
+typedef struct codec_stream_info {
+    int64_t frames_decoded;   /* frames decoded since the last reset */
+    uint32_t error_bits;      /* sticky CODEC_STREAM_ERR_* bits since the last reset */
+    int32_t reserved;
+} codec_stream_info;
+
+typedef struct codec_s codec_t;
+typedef struct codec_state_s codec_state_t;
+
+/* Number of fp32 values of the weight blob for cfg (-1 if cfg is invalid).
+ * Blob order and layouts (PyTorch layouts, fp32):
+ *   Q codebooks [V][E]; pre-conv weight [d][E][pre_k], bias [d];
+ *   per layer: attention RMSNorm gain [d], Wq, Wk, Wv, Wo [d][d] ([out][in]),
+ *     MLP RMSNorm gain [d], W1 [ffn][d], W2 [d][ffn];
+ *   final RMSNorm gain [d];
+ *   per latent ConvT: weight [Cin][Cout][up_k], bias [Cout];
+ *   per stage: Snake alpha [Cin], ConvT weight [Cin][Cout][2 s], bias [Cout],
+ *     then per resblock j, per dilation i: Snake alpha [C], conv weight
+ *     [C][C][rb_k[j]], bias [C];
+ *   final Snake alpha [C_n], conv weight [1][C_n][final_k], bias [1]. */
+CODEC_API int64_t codec_weight_floats(const codec_config* cfg);
+
+/* Validate cfg, repack the weights for the kernels and upload them to the
+ * current CUDA device.  weights: host, codec_weight_floats(cfg) floats; the
+ * library copies them, and the caller may free them on return.
+ * Errors: CODEC_ERR_NULL, CODEC_ERR_CONFIG, CODEC_ERR_WEIGHTS,
+ * CODEC_ERR_NO_DEVICE, CODEC_ERR_OOM, CODEC_ERR_CUDA.  On error *out is NULL. */
+CODEC_API codec_status codec_create(const codec_config* cfg, const float* weights, int64_t n_floats,
+                          codec_t** out);
+
+/* Free the weights.  All states created from it must be destroyed first and
+ * their GPU work finished. */
+CODEC_API void codec_destroy(codec_t* codec);
+
+/* Samples per frame (the product of all upsampling strides; 1920 for the
+ * 12.5 Hz -> 24 kHz decoder). */
+CODEC_API int32_t codec_samples_per_frame(const codec_t* codec);
+
+/* Allocate n_streams stream slots (0 = cfg.max_streams) plus the per-call
+ * workspace, all reset.  Errors: CODEC_ERR_NULL, CODEC_ERR_ARG, CODEC_ERR_OOM,
+ * CODEC_ERR_CUDA. */
+CODEC_API codec_status codec_state_create(codec_t* codec, int32_t n_streams, codec_state_t** out);
+
+/* Free a state.  Synchronises with its device work first. */
+CODEC_API void codec_state_destroy(codec_state_t* state);
+
+/* Reset streams: clear their carried context, frame counters and error bits.
+ * This is the abort / start-of-utterance operation (vllm-omni "Edge TTS
+ * design", section 2.2: IDecoderAdapter::reset; section 2.2 step 4: abort).
+ * stream_ids: host [n] slot ids, or NULL for every slot (n ignored).  Enqueued
+ * on stream; ordered with decode calls on the same stream.
+ * Errors: CODEC_ERR_NULL, CODEC_ERR_ARG, CODEC_ERR_CUDA. */
+CODEC_API codec_status codec_state_reset(codec_state_t* state, const int32_t* stream_ids, int32_t n,
+                               void* stream);
+
+/*
+ * Decode one chunk for each of B streams in one launch sequence.
+ *   codes      device int32 [B][Q][T_max]; stream b's frames are columns 0..n_frames[b]-1.
+ *   n_frames   host int32 [B], each in [0, min(T_max, max_chunk_frames)];
+ *              sum <= max_batch_frames.  0 leaves the stream untouched.
+ *   stream_ids host int32 [B] distinct slot ids, or NULL for slots 0..B-1.
+ *   audio      device float [B][T_max * samples_per_frame]; samples
+ *              0..n_frames[b]*spf-1 of row b are written, the rest untouched.
+ * Each stream continues from its carried state, so its audio is final when
+ * written and chunk sizes may change from call to call (vllm-omni "Edge TTS
+ * design", section 1.4: 1 frame, then 25-frame chunks with the 72-frame
+ * window carried).  The call returns once the work is enqueued on stream; the
+ * caller keeps codes and audio alive until that work completes.
+ * Errors (nothing enqueued): CODEC_ERR_NULL, CODEC_ERR_ARG (B < 1, T_max < 1,
+ * n_frames out of range, slot id out of range or repeated),
+ * CODEC_ERR_CAPACITY; CODEC_ERR_CUDA if a launch fails.
+ * Codes outside [0, V) do not fail the call: they set the stream's sticky
+ * CODEC_STREAM_ERR_BAD_CODE bit and that frame's embedding is zero.
+ */
+CODEC_API codec_status codec_decode_chunk(codec_state_t* state, const int32_t* codes, const int32_t* n_frames,
+                                const int32_t* stream_ids, int32_t B, int32_t T_max, float* audio,
+                                void* stream);
+
+/* As codec_decode_chunk, and also writes the final conv's output before tanh
+ * to pre_tanh (device float, same layout as audio; may be NULL).  For
+ * verification: the tanh saturates most samples of a random-weight decoder. */
+CODEC_API codec_status codec_decode_chunk_ex(codec_state_t* state, const int32_t* codes,
+                                   const int32_t* n_frames, const int32_t* stream_ids, int32_t B,
+                                   int32_t T_max, float* audio, float* pre_tanh, void* stream);
+
+/* The codebook embedding sum alone (the first stage of codec_decode_chunk),
+ * for verification: emb is device float [sum(n_frames)][E], the frames of the
+ * batch rows with n_frames[b] > 0 packed in batch order.  Arguments and
+ * checks as codec_decode_chunk; no carried context changes, but a code
+ * outside [0, V) sets the stream's sticky bad-code bit as in a decode. */
+CODEC_API codec_status codec_embed_chunk(codec_state_t* state, const int32_t* codes, const int32_t* n_frames,
+                               const int32_t* stream_ids, int32_t B, int32_t T_max, float* emb,
+                               void* stream);
+
+/* Host-buffer form: codes_host int32 [B][Q][T_max] and audio_host float
+ * [B][T_max * spf] are host memory (page-locked for asynchronous copies).  The
+ * call copies the codes to a state-owned device buffer, decodes, copies the
+ * audio back and synchronises stream before returning. */
+CODEC_API codec_status codec_decode_chunk_host(codec_state_t* state, const int32_t* codes_host,
+                                     const int32_t* n_frames, const int32_t* stream_ids, int32_t B,
+                                     int32_t T_max, float* audio_host, void* stream);
+
+/* Frames decoded and sticky error bits of one slot.  Synchronises stream
+ * (host-blocking).  Errors: CODEC_ERR_NULL, CODEC_ERR_ARG, CODEC_ERR_CUDA. */
+CODEC_API codec_status codec_state_query(codec_state_t* state, int32_t stream_id, codec_stream_info* info,
+                               void* stream);
+
+/* Number of stream slots of a state. */
+CODEC_API int32_t codec_state_streams(const codec_state_t* state);
+
+/* Number of kernel launches the last decode call enqueued. */
+CODEC_API int32_t codec_state_last_launches(const codec_state_t* state);
+
+/* Static description of a status code. */
+CODEC_API const char* codec_status_string(codec_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GB300_CODEC_H */

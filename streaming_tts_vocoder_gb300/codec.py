@@ -1,0 +1,248 @@
+"""Python binding of the C ABI in include/codec.h (argument marshalling only).
+
+Every computation runs in the CUDA library libcodec_gb300.so; this module only
+converts configs, numpy weight blobs and torch tensors to the plain pointers
+and sizes the C functions take.  It raises if the library is not built: there
+is no other code path.
+"""
+from __future__ import annotations
+
+import ctypes
+import re
+from pathlib import Path
+
+import numpy as np
+
+PKG = Path(__file__).resolve().parent
+LIB_PATH = PKG / "libcodec_gb300.so"
+HEADER = PKG.parent / "include" / "codec.h"
+
+PRECISION_FP32 = 0
+PRECISION_FP16X3 = 1
+STREAM_ERR_BAD_CODE = 1
+
+STATUS = {0: "CODEC_OK", 1: "CODEC_ERR_NULL", 2: "CODEC_ERR_CONFIG", 3: "CODEC_ERR_WEIGHTS",
+          4: "CODEC_ERR_ARG", 5: "CODEC_ERR_CAPACITY", 6: "CODEC_ERR_OOM", 7: "CODEC_ERR_CUDA",
+          8: "CODEC_ERR_NO_DEVICE"}
+
+
+class CodecError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS.get(status, status)} ({_lib().codec_status_string(status).decode()})")
+
+
+class CodecConfigC(ctypes.Structure):
+    _fields_ = [
+        ("Q", ctypes.c_int32), ("V", ctypes.c_int32), ("E", ctypes.c_int32), ("pre_k", ctypes.c_int32),
+        ("d", ctypes.c_int32), ("heads", ctypes.c_int32), ("ffn", ctypes.c_int32),
+        ("layers", ctypes.c_int32), ("window", ctypes.c_int32),
+        ("n_up", ctypes.c_int32), ("up_k", ctypes.c_int32), ("up_s", ctypes.c_int32),
+        ("up_ch", ctypes.c_int32 * 4),
+        ("n_stages", ctypes.c_int32), ("strides", ctypes.c_int32 * 8), ("ch", ctypes.c_int32 * 8),
+        ("n_rb", ctypes.c_int32), ("rb_k", ctypes.c_int32 * 4),
+        ("n_dil", ctypes.c_int32), ("dil", ctypes.c_int32 * 4),
+        ("final_k", ctypes.c_int32), ("rms_eps", ctypes.c_float),
+        ("max_streams", ctypes.c_int32), ("max_chunk_frames", ctypes.c_int32),
+        ("max_batch_frames", ctypes.c_int32), ("precision", ctypes.c_int32),
+    ]
+
+
+class StreamInfoC(ctypes.Structure):
+    _fields_ = [("frames_decoded", ctypes.c_int64), ("error_bits", ctypes.c_uint32),
+                ("reserved", ctypes.c_int32)]
+
+
+_L = None
+_P = ctypes.c_void_p
+_I32P = ctypes.POINTER(ctypes.c_int32)
+
+
+def _lib():
+    global _L
+    if _L is None:
+        if not LIB_PATH.exists():
+            raise RuntimeError(f"CUDA library {LIB_PATH.name} is not built; run __graft_entry__.build()")
+        l = ctypes.CDLL(str(LIB_PATH))
+        i32, i64 = ctypes.c_int32, ctypes.c_int64
+        cfgp = ctypes.POINTER(CodecConfigC)
+        sig = {
+            "codec_weight_floats": (i64, [cfgp]),
+            "codec_create": (i32, [cfgp, ctypes.POINTER(ctypes.c_float), i64, ctypes.POINTER(_P)]),
+            "codec_destroy": (None, [_P]),
+            "codec_samples_per_frame": (i32, [_P]),
+            "codec_state_create": (i32, [_P, i32, ctypes.POINTER(_P)]),
+            "codec_state_destroy": (None, [_P]),
+            "codec_state_reset": (i32, [_P, _I32P, i32, _P]),
+            "codec_decode_chunk": (i32, [_P, _P, _I32P, _I32P, i32, i32, _P, _P]),
+            "codec_decode_chunk_ex": (i32, [_P, _P, _I32P, _I32P, i32, i32, _P, _P, _P]),
+            "codec_decode_chunk_host": (i32, [_P, _P, _I32P, _I32P, i32, i32, _P, _P]),
+            "codec_embed_chunk": (i32, [_P, _P, _I32P, _I32P, i32, i32, _P, _P]),
+            "codec_state_query": (i32, [_P, i32, ctypes.POINTER(StreamInfoC), _P]),
+            "codec_state_streams": (i32, [_P]),
+            "codec_state_last_launches": (i32, [_P]),
+            "codec_status_string": (ctypes.c_char_p, [i32]),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(l, name)
+            fn.restype = res
+            fn.argtypes = args
+        _L = l
+    return _L
+
+
+def header_functions() -> list:
+    """Names of the functions include/codec.h declares."""
+    text = HEADER.read_text()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(codec_[a-z_]+)\s*\(", text)))
+
+
+def config_c(cfg, max_streams=1, max_chunk_frames=97, max_batch_frames=None,
+             precision=PRECISION_FP32) -> CodecConfigC:
+    c = CodecConfigC()
+    c.Q, c.V, c.E, c.pre_k = cfg.Q, cfg.V, cfg.E, cfg.pre_k
+    c.d, c.heads, c.ffn, c.layers, c.window = cfg.d, cfg.heads, cfg.ffn, cfg.layers, cfg.window
+    c.n_up, c.up_k, c.up_s = len(cfg.up_channels), cfg.up_k, cfg.up_s
+    for i, v in enumerate(cfg.up_channels):
+        c.up_ch[i] = v
+    c.n_stages = len(cfg.strides)
+    for i, (s, ch) in enumerate(zip(cfg.strides, cfg.channels)):
+        c.strides[i] = s
+        c.ch[i] = ch
+    c.n_rb = len(cfg.rb_kernels)
+    for i, k in enumerate(cfg.rb_kernels):
+        c.rb_k[i] = k
+    c.n_dil = len(cfg.dilations)
+    for i, dl in enumerate(cfg.dilations):
+        c.dil[i] = dl
+    c.final_k = cfg.final_k
+    c.rms_eps = cfg.rms_eps
+    c.max_streams = max_streams
+    c.max_chunk_frames = max_chunk_frames
+    c.max_batch_frames = max_batch_frames if max_batch_frames is not None else max_chunk_frames * max_streams
+    c.precision = precision
+    return c
+
+
+def weight_floats(cfg_c: CodecConfigC) -> int:
+    return _lib().codec_weight_floats(ctypes.byref(cfg_c))
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        raise CodecError(status, what)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream):
+    if stream is None:
+        import torch
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+class Codec:
+    """codec_create / codec_destroy: the weights on the current CUDA device."""
+
+    def __init__(self, cfg, blob: np.ndarray, **capacity):
+        self.cfg = cfg
+        self.cfg_c = config_c(cfg, **capacity)
+        blob = np.ascontiguousarray(blob, dtype=np.float32)
+        h = ctypes.c_void_p()
+        _check(_lib().codec_create(ctypes.byref(self.cfg_c), blob.ctypes.data_as(ctypes.POINTER(ctypes.c_float)),
+                                   blob.size, ctypes.byref(h)), "codec_create")
+        self._h = h
+        self.samples_per_frame = _lib().codec_samples_per_frame(h)
+
+    def close(self):
+        if getattr(self, "_h", None):
+            _lib().codec_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        self.close()
+
+    def state(self, n_streams: int = 0) -> "CodecState":
+        return CodecState(self, n_streams)
+
+
+class CodecState:
+    """codec_state_*: stream slots plus the per-call workspace."""
+
+    def __init__(self, codec: Codec, n_streams: int = 0):
+        self.codec = codec
+        h = ctypes.c_void_p()
+        _check(_lib().codec_state_create(codec._h, n_streams, ctypes.byref(h)), "codec_state_create")
+        self._h = h
+        self.n_streams = _lib().codec_state_streams(h)
+
+    def close(self):
+        if getattr(self, "_h", None):
+            _lib().codec_state_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        self.close()
+
+    def reset(self, stream_ids=None, stream=None):
+        if stream_ids is None:
+            _check(_lib().codec_state_reset(self._h, None, 0, _stream_handle(stream)), "codec_state_reset")
+        else:
+            ids = np.ascontiguousarray(stream_ids, dtype=np.int32)
+            _check(_lib().codec_state_reset(self._h, ids.ctypes.data_as(_I32P), ids.size, _stream_handle(stream)),
+                   "codec_state_reset")
+
+    def decode(self, codes, n_frames, audio, stream_ids=None, pre_tanh=None, stream=None):
+        """codes: device int32 tensor [B][Q][T_max]; audio: device float32
+        [B][T_max * spf]; n_frames and stream_ids: host sequences of length B."""
+        B, Q, T_max = codes.shape
+        nf = np.ascontiguousarray(n_frames, dtype=np.int32)
+        ids = None if stream_ids is None else np.ascontiguousarray(stream_ids, dtype=np.int32)
+        if nf.size != B or (ids is not None and ids.size != B):
+            raise ValueError("n_frames / stream_ids must have one entry per batch row")
+        if not (codes.is_cuda and codes.dtype.__str__() == "torch.int32" and codes.is_contiguous()):
+            raise ValueError("codes must be a contiguous int32 CUDA tensor")
+        if not (audio.is_cuda and audio.is_contiguous() and audio.numel() >= B * T_max * self.codec.samples_per_frame):
+            raise ValueError("audio must be a contiguous float32 CUDA tensor of B * T_max * spf values")
+        ids_p = None if ids is None else ids.ctypes.data_as(_I32P)
+        st = _stream_handle(stream)
+        if pre_tanh is None:
+            s = _lib().codec_decode_chunk(self._h, _ptr(codes), nf.ctypes.data_as(_I32P), ids_p, B, T_max,
+                                          _ptr(audio), st)
+        else:
+            s = _lib().codec_decode_chunk_ex(self._h, _ptr(codes), nf.ctypes.data_as(_I32P), ids_p, B, T_max,
+                                             _ptr(audio), _ptr(pre_tanh), st)
+        _check(s, "codec_decode_chunk")
+
+    def embed(self, codes, n_frames, emb, stream_ids=None, stream=None):
+        """Codebook sum only: emb device float32 [sum(n_frames)][E]."""
+        B, Q, T_max = codes.shape
+        nf = np.ascontiguousarray(n_frames, dtype=np.int32)
+        ids = None if stream_ids is None else np.ascontiguousarray(stream_ids, dtype=np.int32)
+        ids_p = None if ids is None else ids.ctypes.data_as(_I32P)
+        _check(_lib().codec_embed_chunk(self._h, _ptr(codes), nf.ctypes.data_as(_I32P), ids_p, B, T_max,
+                                        _ptr(emb), _stream_handle(stream)), "codec_embed_chunk")
+
+    def decode_host(self, codes, n_frames, audio, stream_ids=None, stream=None):
+        """Host-buffer form: codes int32 [B][Q][T_max] and audio float32
+        [B][T_max * spf] are CPU tensors (pinned for asynchronous copies)."""
+        B, Q, T_max = codes.shape
+        nf = np.ascontiguousarray(n_frames, dtype=np.int32)
+        ids = None if stream_ids is None else np.ascontiguousarray(stream_ids, dtype=np.int32)
+        ids_p = None if ids is None else ids.ctypes.data_as(_I32P)
+        _check(_lib().codec_decode_chunk_host(self._h, _ptr(codes), nf.ctypes.data_as(_I32P), ids_p, B, T_max,
+                                              _ptr(audio), _stream_handle(stream)), "codec_decode_chunk_host")
+
+    def query(self, stream_id: int, stream=None):
+        info = StreamInfoC()
+        _check(_lib().codec_state_query(self._h, stream_id, ctypes.byref(info), _stream_handle(stream)),
+               "codec_state_query")
+        return int(info.frames_decoded), int(info.error_bits)
+
+    @property
+    def last_launches(self) -> int:
+        return _lib().codec_state_last_launches(self._h)

@@ -1,0 +1,880 @@
+// Host runtime and C ABI of the decoder: configuration checks, weight repack
+// and upload, stream-slot state, per-call planning of ragged multi-stream
+// batches, and the launch sequence.
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <vector>
+
+#include "codec.h"
+#include "kernels.h"
+#include "tc_gemm.h"
+
+using namespace codec;
+
+namespace {
+
+// Weights of one contraction (conv, transposed conv or linear) in the packed
+// implicit-GEMM form: K = ntaps * Cin rows (tap-major), N columns.
+struct Contraction {
+    float* w = nullptr;            // fp32 [K][N] (CUDA-core path)
+    TcWeights tc;                  // fp16 hi/lo planes [N][K] (tensor-core path)
+    bool use_tc = false;
+    float* bias = nullptr;
+    int bias_mod = 1;
+    float* alpha = nullptr;        // Snake on the input, or null
+    float* inv_alpha = nullptr;
+    int Cin = 0, N = 0, K = 0, ntaps = 0;
+    int shift[kMaxTaps] = {};
+};
+
+struct LayerW {
+    float* n1 = nullptr;
+    float* n2 = nullptr;
+    Contraction qkv, o, w1, w2;
+};
+
+bool debug_sync()
+{
+    static int v = -1;
+    if (v < 0) {
+        const char* e = getenv("CODEC_DEBUG_SYNC");
+        v = (e && *e && *e != '0') ? 1 : 0;
+    }
+    return v == 1;
+}
+
+int next_pow2(int x)
+{
+    int r = 1;
+    while (r < x) r <<= 1;
+    return r;
+}
+
+}  // namespace
+
+struct codec_s {
+    codec_config cfg{};
+    int device = 0;
+    int spf = 0;
+    int n_levels = 0;
+    int level_r[16] = {};
+    float* cb = nullptr;
+    Contraction pre;
+    std::vector<LayerW> layers;
+    float* tf_norm = nullptr;
+    Contraction up[4];
+    Contraction st[8];
+    std::vector<Contraction> rb;   // [stage][resblock][dilation]
+    float* out_w = nullptr;        // [final_k][C_n]
+    float* out_b = nullptr;
+    float* out_alpha = nullptr;
+    float* out_inv_alpha = nullptr;
+    std::vector<void*> allocs;
+    int rb_index(int s, int j, int i) const { return (s * cfg.n_rb + j) * cfg.n_dil + i; }
+};
+
+struct codec_state_s {
+    codec_s* c = nullptr;
+    int n_slots = 0;
+    int R = 0;
+    float* kring = nullptr;
+    float* vring = nullptr;
+    long long* frames_d = nullptr;
+    unsigned* err_d = nullptr;
+    std::vector<long long> frames_h;
+    std::vector<HistDesc> hist;
+    HistDesc* hist_d = nullptr;
+    int P[16] = {};
+    float *e = nullptr, *h = nullptr, *u = nullptr, *q = nullptr, *o = nullptr, *f = nullptr, *hf = nullptr;
+    float* up_out[4] = {};
+    float* x0[8] = {};
+    float* rbuf[8][4][4] = {};
+    float* y[8] = {};
+    TcScratch tc_scratch;
+    // plan: device copy and a ring of page-locked host staging copies
+    int plan_ints = 0;
+    int off_pos0 = 0, off_cf = 0, off_slot = 0, off_bidx = 0, off_tc64 = 0, off_tc128 = 0;
+    int* plan_d = nullptr;
+    static constexpr int kPlanRing = 8;
+    int* plan_h[kPlanRing] = {};
+    cudaEvent_t plan_ev[kPlanRing] = {};
+    int plan_next = 0;
+    int* slots_d = nullptr;
+    int* slots_h = nullptr;
+    cudaEvent_t slots_ev = nullptr;
+    int* codes_d = nullptr;        // host-buffer entry point staging
+    float* audio_d = nullptr;
+    int last_launches = 0;
+    std::vector<void*> allocs;
+};
+
+// ------------------------------------------------------------- helpers ----
+
+namespace {
+
+bool cfg_valid(const codec_config* c)
+{
+    auto m4 = [](int v) { return v > 0 && v % 4 == 0; };
+    if (c->Q < 1 || c->Q > 64 || c->V < 1 || !m4(c->E)) return false;
+    if (c->pre_k < 1 || c->pre_k > kMaxTaps) return false;
+    if (!m4(c->d) || c->heads < 1 || c->d % c->heads || c->d / c->heads > 256) return false;
+    if (!m4(c->ffn) || c->layers < 0 || c->layers > 64 || c->window < 1 || c->window > 128) return false;
+    if (c->n_up < 1 || c->n_up > 4 || c->up_s < 1 || c->up_k != 2 * c->up_s) return false;
+    for (int u = 0; u < c->n_up; u++) if (!m4(c->up_ch[u])) return false;
+    if (c->n_stages < 1 || c->n_stages > 8) return false;
+    for (int s = 0; s < c->n_stages; s++) if (c->strides[s] < 1 || !m4(c->ch[s])) return false;
+    if (c->n_rb < 1 || c->n_rb > 3 || c->n_dil < 1 || c->n_dil > 4) return false;
+    for (int j = 0; j < c->n_rb; j++) if (c->rb_k[j] < 1 || c->rb_k[j] > kMaxTaps) return false;
+    for (int i = 0; i < c->n_dil; i++) if (c->dil[i] < 1 || c->dil[i] > 64) return false;
+    if (c->final_k < 1 || c->final_k > kMaxTaps) return false;
+    if (!(c->rms_eps > 0.f)) return false;
+    if (c->max_streams < 1 || c->max_chunk_frames < 1 || c->max_batch_frames < c->max_chunk_frames) return false;
+    if (c->precision != CODEC_PRECISION_FP32) return false;   // the fp16x3 tensor-core path is not built yet
+    long long spf = 1;
+    for (int u = 0; u < c->n_up; u++) spf *= c->up_s;
+    for (int s = 0; s < c->n_stages; s++) spf *= c->strides[s];
+    if (spf > (1 << 20)) return false;
+    if ((long long)c->max_batch_frames * spf > (1LL << 30)) return false;
+    return true;
+}
+
+long long blob_floats(const codec_config* c)
+{
+    long long n = (long long)c->Q * c->V * c->E;
+    n += (long long)c->d * c->E * c->pre_k + c->d;
+    n += (long long)c->layers * (2LL * c->d + 4LL * c->d * c->d + 2LL * c->ffn * c->d);
+    n += c->d;
+    long long cin = c->d;
+    for (int u = 0; u < c->n_up; u++) {
+        n += cin * c->up_ch[u] * c->up_k + c->up_ch[u];
+        cin = c->up_ch[u];
+    }
+    for (int s = 0; s < c->n_stages; s++) {
+        const long long co = c->ch[s];
+        n += cin + cin * co * 2 * c->strides[s] + co;
+        for (int j = 0; j < c->n_rb; j++) n += (long long)c->n_dil * (co + co * co * c->rb_k[j] + co);
+        cin = co;
+    }
+    n += cin + cin * c->final_k + 1;
+    return n;
+}
+
+template <class T>
+T* dev_upload(std::vector<void*>& allocs, const T* src, size_t n, codec_status& st)
+{
+    if (st != CODEC_OK) return nullptr;
+    T* p = nullptr;
+    if (cudaMalloc(&p, sizeof(T) * (n ? n : 1)) != cudaSuccess) { st = CODEC_ERR_OOM; return nullptr; }
+    allocs.push_back(p);
+    if (n && cudaMemcpy(p, src, sizeof(T) * n, cudaMemcpyHostToDevice) != cudaSuccess) {
+        st = CODEC_ERR_CUDA;
+        return nullptr;
+    }
+    return p;
+}
+
+template <class T>
+T* dev_alloc(std::vector<void*>& allocs, size_t n, codec_status& st, bool zero = false)
+{
+    if (st != CODEC_OK) return nullptr;
+    T* p = nullptr;
+    if (cudaMalloc(&p, sizeof(T) * (n ? n : 1)) != cudaSuccess) { st = CODEC_ERR_OOM; return nullptr; }
+    allocs.push_back(p);
+    if (zero && cudaMemset(p, 0, sizeof(T) * (n ? n : 1)) != cudaSuccess) st = CODEC_ERR_CUDA;
+    return p;
+}
+
+// Fill a Contraction from packed host weights [K][N] and upload it.
+void finish_contraction(codec_s* c, Contraction& C, const std::vector<float>& wkn,
+                        const float* bias, int bias_mod, const float* alpha, codec_status& st)
+{
+    C.K = C.ntaps * C.Cin;
+    C.w = dev_upload(c->allocs, wkn.data(), wkn.size(), st);
+    C.bias_mod = bias_mod;
+    if (bias) C.bias = dev_upload(c->allocs, bias, (size_t)bias_mod, st);
+    if (alpha) {
+        std::vector<float> inv(C.Cin);
+        for (int i = 0; i < C.Cin; i++) inv[i] = 1.0f / alpha[i];
+        C.alpha = dev_upload(c->allocs, alpha, (size_t)C.Cin, st);
+        C.inv_alpha = dev_upload(c->allocs, inv.data(), inv.size(), st);
+    }
+    C.use_tc = c->cfg.precision == CODEC_PRECISION_FP16X3 && tc_eligible(C.Cin, C.N);
+    if (C.use_tc && st == CODEC_OK) {
+        if (!tc_pack_weights(wkn.data(), C.ntaps, C.Cin, C.N, &C.tc, c->allocs)) st = CODEC_ERR_OOM;
+    }
+}
+
+// Conv1d weight [Cout][Cin][k] -> [k Cin][Cout]; tap j reads row t - (k-1-j) dil.
+void make_conv(codec_s* c, Contraction& C, const float* w, const float* b, const float* alpha,
+               int Cin, int Cout, int k, int dil, codec_status& st)
+{
+    C.Cin = Cin; C.N = Cout; C.ntaps = k;
+    for (int j = 0; j < k; j++) C.shift[j] = (k - 1 - j) * dil;
+    std::vector<float> p((size_t)k * Cin * Cout);
+    for (int co = 0; co < Cout; co++)
+        for (int ci = 0; ci < Cin; ci++)
+            for (int j = 0; j < k; j++)
+                p[((size_t)j * Cin + ci) * Cout + co] = w[((size_t)co * Cin + ci) * k + j];
+    finish_contraction(c, C, p, b, Cout, alpha, st);
+}
+
+// ConvTranspose1d weight [Cin][Cout][2s] -> phase GEMM [2 Cin][s Cout]:
+// output column p Cout + co of input row n is row n s + p of the upsampled
+// signal; tap 0 reads a[n-1] with W[:, :, p+s], tap 1 reads a[n] with
+// W[:, :, p] (blixt/phonon "Weights": one GEMM per output phase, gathering
+// its inputs, never scattering).
+void make_convt(codec_s* c, Contraction& C, const float* w, const float* b, const float* alpha,
+                int Cin, int Cout, int s, codec_status& st)
+{
+    C.Cin = Cin; C.N = s * Cout; C.ntaps = 2;
+    C.shift[0] = 1;
+    C.shift[1] = 0;
+    const int k = 2 * s;
+    std::vector<float> p((size_t)2 * Cin * s * Cout);
+    for (int ci = 0; ci < Cin; ci++)
+        for (int co = 0; co < Cout; co++)
+            for (int ph = 0; ph < s; ph++) {
+                const size_t n = (size_t)ph * Cout + co;
+                p[(size_t)ci * C.N + n] = w[((size_t)ci * Cout + co) * k + ph + s];
+                p[((size_t)Cin + ci) * C.N + n] = w[((size_t)ci * Cout + co) * k + ph];
+            }
+    finish_contraction(c, C, p, b, Cout, alpha, st);
+}
+
+// Linear weights [Cout][Cin] (several concatenated along Cout) -> [Cin][sum Cout].
+void make_linear(codec_s* c, Contraction& C, std::vector<const float*> ws, int Cin, int Cout_each,
+                 codec_status& st)
+{
+    const int N = Cout_each * (int)ws.size();
+    C.Cin = Cin; C.N = N; C.ntaps = 1; C.shift[0] = 0;
+    std::vector<float> p((size_t)Cin * N);
+    for (size_t m = 0; m < ws.size(); m++)
+        for (int o = 0; o < Cout_each; o++)
+            for (int i = 0; i < Cin; i++)
+                p[(size_t)i * N + m * Cout_each + o] = ws[m][(size_t)o * Cin + i];
+    finish_contraction(c, C, p, nullptr, 1, nullptr, st);
+}
+
+void free_all(std::vector<void*>& v)
+{
+    for (void* p : v) cudaFree(p);
+    v.clear();
+}
+
+}  // namespace
+
+// ------------------------------------------------------------ C ABI -------
+
+extern "C" {
+
+const char* codec_status_string(codec_status s)
+{
+    switch (s) {
+    case CODEC_OK: return "ok";
+    case CODEC_ERR_NULL: return "a required pointer is NULL";
+    case CODEC_ERR_CONFIG: return "invalid or unsupported configuration";
+    case CODEC_ERR_WEIGHTS: return "weight blob length does not match the configuration";
+    case CODEC_ERR_ARG: return "argument out of range or repeated stream id";
+    case CODEC_ERR_CAPACITY: return "request exceeds the configured capacity";
+    case CODEC_ERR_OOM: return "device allocation failed";
+    case CODEC_ERR_CUDA: return "CUDA call failed";
+    case CODEC_ERR_NO_DEVICE: return "no usable sm_103 device";
+    }
+    return "unknown status";
+}
+
+int64_t codec_weight_floats(const codec_config* cfg)
+{
+    if (!cfg || !cfg_valid(cfg)) return -1;
+    return blob_floats(cfg);
+}
+
+int32_t codec_samples_per_frame(const codec_t* c) { return c ? c->spf : 0; }
+
+codec_status codec_create(const codec_config* cfg, const float* weights, int64_t n_floats, codec_t** out)
+{
+    if (!out) return CODEC_ERR_NULL;
+    *out = nullptr;
+    if (!cfg || !weights) return CODEC_ERR_NULL;
+    if (!cfg_valid(cfg)) return CODEC_ERR_CONFIG;
+    if (n_floats != blob_floats(cfg)) return CODEC_ERR_WEIGHTS;
+    int dev = 0;
+    cudaDeviceProp prop;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaGetDeviceProperties(&prop, dev) != cudaSuccess)
+        return CODEC_ERR_NO_DEVICE;
+    if (prop.major != 10 || prop.minor != 3) return CODEC_ERR_NO_DEVICE;
+
+    codec_s* c = new codec_s();
+    c->cfg = *cfg;
+    c->device = dev;
+    const codec_config& g = c->cfg;
+    codec_status st = CODEC_OK;
+    c->spf = 1;
+    c->level_r[0] = 1;
+    c->n_levels = 1;
+    for (int u = 0; u < g.n_up; u++) { c->spf *= g.up_s; c->level_r[c->n_levels++] = c->spf; }
+    for (int s = 0; s < g.n_stages; s++) { c->spf *= g.strides[s]; c->level_r[c->n_levels++] = c->spf; }
+
+    const float* p = weights;
+    auto take = [&](long long n) { const float* r = p; p += n; return r; };
+    c->cb = dev_upload(c->allocs, take((long long)g.Q * g.V * g.E), (size_t)g.Q * g.V * g.E, st);
+    {
+        const float* w = take((long long)g.d * g.E * g.pre_k);
+        const float* b = take(g.d);
+        make_conv(c, c->pre, w, b, nullptr, g.E, g.d, g.pre_k, 1, st);
+    }
+    c->layers.resize(g.layers);
+    for (int l = 0; l < g.layers; l++) {
+        LayerW& L = c->layers[l];
+        const long long dd = (long long)g.d * g.d;
+        L.n1 = dev_upload(c->allocs, take(g.d), g.d, st);
+        const float* wq = take(dd);
+        const float* wk = take(dd);
+        const float* wv = take(dd);
+        const float* wo = take(dd);
+        make_linear(c, L.qkv, {wq, wk, wv}, g.d, g.d, st);
+        make_linear(c, L.o, {wo}, g.d, g.d, st);
+        L.n2 = dev_upload(c->allocs, take(g.d), g.d, st);
+        const float* w1 = take((long long)g.ffn * g.d);
+        const float* w2 = take((long long)g.d * g.ffn);
+        make_linear(c, L.w1, {w1}, g.d, g.ffn, st);
+        make_linear(c, L.w2, {w2}, g.ffn, g.d, st);
+    }
+    c->tf_norm = dev_upload(c->allocs, take(g.d), g.d, st);
+    int cin = g.d;
+    for (int u = 0; u < g.n_up; u++) {
+        const int co = g.up_ch[u];
+        const float* w = take((long long)cin * co * g.up_k);
+        const float* b = take(co);
+        make_convt(c, c->up[u], w, b, nullptr, cin, co, g.up_s, st);
+        cin = co;
+    }
+    c->rb.resize((size_t)g.n_stages * g.n_rb * g.n_dil);
+    for (int s = 0; s < g.n_stages; s++) {
+        const int co = g.ch[s];
+        const float* alpha = take(cin);
+        const float* w = take((long long)cin * co * 2 * g.strides[s]);
+        const float* b = take(co);
+        make_convt(c, c->st[s], w, b, alpha, cin, co, g.strides[s], st);
+        for (int j = 0; j < g.n_rb; j++)
+            for (int i = 0; i < g.n_dil; i++) {
+                const float* a2 = take(co);
+                const float* w2 = take((long long)co * co * g.rb_k[j]);
+                const float* b2 = take(co);
+                make_conv(c, c->rb[c->rb_index(s, j, i)], w2, b2, a2, co, co, g.rb_k[j], g.dil[i], st);
+            }
+        cin = co;
+    }
+    {
+        const float* alpha = take(cin);
+        const float* w = take((long long)cin * g.final_k);
+        const float* b = take(1);
+        std::vector<float> wt((size_t)g.final_k * cin), inv(cin);
+        for (int ci = 0; ci < cin; ci++) {
+            inv[ci] = 1.0f / alpha[ci];
+            for (int j = 0; j < g.final_k; j++) wt[(size_t)j * cin + ci] = w[(size_t)ci * g.final_k + j];
+        }
+        c->out_w = dev_upload(c->allocs, wt.data(), wt.size(), st);
+        c->out_b = dev_upload(c->allocs, b, 1, st);
+        c->out_alpha = dev_upload(c->allocs, alpha, (size_t)cin, st);
+        c->out_inv_alpha = dev_upload(c->allocs, inv.data(), inv.size(), st);
+    }
+    if (st == CODEC_OK && cudaDeviceSynchronize() != cudaSuccess) st = CODEC_ERR_CUDA;
+    if (st != CODEC_OK) {
+        free_all(c->allocs);
+        delete c;
+        return st;
+    }
+    *out = c;
+    return CODEC_OK;
+}
+
+void codec_destroy(codec_t* c)
+{
+    if (!c) return;
+    cudaDeviceSynchronize();
+    free_all(c->allocs);
+    delete c;
+}
+
+codec_status codec_state_create(codec_t* c, int32_t n_streams, codec_state_t** out)
+{
+    if (!out) return CODEC_ERR_NULL;
+    *out = nullptr;
+    if (!c) return CODEC_ERR_NULL;
+    const codec_config& g = c->cfg;
+    if (n_streams < 0 || n_streams > (1 << 16)) return CODEC_ERR_ARG;
+    codec_state_s* s = new codec_state_s();
+    s->c = c;
+    s->n_slots = n_streams ? n_streams : g.max_streams;
+    const int S = s->n_slots;
+    codec_status st = CODEC_OK;
+
+    // per-level history rows in front of every segment
+    const int last = c->n_levels - 1;
+    s->P[0] = std::max(g.pre_k - 1, 1);
+    for (int u = 0; u < g.n_up; u++) s->P[1 + u] = 1;
+    for (int si = 0; si < g.n_stages; si++) {
+        int P = 1;
+        for (int j = 0; j < g.n_rb; j++)
+            for (int i = 0; i < g.n_dil; i++) P = std::max(P, (g.rb_k[j] - 1) * g.dil[i]);
+        if (si == g.n_stages - 1) P = std::max(P, g.final_k - 1);
+        s->P[g.n_up + 1 + si] = P;
+    }
+    auto rows = [&](int lvl, bool pref) {
+        return (size_t)g.max_batch_frames * c->level_r[lvl] + (pref ? (size_t)S * s->P[lvl] : 0);
+    };
+    auto& A = s->allocs;
+    const size_t r0 = rows(0, false);
+    s->e = dev_alloc<float>(A, rows(0, true) * g.E, st);
+    s->h = dev_alloc<float>(A, r0 * g.d, st);
+    s->u = dev_alloc<float>(A, r0 * g.d, st);
+    s->q = dev_alloc<float>(A, r0 * g.d, st);
+    s->o = dev_alloc<float>(A, r0 * g.d, st);
+    s->f = dev_alloc<float>(A, r0 * g.ffn, st);
+    s->hf = dev_alloc<float>(A, rows(0, true) * g.d, st);
+    for (int u = 0; u < g.n_up; u++) s->up_out[u] = dev_alloc<float>(A, rows(1 + u, true) * g.up_ch[u], st);
+    for (int si = 0; si < g.n_stages; si++) {
+        const int lvl = g.n_up + 1 + si;
+        const size_t n = rows(lvl, true) * g.ch[si];
+        s->x0[si] = dev_alloc<float>(A, n, st);
+        for (int j = 0; j < g.n_rb; j++)
+            for (int i = 1; i < g.n_dil; i++) s->rbuf[si][j][i] = dev_alloc<float>(A, n, st);
+        s->y[si] = dev_alloc<float>(A, n, st);
+    }
+    (void)last;
+
+    // carried state: histories, ring KV, counters
+    auto add_hist = [&](float* buf, int C, int H, int lvl) {
+        if (H <= 0) return;
+        HistDesc d;
+        d.buf = buf; d.C = C; d.H = H; d.l = Layout{c->level_r[lvl], s->P[lvl]};
+        d.state = dev_alloc<float>(A, (size_t)S * H * C, st, true);
+        s->hist.push_back(d);
+    };
+    add_hist(s->e, g.E, g.pre_k - 1, 0);
+    add_hist(s->hf, g.d, 1, 0);
+    for (int u = 0; u < g.n_up; u++) add_hist(s->up_out[u], g.up_ch[u], 1, 1 + u);
+    for (int si = 0; si < g.n_stages; si++) {
+        const int lvl = g.n_up + 1 + si;
+        int h0 = 0;
+        for (int j = 0; j < g.n_rb; j++) h0 = std::max(h0, (g.rb_k[j] - 1) * g.dil[0]);
+        add_hist(s->x0[si], g.ch[si], h0, lvl);
+        for (int j = 0; j < g.n_rb; j++)
+            for (int i = 1; i < g.n_dil; i++) add_hist(s->rbuf[si][j][i], g.ch[si], (g.rb_k[j] - 1) * g.dil[i], lvl);
+        add_hist(s->y[si], g.ch[si], si == g.n_stages - 1 ? g.final_k - 1 : 1, lvl);
+    }
+    s->hist_d = dev_upload(A, s->hist.data(), s->hist.size(), st);
+    s->R = next_pow2(g.max_chunk_frames + g.window - 1);
+    const size_t ring = (size_t)std::max(g.layers, 1) * S * s->R * g.d;
+    s->kring = dev_alloc<float>(A, ring, st, true);
+    s->vring = dev_alloc<float>(A, ring, st, true);
+    s->frames_d = dev_alloc<long long>(A, S, st, true);
+    s->err_d = dev_alloc<unsigned>(A, S, st, true);
+    s->frames_h.assign(S, 0);
+
+    // plan layout (ints); pos0 first for 8-byte alignment
+    s->off_pos0 = 0;
+    s->off_cf = 2 * S;
+    s->off_slot = s->off_cf + S + 1;
+    s->off_bidx = s->off_slot + S;
+    s->off_tc64 = s->off_bidx + S;
+    s->off_tc128 = s->off_tc64 + c->n_levels * (S + 1);
+    s->plan_ints = s->off_tc128 + c->n_levels * (S + 1);
+    s->plan_d = dev_alloc<int>(A, s->plan_ints, st, true);
+    for (int i = 0; i < codec_state_s::kPlanRing && st == CODEC_OK; i++) {
+        if (cudaMallocHost(&s->plan_h[i], sizeof(int) * s->plan_ints) != cudaSuccess) st = CODEC_ERR_OOM;
+        else if (cudaEventCreateWithFlags(&s->plan_ev[i], cudaEventDisableTiming) != cudaSuccess) st = CODEC_ERR_CUDA;
+    }
+    s->slots_d = dev_alloc<int>(A, S, st);
+    if (st == CODEC_OK) {
+        if (cudaMallocHost(&s->slots_h, sizeof(int) * S) != cudaSuccess) st = CODEC_ERR_OOM;
+        else if (cudaEventCreateWithFlags(&s->slots_ev, cudaEventDisableTiming) != cudaSuccess) st = CODEC_ERR_CUDA;
+    }
+    s->codes_d = dev_alloc<int>(A, (size_t)S * g.Q * g.max_chunk_frames, st);
+    s->audio_d = dev_alloc<float>(A, (size_t)S * g.max_chunk_frames * c->spf, st);
+    if (st == CODEC_OK && g.precision == CODEC_PRECISION_FP16X3) {
+        size_t max_rows = 0, max_c = 0;
+        for (int lvl = 0; lvl < c->n_levels; lvl++) max_rows = std::max(max_rows, rows(lvl, true));
+        max_c = std::max({(size_t)g.E, (size_t)g.d, (size_t)g.ffn});
+        for (int u = 0; u < g.n_up; u++) max_c = std::max(max_c, (size_t)g.up_ch[u]);
+        size_t elems = 0;
+        for (int lvl = 0; lvl < c->n_levels; lvl++) {
+            size_t ch = lvl == 0 ? max_c : (lvl <= g.n_up ? (size_t)g.up_ch[lvl - 1] : (size_t)g.ch[lvl - g.n_up - 1]);
+            if (lvl > 0 && lvl <= g.n_up) ch = std::max(ch, (size_t)(lvl == g.n_up ? g.up_ch[lvl - 1] : g.up_ch[lvl - 1]));
+            elems = std::max(elems, rows(lvl, true) * ch);
+        }
+        // the stage ConvT reads the previous level, whose widths are covered above
+        if (!tc_scratch_alloc(&s->tc_scratch, elems, A)) st = CODEC_ERR_OOM;
+    }
+    if (st == CODEC_OK && cudaDeviceSynchronize() != cudaSuccess) st = CODEC_ERR_CUDA;
+    if (st != CODEC_OK) {
+        for (int i = 0; i < codec_state_s::kPlanRing; i++) {
+            if (s->plan_h[i]) cudaFreeHost(s->plan_h[i]);
+            if (s->plan_ev[i]) cudaEventDestroy(s->plan_ev[i]);
+        }
+        if (s->slots_h) cudaFreeHost(s->slots_h);
+        if (s->slots_ev) cudaEventDestroy(s->slots_ev);
+        free_all(A);
+        delete s;
+        return st;
+    }
+    *out = s;
+    return CODEC_OK;
+}
+
+void codec_state_destroy(codec_state_t* s)
+{
+    if (!s) return;
+    cudaDeviceSynchronize();
+    for (int i = 0; i < codec_state_s::kPlanRing; i++) {
+        if (s->plan_h[i]) cudaFreeHost(s->plan_h[i]);
+        if (s->plan_ev[i]) cudaEventDestroy(s->plan_ev[i]);
+    }
+    if (s->slots_h) cudaFreeHost(s->slots_h);
+    if (s->slots_ev) cudaEventDestroy(s->slots_ev);
+    free_all(s->allocs);
+    delete s;
+}
+
+int32_t codec_state_streams(const codec_state_t* s) { return s ? s->n_slots : 0; }
+int32_t codec_state_last_launches(const codec_state_t* s) { return s ? s->last_launches : 0; }
+
+codec_status codec_state_reset(codec_state_t* s, const int32_t* ids, int32_t n, void* stream)
+{
+    if (!s) return CODEC_ERR_NULL;
+    const int S = s->n_slots;
+    std::vector<int> list;
+    if (!ids) {
+        for (int i = 0; i < S; i++) list.push_back(i);
+    } else {
+        if (n < 0 || n > S) return CODEC_ERR_ARG;
+        std::vector<char> seen(S, 0);
+        for (int i = 0; i < n; i++) {
+            if (ids[i] < 0 || ids[i] >= S || seen[ids[i]]) return CODEC_ERR_ARG;
+            seen[ids[i]] = 1;
+            list.push_back(ids[i]);
+        }
+    }
+    if (list.empty()) return CODEC_OK;
+    cudaStream_t cs = (cudaStream_t)stream;
+    if (cudaEventSynchronize(s->slots_ev) != cudaSuccess) return CODEC_ERR_CUDA;
+    std::memcpy(s->slots_h, list.data(), sizeof(int) * list.size());
+    if (cudaMemcpyAsync(s->slots_d, s->slots_h, sizeof(int) * list.size(), cudaMemcpyHostToDevice, cs) != cudaSuccess)
+        return CODEC_ERR_CUDA;
+    if (cudaEventRecord(s->slots_ev, cs) != cudaSuccess) return CODEC_ERR_CUDA;
+    if (launch_state_reset(s->hist_d, (int)s->hist.size(), s->slots_d, (int)list.size(), s->frames_d,
+                           s->err_d, cs) != cudaSuccess)
+        return CODEC_ERR_CUDA;
+    for (int i : list) s->frames_h[i] = 0;
+    return CODEC_OK;
+}
+
+codec_status codec_state_query(codec_state_t* s, int32_t id, codec_stream_info* info, void* stream)
+{
+    if (!s || !info) return CODEC_ERR_NULL;
+    if (id < 0 || id >= s->n_slots) return CODEC_ERR_ARG;
+    cudaStream_t cs = (cudaStream_t)stream;
+    long long fr = 0;
+    unsigned err = 0;
+    if (cudaStreamSynchronize(cs) != cudaSuccess) return CODEC_ERR_CUDA;
+    if (cudaMemcpy(&fr, s->frames_d + id, sizeof(fr), cudaMemcpyDeviceToHost) != cudaSuccess) return CODEC_ERR_CUDA;
+    if (cudaMemcpy(&err, s->err_d + id, sizeof(err), cudaMemcpyDeviceToHost) != cudaSuccess) return CODEC_ERR_CUDA;
+    info->frames_decoded = fr;
+    info->error_bits = err;
+    info->reserved = 0;
+    return CODEC_OK;
+}
+
+}  // extern "C"
+
+// ------------------------------------------------------- decode call ------
+
+namespace {
+
+struct Launcher {
+    codec_state_s* s;
+    cudaStream_t cs;
+    PlanView pv;
+    const int* tc64;     // device, [levels][S + 1]
+    const int* tc128;
+    std::vector<int> ntiles64, ntiles128;   // per level
+    std::vector<int> slot_h, n_h;           // host copies of the compacted batch
+    int launches = 0;
+    cudaError_t err = cudaSuccess;
+    const char* where = "";
+
+    bool check(cudaError_t e, const char* what)
+    {
+        launches++;
+        if (e != cudaSuccess && err == cudaSuccess) { err = e; where = what; }
+        if (err == cudaSuccess && debug_sync()) {
+            cudaError_t e2 = cudaStreamSynchronize(cs);
+            if (e2 != cudaSuccess) { err = e2; where = what; }
+        }
+        return err == cudaSuccess;
+    }
+
+    void gemm(const Contraction& C, const float* in, Layout il, int in_lvl, float* out, Layout ol,
+              int out_C, int out_step, const float* res, int epi, float scale, int layer_ring,
+              const char* what)
+    {
+        if (err != cudaSuccess) return;
+        const int S1 = s->n_slots + 1;
+        GemmArgs a{};
+        a.in = in; a.in_l = il; a.Cin = C.Cin; a.ntaps = C.ntaps;
+        for (int j = 0; j < C.ntaps; j++) a.shift[j] = C.shift[j];
+        a.alpha = C.alpha; a.inv_alpha = C.inv_alpha;
+        a.N = C.N; a.K = C.K; a.w = C.w;
+        a.bias = C.bias; a.bias_mod = C.bias_mod;
+        a.out = out; a.out_l = ol; a.out_C = out_C; a.out_step = out_step;
+        a.res = res; a.epi = epi; a.scale = scale;
+        if (epi == EPI_QKV) {
+            const size_t per_layer = (size_t)s->n_slots * s->R * s->c->cfg.d;
+            a.kring = s->kring + per_layer * layer_ring;
+            a.vring = s->vring + per_layer * layer_ring;
+            a.ring_R = s->R;
+            a.d = s->c->cfg.d;
+        }
+        if (C.use_tc) {
+            a.tcum = tc128 + (size_t)in_lvl * S1;
+            a.bm = 128;
+            check(launch_gemm_tc(a, C.tc, pv, ntiles128[in_lvl], &s->tc_scratch, cs, &launches), what);
+        } else {
+            a.tcum = tc64 + (size_t)in_lvl * S1;
+            a.bm = 64;
+            check(launch_gemm_simt(a, pv, ntiles64[in_lvl], cs), what);
+        }
+    }
+};
+
+// Validate a call's batch, build its plan (cumulative frames, slots, tile
+// counts per level) in a page-locked staging buffer and enqueue the upload.
+codec_status plan_call(codec_state_t* s, const int32_t* n_frames, const int32_t* ids, int32_t B,
+                       int32_t T_max, cudaStream_t cs, Launcher& L, int& rows0)
+{
+    codec_s* c = s->c;
+    const codec_config& g = c->cfg;
+    const int S = s->n_slots;
+    if (B < 1 || T_max < 1) return CODEC_ERR_ARG;
+    if (B > S) return CODEC_ERR_CAPACITY;
+    std::vector<char> seen(S, 0);
+    long long total = 0;
+    for (int b = 0; b < B; b++) {
+        const int id = ids ? ids[b] : b;
+        if (id < 0 || id >= S || seen[id]) return CODEC_ERR_ARG;
+        seen[id] = 1;
+        if (n_frames[b] < 0 || n_frames[b] > T_max) return CODEC_ERR_ARG;
+        if (n_frames[b] > g.max_chunk_frames) return CODEC_ERR_CAPACITY;
+        total += n_frames[b];
+    }
+    if (total > g.max_batch_frames) return CODEC_ERR_CAPACITY;
+    rows0 = (int)total;
+    if (total == 0) return CODEC_OK;
+
+    const int i = s->plan_next;
+    s->plan_next = (i + 1) % codec_state_s::kPlanRing;
+    if (cudaEventSynchronize(s->plan_ev[i]) != cudaSuccess) return CODEC_ERR_CUDA;
+    int* P = s->plan_h[i];
+    long long* pos0 = reinterpret_cast<long long*>(P + s->off_pos0);
+    int* cf = P + s->off_cf;
+    int* slot = P + s->off_slot;
+    int* bidx = P + s->off_bidx;
+    int Bc = 0;
+    cf[0] = 0;
+    for (int b = 0; b < B; b++) {
+        if (n_frames[b] == 0) continue;
+        const int id = ids ? ids[b] : b;
+        slot[Bc] = id;
+        bidx[Bc] = b;
+        pos0[Bc] = s->frames_h[id];
+        cf[Bc + 1] = cf[Bc] + n_frames[b];
+        Bc++;
+    }
+    const int S1 = S + 1;
+    L.s = s;
+    L.cs = cs;
+    L.ntiles64.assign(c->n_levels, 0);
+    L.ntiles128.assign(c->n_levels, 0);
+    for (int lvl = 0; lvl < c->n_levels; lvl++) {
+        int* t64 = P + s->off_tc64 + lvl * S1;
+        int* t128 = P + s->off_tc128 + lvl * S1;
+        t64[0] = t128[0] = 0;
+        for (int b = 0; b < Bc; b++) {
+            const long long rows = (long long)(cf[b + 1] - cf[b]) * c->level_r[lvl];
+            t64[b + 1] = t64[b] + (int)((rows + 63) / 64);
+            t128[b + 1] = t128[b] + (int)((rows + 127) / 128);
+        }
+        L.ntiles64[lvl] = t64[Bc];
+        L.ntiles128[lvl] = t128[Bc];
+    }
+    if (cudaMemcpyAsync(s->plan_d, P, sizeof(int) * s->plan_ints, cudaMemcpyHostToDevice, cs) != cudaSuccess)
+        return CODEC_ERR_CUDA;
+    if (cudaEventRecord(s->plan_ev[i], cs) != cudaSuccess) return CODEC_ERR_CUDA;
+    const int* D = s->plan_d;
+    L.pv = PlanView{Bc, D + s->off_cf, D + s->off_slot,
+                    reinterpret_cast<const long long*>(D + s->off_pos0), D + s->off_bidx};
+    L.tc64 = D + s->off_tc64;
+    L.tc128 = D + s->off_tc128;
+    L.slot_h.assign(slot, slot + Bc);
+    L.n_h.resize(Bc);
+    for (int b = 0; b < Bc; b++) L.n_h[b] = cf[b + 1] - cf[b];
+    return CODEC_OK;
+}
+
+codec_status decode_impl(codec_state_t* s, const int32_t* codes, const int32_t* n_frames,
+                         const int32_t* ids, int32_t B, int32_t T_max, float* audio, float* pre_tanh,
+                         cudaStream_t cs)
+{
+    if (!s || !codes || !n_frames || !audio) return CODEC_ERR_NULL;
+    codec_s* c = s->c;
+    const codec_config& g = c->cfg;
+    const int S = s->n_slots;
+    s->last_launches = 0;
+    Launcher L;
+    int rows0 = 0;
+    codec_status pst = plan_call(s, n_frames, ids, B, T_max, cs, L, rows0);
+    if (pst != CODEC_OK || rows0 == 0) return pst;
+
+    const Layout L0d{1, 0}, L0p{1, s->P[0]};
+    auto lay = [&](int lvl) { return Layout{c->level_r[lvl], s->P[lvl]}; };
+
+    L.check(launch_hist_fill(s->hist_d, (int)s->hist.size(), L.pv, cs), "history fill");
+    if (L.err == cudaSuccess)
+        L.check(launch_rvq_gather(c->cb, g.Q, g.V, g.E, codes, T_max, L.pv, s->e, L0p, s->err_d, rows0, cs),
+                "codebook gather");
+    L.gemm(c->pre, s->e, L0p, 0, s->h, L0d, g.d, 1, nullptr, EPI_STORE, 1.f, 0, "pre-conv");
+    for (int l = 0; l < g.layers; l++) {
+        const LayerW& W = c->layers[l];
+        if (L.err == cudaSuccess)
+            L.check(launch_rms_norm(s->h, L0d, W.n1, g.rms_eps, s->u, L0d, g.d, L.pv, rows0, cs), "rmsnorm 1");
+        L.gemm(W.qkv, s->u, L0d, 0, s->q, L0d, g.d, 1, nullptr, EPI_QKV, 1.f, l, "qkv");
+        if (L.err == cudaSuccess) {
+            const size_t per_layer = (size_t)S * s->R * g.d;
+            L.check(launch_swa(s->q, s->o, s->kring + per_layer * l, s->vring + per_layer * l, g.d, g.heads,
+                               g.window, s->R, L.pv, rows0, cs),
+                    "attention");
+        }
+        L.gemm(W.o, s->o, L0d, 0, s->h, L0d, g.d, 1, s->h, EPI_RESID, 1.f, 0, "out-proj");
+        if (L.err == cudaSuccess)
+            L.check(launch_rms_norm(s->h, L0d, W.n2, g.rms_eps, s->u, L0d, g.d, L.pv, rows0, cs), "rmsnorm 2");
+        L.gemm(W.w1, s->u, L0d, 0, s->f, L0d, g.ffn, 1, nullptr, EPI_GELU, 1.f, 0, "mlp 1");
+        L.gemm(W.w2, s->f, L0d, 0, s->h, L0d, g.d, 1, s->h, EPI_RESID, 1.f, 0, "mlp 2");
+    }
+    if (L.err == cudaSuccess)
+        L.check(launch_rms_norm(s->h, L0d, c->tf_norm, g.rms_eps, s->hf, L0p, g.d, L.pv, rows0, cs),
+                "final rmsnorm");
+    const float* x = s->hf;
+    int xl = 0;
+    for (int u = 0; u < g.n_up; u++) {
+        L.gemm(c->up[u], x, lay(xl), xl, s->up_out[u], lay(xl + 1), g.up_ch[u], g.up_s, nullptr, EPI_STORE,
+               1.f, 0, "latent upsample");
+        x = s->up_out[u];
+        xl++;
+    }
+    for (int si = 0; si < g.n_stages; si++) {
+        const int lvl = xl + 1;
+        const int C = g.ch[si];
+        L.gemm(c->st[si], x, lay(xl), xl, s->x0[si], lay(lvl), C, g.strides[si], nullptr, EPI_STORE, 1.f, 0,
+               "stage upsample");
+        for (int j = 0; j < g.n_rb; j++) {
+            const float* rin = s->x0[si];
+            for (int ii = 0; ii < g.n_dil; ii++) {
+                const bool last_d = ii == g.n_dil - 1;
+                float* out = last_d ? s->y[si] : s->rbuf[si][j][ii + 1];
+                int epi = EPI_RESID;
+                if (last_d && g.n_rb > 1) epi = j == 0 ? EPI_MRF_FIRST : (j == g.n_rb - 1 ? EPI_MRF_LAST : EPI_MRF_ADD);
+                L.gemm(c->rb[c->rb_index(si, j, ii)], rin, lay(lvl), lvl, out, lay(lvl), C, 1, rin, epi,
+                       1.0f / (float)g.n_rb, 0, "resblock conv");
+                rin = out;
+            }
+        }
+        x = s->y[si];
+        xl = lvl;
+    }
+    if (L.err == cudaSuccess) {
+        const int S1l = S + 1;
+        L.check(launch_final_conv(x, lay(xl), g.ch[g.n_stages - 1], c->out_w, c->out_b, c->out_alpha,
+                                  c->out_inv_alpha, g.final_k, audio, pre_tanh,
+                                  (long long)T_max * c->spf, L.pv, L.tc128 + (size_t)xl * S1l,
+                                  L.ntiles128[xl], cs),
+                "final conv");
+    }
+    if (L.err == cudaSuccess)
+        L.check(launch_hist_commit(s->hist_d, (int)s->hist.size(), L.pv, nullptr, s->frames_d, cs), "history commit");
+    s->last_launches = L.launches;
+    if (L.err != cudaSuccess) {
+        if (debug_sync()) fprintf(stderr, "codec: %s failed: %s\n", L.where, cudaGetErrorString(L.err));
+        return CODEC_ERR_CUDA;
+    }
+    for (size_t b = 0; b < L.slot_h.size(); b++) s->frames_h[L.slot_h[b]] += L.n_h[b];
+    return CODEC_OK;
+}
+
+codec_status embed_impl(codec_state_t* s, const int32_t* codes, const int32_t* n_frames, const int32_t* ids,
+                        int32_t B, int32_t T_max, float* emb, cudaStream_t cs)
+{
+    if (!s || !codes || !n_frames || !emb) return CODEC_ERR_NULL;
+    const codec_config& g = s->c->cfg;
+    Launcher L;
+    int rows0 = 0;
+    codec_status pst = plan_call(s, n_frames, ids, B, T_max, cs, L, rows0);
+    if (pst != CODEC_OK || rows0 == 0) return pst;
+    L.check(launch_rvq_gather(s->c->cb, g.Q, g.V, g.E, codes, T_max, L.pv, emb, Layout{1, 0}, s->err_d, rows0, cs),
+            "codebook gather");
+    s->last_launches = L.launches;
+    return L.err == cudaSuccess ? CODEC_OK : CODEC_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+codec_status codec_decode_chunk(codec_state_t* s, const int32_t* codes, const int32_t* n_frames,
+                                const int32_t* ids, int32_t B, int32_t T_max, float* audio, void* stream)
+{
+    return decode_impl(s, codes, n_frames, ids, B, T_max, audio, nullptr, (cudaStream_t)stream);
+}
+
+codec_status codec_decode_chunk_ex(codec_state_t* s, const int32_t* codes, const int32_t* n_frames,
+                                   const int32_t* ids, int32_t B, int32_t T_max, float* audio,
+                                   float* pre_tanh, void* stream)
+{
+    return decode_impl(s, codes, n_frames, ids, B, T_max, audio, pre_tanh, (cudaStream_t)stream);
+}
+
+codec_status codec_embed_chunk(codec_state_t* s, const int32_t* codes, const int32_t* n_frames,
+                               const int32_t* ids, int32_t B, int32_t T_max, float* emb, void* stream)
+{
+    return embed_impl(s, codes, n_frames, ids, B, T_max, emb, (cudaStream_t)stream);
+}
+
+codec_status codec_decode_chunk_host(codec_state_t* s, const int32_t* codes_host, const int32_t* n_frames,
+                                     const int32_t* ids, int32_t B, int32_t T_max, float* audio_host,
+                                     void* stream)
+{
+    if (!s || !codes_host || !n_frames || !audio_host) return CODEC_ERR_NULL;
+    const codec_config& g = s->c->cfg;
+    if (B < 1 || T_max < 1) return CODEC_ERR_ARG;
+    if (B > s->n_slots || T_max > g.max_chunk_frames) return CODEC_ERR_CAPACITY;
+    cudaStream_t cs = (cudaStream_t)stream;
+    if (cudaMemcpyAsync(s->codes_d, codes_host, sizeof(int32_t) * (size_t)B * g.Q * T_max,
+                        cudaMemcpyHostToDevice, cs) != cudaSuccess)
+        return CODEC_ERR_CUDA;
+    codec_status st = decode_impl(s, s->codes_d, n_frames, ids, B, T_max, s->audio_d, nullptr, cs);
+    if (st != CODEC_OK) return st;
+    const size_t ld = (size_t)T_max * s->c->spf;
+    for (int b = 0; b < B; b++) {
+        if (n_frames[b] <= 0) continue;
+        if (cudaMemcpyAsync(audio_host + b * ld, s->audio_d + b * ld, sizeof(float) * (size_t)n_frames[b] * s->c->spf,
+                            cudaMemcpyDeviceToHost, cs) != cudaSuccess)
+            return CODEC_ERR_CUDA;
+    }
+    if (cudaStreamSynchronize(cs) != cudaSuccess) return CODEC_ERR_CUDA;
+    return CODEC_OK;
+}
+
+}  // extern "C"

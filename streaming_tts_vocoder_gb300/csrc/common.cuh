@@ -1,0 +1,103 @@
+// Shared definitions of the CUDA library: launch descriptors, per-call plan
+// layout and the small device helpers every kernel uses.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace codec {
+
+constexpr int kMaxTaps = 16;
+
+// Epilogue modes of the implicit-GEMM kernels (what happens to acc = A*B).
+enum Epi : int {
+    EPI_STORE = 0,   // out = acc + bias
+    EPI_RESID = 1,   // out = res + acc + bias
+    EPI_GELU = 2,    // out = gelu(acc + bias)
+    EPI_MRF_FIRST = 3,  // out = res + acc + bias                (first resblock of an MRF)
+    EPI_MRF_ADD = 4,    // out = out + (res + acc + bias)
+    EPI_MRF_LAST = 5,   // out = (out + (res + acc + bias)) * scale
+    EPI_QKV = 6,     // n < d: q[row][n] = acc; d <= n < 2d: K ring; 2d <= n: V ring
+};
+
+// Rows of a tensor in the per-call packed layout.  Stream segment b of a
+// "level" with rate r (rows per frame) holds n_b * r chunk rows.  A prefixed
+// layout puts P history rows in front of every segment, so that segment b's
+// chunk row 0 sits at cf[b] * r + (b + 1) * P; a dense layout (P = 0) packs the
+// chunk rows back to back.
+struct Layout {
+    int r;     // rows per frame
+    int P;     // history rows in front of each segment (0 = dense)
+};
+
+__host__ __device__ inline long long seg_base(const Layout& L, const int* cf, int b)
+{
+    return (long long)cf[b] * L.r + (long long)(b + 1) * L.P;
+}
+
+// Per-call plan, uploaded to the device before the launches.  All arrays are
+// indexed by batch entry b < B.
+struct PlanView {
+    int B;
+    const int* cf;          // [B + 1] cumulative frames
+    const int* slot;        // [B] state slot of batch entry b
+    const long long* pos0;  // [B] frames the stream had decoded before this call
+    const int* bidx;        // [B] row of b in the caller's codes / audio arrays
+};
+
+// Implicit-GEMM launch descriptor: out rows t of segment b are
+//   epi( sum_{tap j} sum_{ci} A(in[base_in(b) + t - shift_j][ci]) * W[j*Cin + ci][n] ).
+struct GemmArgs {
+    const float* in;
+    Layout in_l;
+    int Cin;
+    int ntaps;
+    int shift[kMaxTaps];
+    const float* alpha;      // Snake parameters on the A operand, or null
+    const float* inv_alpha;
+    int N, K;                // K = ntaps * Cin
+    const float* w;          // fp32 [K][N] (CUDA-core path)
+    const float* bias;       // bias[n % bias_mod] or null
+    int bias_mod;
+    float* out;
+    Layout out_l;
+    int out_C;               // elements per output row
+    int out_step;            // output rows per input row (transposed-conv stride, else 1)
+    const float* res;        // residual, same layout as out
+    int epi;
+    float scale;             // EPI_MRF_LAST
+    // EPI_QKV
+    float* kring;
+    float* vring;
+    int ring_R;              // ring rows per slot (power of two)
+    int d;
+    // tiling
+    const int* tcum;         // [B + 1] cumulative row tiles of the input level
+    int bm;
+};
+
+__device__ __forceinline__ int find_seg(const int* cum, int B, int x)
+{
+    // largest b with cum[b] <= x (cum[0] = 0, cum nondecreasing)
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (__ldg(cum + mid) <= x) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+// Snake, x + sin(a x)^2 / a, with explicit roundings so every kernel that
+// evaluates it produces the same bits for the same input.
+__device__ __forceinline__ float snake_f(float x, float a, float inv_a)
+{
+    float s = sinf(__fmul_rn(a, x));
+    return __fadd_rn(x, __fmul_rn(__fmul_rn(s, s), inv_a));
+}
+
+__device__ __forceinline__ float gelu_f(float x)
+{
+    return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f));
+}
+
+}  // namespace codec

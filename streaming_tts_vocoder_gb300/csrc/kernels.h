@@ -1,0 +1,41 @@
+// Host-side launchers of the decoder kernels.  Every launcher enqueues on the
+// given stream and returns the launch status; none synchronises.
+#pragma once
+
+#include "common.cuh"
+
+namespace codec {
+
+// A history tensor: the last H rows of a prefixed buffer carried per slot.
+struct HistDesc {
+    float* buf;        // packed activation buffer (prefixed layout)
+    float* state;      // [slots][H][C]
+    int C, H;
+    Layout l;
+};
+
+cudaError_t launch_rvq_gather(const float* cb, int Q, int V, int E, const int* codes, int T_max,
+                              PlanView plan, float* e, Layout el, unsigned* err_words,
+                              int total_rows, cudaStream_t s);
+
+cudaError_t launch_gemm_simt(const GemmArgs& a, PlanView plan, int n_row_tiles, cudaStream_t s);
+
+cudaError_t launch_rms_norm(const float* x, Layout xl, const float* g, float eps, float* y, Layout yl,
+                            int d, PlanView plan, int total_rows, cudaStream_t s);
+
+cudaError_t launch_swa(const float* q, float* o, const float* kring, const float* vring, int d,
+                       int heads, int window, int ring_R, PlanView plan, int total_rows,
+                       cudaStream_t s);
+
+cudaError_t launch_final_conv(const float* x, Layout xl, int C, const float* w, const float* bias,
+                              const float* alpha, const float* inv_alpha, int k, float* audio,
+                              float* pre_tanh, long long audio_ld, PlanView plan, const int* tcum,
+                              int n_row_tiles, cudaStream_t s);
+
+cudaError_t launch_hist_fill(const HistDesc* d, int nd, PlanView plan, cudaStream_t s);
+cudaError_t launch_hist_commit(const HistDesc* d, int nd, PlanView plan, const int* n_frames,
+                               long long* frames, cudaStream_t s);
+cudaError_t launch_state_reset(const HistDesc* d, int nd, const int* slots, int n_slots,
+                               long long* frames, unsigned* err_words, cudaStream_t s);
+
+}  // namespace codec

@@ -1,0 +1,433 @@
+// CUDA-core kernels of the decoder: codebook gather-sum, fp32 implicit-GEMM
+// convolution (the reference-precision contraction and the path for layers too
+// narrow for the tensor cores), RMSNorm, sliding-window attention over the
+// ring KV, the final Snake + conv + tanh stencil, and the per-call history
+// bookkeeping (fill, commit, reset).
+#include <math.h>
+
+#include "kernels.h"
+
+namespace codec {
+
+// ---------------------------------------------------------------- gather --
+// e[row] = sum_q CB_q[code[q][t]] in fp32, q ascending (vllm-omni "Edge TTS
+// design", section 1.3: RVQ embedding sum).  One block per frame row, one
+// float4 of channels per thread: every load is a 128-bit load of a codebook
+// row.  A code outside [0, V) zeroes the row and sets the slot's sticky bit.
+__global__ void __launch_bounds__(128) rvq_gather_kernel(
+    const float* __restrict__ cb, int Q, int V, int E, const int* __restrict__ codes, int T_max,
+    PlanView plan, const int* __restrict__ bidx, float* __restrict__ e, Layout el,
+    unsigned* __restrict__ err_words)
+{
+    __shared__ int sc[64];
+    __shared__ int sbad;
+    const int row = blockIdx.x;
+    const int b = find_seg(plan.cf, plan.B, row);
+    const int t = row - __ldg(plan.cf + b);
+    if (threadIdx.x == 0) sbad = 0;
+    __syncthreads();
+    const int* cr = codes + ((long long)__ldg(bidx + b) * Q) * T_max + t;
+    for (int q = threadIdx.x; q < Q; q += blockDim.x) {
+        int c = __ldg(cr + (long long)q * T_max);
+        sc[q] = c;
+        if (c < 0 || c >= V) atomicOr(&sbad, 1);
+    }
+    __syncthreads();
+    float4* out = reinterpret_cast<float4*>(e + (seg_base(el, plan.cf, b) + t) * E);
+    const int E4 = E >> 2;
+    if (sbad) {
+        for (int c4 = threadIdx.x; c4 < E4; c4 += blockDim.x) out[c4] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (threadIdx.x == 0) atomicOr(err_words + __ldg(plan.slot + b), 1u);
+        return;
+    }
+    for (int c4 = threadIdx.x; c4 < E4; c4 += blockDim.x) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int q = 0; q < Q; q++) {
+            const float4 v = __ldg(reinterpret_cast<const float4*>(cb + ((long long)q * V + sc[q]) * E) + c4);
+            acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+        }
+        out[c4] = acc;
+    }
+}
+
+cudaError_t launch_rvq_gather(const float* cb, int Q, int V, int E, const int* codes, int T_max,
+                              PlanView plan, float* e, Layout el, unsigned* err_words,
+                              int total_rows, cudaStream_t s)
+{
+    if (total_rows <= 0) return cudaSuccess;
+    rvq_gather_kernel<<<total_rows, 128, 0, s>>>(cb, Q, V, E, codes, T_max, plan, plan.bidx, e,
+                                                 el, err_words);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------ fp32 implicit GEMM --
+// out[t][n] = epi( sum_j sum_ci A(in[base(b) + t - shift_j][ci]) W[j Cin + ci][n] )
+// 64 x 64 output tile per block, 16-deep K slices in shared memory, 4 x 4
+// outputs per thread.  Each output's sum runs over (tap, channel) in
+// ascending order whatever the tile or batch it falls in, so the result of a
+// row does not depend on how the streams were packed.
+constexpr int SB_M = 64, SB_N = 64, SB_K = 16;
+
+__device__ __forceinline__ void gemm_store(const GemmArgs& a, const PlanView& plan, int b, int t,
+                                           long long out_row, int n, float acc)
+{
+    float v = acc;
+    if (a.bias) v += __ldg(a.bias + (n % a.bias_mod));
+    const long long idx = out_row * a.out_C + n;
+    switch (a.epi) {
+    case EPI_STORE: a.out[idx] = v; break;
+    case EPI_RESID: a.out[idx] = a.res[idx] + v; break;
+    case EPI_GELU: a.out[idx] = gelu_f(v); break;
+    case EPI_MRF_FIRST: a.out[idx] = a.res[idx] + v; break;
+    case EPI_MRF_ADD: a.out[idx] = a.out[idx] + (a.res[idx] + v); break;
+    case EPI_MRF_LAST: a.out[idx] = (a.out[idx] + (a.res[idx] + v)) * a.scale; break;
+    case EPI_QKV: {
+        if (n < a.d) {
+            a.out[out_row * a.d + n] = v;
+        } else {
+            const long long pos = __ldg(plan.pos0 + b) + t;
+            const long long rr = (long long)__ldg(plan.slot + b) * a.ring_R + (pos & (a.ring_R - 1));
+            if (n < 2 * a.d) a.kring[rr * a.d + (n - a.d)] = v;
+            else a.vring[rr * a.d + (n - 2 * a.d)] = v;
+        }
+        break;
+    }
+    default: break;
+    }
+}
+
+__global__ void __launch_bounds__(256) gemm_simt_kernel(GemmArgs a, PlanView plan)
+{
+    __shared__ float As[SB_K][SB_M + 4];
+    __shared__ float Bs[SB_K][SB_N + 4];
+    const int tile = blockIdx.x;
+    const int b = find_seg(a.tcum, plan.B, tile);
+    const int seg_rows = (__ldg(plan.cf + b + 1) - __ldg(plan.cf + b)) * a.in_l.r;
+    const int t0 = (tile - __ldg(a.tcum + b)) * SB_M;
+    const int nrows = min(SB_M, seg_rows - t0);
+    const long long in_base = seg_base(a.in_l, plan.cf, b) + t0;
+    const int n0 = blockIdx.y * SB_N;
+    const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+
+    float acc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; i++)
+#pragma unroll
+        for (int j = 0; j < 4; j++) acc[i][j] = 0.f;
+
+    const int am = tid >> 2, ak = (tid & 3) * 4;   // A: row am, channels ak..ak+3
+    const int bk = tid >> 4, bn = (tid & 15) * 4;  // B: k row bk, columns bn..bn+3
+    for (int j = 0; j < a.ntaps; j++) {
+        const long long rowA = in_base - a.shift[j];
+        for (int c0 = 0; c0 < a.Cin; c0 += SB_K) {
+            float av[4] = {0.f, 0.f, 0.f, 0.f};
+            if (am < nrows && c0 + ak < a.Cin) {
+                const float4 x = __ldg(reinterpret_cast<const float4*>(a.in + (rowA + am) * a.Cin + c0 + ak));
+                av[0] = x.x; av[1] = x.y; av[2] = x.z; av[3] = x.w;
+                if (a.alpha) {
+#pragma unroll
+                    for (int i = 0; i < 4; i++)
+                        av[i] = snake_f(av[i], __ldg(a.alpha + c0 + ak + i), __ldg(a.inv_alpha + c0 + ak + i));
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 4; i++) As[ak + i][am] = av[i];
+            float4 w = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (c0 + bk < a.Cin && n0 + bn < a.N)
+                w = __ldg(reinterpret_cast<const float4*>(a.w + (long long)(j * a.Cin + c0 + bk) * a.N + n0 + bn));
+            Bs[bk][bn + 0] = w.x; Bs[bk][bn + 1] = w.y; Bs[bk][bn + 2] = w.z; Bs[bk][bn + 3] = w.w;
+            __syncthreads();
+#pragma unroll
+            for (int k = 0; k < SB_K; k++) {
+                float ar[4], br[4];
+#pragma unroll
+                for (int i = 0; i < 4; i++) { ar[i] = As[k][ty * 4 + i]; br[i] = Bs[k][tx * 4 + i]; }
+#pragma unroll
+                for (int i = 0; i < 4; i++)
+#pragma unroll
+                    for (int jj = 0; jj < 4; jj++) acc[i][jj] = fmaf(ar[i], br[jj], acc[i][jj]);
+            }
+            __syncthreads();
+        }
+    }
+    const long long out_base = seg_base(a.out_l, plan.cf, b);
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        const int m = ty * 4 + i;
+        if (m >= nrows) continue;
+        const int t = t0 + m;
+        const long long out_row = out_base + (long long)t * a.out_step;
+#pragma unroll
+        for (int jj = 0; jj < 4; jj++) {
+            const int n = n0 + tx * 4 + jj;
+            if (n < a.N) gemm_store(a, plan, b, t, out_row, n, acc[i][jj]);
+        }
+    }
+}
+
+cudaError_t launch_gemm_simt(const GemmArgs& a, PlanView plan, int n_row_tiles, cudaStream_t s)
+{
+    if (n_row_tiles <= 0) return cudaSuccess;
+    dim3 grid(n_row_tiles, (a.N + SB_N - 1) / SB_N);
+    gemm_simt_kernel<<<grid, 256, 0, s>>>(a, plan);
+    return cudaGetLastError();
+}
+
+// --------------------------------------------------------------- RMSNorm --
+// y = x / sqrt(mean(x^2) + eps) * g, one warp per row; the row's sum of
+// squares runs lane-strided then through a fixed butterfly.
+__global__ void rms_norm_kernel(const float* __restrict__ x, Layout xl, const float* __restrict__ g,
+                                float eps, float* __restrict__ y, Layout yl, int d, PlanView plan,
+                                int total_rows)
+{
+    const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (row >= total_rows) return;
+    const int b = find_seg(plan.cf, plan.B, row);
+    const int t = row - __ldg(plan.cf + b);
+    const float4* xr = reinterpret_cast<const float4*>(x + (seg_base(xl, plan.cf, b) + t) * d);
+    float4* yr = reinterpret_cast<float4*>(y + (seg_base(yl, plan.cf, b) + t) * d);
+    const int d4 = d >> 2;
+    float ss = 0.f;
+    for (int c = lane; c < d4; c += 32) {
+        const float4 v = xr[c];
+        ss = fmaf(v.x, v.x, ss); ss = fmaf(v.y, v.y, ss); ss = fmaf(v.z, v.z, ss); ss = fmaf(v.w, v.w, ss);
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float r = rsqrtf(ss / (float)d + eps);
+    const float4* g4 = reinterpret_cast<const float4*>(g);
+    for (int c = lane; c < d4; c += 32) {
+        const float4 v = xr[c], w = __ldg(g4 + c);
+        yr[c] = make_float4(v.x * r * w.x, v.y * r * w.y, v.z * r * w.z, v.w * r * w.w);
+    }
+}
+
+cudaError_t launch_rms_norm(const float* x, Layout xl, const float* g, float eps, float* y, Layout yl,
+                            int d, PlanView plan, int total_rows, cudaStream_t s)
+{
+    if (total_rows <= 0) return cudaSuccess;
+    const int threads = 256, rows_per_block = threads / 32;
+    rms_norm_kernel<<<(total_rows + rows_per_block - 1) / rows_per_block, threads, 0, s>>>(
+        x, xl, g, eps, y, yl, d, plan, total_rows);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------- sliding-window attention --
+// One warp per (query row, head).  Query at absolute position p attends the
+// keys of positions max(0, p - W + 1) .. p, read from the stream's ring
+// (position p lives in ring row p mod R).  Lane i scores keys lo + i, lo + 32 +
+// i, ...; max and denominator go through a fixed butterfly, the value sum runs
+// over the keys in position order, so a query's result depends only on its
+// position and the keys, never on the chunking (blixt/phonon "Speed" item 7
+// ring; item 11 softmax with max subtraction).
+constexpr int kSwaMaxW = 128;
+constexpr int kSwaMaxDh = 256;
+constexpr int kSwaWarps = 8;
+
+__global__ void __launch_bounds__(kSwaWarps * 32) swa_kernel(
+    const float* __restrict__ q, float* __restrict__ o, const float* __restrict__ kring,
+    const float* __restrict__ vring, int d, int heads, int W, int R, PlanView plan, int total_rows)
+{
+    __shared__ float sp[kSwaWarps][kSwaMaxW];
+    __shared__ float sq[kSwaWarps][kSwaMaxDh];
+    const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gw = blockIdx.x * kSwaWarps + wib;
+    const int row = gw / heads, h = gw - row * heads;
+    if (row >= total_rows) return;
+    const int b = find_seg(plan.cf, plan.B, row);
+    const int t = row - __ldg(plan.cf + b);
+    const long long pos = __ldg(plan.pos0 + b) + t;
+    const long long lo = pos - W + 1 > 0 ? pos - W + 1 : 0;
+    const int nk = (int)(pos - lo + 1);
+    const int dh = d / heads;
+    const float* qr = q + (long long)row * d + h * dh;
+    for (int c = lane; c < dh; c += 32) sq[wib][c] = qr[c];
+    __syncwarp();
+    const float scale = 1.0f / sqrtf((float)dh);
+    const long long slot_base = (long long)__ldg(plan.slot + b) * R;
+    const float* kb = kring + h * dh;
+    const float* vb = vring + h * dh;
+    float sc[kSwaMaxW / 32];
+    float m = -INFINITY;
+#pragma unroll
+    for (int u = 0; u < kSwaMaxW / 32; u++) {
+        const int i = lane + 32 * u;
+        sc[u] = -INFINITY;
+        if (i < nk) {
+            const float* kr = kb + (slot_base + ((lo + i) & (R - 1))) * d;
+            float dot = 0.f;
+            for (int c = 0; c < dh; c++) dot = fmaf(sq[wib][c], __ldg(kr + c), dot);
+            sc[u] = dot * scale;
+            m = fmaxf(m, sc[u]);
+        }
+    }
+#pragma unroll
+    for (int off = 16; off; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    float z = 0.f;
+#pragma unroll
+    for (int u = 0; u < kSwaMaxW / 32; u++) {
+        const int i = lane + 32 * u;
+        if (i < nk) {
+            const float p = expf(sc[u] - m);
+            sp[wib][i] = p;
+            z += p;
+        }
+    }
+#pragma unroll
+    for (int off = 16; off; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+    __syncwarp();
+    const float inv_z = 1.0f / z;
+    for (int c = lane; c < dh; c += 32) {
+        float acc = 0.f;
+        for (int i = 0; i < nk; i++)
+            acc = fmaf(sp[wib][i], __ldg(vb + (slot_base + ((lo + i) & (R - 1))) * d + c), acc);
+        o[(long long)row * d + h * dh + c] = acc * inv_z;
+    }
+}
+
+cudaError_t launch_swa(const float* q, float* o, const float* kring, const float* vring, int d,
+                       int heads, int window, int ring_R, PlanView plan, int total_rows,
+                       cudaStream_t s)
+{
+    if (total_rows <= 0) return cudaSuccess;
+    const long long warps = (long long)total_rows * heads;
+    swa_kernel<<<(unsigned)((warps + kSwaWarps - 1) / kSwaWarps), kSwaWarps * 32, 0, s>>>(
+        q, o, kring, vring, d, heads, window, ring_R, plan, total_rows);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------ final Snake-conv-tanh --
+// y[t] = tanh(b + sum_j sum_c w[j][c] snake(x[t - (k-1) + j][c])), C -> 1.
+// A 128-row tile plus its k-1 history rows is staged in shared memory with
+// Snake applied once per element (row stride C + 1 against bank conflicts);
+// each thread then produces one sample.  Bandwidth-bound: one input row in,
+// one sample out (blixt/phonon "Open work": a direct kernel for the last
+// convolution with 1 output channel).
+constexpr int kFinalTile = 128;
+
+__global__ void __launch_bounds__(kFinalTile) final_conv_kernel(
+    const float* __restrict__ x, Layout xl, int C, const float* __restrict__ w,
+    const float* __restrict__ bias, const float* __restrict__ alpha,
+    const float* __restrict__ inv_alpha, int k, float* __restrict__ audio,
+    float* __restrict__ pre_tanh, long long audio_ld, PlanView plan, const int* __restrict__ bidx,
+    const int* __restrict__ tcum)
+{
+    extern __shared__ float sm[];
+    const int ld = C + 1;
+    float* sa = sm;                                   // [kFinalTile + k - 1][C + 1]
+    float* sw = sm + (kFinalTile + k - 1) * ld;       // [k][C]
+    const int tile = blockIdx.x;
+    const int b = find_seg(tcum, plan.B, tile);
+    const int seg_rows = (__ldg(plan.cf + b + 1) - __ldg(plan.cf + b)) * xl.r;
+    const int t0 = (tile - __ldg(tcum + b)) * kFinalTile;
+    const int nrows = min(kFinalTile, seg_rows - t0);
+    const long long base = seg_base(xl, plan.cf, b) + t0 - (k - 1);
+    const int rows = nrows + k - 1;
+    for (int i = threadIdx.x; i < rows * C; i += blockDim.x) {
+        const int r = i / C, c = i - r * C;
+        sa[r * ld + c] = snake_f(__ldg(x + (base + r) * C + c), __ldg(alpha + c), __ldg(inv_alpha + c));
+    }
+    for (int i = threadIdx.x; i < k * C; i += blockDim.x) sw[i] = __ldg(w + i);
+    __syncthreads();
+    const int m = threadIdx.x;
+    if (m < nrows) {
+        float acc = 0.f;
+        for (int j = 0; j < k; j++) {
+            const float* ar = sa + (m + j) * ld;
+            const float* wr = sw + j * C;
+            for (int c = 0; c < C; c++) acc = fmaf(wr[c], ar[c], acc);
+        }
+        const float y = acc + __ldg(bias);
+        const long long idx = (long long)__ldg(bidx + b) * audio_ld + t0 + m;
+        audio[idx] = tanhf(y);
+        if (pre_tanh) pre_tanh[idx] = y;
+    }
+}
+
+cudaError_t launch_final_conv(const float* x, Layout xl, int C, const float* w, const float* bias,
+                              const float* alpha, const float* inv_alpha, int k, float* audio,
+                              float* pre_tanh, long long audio_ld, PlanView plan, const int* tcum,
+                              int n_row_tiles, cudaStream_t s)
+{
+    if (n_row_tiles <= 0) return cudaSuccess;
+    const size_t smem = sizeof(float) * ((size_t)(kFinalTile + k - 1) * (C + 1) + (size_t)k * C);
+    cudaError_t e = cudaFuncSetAttribute(final_conv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    final_conv_kernel<<<n_row_tiles, kFinalTile, smem, s>>>(x, xl, C, w, bias, alpha, inv_alpha, k,
+                                                            audio, pre_tanh, audio_ld, plan,
+                                                            plan.bidx, tcum);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------ history bookkeeping --
+// Fill: the H history rows in front of segment b <- the slot's carried rows.
+// Commit: the slot's carried rows <- the last H rows of [history | chunk]
+// (blixt/phonon "Speed" item 7: after each chunk a small kernel moves each
+// stage's last rows to its front).  One block per (tensor, batch entry).
+__global__ void hist_fill_kernel(const HistDesc* __restrict__ dsc, PlanView plan)
+{
+    const HistDesc h = dsc[blockIdx.x];
+    const int b = blockIdx.y;
+    if (h.H == 0) return;
+    const long long dst_row = seg_base(h.l, plan.cf, b) - h.H;
+    const float4* src = reinterpret_cast<const float4*>(h.state + (long long)__ldg(plan.slot + b) * h.H * h.C);
+    float4* dst = reinterpret_cast<float4*>(h.buf + dst_row * h.C);
+    const int n4 = (h.H * h.C) >> 2;
+    for (int i = threadIdx.x; i < n4; i += blockDim.x) dst[i] = src[i];
+}
+
+__global__ void hist_commit_kernel(const HistDesc* __restrict__ dsc, PlanView plan,
+                                   long long* __restrict__ frames)
+{
+    const HistDesc h = dsc[blockIdx.x];
+    const int b = blockIdx.y;
+    const int n = __ldg(plan.cf + b + 1) - __ldg(plan.cf + b);
+    if (blockIdx.x == 0 && threadIdx.x == 0) frames[__ldg(plan.slot + b)] += n;
+    if (h.H == 0) return;
+    const long long src_row = seg_base(h.l, plan.cf, b) + (long long)n * h.l.r - h.H;
+    const float4* src = reinterpret_cast<const float4*>(h.buf + src_row * h.C);
+    float4* dst = reinterpret_cast<float4*>(h.state + (long long)__ldg(plan.slot + b) * h.H * h.C);
+    const int n4 = (h.H * h.C) >> 2;
+    for (int i = threadIdx.x; i < n4; i += blockDim.x) dst[i] = src[i];
+}
+
+__global__ void state_reset_kernel(const HistDesc* __restrict__ dsc, int nd, const int* __restrict__ slots,
+                                   long long* __restrict__ frames, unsigned* __restrict__ err_words)
+{
+    const int slot = slots[blockIdx.y];
+    if ((int)blockIdx.x == nd) {
+        if (threadIdx.x == 0) { frames[slot] = 0; err_words[slot] = 0u; }
+        return;
+    }
+    const HistDesc h = dsc[blockIdx.x];
+    float4* dst = reinterpret_cast<float4*>(h.state + (long long)slot * h.H * h.C);
+    const int n4 = (h.H * h.C) >> 2;
+    for (int i = threadIdx.x; i < n4; i += blockDim.x) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+cudaError_t launch_hist_fill(const HistDesc* d, int nd, PlanView plan, cudaStream_t s)
+{
+    if (nd <= 0 || plan.B <= 0) return cudaSuccess;
+    hist_fill_kernel<<<dim3(nd, plan.B), 256, 0, s>>>(d, plan);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_hist_commit(const HistDesc* d, int nd, PlanView plan, const int* /*n_frames*/,
+                               long long* frames, cudaStream_t s)
+{
+    if (nd <= 0 || plan.B <= 0) return cudaSuccess;
+    hist_commit_kernel<<<dim3(nd, plan.B), 256, 0, s>>>(d, plan, frames);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_state_reset(const HistDesc* d, int nd, const int* slots, int n_slots,
+                               long long* frames, unsigned* err_words, cudaStream_t s)
+{
+    if (n_slots <= 0) return cudaSuccess;
+    state_reset_kernel<<<dim3(nd + 1, n_slots), 256, 0, s>>>(d, nd, slots, frames, err_words);
+    return cudaGetLastError();
+}
+
+}  // namespace codec
