@@ -1,0 +1,401 @@
+#!/usr/bin/env python
+"""Throughput of the streaming codec decoder on one GB300 (or N replicas).
+
+Workload (one "step"): 64 independent streams of the Qwen3-TTS-12Hz-shaped
+decoder, 250 frames (20 s of 24 kHz audio) each, stream s starting at global
+frame s mod 25 and decoded in ragged ticks of up to 25 frames per stream with
+the 72-frame attention window and every conv context carried between ticks;
+the streams are reset at the start of each step.  Synthetic codes (uniform,
+seed + stream id) and random N(0, 1/fan_in) weights.
+
+value: seconds of audio decoded per second, all GPUs, inputs resident in HBM.
+e2e:   the same through codec_decode_chunk_host: every tick copies its codes
+       from page-locked host memory and its audio back.
+Also reported: per-kernel roofline of the dominant kernel (CUDA events around
+every launch, inside the timed region), the first-audio latency (1 frame from
+an empty state), SM clocks sampled during the timed region, and the CPU
+oracle timed on the host cores on a bounded sample (cpu_baseline).
+
+--impl reference times the CPU oracle itself on the same workload's unit.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+from pathlib import Path
+
+import numpy as np
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+from streaming_tts_vocoder_gb300.synthetic import (FRAME_RATE_HZ, make_codes, make_weights, pack_blob,  # noqa: E402
+                                                   qwen3_config, staggered_schedule, tiny_config)
+
+METRIC = "codec decode audio-sec/sec at 64 streams (x real time)"
+UNIT = "audio-s/s"
+PEAKS_FILE = ROOT / "MEASURED_PEAKS.json"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "sm_max_mhz": 2070.0}
+SMS = 152
+FP32_LANES_PER_SM = 128
+
+
+def peaks():
+    try:
+        p = json.loads(PEAKS_FILE.read_text())
+        return p, "measured"
+    except Exception:
+        return FALLBACK_PEAKS, "fallback"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--decoder", choices=["qwen3", "tiny"], default="qwen3")
+    ap.add_argument("--precision", choices=["fp32", "fp16x3"], default="fp32")
+    ap.add_argument("--streams", type=int, default=64)
+    ap.add_argument("--frames", type=int, default=250)
+    ap.add_argument("--chunk", type=int, default=25)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the cpu_baseline oracle timing")
+    ap.add_argument("--first-audio-runs", type=int, default=100)
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def config_dict(args, precision):
+    return {
+        "workload": f"{args.streams} staggered streams x {args.frames} frames, ragged ticks of <= {args.chunk} frames, "
+                    f"{'Qwen3-TTS-12Hz-shaped' if args.decoder == 'qwen3' else 'tiny'} decoder",
+        "decoder": args.decoder,
+        "streams": args.streams,
+        "frames_per_stream": args.frames,
+        "chunk_frames": args.chunk,
+        "stagger": f"stream s starts at frame s mod {args.chunk}",
+        "precision": precision,
+        "samples_per_frame": 1920,
+        "l2": "inputs larger than L2: each tick writes and reads GBs of activations",
+        "parallelism": "replicas (one independent decoder per GPU, no collective)",
+    }
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index),
+                 "--query-gpu=clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [ln.strip().split(",") for ln in self.file.read().splitlines() if ln.strip()]
+        os.unlink(self.file.name)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[0]))
+                mx = float(r[1])
+                for nm, v in zip(names, r[4:8]):
+                    if v.strip().lower() == "active":
+                        reasons.add(nm)
+            except (ValueError, IndexError):
+                continue
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def traffic_for(kernel: str, src_digest: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it
+    was taken on the current kernel source."""
+    f = ROOT / "profiles" / "traffic.json"
+    try:
+        d = json.loads(f.read_text())
+        e = d.get(kernel)
+        if e and e.get("source_sha256") == src_digest:
+            return e.get("dram_bytes_per_launch")
+    except Exception:
+        pass
+    return None
+
+
+def kernel_source_digest(files):
+    h = hashlib.sha256()
+    for f in files:
+        h.update((ROOT / "streaming_tts_vocoder_gb300" / "csrc" / f).read_bytes())
+    return h.hexdigest()
+
+
+def oracle_sample(cfg, blob, frames, seed=1000):
+    """Time the CPU oracle decoding `frames` frames of one stream."""
+    from oracle import oracle as O
+    m = O.OracleModel(cfg, blob)
+    codes = make_codes(cfg, frames, seed)
+    s = m.stream()
+    t0 = time.perf_counter()
+    s.decode(codes)
+    dt = time.perf_counter() - t0
+    return frames / FRAME_RATE_HZ / dt, dt, O.max_threads()
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    cfg = qwen3_config() if args.decoder == "qwen3" else tiny_config()
+    blob = pack_blob(cfg, make_weights(cfg, 0))
+    from oracle import oracle as O
+    m = O.OracleModel(cfg, blob)
+    frames = 25 if args.decoder == "qwen3" else 250
+    times = []
+    for i in range(args.warmup + args.steps):
+        s = m.stream()
+        codes = make_codes(cfg, frames, 1000 + i)
+        t0 = time.perf_counter()
+        s.decode(codes)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(dt)
+    total = sum(times)
+    value = args.steps * frames / FRAME_RATE_HZ / total
+    sample = f"one stream x {frames} frames of the workload per step (one {frames}-frame chunk from an empty state)"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32 storage, f64 accumulation", "data": "synthetic",
+        "config": config_dict(args, "oracle"),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": O.max_threads(), "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import torch
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from streaming_tts_vocoder_gb300 import codec as C
+
+    cfg = qwen3_config() if args.decoder == "qwen3" else tiny_config()
+    prec = C.PRECISION_FP16X3 if args.precision == "fp16x3" else C.PRECISION_FP32
+    blob = pack_blob(cfg, make_weights(cfg, 0))
+    S, F, CH = args.streams, args.frames, args.chunk
+    cod = C.Codec(cfg, blob, max_streams=S, max_chunk_frames=CH, max_batch_frames=S * CH, precision=prec)
+    st = cod.state()
+    spf = cod.samples_per_frame
+
+    # inputs resident in HBM: one codes tensor per tick
+    codes = [make_codes(cfg, F, 1000 + s) for s in range(S)]
+    ticks = staggered_schedule(S, F, CH)
+    tick_inputs = []
+    h2d = d2h = 0
+    for tick in ticks:
+        arr = np.zeros((len(tick), cfg.Q, CH), np.int32)
+        for b, (s, a, n) in enumerate(tick):
+            arr[b, :, :n] = codes[s][:, a:a + n]
+        nf = [n for _, _, n in tick]
+        ids = [s for s, _, _ in tick]
+        tick_inputs.append((torch.from_numpy(arr).to(dev), nf, ids, torch.from_numpy(arr).pin_memory()))
+        h2d += arr.nbytes
+        d2h += sum(nf) * spf * 4
+    audio = torch.empty(S, CH * spf, device=dev)
+    audio_h = torch.empty(S, CH * spf).pin_memory()
+    stream = torch.cuda.current_stream()
+    audio_s_per_step = S * F / FRAME_RATE_HZ
+
+    launches = [0]
+
+    def step():
+        st.reset(stream=stream)
+        launches[0] += 1
+        for codes_d, nf, ids, _ in tick_inputs:
+            st.decode(codes_d, nf, audio, stream_ids=ids, stream=stream)
+            launches[0] += st.last_launches
+
+    def step_host():
+        st.reset(stream=stream)
+        for _, nf, ids, codes_h in tick_inputs:
+            st.decode_host(codes_h, nf, audio_h, stream_ids=ids, stream=stream)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    def max_over_ranks(x):
+        if world > 1:
+            import torch.distributed as dist
+            t = torch.tensor([x], dtype=torch.float64)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            return float(t.item())
+        return x
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    # timed region (device time, CUDA events on the launching stream)
+    clocks = ClockSampler(local)
+    clocks.start()
+    st.profile_begin(max_records=200000)
+    launches[0] = 0
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1))
+    barrier()
+    kstats = st.profile_end(stream=stream)
+    clk = clocks.stop()
+    gpu_launches = launches[0]
+    value = world * args.steps * audio_s_per_step / (ms / 1e3)
+
+    # end to end through the host-buffer entry point
+    e2e = None
+    if not args.no_e2e:
+        step_host()
+        torch.cuda.synchronize()
+        barrier()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            step_host()
+        torch.cuda.synchronize()
+        wall = max_over_ranks(time.perf_counter() - t0)
+        e2e = {"value": world * args.steps * audio_s_per_step / wall, "unit": UNIT,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+    # first-audio latency: 1 frame from an empty state
+    fa = None
+    if args.first_audio_runs > 0:
+        one = torch.from_numpy(np.ascontiguousarray(codes[0][:, :1])).reshape(1, cfg.Q, 1).to(dev)
+        a1 = torch.empty(1, spf, device=dev)
+        dev_us, wall_us = [], []
+        for i in range(args.first_audio_runs + 5):
+            st.reset([0], stream=stream)
+            torch.cuda.synchronize()
+            s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t0 = time.perf_counter()
+            s0.record(stream)
+            st.decode(one, [1], a1, stream_ids=[0], stream=stream)
+            s1.record(stream)
+            s1.synchronize()
+            t1 = time.perf_counter()
+            if i >= 5:
+                dev_us.append(1e3 * s0.elapsed_time(s1))
+                wall_us.append(1e6 * (t1 - t0))
+        fa = {"device_us_median": statistics.median(dev_us), "wall_us_median": statistics.median(wall_us),
+              "runs": len(dev_us), "launches": st.last_launches}
+
+    # roofline of the dominant kernel
+    pk, pk_src = peaks()
+    dom = max(kstats.items(), key=lambda kv: kv[1]["ms"])
+    name, ks = dom
+    roof = None
+    if ks["launches"]:
+        per_launch_s = ks["ms"] / 1e3 / ks["launches"]
+        if name == "gemm_tc":
+            achieved = ks["flops"] / ks["launches"] / per_launch_s / 1e12
+            peak = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
+            roof = {"bound": "tensor", "unit": "TFLOP/s", "peak_note": f"{pk_src} sustained bf16 (fp16 same rate)"}
+            src = ["tc_gemm.cu", "common.cuh"]
+        elif name == "gemm_simt":
+            achieved = ks["flops"] / ks["launches"] / per_launch_s / 1e12
+            peak = SMS * FP32_LANES_PER_SM * 2 * pk.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+            roof = {"bound": "alu", "unit": "TFLOP/s",
+                    "peak_note": "fp32 FMA: 152 SMs x 128 lanes x 2 flop x max SM clock"}
+            src = ["kernels_simt.cu", "common.cuh"]
+        else:
+            achieved = ks["bytes"] / ks["launches"] / per_launch_s / 1e9
+            peak = pk["hbm_gbs"]
+            roof = {"bound": "hbm", "unit": "GB/s", "peak_note": f"{pk_src} copy bandwidth"}
+            src = ["kernels_simt.cu", "common.cuh"]
+        roof.update({"kernel": name, "achieved": achieved, "peak": peak, "frac": achieved / peak,
+                     "launches": ks["launches"], "traffic": traffic_for(name, kernel_source_digest(src))})
+    kernels = {k: {"launches": v["launches"], "ms": round(v["ms"], 3),
+                   "share": round(v["ms"] / max(1e-9, sum(x["ms"] for x in kstats.values())), 4)}
+               for k, v in kstats.items() if v["launches"]}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        frames = 40 if args.decoder == "qwen3" else 400
+        v, dt, cores = oracle_sample(cfg, blob, frames)
+        cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"one stream x {frames} frames of the workload's decoder from an empty state ({dt:.1f} s)"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32" if args.precision == "fp32" else "fp16x3 (hi/lo split, f32 accumulate)",
+            "data": "synthetic (uniform codes, random N(0,1/fan_in) weights)",
+            "config": config_dict(args, args.precision),
+            "roofline": roof, "kernels": kernels, "gpu_launches": gpu_launches,
+            "e2e": e2e, "first_audio": fa, "clocks": clk, "cpu_baseline": cpu,
+            "frames_per_s": world * args.steps * S * F / (ms / 1e3),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

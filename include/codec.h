@@ -53,6 +53,11 @@ typedef enum codec_status {
 
 /* Sticky per-stream device error bits, read with codec_state_query. */
 #define CODEC_STREAM_ERR_BAD_CODE 1u   /* a code outside [0, V): that frame's embedding was zeroed */
+/* State-wide: a tensor-core kernel gave up on one of its bounded waits in a
+ * call since the last reset of all slots; the audio of that call is not
+ * valid.  Reported on every slot's query; cleared by codec_state_reset with
+ * stream_ids == NULL. */
+#define CODEC_STREAM_ERR_KERNEL_TIMEOUT 0x80000000u
 
 typedef enum codec_precision {
     /* fp32 operands on CUDA cores for every stage. */
@@ -202,6 +207,39 @@ CODEC_API int32_t codec_state_streams(const codec_state_t* state);
 
 /* Number of kernel launches the last decode call enqueued. */
 CODEC_API int32_t codec_state_last_launches(const codec_state_t* state);
+
+/* Per-launch timing for measurement.  codec_profile_begin makes later decode
+ * calls on this state record a CUDA event pair around every kernel they
+ * launch (up to max_records launches; the events are created here, never in
+ * a decode call).  codec_profile_end synchronises the stream the calls used,
+ * sums the event intervals per kernel kind and stops recording.  Each
+ * record also carries the algorithmic work of its launch: useful
+ * floating-point operations (2 per multiply-add) and the bytes the operation
+ * must move at minimum (inputs read once, outputs written once). */
+typedef enum codec_kernel_kind {
+    CODEC_KERNEL_GATHER = 0,
+    CODEC_KERNEL_GEMM_SIMT = 1,
+    CODEC_KERNEL_GEMM_TC = 2,
+    CODEC_KERNEL_OPERAND_PREP = 3,
+    CODEC_KERNEL_RMSNORM = 4,
+    CODEC_KERNEL_ATTENTION = 5,
+    CODEC_KERNEL_FINAL_CONV = 6,
+    CODEC_KERNEL_HISTORY = 7,
+    CODEC_KERNEL_KINDS = 8
+} codec_kernel_kind;
+
+typedef struct codec_kernel_stats {
+    int32_t kind;            /* codec_kernel_kind */
+    int32_t launches;
+    double ms;               /* summed event intervals */
+    double flops;            /* summed algorithmic flops */
+    double bytes;            /* summed algorithmic bytes */
+} codec_kernel_stats;
+
+CODEC_API codec_status codec_profile_begin(codec_state_t* state, int32_t max_records);
+/* out: host [CODEC_KERNEL_KINDS]; entry i describes kind i.  Records beyond
+ * max_records are dropped (launches still run). */
+CODEC_API codec_status codec_profile_end(codec_state_t* state, codec_kernel_stats* out, void* stream);
 
 /* Static description of a status code. */
 CODEC_API const char* codec_status_string(codec_status status);

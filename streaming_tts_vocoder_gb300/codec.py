@@ -48,6 +48,15 @@ class CodecConfigC(ctypes.Structure):
     ]
 
 
+KERNEL_KINDS = ["gather", "gemm_simt", "gemm_tc", "operand_prep", "rmsnorm", "attention", "final_conv",
+                "history"]
+
+
+class KernelStatsC(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("launches", ctypes.c_int32), ("ms", ctypes.c_double),
+                ("flops", ctypes.c_double), ("bytes", ctypes.c_double)]
+
+
 class StreamInfoC(ctypes.Structure):
     _fields_ = [("frames_decoded", ctypes.c_int64), ("error_bits", ctypes.c_uint32),
                 ("reserved", ctypes.c_int32)]
@@ -82,6 +91,8 @@ def _lib():
             "codec_state_streams": (i32, [_P]),
             "codec_state_last_launches": (i32, [_P]),
             "codec_status_string": (ctypes.c_char_p, [i32]),
+            "codec_profile_begin": (i32, [_P, i32]),
+            "codec_profile_end": (i32, [_P, ctypes.POINTER(KernelStatsC), _P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(l, name)
@@ -242,6 +253,16 @@ class CodecState:
         _check(_lib().codec_state_query(self._h, stream_id, ctypes.byref(info), _stream_handle(stream)),
                "codec_state_query")
         return int(info.frames_decoded), int(info.error_bits)
+
+    def profile_begin(self, max_records: int = 65536):
+        _check(_lib().codec_profile_begin(self._h, max_records), "codec_profile_begin")
+
+    def profile_end(self, stream=None) -> dict:
+        """Per kernel kind: launches, summed event ms, algorithmic flops and bytes."""
+        arr = (KernelStatsC * len(KERNEL_KINDS))()
+        _check(_lib().codec_profile_end(self._h, arr, _stream_handle(stream)), "codec_profile_end")
+        return {KERNEL_KINDS[i]: dict(launches=arr[i].launches, ms=arr[i].ms, flops=arr[i].flops,
+                                      bytes=arr[i].bytes) for i in range(len(KERNEL_KINDS))}
 
     @property
     def last_launches(self) -> int:

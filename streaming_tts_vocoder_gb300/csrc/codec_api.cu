@@ -46,6 +46,11 @@ bool debug_sync()
     return v == 1;
 }
 
+struct ProfRec {
+    int kind;
+    double flops, bytes;
+};
+
 int next_pow2(int x)
 {
     int r = 1;
@@ -61,6 +66,7 @@ struct codec_s {
     int spf = 0;
     int n_levels = 0;
     int level_r[16] = {};
+    int num_sms = 0;
     float* cb = nullptr;
     Contraction pre;
     std::vector<LayerW> layers;
@@ -108,6 +114,12 @@ struct codec_state_s {
     int* codes_d = nullptr;        // host-buffer entry point staging
     float* audio_d = nullptr;
     int last_launches = 0;
+    double hist_floats_per_slot = 0.0;
+    // per-launch timing (codec_profile_begin / _end)
+    bool prof_on = false;
+    int prof_n = 0, prof_max = 0;
+    std::vector<cudaEvent_t> prof_ev;
+    std::vector<ProfRec> prof_rec;
     std::vector<void*> allocs;
 };
 
@@ -132,7 +144,7 @@ bool cfg_valid(const codec_config* c)
     if (c->final_k < 1 || c->final_k > kMaxTaps) return false;
     if (!(c->rms_eps > 0.f)) return false;
     if (c->max_streams < 1 || c->max_chunk_frames < 1 || c->max_batch_frames < c->max_chunk_frames) return false;
-    if (c->precision != CODEC_PRECISION_FP32) return false;   // the fp16x3 tensor-core path is not built yet
+    if (c->precision != CODEC_PRECISION_FP32 && c->precision != CODEC_PRECISION_FP16X3) return false;
     long long spf = 1;
     for (int u = 0; u < c->n_up; u++) spf *= c->up_s;
     for (int s = 0; s < c->n_stages; s++) spf *= c->strides[s];
@@ -310,6 +322,7 @@ codec_status codec_create(const codec_config* cfg, const float* weights, int64_t
     codec_s* c = new codec_s();
     c->cfg = *cfg;
     c->device = dev;
+    c->num_sms = prop.multiProcessorCount;
     const codec_config& g = c->cfg;
     codec_status st = CODEC_OK;
     c->spf = 1;
@@ -454,6 +467,7 @@ codec_status codec_state_create(codec_t* c, int32_t n_streams, codec_state_t** o
         d.buf = buf; d.C = C; d.H = H; d.l = Layout{c->level_r[lvl], s->P[lvl]};
         d.state = dev_alloc<float>(A, (size_t)S * H * C, st, true);
         s->hist.push_back(d);
+        s->hist_floats_per_slot += (double)H * C;
     };
     add_hist(s->e, g.E, g.pre_k - 1, 0);
     add_hist(s->hf, g.d, 1, 0);
@@ -497,18 +511,25 @@ codec_status codec_state_create(codec_t* c, int32_t n_streams, codec_state_t** o
     s->codes_d = dev_alloc<int>(A, (size_t)S * g.Q * g.max_chunk_frames, st);
     s->audio_d = dev_alloc<float>(A, (size_t)S * g.max_chunk_frames * c->spf, st);
     if (st == CODEC_OK && g.precision == CODEC_PRECISION_FP16X3) {
-        size_t max_rows = 0, max_c = 0;
-        for (int lvl = 0; lvl < c->n_levels; lvl++) max_rows = std::max(max_rows, rows(lvl, true));
-        max_c = std::max({(size_t)g.E, (size_t)g.d, (size_t)g.ffn});
-        for (int u = 0; u < g.n_up; u++) max_c = std::max(max_c, (size_t)g.up_ch[u]);
+        // operand planes for the widest tensor-core input: (contraction, input level, prefixed?)
         size_t elems = 0;
-        for (int lvl = 0; lvl < c->n_levels; lvl++) {
-            size_t ch = lvl == 0 ? max_c : (lvl <= g.n_up ? (size_t)g.up_ch[lvl - 1] : (size_t)g.ch[lvl - g.n_up - 1]);
-            if (lvl > 0 && lvl <= g.n_up) ch = std::max(ch, (size_t)(lvl == g.n_up ? g.up_ch[lvl - 1] : g.up_ch[lvl - 1]));
-            elems = std::max(elems, rows(lvl, true) * ch);
+        auto need = [&](const Contraction& C, int lvl, bool pref) {
+            if (C.use_tc) elems = std::max(elems, rows(lvl, pref) * (size_t)C.Cin);
+        };
+        need(c->pre, 0, true);
+        for (const LayerW& L : c->layers) {
+            need(L.qkv, 0, false);
+            need(L.o, 0, false);
+            need(L.w1, 0, false);
+            need(L.w2, 0, false);
         }
-        // the stage ConvT reads the previous level, whose widths are covered above
-        if (!tc_scratch_alloc(&s->tc_scratch, elems, A)) st = CODEC_ERR_OOM;
+        for (int u = 0; u < g.n_up; u++) need(c->up[u], u, true);
+        for (int si = 0; si < g.n_stages; si++) {
+            need(c->st[si], g.n_up + si, true);
+            for (int j = 0; j < g.n_rb; j++)
+                for (int i = 0; i < g.n_dil; i++) need(c->rb[c->rb_index(si, j, i)], g.n_up + 1 + si, true);
+        }
+        if (!tc_scratch_alloc(&s->tc_scratch, std::max<size_t>(elems, 4), A)) st = CODEC_ERR_OOM;
     }
     if (st == CODEC_OK && cudaDeviceSynchronize() != cudaSuccess) st = CODEC_ERR_CUDA;
     if (st != CODEC_OK) {
@@ -536,8 +557,44 @@ void codec_state_destroy(codec_state_t* s)
     }
     if (s->slots_h) cudaFreeHost(s->slots_h);
     if (s->slots_ev) cudaEventDestroy(s->slots_ev);
+    for (cudaEvent_t e : s->prof_ev) cudaEventDestroy(e);
     free_all(s->allocs);
     delete s;
+}
+
+codec_status codec_profile_begin(codec_state_t* s, int32_t max_records)
+{
+    if (!s) return CODEC_ERR_NULL;
+    if (max_records < 1 || max_records > (1 << 20)) return CODEC_ERR_ARG;
+    while ((int)s->prof_ev.size() < 2 * max_records) {
+        cudaEvent_t e;
+        if (cudaEventCreate(&e) != cudaSuccess) return CODEC_ERR_CUDA;
+        s->prof_ev.push_back(e);
+    }
+    s->prof_rec.assign(max_records, ProfRec{0, 0.0, 0.0});
+    s->prof_max = max_records;
+    s->prof_n = 0;
+    s->prof_on = true;
+    return CODEC_OK;
+}
+
+codec_status codec_profile_end(codec_state_t* s, codec_kernel_stats* out, void* stream)
+{
+    if (!s || !out) return CODEC_ERR_NULL;
+    s->prof_on = false;
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return CODEC_ERR_CUDA;
+    for (int k = 0; k < CODEC_KERNEL_KINDS; k++) out[k] = codec_kernel_stats{k, 0, 0.0, 0.0, 0.0};
+    for (int i = 0; i < s->prof_n; i++) {
+        float ms = 0.f;
+        if (cudaEventElapsedTime(&ms, s->prof_ev[2 * i], s->prof_ev[2 * i + 1]) != cudaSuccess) return CODEC_ERR_CUDA;
+        codec_kernel_stats& o = out[s->prof_rec[i].kind];
+        o.launches++;
+        o.ms += ms;
+        o.flops += s->prof_rec[i].flops;
+        o.bytes += s->prof_rec[i].bytes;
+    }
+    s->prof_n = 0;
+    return CODEC_OK;
 }
 
 int32_t codec_state_streams(const codec_state_t* s) { return s ? s->n_slots : 0; }
@@ -569,6 +626,8 @@ codec_status codec_state_reset(codec_state_t* s, const int32_t* ids, int32_t n, 
     if (launch_state_reset(s->hist_d, (int)s->hist.size(), s->slots_d, (int)list.size(), s->frames_d,
                            s->err_d, cs) != cudaSuccess)
         return CODEC_ERR_CUDA;
+    if (!ids && s->tc_scratch.err && cudaMemsetAsync(s->tc_scratch.err, 0, sizeof(int), cs) != cudaSuccess)
+        return CODEC_ERR_CUDA;
     for (int i : list) s->frames_h[i] = 0;
     return CODEC_OK;
 }
@@ -583,6 +642,11 @@ codec_status codec_state_query(codec_state_t* s, int32_t id, codec_stream_info* 
     if (cudaStreamSynchronize(cs) != cudaSuccess) return CODEC_ERR_CUDA;
     if (cudaMemcpy(&fr, s->frames_d + id, sizeof(fr), cudaMemcpyDeviceToHost) != cudaSuccess) return CODEC_ERR_CUDA;
     if (cudaMemcpy(&err, s->err_d + id, sizeof(err), cudaMemcpyDeviceToHost) != cudaSuccess) return CODEC_ERR_CUDA;
+    if (s->tc_scratch.err) {
+        int te = 0;
+        if (cudaMemcpy(&te, s->tc_scratch.err, sizeof(te), cudaMemcpyDeviceToHost) != cudaSuccess) return CODEC_ERR_CUDA;
+        if (te) err |= CODEC_STREAM_ERR_KERNEL_TIMEOUT;
+    }
     info->frames_decoded = fr;
     info->error_bits = err;
     info->reserved = 0;
@@ -603,20 +667,37 @@ struct Launcher {
     const int* tc128;
     std::vector<int> ntiles64, ntiles128;   // per level
     std::vector<int> slot_h, n_h;           // host copies of the compacted batch
+    long long frames = 0;                   // frames in this call
+    int Bc = 0;                             // streams with frames in this call
     int launches = 0;
     cudaError_t err = cudaSuccess;
     const char* where = "";
 
-    bool check(cudaError_t e, const char* what)
+    // Enqueue one kernel through f(), with an event pair around it when the
+    // state is recording, and note its algorithmic work.
+    template <class F>
+    bool run(int kind, double flops, double bytes, const char* what, F&& f)
     {
+        if (err != cudaSuccess) return false;
+        const bool rec = s->prof_on && s->prof_n < s->prof_max;
+        if (rec) cudaEventRecord(s->prof_ev[2 * s->prof_n], cs);
+        cudaError_t e = f();
         launches++;
-        if (e != cudaSuccess && err == cudaSuccess) { err = e; where = what; }
+        if (rec) {
+            cudaEventRecord(s->prof_ev[2 * s->prof_n + 1], cs);
+            s->prof_rec[s->prof_n] = ProfRec{kind, flops, bytes};
+            s->prof_n++;
+        }
+        if (e != cudaSuccess) { err = e; where = what; }
         if (err == cudaSuccess && debug_sync()) {
             cudaError_t e2 = cudaStreamSynchronize(cs);
             if (e2 != cudaSuccess) { err = e2; where = what; }
         }
         return err == cudaSuccess;
     }
+
+    long long rows(int lvl) const { return frames * s->c->level_r[lvl]; }
+    long long rows_pref(int lvl, Layout l) const { return frames * s->c->level_r[lvl] + (long long)Bc * l.P; }
 
     void gemm(const Contraction& C, const float* in, Layout il, int in_lvl, float* out, Layout ol,
               int out_C, int out_step, const float* res, int epi, float scale, int layer_ring,
@@ -639,14 +720,25 @@ struct Launcher {
             a.ring_R = s->R;
             a.d = s->c->cfg.d;
         }
+        const double M = (double)rows(in_lvl);
+        const double flops = 2.0 * M * C.N * C.K;
+        const double out_rw = (epi == EPI_RESID || epi == EPI_MRF_FIRST) ? 2.0
+                              : (epi == EPI_MRF_ADD || epi == EPI_MRF_LAST) ? 3.0 : 1.0;
+        const double bytes = 4.0 * ((M + (double)Bc * C.shift[0]) * C.Cin + (double)C.K * C.N + M * C.N * out_rw);
         if (C.use_tc) {
             a.tcum = tc128 + (size_t)in_lvl * S1;
             a.bm = 128;
-            check(launch_gemm_tc(a, C.tc, pv, ntiles128[in_lvl], &s->tc_scratch, cs, &launches), what);
+            const long long arows = il.P ? rows_pref(in_lvl, il) : rows(in_lvl);
+            run(CODEC_KERNEL_OPERAND_PREP, 0.0, 8.0 * (double)arows * C.Cin, what, [&] {
+                return launch_tc_prep(in, C.alpha, C.inv_alpha, arows, C.Cin, &s->tc_scratch, cs);
+            });
+            run(CODEC_KERNEL_GEMM_TC, flops, bytes, what, [&] {
+                return launch_tc_gemm(a, C.tc, pv, ntiles128[in_lvl], &s->tc_scratch, arows, s->c->num_sms, cs);
+            });
         } else {
             a.tcum = tc64 + (size_t)in_lvl * S1;
             a.bm = 64;
-            check(launch_gemm_simt(a, pv, ntiles64[in_lvl], cs), what);
+            run(CODEC_KERNEL_GEMM_SIMT, flops, bytes, what, [&] { return launch_gemm_simt(a, pv, ntiles64[in_lvl], cs); });
         }
     }
 };
@@ -719,6 +811,8 @@ codec_status plan_call(codec_state_t* s, const int32_t* n_frames, const int32_t*
                     reinterpret_cast<const long long*>(D + s->off_pos0), D + s->off_bidx};
     L.tc64 = D + s->off_tc64;
     L.tc128 = D + s->off_tc128;
+    L.frames = total;
+    L.Bc = Bc;
     L.slot_h.assign(slot, slot + Bc);
     L.n_h.resize(Bc);
     for (int b = 0; b < Bc; b++) L.n_h[b] = cf[b + 1] - cf[b];
@@ -742,31 +836,37 @@ codec_status decode_impl(codec_state_t* s, const int32_t* codes, const int32_t* 
     const Layout L0d{1, 0}, L0p{1, s->P[0]};
     auto lay = [&](int lvl) { return Layout{c->level_r[lvl], s->P[lvl]}; };
 
-    L.check(launch_hist_fill(s->hist_d, (int)s->hist.size(), L.pv, cs), "history fill");
-    if (L.err == cudaSuccess)
-        L.check(launch_rvq_gather(c->cb, g.Q, g.V, g.E, codes, T_max, L.pv, s->e, L0p, s->err_d, rows0, cs),
-                "codebook gather");
+    const double hist_bytes = 8.0 * s->hist_floats_per_slot * (double)L.Bc;
+    L.run(CODEC_KERNEL_HISTORY, 0.0, hist_bytes, "history fill",
+          [&] { return launch_hist_fill(s->hist_d, (int)s->hist.size(), L.pv, cs); });
+    L.run(CODEC_KERNEL_GATHER, (double)rows0 * g.Q * g.E, 4.0 * rows0 * ((double)g.Q * (1 + g.E) + g.E), "codebook gather",
+          [&] { return launch_rvq_gather(c->cb, g.Q, g.V, g.E, codes, T_max, L.pv, s->e, L0p, s->err_d, rows0, cs); });
     L.gemm(c->pre, s->e, L0p, 0, s->h, L0d, g.d, 1, nullptr, EPI_STORE, 1.f, 0, "pre-conv");
+    const double norm_flops = 3.0 * rows0 * g.d, norm_bytes = 8.0 * rows0 * g.d;
+    double attn_flops = 0.0, attn_bytes = 8.0 * rows0 * g.d;
+    for (size_t b = 0; b < L.n_h.size(); b++) {
+        const long long p0 = s->frames_h[L.slot_h[b]];
+        for (int t = 0; t < L.n_h[b]; t++) attn_flops += 4.0 * g.d * (double)std::min<long long>(p0 + t + 1, g.window);
+        attn_bytes += 8.0 * g.d * (double)(L.n_h[b] + std::min<long long>(p0, g.window - 1));
+    }
     for (int l = 0; l < g.layers; l++) {
         const LayerW& W = c->layers[l];
-        if (L.err == cudaSuccess)
-            L.check(launch_rms_norm(s->h, L0d, W.n1, g.rms_eps, s->u, L0d, g.d, L.pv, rows0, cs), "rmsnorm 1");
+        L.run(CODEC_KERNEL_RMSNORM, norm_flops, norm_bytes, "rmsnorm 1",
+              [&] { return launch_rms_norm(s->h, L0d, W.n1, g.rms_eps, s->u, L0d, g.d, L.pv, rows0, cs); });
         L.gemm(W.qkv, s->u, L0d, 0, s->q, L0d, g.d, 1, nullptr, EPI_QKV, 1.f, l, "qkv");
-        if (L.err == cudaSuccess) {
-            const size_t per_layer = (size_t)S * s->R * g.d;
-            L.check(launch_swa(s->q, s->o, s->kring + per_layer * l, s->vring + per_layer * l, g.d, g.heads,
-                               g.window, s->R, L.pv, rows0, cs),
-                    "attention");
-        }
+        const size_t per_layer = (size_t)S * s->R * g.d;
+        L.run(CODEC_KERNEL_ATTENTION, attn_flops, attn_bytes, "attention", [&] {
+            return launch_swa(s->q, s->o, s->kring + per_layer * l, s->vring + per_layer * l, g.d, g.heads,
+                              g.window, s->R, L.pv, rows0, cs);
+        });
         L.gemm(W.o, s->o, L0d, 0, s->h, L0d, g.d, 1, s->h, EPI_RESID, 1.f, 0, "out-proj");
-        if (L.err == cudaSuccess)
-            L.check(launch_rms_norm(s->h, L0d, W.n2, g.rms_eps, s->u, L0d, g.d, L.pv, rows0, cs), "rmsnorm 2");
+        L.run(CODEC_KERNEL_RMSNORM, norm_flops, norm_bytes, "rmsnorm 2",
+              [&] { return launch_rms_norm(s->h, L0d, W.n2, g.rms_eps, s->u, L0d, g.d, L.pv, rows0, cs); });
         L.gemm(W.w1, s->u, L0d, 0, s->f, L0d, g.ffn, 1, nullptr, EPI_GELU, 1.f, 0, "mlp 1");
         L.gemm(W.w2, s->f, L0d, 0, s->h, L0d, g.d, 1, s->h, EPI_RESID, 1.f, 0, "mlp 2");
     }
-    if (L.err == cudaSuccess)
-        L.check(launch_rms_norm(s->h, L0d, c->tf_norm, g.rms_eps, s->hf, L0p, g.d, L.pv, rows0, cs),
-                "final rmsnorm");
+    L.run(CODEC_KERNEL_RMSNORM, norm_flops, norm_bytes, "final rmsnorm",
+          [&] { return launch_rms_norm(s->h, L0d, c->tf_norm, g.rms_eps, s->hf, L0p, g.d, L.pv, rows0, cs); });
     const float* x = s->hf;
     int xl = 0;
     for (int u = 0; u < g.n_up; u++) {
@@ -795,16 +895,18 @@ codec_status decode_impl(codec_state_t* s, const int32_t* codes, const int32_t* 
         x = s->y[si];
         xl = lvl;
     }
-    if (L.err == cudaSuccess) {
-        const int S1l = S + 1;
-        L.check(launch_final_conv(x, lay(xl), g.ch[g.n_stages - 1], c->out_w, c->out_b, c->out_alpha,
-                                  c->out_inv_alpha, g.final_k, audio, pre_tanh,
-                                  (long long)T_max * c->spf, L.pv, L.tc128 + (size_t)xl * S1l,
-                                  L.ntiles128[xl], cs),
-                "final conv");
+    {
+        const int Cl = g.ch[g.n_stages - 1];
+        const double R = (double)L.rows(xl);
+        L.run(CODEC_KERNEL_FINAL_CONV, 2.0 * R * Cl * g.final_k, 4.0 * R * (Cl + (pre_tanh ? 2 : 1)), "final conv",
+              [&] {
+                  return launch_final_conv(x, lay(xl), Cl, c->out_w, c->out_b, c->out_alpha, c->out_inv_alpha,
+                                           g.final_k, audio, pre_tanh, (long long)T_max * c->spf, L.pv,
+                                           L.tc128 + (size_t)xl * (S + 1), L.ntiles128[xl], cs);
+              });
     }
-    if (L.err == cudaSuccess)
-        L.check(launch_hist_commit(s->hist_d, (int)s->hist.size(), L.pv, nullptr, s->frames_d, cs), "history commit");
+    L.run(CODEC_KERNEL_HISTORY, 0.0, hist_bytes, "history commit",
+          [&] { return launch_hist_commit(s->hist_d, (int)s->hist.size(), L.pv, nullptr, s->frames_d, cs); });
     s->last_launches = L.launches;
     if (L.err != cudaSuccess) {
         if (debug_sync()) fprintf(stderr, "codec: %s failed: %s\n", L.where, cudaGetErrorString(L.err));
@@ -823,8 +925,9 @@ codec_status embed_impl(codec_state_t* s, const int32_t* codes, const int32_t* n
     int rows0 = 0;
     codec_status pst = plan_call(s, n_frames, ids, B, T_max, cs, L, rows0);
     if (pst != CODEC_OK || rows0 == 0) return pst;
-    L.check(launch_rvq_gather(s->c->cb, g.Q, g.V, g.E, codes, T_max, L.pv, emb, Layout{1, 0}, s->err_d, rows0, cs),
-            "codebook gather");
+    L.run(CODEC_KERNEL_GATHER, (double)rows0 * g.Q * g.E, 4.0 * rows0 * ((double)g.Q * (1 + g.E) + g.E),
+          "codebook gather",
+          [&] { return launch_rvq_gather(s->c->cb, g.Q, g.V, g.E, codes, T_max, L.pv, emb, Layout{1, 0}, s->err_d, rows0, cs); });
     s->last_launches = L.launches;
     return L.err == cudaSuccess ? CODEC_OK : CODEC_ERR_CUDA;
 }

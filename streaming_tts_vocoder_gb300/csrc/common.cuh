@@ -100,4 +100,35 @@ __device__ __forceinline__ float gelu_f(float x)
     return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f));
 }
 
+// Epilogue of both GEMM paths for one output element: acc is the finished
+// dot product of output row t of batch entry b (row out_row of the output
+// layout), column n.
+__device__ __forceinline__ void gemm_store(const GemmArgs& a, const PlanView& plan, int b, int t,
+                                           long long out_row, int n, float acc)
+{
+    float v = acc;
+    if (a.bias) v += __ldg(a.bias + (n % a.bias_mod));
+    const long long idx = out_row * a.out_C + n;
+    switch (a.epi) {
+    case EPI_STORE: a.out[idx] = v; break;
+    case EPI_RESID: a.out[idx] = a.res[idx] + v; break;
+    case EPI_GELU: a.out[idx] = gelu_f(v); break;
+    case EPI_MRF_FIRST: a.out[idx] = a.res[idx] + v; break;
+    case EPI_MRF_ADD: a.out[idx] = a.out[idx] + (a.res[idx] + v); break;
+    case EPI_MRF_LAST: a.out[idx] = (a.out[idx] + (a.res[idx] + v)) * a.scale; break;
+    case EPI_QKV: {
+        if (n < a.d) {
+            a.out[out_row * a.d + n] = v;
+        } else {
+            const long long pos = __ldg(plan.pos0 + b) + t;
+            const long long rr = (long long)__ldg(plan.slot + b) * a.ring_R + (pos & (a.ring_R - 1));
+            if (n < 2 * a.d) a.kring[rr * a.d + (n - a.d)] = v;
+            else a.vring[rr * a.d + (n - 2 * a.d)] = v;
+        }
+        break;
+    }
+    default: break;
+    }
+}
+
 }  // namespace codec

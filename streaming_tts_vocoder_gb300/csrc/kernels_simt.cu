@@ -68,34 +68,6 @@ cudaError_t launch_rvq_gather(const float* cb, int Q, int V, int E, const int* c
 // row does not depend on how the streams were packed.
 constexpr int SB_M = 64, SB_N = 64, SB_K = 16;
 
-__device__ __forceinline__ void gemm_store(const GemmArgs& a, const PlanView& plan, int b, int t,
-                                           long long out_row, int n, float acc)
-{
-    float v = acc;
-    if (a.bias) v += __ldg(a.bias + (n % a.bias_mod));
-    const long long idx = out_row * a.out_C + n;
-    switch (a.epi) {
-    case EPI_STORE: a.out[idx] = v; break;
-    case EPI_RESID: a.out[idx] = a.res[idx] + v; break;
-    case EPI_GELU: a.out[idx] = gelu_f(v); break;
-    case EPI_MRF_FIRST: a.out[idx] = a.res[idx] + v; break;
-    case EPI_MRF_ADD: a.out[idx] = a.out[idx] + (a.res[idx] + v); break;
-    case EPI_MRF_LAST: a.out[idx] = (a.out[idx] + (a.res[idx] + v)) * a.scale; break;
-    case EPI_QKV: {
-        if (n < a.d) {
-            a.out[out_row * a.d + n] = v;
-        } else {
-            const long long pos = __ldg(plan.pos0 + b) + t;
-            const long long rr = (long long)__ldg(plan.slot + b) * a.ring_R + (pos & (a.ring_R - 1));
-            if (n < 2 * a.d) a.kring[rr * a.d + (n - a.d)] = v;
-            else a.vring[rr * a.d + (n - 2 * a.d)] = v;
-        }
-        break;
-    }
-    default: break;
-    }
-}
-
 __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmArgs a, PlanView plan)
 {
     __shared__ float As[SB_K][SB_M + 4];

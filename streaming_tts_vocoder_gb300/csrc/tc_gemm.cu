@@ -1,15 +1,553 @@
-// Tensor-core implicit GEMM (tcgen05): not built yet; the configuration check
-// rejects the fp16x3 precision until it is.
+// Tensor-core implicit GEMM for the decoder's dense contractions (causal and
+// dilated Conv1d, the transposed convs in their phase-GEMM form, the
+// transformer linears) on sm_103a: TMA loads of 128 x 32 operand tiles into
+// 64-byte-swizzled shared memory, tcgen05.mma issued by one thread with the
+// fp32 accumulator in TMEM, and an epilogue that reads TMEM back with
+// tcgen05.ld and applies bias / residual / MRF average / GELU / ring scatter.
+//
+// Precision: each operand is split into fp16 hi + lo parts (x = hi + lo to
+// about 22 bits) and every k-step issues hi*hi + hi*lo + lo*hi, so the result
+// carries close to fp32 operand accuracy while running on the f16 tensor
+// pipe.  A single fp16 or bf16 pass misses the decoder's 1e-3 waveform bound
+// by more than 10x on random weights; this split meets it with a wide margin.
+//
+// Implicit GEMM: output row t of stream segment b takes, for tap j, the
+// input row base(b) + t - shift_j, so a k-block is one TMA box at a shifted
+// row coordinate; the [history | chunk] rows in front of each segment supply
+// the causal left context, and a tile never crosses a stream segment.
+//
+// Roles (192 threads, one CTA per SM, persistent over tiles):
+//   warp 0     TMA producer (one thread)
+//   warp 1     TMEM allocator and MMA issuer (one thread)
+//   warps 2-5  epilogue, warp w reading TMEM lanes 32 (w % 4) .. +31
+// Two TMEM accumulators (2 x 256 columns) let the epilogue of one tile run
+// under the main loop of the next.  Every wait is bounded: when one expires
+// the CTA raises a flag, stops, drains its copies and MMAs, frees TMEM and
+// returns.
+#include <cudaTypedefs.h>
+#include <cuda_fp16.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
 #include "tc_gemm.h"
 
 namespace codec {
 
-bool tc_eligible(int, int) { return false; }
-bool tc_pack_weights(const float*, int, int, int, TcWeights*, std::vector<void*>&) { return false; }
-bool tc_scratch_alloc(TcScratch*, size_t, std::vector<void*>&) { return false; }
-cudaError_t launch_gemm_tc(const GemmArgs&, const TcWeights&, PlanView, int, TcScratch*, cudaStream_t, int*)
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBK = 32;              // fp16 per k-block: 64-byte rows, 64-byte swizzle
+constexpr int kThreads = 192;
+constexpr int kMaxBN = 256;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kSpinLimit = 1u << 25;
+constexpr int kSmemBudget = 220 * 1024;
+constexpr uint32_t kAPlaneBytes = kBM * kBK * 2;   // 8 KB
+
+struct TcParams {
+    int n_row_tiles;
+    int n_tiles_n;
+    int BN;
+    int nkb;            // k-blocks: ntaps * Cin / kBK
+    int cin_blocks;     // Cin / kBK
+    int stages;
+    uint32_t b_stride;  // bytes of one B plane in a stage (1024-aligned)
+    uint32_t stage_bytes;
+    uint32_t tx_bytes;  // bytes the four TMA loads of a stage deliver
+    uint32_t idesc;
+    float unscale;
+    int* err;
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p)
 {
-    return cudaErrorNotSupported;
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase of the given parity; false if it did not complete
+// within the poll limit or another role of the CTA gave up first.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag)
+{
+    for (uint32_t i = 0;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (i >= kSpinLimit) {
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+
+// Bounded wait that ignores the abort flag (used to drain in-flight work).
+__device__ __forceinline__ bool mbar_drain(uint64_t* bar, uint32_t parity)
+{
+    for (uint32_t i = 0; i < kSpinLimit; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
+            smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// K-major operand tile with 64-byte swizzle: rows of 64 bytes, 8-row groups
+// 512 bytes apart (stride byte offset); the leading byte offset is unused for
+// swizzled K-major layouts.  Bits 46-47 carry the descriptor version.
+__device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr)
+{
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(512 >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)4 << 61);
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                        uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v)
+{
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[i]);
+}
+
+// Instruction descriptor of kind::f16: D f32, A and B f16, both K-major.
+constexpr uint32_t idesc_f16(int M, int N)
+{
+    return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+struct TileRows {
+    int b, t0, nrows;
+    long long in_base;    // input row of output row t0 (tap shift 0)
+};
+
+__device__ __forceinline__ TileRows tile_rows(const GemmArgs& a, const PlanView& plan, int mt)
+{
+    TileRows r;
+    r.b = find_seg(a.tcum, plan.B, mt);
+    const int seg_rows = (__ldg(plan.cf + r.b + 1) - __ldg(plan.cf + r.b)) * a.in_l.r;
+    r.t0 = (mt - __ldg(a.tcum + r.b)) * kBM;
+    r.nrows = min(kBM, seg_rows - r.t0);
+    r.in_base = seg_base(a.in_l, plan.cf, r.b) + r.t0;
+    return r;
+}
+
+// 32 consecutive output columns n0 .. n0+31 of one row (count of them valid).
+__device__ __forceinline__ void epi_store32(const GemmArgs& a, const PlanView& plan, int b, int t,
+                                            long long out_row, int n0, int count, const float* v, float unscale)
+{
+    const bool vec = count == 32 && a.epi != EPI_QKV && ((out_row * a.out_C + n0) & 3) == 0 &&
+                     (a.bias == nullptr || (n0 % a.bias_mod) + 32 <= a.bias_mod);
+    if (!vec) {
+        for (int i = 0; i < count; i++) gemm_store(a, plan, b, t, out_row, n0 + i, v[i] * unscale);
+        return;
+    }
+    const long long idx = out_row * a.out_C + n0;
+    float4* o4 = reinterpret_cast<float4*>(a.out + idx);
+    const float4* r4 = reinterpret_cast<const float4*>(a.res ? a.res + idx : a.out + idx);
+    const float* bias = a.bias ? a.bias + (n0 % a.bias_mod) : nullptr;
+#pragma unroll
+    for (int q = 0; q < 8; q++) {
+        float x[4];
+#pragma unroll
+        for (int i = 0; i < 4; i++) x[i] = v[4 * q + i] * unscale + (bias ? __ldg(bias + 4 * q + i) : 0.f);
+        float4 y;
+        switch (a.epi) {
+        case EPI_STORE: y = make_float4(x[0], x[1], x[2], x[3]); break;
+        case EPI_GELU: y = make_float4(gelu_f(x[0]), gelu_f(x[1]), gelu_f(x[2]), gelu_f(x[3])); break;
+        case EPI_RESID:
+        case EPI_MRF_FIRST: {
+            const float4 r = r4[q];
+            y = make_float4(r.x + x[0], r.y + x[1], r.z + x[2], r.w + x[3]);
+            break;
+        }
+        case EPI_MRF_ADD: {
+            const float4 r = r4[q], o = o4[q];
+            y = make_float4(o.x + (r.x + x[0]), o.y + (r.y + x[1]), o.z + (r.z + x[2]), o.w + (r.w + x[3]));
+            break;
+        }
+        default: {  // EPI_MRF_LAST
+            const float4 r = r4[q], o = o4[q];
+            y = make_float4((o.x + (r.x + x[0])) * a.scale, (o.y + (r.y + x[1])) * a.scale,
+                            (o.z + (r.z + x[2])) * a.scale, (o.w + (r.w + x[3])) * a.scale);
+            break;
+        }
+        }
+        o4[q] = y;
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(
+    const __grid_constant__ CUtensorMap ma_hi, const __grid_constant__ CUtensorMap ma_lo,
+    const __grid_constant__ CUtensorMap mb_hi, const __grid_constant__ CUtensorMap mb_lo, const GemmArgs a,
+    const PlanView plan, const TcParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)p.stages * p.stage_bytes);
+    uint64_t* full = bars;
+    uint64_t* empty = bars + p.stages;
+    uint64_t* tfull = bars + 2 * p.stages;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* drain = tempty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < p.stages; s++) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int i = 0; i < 2; i++) {
+            mbar_init(&tfull[i], 1);
+            mbar_init(&tempty[i], 4);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int total_tiles = p.n_row_tiles * p.n_tiles_n;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------------------------------------------- producer --
+            int it = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+                const TileRows tr = tile_rows(a, plan, tile / p.n_tiles_n);
+                const int n0 = (tile % p.n_tiles_n) * p.BN;
+                for (int kb = 0; kb < p.nkb; kb++, it++) {
+                    const int s = it % p.stages;
+                    const uint32_t ph = (uint32_t)(it / p.stages) & 1u;
+                    if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag)) { ok = false; break; }
+                    const int j = kb / p.cin_blocks;
+                    const int c0 = (kb - j * p.cin_blocks) * kBK;
+                    const int row = (int)(tr.in_base - a.shift[j]);
+                    uint8_t* st = smem + (size_t)s * p.stage_bytes;
+                    mbar_expect_tx(&full[s], p.tx_bytes);
+                    tma_load_2d(st, &ma_hi, &full[s], c0, row);
+                    tma_load_2d(st + kAPlaneBytes, &ma_lo, &full[s], c0, row);
+                    tma_load_2d(st + 2 * kAPlaneBytes, &mb_hi, &full[s], kb * kBK, n0);
+                    tma_load_2d(st + 2 * kAPlaneBytes + p.b_stride, &mb_lo, &full[s], kb * kBK, n0);
+                }
+            }
+            // drain: every stage's last armed load has landed before exit
+            for (int s = 0; s < p.stages && s < it; s++) {
+                const int last = s + ((it - 1 - s) / p.stages) * p.stages;
+                mbar_drain(&full[s], (uint32_t)(last / p.stages) & 1u);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // --------------------------------------------------- MMA issue --
+            int it = 0, acc_it = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x, acc_it++) {
+                const int acc = acc_it & 1;
+                const uint32_t aph = (uint32_t)(acc_it >> 1) & 1u;
+                if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kMaxBN);
+                for (int kb = 0; kb < p.nkb; kb++, it++) {
+                    const int s = it % p.stages;
+                    const uint32_t ph = (uint32_t)(it / p.stages) & 1u;
+                    if (!mbar_wait(&full[s], ph, abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(smem + (size_t)s * p.stage_bytes);
+                    const uint64_t dah = sdesc_sw64(sa);
+                    const uint64_t dal = sdesc_sw64(sa + kAPlaneBytes);
+                    const uint64_t dbh = sdesc_sw64(sa + 2 * kAPlaneBytes);
+                    const uint64_t dbl = sdesc_sw64(sa + 2 * kAPlaneBytes + p.b_stride);
+#pragma unroll
+                    for (int k = 0; k < kBK / 16; k++) {
+                        const uint64_t o = (uint64_t)((k * 32) >> 4);
+                        mma_f16(d_tmem, dah + o, dbh + o, p.idesc, (kb | k) != 0 ? 1u : 0u);
+                        mma_f16(d_tmem, dah + o, dbl + o, p.idesc, 1u);
+                        mma_f16(d_tmem, dal + o, dbh + o, p.idesc, 1u);
+                    }
+                    mma_commit(&empty[s]);
+                }
+                if (!ok) break;
+                mma_commit(&tfull[acc]);
+            }
+            // all issued MMAs complete before TMEM is released
+            mma_commit(drain);
+            mbar_drain(drain, 0);
+        }
+    } else {
+        // ------------------------------------------------------ epilogue --
+        const int q = warp & 3;
+        const int m = q * 32 + lane;
+        int acc_it = 0;
+        for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, acc_it++) {
+            const int acc = acc_it & 1;
+            const uint32_t aph = (uint32_t)(acc_it >> 1) & 1u;
+            // one lane polls, the warp follows its verdict (tcgen05.ld needs a converged warp)
+            int ok = 1;
+            if (lane == 0) ok = mbar_wait(&tfull[acc], aph, abort_flag) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            tc_fence_after();
+            const TileRows tr = tile_rows(a, plan, tile / p.n_tiles_n);
+            const int n0 = (tile % p.n_tiles_n) * p.BN;
+            const bool valid = m < tr.nrows;
+            const int t = tr.t0 + m;
+            const long long out_row = seg_base(a.out_l, plan.cf, tr.b) + (long long)t * a.out_step;
+            for (int c = 0; c < p.BN; c += 32) {
+                float v[32];
+                tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kMaxBN + c), v);
+                if (valid) {
+                    int count = min(32, p.BN - c);
+                    count = min(count, a.N - (n0 + c));
+                    if (count > 0) epi_store32(a, plan, tr.b, t, out_row, n0 + c, count, v, p.unscale);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[acc]);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols)
+                     : "memory");
+    }
+    if (threadIdx.x == 0 && *abort_flag) atomicExch(p.err, 1);
+}
+
+// hi = fp16(a), lo = fp16(a - hi), a = Snake(x) or x; four channels per thread.
+__global__ void tc_prep_kernel(const float4* __restrict__ x, const float* __restrict__ alpha,
+                               const float* __restrict__ inv_alpha, long long n4, int cin4,
+                               __half2* __restrict__ hi, __half2* __restrict__ lo)
+{
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4; i += (long long)gridDim.x * blockDim.x) {
+        float4 v = x[i];
+        if (alpha) {
+            const int c = (int)(i % cin4) * 4;
+            v.x = snake_f(v.x, __ldg(alpha + c), __ldg(inv_alpha + c));
+            v.y = snake_f(v.y, __ldg(alpha + c + 1), __ldg(inv_alpha + c + 1));
+            v.z = snake_f(v.z, __ldg(alpha + c + 2), __ldg(inv_alpha + c + 2));
+            v.w = snake_f(v.w, __ldg(alpha + c + 3), __ldg(inv_alpha + c + 3));
+        }
+        const __half hx = __float2half_rn(v.x), hy = __float2half_rn(v.y);
+        const __half hz = __float2half_rn(v.z), hw = __float2half_rn(v.w);
+        hi[2 * i] = __halves2half2(hx, hy);
+        hi[2 * i + 1] = __halves2half2(hz, hw);
+        lo[2 * i] = __halves2half2(__float2half_rn(v.x - __half2float(hx)), __float2half_rn(v.y - __half2float(hy)));
+        lo[2 * i + 1] = __halves2half2(__float2half_rn(v.z - __half2float(hz)), __float2half_rn(v.w - __half2float(hw)));
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2D fp16 tensor map over [outer][inner] with a box of box_inner x box_outer
+// and 64-byte swizzle; out-of-range rows read as zero.
+bool make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
+              uint32_t box_outer)
+{
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner * 2};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+uint32_t round1024(uint32_t x) { return (x + 1023u) & ~1023u; }
+
+}  // namespace
+
+bool tc_eligible(int Cin, int N) { return Cin >= kBK && Cin % kBK == 0 && N >= 16 && N % 16 == 0; }
+
+bool tc_pack_weights(const float* wkn, int ntaps, int Cin, int N, TcWeights* out, std::vector<void*>& allocs)
+{
+    const size_t K = (size_t)ntaps * Cin;
+    float mx = 0.f;
+    for (size_t i = 0; i < K * (size_t)N; i++) mx = std::fmax(mx, std::fabs(wkn[i]));
+    const int e = mx > 0.f ? -(int)std::floor(std::log2(mx)) : 0;
+    const float scale = std::ldexp(1.0f, e);
+    std::vector<__half> hi(K * N), lo(K * N);
+    for (int n = 0; n < N; n++)
+        for (size_t k = 0; k < K; k++) {
+            const float w = wkn[k * N + n] * scale;
+            const __half h = __float2half_rn(w);
+            hi[(size_t)n * K + k] = h;
+            lo[(size_t)n * K + k] = __float2half_rn(w - __half2float(h));
+        }
+    void *dh = nullptr, *dl = nullptr;
+    if (cudaMalloc(&dh, hi.size() * sizeof(__half)) != cudaSuccess) return false;
+    allocs.push_back(dh);
+    if (cudaMalloc(&dl, lo.size() * sizeof(__half)) != cudaSuccess) return false;
+    allocs.push_back(dl);
+    if (cudaMemcpy(dh, hi.data(), hi.size() * sizeof(__half), cudaMemcpyHostToDevice) != cudaSuccess) return false;
+    if (cudaMemcpy(dl, lo.data(), lo.size() * sizeof(__half), cudaMemcpyHostToDevice) != cudaSuccess) return false;
+    out->hi = dh;
+    out->lo = dl;
+    out->unscale = std::ldexp(1.0f, -e);
+    const int nt = (N + kMaxBN - 1) / kMaxBN;
+    out->BN = ((N + nt - 1) / nt + 15) / 16 * 16;
+    out->n_tiles = (N + out->BN - 1) / out->BN;
+    if (!make_map(&out->map_hi, dh, K, (uint64_t)N, kBK, (uint32_t)out->BN)) return false;
+    if (!make_map(&out->map_lo, dl, K, (uint64_t)N, kBK, (uint32_t)out->BN)) return false;
+    return true;
+}
+
+bool tc_scratch_alloc(TcScratch* s, size_t elems, std::vector<void*>& allocs)
+{
+    if (cudaMalloc(&s->a_hi, elems * sizeof(__half)) != cudaSuccess) return false;
+    allocs.push_back(s->a_hi);
+    if (cudaMalloc(&s->a_lo, elems * sizeof(__half)) != cudaSuccess) return false;
+    allocs.push_back(s->a_lo);
+    if (cudaMalloc(&s->err, sizeof(int)) != cudaSuccess) return false;
+    allocs.push_back(s->err);
+    if (cudaMemset(s->err, 0, sizeof(int)) != cudaSuccess) return false;
+    s->elems = elems;
+    return true;
+}
+
+cudaError_t launch_tc_prep(const float* x, const float* alpha, const float* inv_alpha, long long rows, int Cin,
+                           TcScratch* scratch, cudaStream_t s)
+{
+    const long long n = rows * Cin;
+    if (n <= 0) return cudaSuccess;
+    if ((size_t)n > scratch->elems) return cudaErrorInvalidValue;
+    const long long n4 = n / 4;
+    const int threads = 256;
+    const long long blocks = std::min<long long>((n4 + threads - 1) / threads, 152LL * 16);
+    tc_prep_kernel<<<(unsigned)blocks, threads, 0, s>>>(reinterpret_cast<const float4*>(x), alpha, inv_alpha, n4,
+                                                         Cin / 4, reinterpret_cast<__half2*>(scratch->a_hi),
+                                                         reinterpret_cast<__half2*>(scratch->a_lo));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_tc_gemm(const GemmArgs& a, const TcWeights& w, PlanView plan, int n_row_tiles,
+                           const TcScratch* scratch, long long a_rows, int num_sms, cudaStream_t s)
+{
+    if (n_row_tiles <= 0) return cudaSuccess;
+    alignas(64) CUtensorMap ma_hi, ma_lo;
+    if (!make_map(&ma_hi, scratch->a_hi, (uint64_t)a.Cin, (uint64_t)a_rows, kBK, kBM)) return cudaErrorInvalidValue;
+    if (!make_map(&ma_lo, scratch->a_lo, (uint64_t)a.Cin, (uint64_t)a_rows, kBK, kBM)) return cudaErrorInvalidValue;
+    TcParams p;
+    p.n_row_tiles = n_row_tiles;
+    p.n_tiles_n = w.n_tiles;
+    p.BN = w.BN;
+    p.cin_blocks = a.Cin / kBK;
+    p.nkb = a.ntaps * p.cin_blocks;
+    p.b_stride = round1024((uint32_t)w.BN * kBK * 2);
+    p.stage_bytes = 2 * kAPlaneBytes + 2 * p.b_stride;
+    p.tx_bytes = 2 * kAPlaneBytes + 2 * (uint32_t)w.BN * kBK * 2;
+    const int extra = 1024 + 256;
+    p.stages = std::min(8, (kSmemBudget - extra) / (int)p.stage_bytes);
+    if (p.stages < 2) return cudaErrorInvalidValue;
+    p.idesc = idesc_f16(kBM, w.BN);
+    p.unscale = w.unscale;
+    p.err = scratch->err;
+    const size_t smem = (size_t)p.stages * p.stage_bytes + extra;
+    static int configured = 0;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
+        if (e != cudaSuccess) return e;
+        configured = 1;
+    }
+    const int tiles = n_row_tiles * w.n_tiles;
+    const int grid = std::min(tiles, num_sms > 0 ? num_sms : 152);
+    tc_gemm_kernel<<<grid, kThreads, smem, s>>>(ma_hi, ma_lo, w.map_hi, w.map_lo, a, plan, p);
+    return cudaGetLastError();
 }
 
 }  // namespace codec

@@ -2,33 +2,47 @@
 // split operands.  Declarations shared by the host runtime and tc_gemm.cu.
 #pragma once
 
+#include <cuda.h>
+
 #include <vector>
 
 #include "common.cuh"
 
 namespace codec {
 
-// Weight planes of one contraction for the tensor cores: B = W^T in K-major
-// [N][K] fp16 hi and lo planes, scaled by 2^wexp before the split.
+// Weight planes of one contraction for the tensor cores: B = W^T, K-major
+// [N][K], scaled by 2^e (max |W 2^e| in [1, 2)) and split into fp16 hi and lo.
 struct TcWeights {
+    alignas(64) CUtensorMap map_hi;
+    alignas(64) CUtensorMap map_lo;
     void* hi = nullptr;      // __half [N][K]
     void* lo = nullptr;
-    float unscale = 1.f;     // 2^-wexp, applied to the accumulator
+    float unscale = 1.f;     // 2^-e, applied to the accumulator
+    int BN = 0;              // N tile (multiple of 16, <= 256)
+    int n_tiles = 0;
 };
 
-// Per-state scratch for the A-operand planes (Snake applied, split into
-// fp16 hi and lo), big enough for the widest input of any contraction.
+// Per-state scratch for the A-operand planes (Snake applied, split into fp16
+// hi and lo), big enough for the widest input of any contraction, plus the
+// sticky flag a kernel sets when one of its bounded waits expires.
 struct TcScratch {
     void* a_hi = nullptr;
     void* a_lo = nullptr;
     size_t elems = 0;
+    int* err = nullptr;
 };
 
 bool tc_eligible(int Cin, int N);
 bool tc_pack_weights(const float* wkn, int ntaps, int Cin, int N, TcWeights* out,
                      std::vector<void*>& allocs);
 bool tc_scratch_alloc(TcScratch* s, size_t elems, std::vector<void*>& allocs);
-cudaError_t launch_gemm_tc(const GemmArgs& a, const TcWeights& w, PlanView plan, int n_row_tiles,
-                           TcScratch* scratch, cudaStream_t s, int* launches);
+
+// A-operand planes of rows x Cin: hi = fp16(a), lo = fp16(a - hi) with
+// a = Snake(x) when alpha is given, else x.
+cudaError_t launch_tc_prep(const float* x, const float* alpha, const float* inv_alpha, long long rows, int Cin,
+                           TcScratch* scratch, cudaStream_t s);
+// The GEMM over the planes prepared by launch_tc_prep (a_rows rows).
+cudaError_t launch_tc_gemm(const GemmArgs& a, const TcWeights& w, PlanView plan, int n_row_tiles,
+                           const TcScratch* scratch, long long a_rows, int num_sms, cudaStream_t s);
 
 }  // namespace codec
