@@ -62,7 +62,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--decoder", choices=["qwen3", "tiny"], default="qwen3")
-    ap.add_argument("--precision", choices=["fp32", "fp16x3"], default="fp32")
+    ap.add_argument("--precision", choices=["fp32", "fp16x3"], default="fp16x3")
     ap.add_argument("--streams", type=int, default=64)
     ap.add_argument("--frames", type=int, default=250)
     ap.add_argument("--chunk", type=int, default=25)

@@ -17,7 +17,7 @@ from streaming_tts_vocoder_gb300.synthetic import (make_codes, make_weights, pac
 
 pytestmark = pytest.mark.gpu
 
-PRECISIONS = [C.PRECISION_FP32]
+PRECISIONS = [C.PRECISION_FP32, C.PRECISION_FP16X3]
 
 
 @pytest.fixture(scope="module")
