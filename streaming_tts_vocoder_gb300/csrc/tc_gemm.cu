@@ -12,22 +12,28 @@
 // by more than 10x on random weights.  The tensor core adds each MMA's
 // products to the fp32 accumulator with truncation, not rounding; over the
 // hundreds of k-steps of a long conv that bias alone costs about 20x in the
-// output error.  The hi*hi products therefore go to one TMEM accumulator and
-// the two cross terms (about 2^-11 of its size, so their truncation is
-// negligible) to a second one; the epilogue adds the two with a rounded fp32
-// add.  That keeps the decoder's output error well inside the bound.
+// output error.  So the hi*hi products go to one TMEM accumulator and the two
+// cross terms (about 2^-11 of its size) to a second one, and a tile's k-loop
+// is cut into chunks of 16 k-steps: each chunk starts from a zero
+// accumulator, and the epilogue folds every chunk into per-row fp32 sums in
+// registers with rounded adds, in chunk order.  The truncation then acts on
+// 16-step partial sums only, and the GEMM is about as accurate as an fp32 FMA
+// loop.
 //
 // Implicit GEMM: output row t of stream segment b takes, for tap j, the
 // input row base(b) + t - shift_j, so a k-block is one TMA box at a shifted
 // row coordinate; the [history | chunk] rows in front of each segment supply
 // the causal left context, and a tile never crosses a stream segment.
 //
-// Roles (192 threads, one CTA per SM, persistent over tiles):
+// Roles (320 threads, one CTA per SM, persistent over tiles):
 //   warp 0     TMA producer (one thread)
 //   warp 1     TMEM allocator and MMA issuer (one thread)
-//   warps 2-5  epilogue, warp w reading TMEM lanes 32 (w % 4) .. +31
-// Two TMEM accumulator pairs (4 x at most 128 columns) let the epilogue of one
-// tile run under the main loop of the next.  Every wait is bounded: when one expires
+//   warps 2-9  epilogue in two groups of four: warp w reads TMEM lanes
+//              32 (w % 4) .. +31, group (w - 2) / 4 takes the even or the odd
+//              32-column slices of the tile
+// Two TMEM buffers, each a (main, cross) accumulator pair of at most 128
+// columns, alternate between chunks, so the epilogue drains one while the MMA
+// fills the other.  Every wait is bounded: when one expires
 // the CTA raises a flag, stops, drains its copies and MMAs, frees TMEM and
 // returns.
 #include <cudaTypedefs.h>
@@ -46,12 +52,14 @@ namespace {
 
 constexpr int kBM = 128;
 constexpr int kBK = 32;              // fp16 per k-block: 64-byte rows, 64-byte swizzle
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;             // 10 warps
+constexpr int kEpiWarps = 8;
 constexpr int kMaxBN = 128;            // 2 buffers x (main + cross) x 128 columns = 512
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSpinLimit = 1u << 25;
 constexpr int kSmemBudget = 220 * 1024;
 constexpr uint32_t kAPlaneBytes = kBM * kBK * 2;   // 8 KB
+constexpr int kChunkKb = 8;          // 8 k-blocks = 256 of K = 16 MMA k-steps per TMEM chunk
 
 struct TcParams {
     int n_row_tiles;
@@ -66,6 +74,7 @@ struct TcParams {
     uint32_t idesc;
     uint32_t cross_off;   // TMEM column of the cross-term accumulator within a buffer
     uint32_t buf_cols;    // TMEM columns per buffer (main + cross)
+    int chunk_kb;         // k-blocks accumulated in TMEM before the epilogue folds them in
     float unscale;
     int* err;
 };
@@ -181,6 +190,20 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v)
     for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[i]);
 }
 
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v)
+{
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; i++) v[i] = __uint_as_float(r[i]);
+}
+
 // Instruction descriptor of kind::f16: D f32, A and B f16, both K-major.
 constexpr uint32_t idesc_f16(int M, int N)
 {
@@ -210,41 +233,46 @@ __device__ __forceinline__ void epi_store32(const GemmArgs& a, const PlanView& p
     const bool vec = count == 32 && a.epi != EPI_QKV && ((out_row * a.out_C + n0) & 3) == 0 &&
                      (a.bias == nullptr || (n0 % a.bias_mod) + 32 <= a.bias_mod);
     if (!vec) {
-        for (int i = 0; i < count; i++) gemm_store(a, plan, b, t, out_row, n0 + i, v[i] * unscale);
+#pragma unroll
+        for (int i = 0; i < 32; i++)
+            if (i < count) gemm_store(a, plan, b, t, out_row, n0 + i, v[i] * unscale);
         return;
     }
     const long long idx = out_row * a.out_C + n0;
     float4* o4 = reinterpret_cast<float4*>(a.out + idx);
     const float4* r4 = reinterpret_cast<const float4*>(a.res ? a.res + idx : a.out + idx);
     const float* bias = a.bias ? a.bias + (n0 % a.bias_mod) : nullptr;
+    const bool has_res = a.epi == EPI_RESID || a.epi == EPI_MRF_FIRST || a.epi == EPI_MRF_ADD || a.epi == EPI_MRF_LAST;
+    const bool has_old = a.epi == EPI_MRF_ADD || a.epi == EPI_MRF_LAST;
 #pragma unroll
-    for (int q = 0; q < 8; q++) {
-        float x[4];
+    for (int half = 0; half < 2; half++) {
+        // loads of this half first (memory-level parallelism), then the math
+        float4 r[4], o[4];
 #pragma unroll
-        for (int i = 0; i < 4; i++) x[i] = v[4 * q + i] * unscale + (bias ? __ldg(bias + 4 * q + i) : 0.f);
-        float4 y;
-        switch (a.epi) {
-        case EPI_STORE: y = make_float4(x[0], x[1], x[2], x[3]); break;
-        case EPI_GELU: y = make_float4(gelu_f(x[0]), gelu_f(x[1]), gelu_f(x[2]), gelu_f(x[3])); break;
-        case EPI_RESID:
-        case EPI_MRF_FIRST: {
-            const float4 r = r4[q];
-            y = make_float4(r.x + x[0], r.y + x[1], r.z + x[2], r.w + x[3]);
-            break;
+        for (int q = 0; q < 4; q++) {
+            if (has_res) r[q] = r4[half * 4 + q];
+            if (has_old) o[q] = o4[half * 4 + q];
         }
-        case EPI_MRF_ADD: {
-            const float4 r = r4[q], o = o4[q];
-            y = make_float4(o.x + (r.x + x[0]), o.y + (r.y + x[1]), o.z + (r.z + x[2]), o.w + (r.w + x[3]));
-            break;
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            const int i0 = half * 16 + 4 * q;
+            float y[4];
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+                y[e] = v[i0 + e] * unscale + (bias ? __ldg(bias + i0 + e) : 0.f);
+                if (a.epi == EPI_GELU) y[e] = gelu_f(y[e]);
+            }
+            if (has_res) {
+                y[0] = r[q].x + y[0]; y[1] = r[q].y + y[1]; y[2] = r[q].z + y[2]; y[3] = r[q].w + y[3];
+            }
+            if (has_old) {
+                y[0] = o[q].x + y[0]; y[1] = o[q].y + y[1]; y[2] = o[q].z + y[2]; y[3] = o[q].w + y[3];
+                if (a.epi == EPI_MRF_LAST) {
+                    y[0] *= a.scale; y[1] *= a.scale; y[2] *= a.scale; y[3] *= a.scale;
+                }
+            }
+            o4[half * 4 + q] = make_float4(y[0], y[1], y[2], y[3]);
         }
-        default: {  // EPI_MRF_LAST
-            const float4 r = r4[q], o = o4[q];
-            y = make_float4((o.x + (r.x + x[0])) * a.scale, (o.y + (r.y + x[1])) * a.scale,
-                            (o.z + (r.z + x[2])) * a.scale, (o.w + (r.w + x[3])) * a.scale);
-            break;
-        }
-        }
-        o4[q] = y;
     }
 }
 
@@ -272,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(
         }
         for (int i = 0; i < 2; i++) {
             mbar_init(&tfull[i], 1);
-            mbar_init(&tempty[i], 4);
+            mbar_init(&tempty[i], kEpiWarps);
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -322,37 +350,44 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(
     } else if (warp == 1) {
         if (lane == 0) {
             // --------------------------------------------------- MMA issue --
-            int it = 0, acc_it = 0;
+            // The k-loop of a tile is cut into chunks of chunk_kb k-blocks; each
+            // chunk accumulates from zero into one of the two TMEM buffers,
+            // which the epilogue folds into rounded fp32 sums while the next
+            // chunk runs.
+            int it = 0, chunk_it = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x, acc_it++) {
-                const int acc = acc_it & 1;
-                const uint32_t aph = (uint32_t)(acc_it >> 1) & 1u;
-                if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag)) break;
-                tc_fence_after();
-                const uint32_t d_main = tmem_base + (uint32_t)acc * p.buf_cols;
-                const uint32_t d_cross = d_main + p.cross_off;
-                for (int kb = 0; kb < p.nkb; kb++, it++) {
-                    const int s = it % p.stages;
-                    const uint32_t ph = (uint32_t)(it / p.stages) & 1u;
-                    if (!mbar_wait(&full[s], ph, abort_flag)) { ok = false; break; }
+            for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+                for (int kb0 = 0; kb0 < p.nkb && ok; kb0 += p.chunk_kb, chunk_it++) {
+                    const int acc = chunk_it & 1;
+                    const uint32_t aph = (uint32_t)(chunk_it >> 1) & 1u;
+                    if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t sa = smem_u32(smem + (size_t)s * p.stage_bytes);
-                    const uint64_t dah = sdesc_sw64(sa);
-                    const uint64_t dal = sdesc_sw64(sa + kAPlaneBytes);
-                    const uint64_t dbh = sdesc_sw64(sa + 2 * kAPlaneBytes);
-                    const uint64_t dbl = sdesc_sw64(sa + 2 * kAPlaneBytes + p.b_stride);
+                    const uint32_t d_main = tmem_base + (uint32_t)acc * p.buf_cols;
+                    const uint32_t d_cross = d_main + p.cross_off;
+                    const int kb1 = min(p.nkb, kb0 + p.chunk_kb);
+                    for (int kb = kb0; kb < kb1; kb++, it++) {
+                        const int s = it % p.stages;
+                        const uint32_t ph = (uint32_t)(it / p.stages) & 1u;
+                        if (!mbar_wait(&full[s], ph, abort_flag)) { ok = false; break; }
+                        tc_fence_after();
+                        const uint32_t sa = smem_u32(smem + (size_t)s * p.stage_bytes);
+                        const uint64_t dah = sdesc_sw64(sa);
+                        const uint64_t dal = sdesc_sw64(sa + kAPlaneBytes);
+                        const uint64_t dbh = sdesc_sw64(sa + 2 * kAPlaneBytes);
+                        const uint64_t dbl = sdesc_sw64(sa + 2 * kAPlaneBytes + p.b_stride);
 #pragma unroll
-                    for (int k = 0; k < kBK / 16; k++) {
-                        const uint64_t o = (uint64_t)((k * 32) >> 4);
-                        const uint32_t accum = (kb | k) != 0 ? 1u : 0u;
-                        mma_f16(d_main, dah + o, dbh + o, p.idesc, accum);
-                        mma_f16(d_cross, dah + o, dbl + o, p.idesc, accum);
-                        mma_f16(d_cross, dal + o, dbh + o, p.idesc, 1u);
+                        for (int k = 0; k < kBK / 16; k++) {
+                            const uint64_t o = (uint64_t)((k * 32) >> 4);
+                            const uint32_t accum = (kb != kb0 || k != 0) ? 1u : 0u;
+                            mma_f16(d_main, dah + o, dbh + o, p.idesc, accum);
+                            mma_f16(d_cross, dah + o, dbl + o, p.idesc, accum);
+                            mma_f16(d_cross, dal + o, dbh + o, p.idesc, 1u);
+                        }
+                        mma_commit(&empty[s]);
                     }
-                    mma_commit(&empty[s]);
+                    if (!ok) break;
+                    mma_commit(&tfull[acc]);
                 }
-                if (!ok) break;
-                mma_commit(&tfull[acc]);
             }
             // all issued MMAs complete before TMEM is released
             mma_commit(drain);
@@ -360,39 +395,66 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(
         }
     } else {
         // ------------------------------------------------------ epilogue --
+        // Thread (warp w, lane l) owns output row 32 (w % 4) + l of the tile and
+        // keeps the sums of its group's (at most 2 x 32) columns in registers
+        // across the chunks.
         const int q = warp & 3;
+        const int eg = (warp - 2) >> 2;
         const int m = q * 32 + lane;
-        int acc_it = 0;
-        for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, acc_it++) {
-            const int acc = acc_it & 1;
-            const uint32_t aph = (uint32_t)(acc_it >> 1) & 1u;
-            // one lane polls, the warp follows its verdict (tcgen05.ld needs a converged warp)
-            int ok = 1;
-            if (lane == 0) ok = mbar_wait(&tfull[acc], aph, abort_flag) ? 1 : 0;
-            ok = __shfl_sync(0xffffffffu, ok, 0);
+        int chunk_it = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+            float sum[64];
+#pragma unroll
+            for (int i = 0; i < 64; i++) sum[i] = 0.f;
+            for (int kb0 = 0; kb0 < p.nkb; kb0 += p.chunk_kb, chunk_it++) {
+                const int acc = chunk_it & 1;
+                const uint32_t aph = (uint32_t)(chunk_it >> 1) & 1u;
+                // one lane polls, the warp follows its verdict (tcgen05.ld needs a converged warp)
+                int w_ok = 1;
+                if (lane == 0) w_ok = mbar_wait(&tfull[acc], aph, abort_flag) ? 1 : 0;
+                w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
+                if (!w_ok) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)acc * p.buf_cols;
+#pragma unroll
+                for (int h = 0; h < 2; h++) {
+                    const int c = (2 * h + eg) * 32;
+                    if (c < p.BN) {
+#pragma unroll
+                        for (int g = 0; g < 2; g++) {
+                            float v[16], x[16];
+                            tmem_ld16(lane_base + (uint32_t)(c + 16 * g), v);
+                            tmem_ld16(lane_base + p.cross_off + (uint32_t)(c + 16 * g), x);
+#pragma unroll
+                            for (int i = 0; i < 16; i++)
+                                sum[h * 32 + 16 * g + i] = __fadd_rn(sum[h * 32 + 16 * g + i], __fadd_rn(v[i], x[i]));
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tempty[acc]);
+            }
             if (!ok) break;
-            tc_fence_after();
             const TileRows tr = tile_rows(a, plan, tile / p.n_tiles_n);
             const int n0 = (tile % p.n_tiles_n) * p.BN;
-            const bool valid = m < tr.nrows;
-            const int t = tr.t0 + m;
-            const long long out_row = seg_base(a.out_l, plan.cf, tr.b) + (long long)t * a.out_step;
-            const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)acc * p.buf_cols;
-            for (int c = 0; c < p.BN; c += 32) {
-                float v[32], x[32];
-                tmem_ld32(lane_base + (uint32_t)c, v);
-                tmem_ld32(lane_base + p.cross_off + (uint32_t)c, x);
+            if (m < tr.nrows) {
+                const int t = tr.t0 + m;
+                const long long out_row = seg_base(a.out_l, plan.cf, tr.b) + (long long)t * a.out_step;
 #pragma unroll
-                for (int i = 0; i < 32; i++) v[i] = __fadd_rn(v[i], x[i]);
-                if (valid) {
-                    int count = min(32, p.BN - c);
-                    count = min(count, a.N - (n0 + c));
-                    if (count > 0) epi_store32(a, plan, tr.b, t, out_row, n0 + c, count, v, p.unscale);
+                for (int h = 0; h < 2; h++) {
+                    const int c = (2 * h + eg) * 32;
+                    if (c < p.BN) {
+                        int count = min(32, p.BN - c);
+                        count = min(count, a.N - (n0 + c));
+                        float v[32];
+#pragma unroll
+                        for (int i = 0; i < 32; i++) v[i] = sum[h * 32 + i];
+                        if (count > 0) epi_store32(a, plan, tr.b, t, out_row, n0 + c, count, v, p.unscale);
+                    }
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&tempty[acc]);
         }
     }
 
@@ -406,7 +468,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(
     }
     if (threadIdx.x == 0 && *abort_flag) atomicExch(p.err, 1);
 }
-
 // hi = fp16(a), lo = fp16(a - hi), a = Snake(x) or x; four channels per thread.
 __global__ void tc_prep_kernel(const float4* __restrict__ x, const float* __restrict__ alpha,
                                const float* __restrict__ inv_alpha, long long n4, int cin4,
@@ -551,6 +612,7 @@ cudaError_t launch_tc_gemm(const GemmArgs& a, const TcWeights& w, PlanView plan,
     p.idesc = idesc_f16(kBM, w.BN);
     p.cross_off = (uint32_t)((w.BN + 31) / 32 * 32);
     p.buf_cols = 2 * p.cross_off;
+    p.chunk_kb = kChunkKb;
     p.unscale = w.unscale;
     p.err = scratch->err;
     const size_t smem = (size_t)p.stages * p.stage_bytes + extra;

@@ -13,12 +13,12 @@ namespace codec {
 // Weight planes of one contraction for the tensor cores: B = W^T, K-major
 // [N][K], scaled by 2^e (max |W 2^e| in [1, 2)) and split into fp16 hi and lo.
 struct TcWeights {
-    alignas(64) CUtensorMap map_hi;
-    alignas(64) CUtensorMap map_lo;
+    CUtensorMap map_hi;          // CUtensorMap is itself 64-byte aligned
+    CUtensorMap map_lo;
     void* hi = nullptr;      // __half [N][K]
     void* lo = nullptr;
     float unscale = 1.f;     // 2^-e, applied to the accumulator
-    int BN = 0;              // N tile (multiple of 16, <= 256)
+    int BN = 0;              // N tile (multiple of 16, <= 128)
     int n_tiles = 0;
 };
 
