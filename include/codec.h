@@ -238,8 +238,21 @@ typedef struct codec_kernel_stats {
 
 CODEC_API codec_status codec_profile_begin(codec_state_t* state, int32_t max_records);
 /* out: host [CODEC_KERNEL_KINDS]; entry i describes kind i.  Records beyond
- * max_records are dropped (launches still run). */
+ * max_records are dropped (launches still run).  The per-launch records stay
+ * readable with codec_profile_launches until the next codec_profile_begin. */
 CODEC_API codec_status codec_profile_end(codec_state_t* state, codec_kernel_stats* out, void* stream);
+
+typedef struct codec_launch_record {
+    int32_t kind;            /* codec_kernel_kind */
+    int32_t reserved;
+    double ms, flops, bytes;
+} codec_launch_record;
+
+/* The records of the last profiled interval, in launch order: out host
+ * [max_out]; *n_out receives the number written.  Call after
+ * codec_profile_end. */
+CODEC_API codec_status codec_profile_launches(codec_state_t* state, codec_launch_record* out, int32_t max_out,
+                                              int32_t* n_out);
 
 /* Static description of a status code. */
 CODEC_API const char* codec_status_string(codec_status status);

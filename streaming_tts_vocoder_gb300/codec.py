@@ -57,6 +57,11 @@ class KernelStatsC(ctypes.Structure):
                 ("flops", ctypes.c_double), ("bytes", ctypes.c_double)]
 
 
+class LaunchRecordC(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("reserved", ctypes.c_int32), ("ms", ctypes.c_double),
+                ("flops", ctypes.c_double), ("bytes", ctypes.c_double)]
+
+
 class StreamInfoC(ctypes.Structure):
     _fields_ = [("frames_decoded", ctypes.c_int64), ("error_bits", ctypes.c_uint32),
                 ("reserved", ctypes.c_int32)]
@@ -93,6 +98,7 @@ def _lib():
             "codec_status_string": (ctypes.c_char_p, [i32]),
             "codec_profile_begin": (i32, [_P, i32]),
             "codec_profile_end": (i32, [_P, ctypes.POINTER(KernelStatsC), _P]),
+            "codec_profile_launches": (i32, [_P, ctypes.POINTER(LaunchRecordC), i32, ctypes.POINTER(i32)]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(l, name)
@@ -263,6 +269,13 @@ class CodecState:
         _check(_lib().codec_profile_end(self._h, arr, _stream_handle(stream)), "codec_profile_end")
         return {KERNEL_KINDS[i]: dict(launches=arr[i].launches, ms=arr[i].ms, flops=arr[i].flops,
                                       bytes=arr[i].bytes) for i in range(len(KERNEL_KINDS))}
+
+    def profile_launches(self, max_out: int = 1 << 20) -> list:
+        """Per-launch (kind, ms, flops, bytes) of the last profiled interval, in order."""
+        arr = (LaunchRecordC * max_out)()
+        n = ctypes.c_int32()
+        _check(_lib().codec_profile_launches(self._h, arr, max_out, ctypes.byref(n)), "codec_profile_launches")
+        return [(KERNEL_KINDS[arr[i].kind], arr[i].ms, arr[i].flops, arr[i].bytes) for i in range(n.value)]
 
     @property
     def last_launches(self) -> int:

@@ -49,6 +49,7 @@ bool debug_sync()
 struct ProfRec {
     int kind;
     double flops, bytes;
+    double ms;
 };
 
 int next_pow2(int x)
@@ -102,7 +103,7 @@ struct codec_state_s {
     TcScratch tc_scratch;
     // plan: device copy and a ring of page-locked host staging copies
     int plan_ints = 0;
-    int off_pos0 = 0, off_cf = 0, off_slot = 0, off_bidx = 0, off_tc64 = 0, off_tc128 = 0;
+    int off_pos0 = 0, off_cf = 0, off_slot = 0, off_bidx = 0, off_tc64 = 0, off_tc128 = 0, off_q16 = 0;
     int* plan_d = nullptr;
     static constexpr int kPlanRing = 8;
     int* plan_h[kPlanRing] = {};
@@ -117,7 +118,7 @@ struct codec_state_s {
     double hist_floats_per_slot = 0.0;
     // per-launch timing (codec_profile_begin / _end)
     bool prof_on = false;
-    int prof_n = 0, prof_max = 0;
+    int prof_n = 0, prof_max = 0, prof_done = 0;
     std::vector<cudaEvent_t> prof_ev;
     std::vector<ProfRec> prof_rec;
     std::vector<void*> allocs;
@@ -132,7 +133,7 @@ bool cfg_valid(const codec_config* c)
     auto m4 = [](int v) { return v > 0 && v % 4 == 0; };
     if (c->Q < 1 || c->Q > 64 || c->V < 1 || !m4(c->E)) return false;
     if (c->pre_k < 1 || c->pre_k > kMaxTaps) return false;
-    if (!m4(c->d) || c->heads < 1 || c->d % c->heads || c->d / c->heads > 256) return false;
+    if (!m4(c->d) || c->heads < 1 || c->d % c->heads || c->d / c->heads > 128) return false;
     if (!m4(c->ffn) || c->layers < 0 || c->layers > 64 || c->window < 1 || c->window > 128) return false;
     if (c->n_up < 1 || c->n_up > 4 || c->up_s < 1 || c->up_k != 2 * c->up_s) return false;
     for (int u = 0; u < c->n_up; u++) if (!m4(c->up_ch[u])) return false;
@@ -497,7 +498,8 @@ codec_status codec_state_create(codec_t* c, int32_t n_streams, codec_state_t** o
     s->off_bidx = s->off_slot + S;
     s->off_tc64 = s->off_bidx + S;
     s->off_tc128 = s->off_tc64 + c->n_levels * (S + 1);
-    s->plan_ints = s->off_tc128 + c->n_levels * (S + 1);
+    s->off_q16 = s->off_tc128 + c->n_levels * (S + 1);
+    s->plan_ints = s->off_q16 + (S + 1);
     s->plan_d = dev_alloc<int>(A, s->plan_ints, st, true);
     for (int i = 0; i < codec_state_s::kPlanRing && st == CODEC_OK; i++) {
         if (cudaMallocHost(&s->plan_h[i], sizeof(int) * s->plan_ints) != cudaSuccess) st = CODEC_ERR_OOM;
@@ -571,7 +573,8 @@ codec_status codec_profile_begin(codec_state_t* s, int32_t max_records)
         if (cudaEventCreate(&e) != cudaSuccess) return CODEC_ERR_CUDA;
         s->prof_ev.push_back(e);
     }
-    s->prof_rec.assign(max_records, ProfRec{0, 0.0, 0.0});
+    s->prof_rec.assign(max_records, ProfRec{0, 0.0, 0.0, 0.0});
+    s->prof_done = 0;
     s->prof_max = max_records;
     s->prof_n = 0;
     s->prof_on = true;
@@ -592,8 +595,22 @@ codec_status codec_profile_end(codec_state_t* s, codec_kernel_stats* out, void* 
         o.ms += ms;
         o.flops += s->prof_rec[i].flops;
         o.bytes += s->prof_rec[i].bytes;
+        s->prof_rec[i].ms = ms;
     }
+    s->prof_done = s->prof_n;
     s->prof_n = 0;
+    return CODEC_OK;
+}
+
+codec_status codec_profile_launches(codec_state_t* s, codec_launch_record* out, int32_t max_out, int32_t* n_out)
+{
+    if (!s || !out || !n_out) return CODEC_ERR_NULL;
+    if (max_out < 0) return CODEC_ERR_ARG;
+    const int n = std::min(max_out, s->prof_done);
+    for (int i = 0; i < n; i++)
+        out[i] = codec_launch_record{s->prof_rec[i].kind, 0, s->prof_rec[i].ms, s->prof_rec[i].flops,
+                                     s->prof_rec[i].bytes};
+    *n_out = n;
     return CODEC_OK;
 }
 
@@ -665,6 +682,8 @@ struct Launcher {
     PlanView pv;
     const int* tc64;     // device, [levels][S + 1]
     const int* tc128;
+    const int* q16;                         // device, [S + 1] blocks of 16 frames
+    int nq16 = 0;
     std::vector<int> ntiles64, ntiles128;   // per level
     std::vector<int> slot_h, n_h;           // host copies of the compacted batch
     long long frames = 0;                   // frames in this call
@@ -685,7 +704,7 @@ struct Launcher {
         launches++;
         if (rec) {
             cudaEventRecord(s->prof_ev[2 * s->prof_n + 1], cs);
-            s->prof_rec[s->prof_n] = ProfRec{kind, flops, bytes};
+            s->prof_rec[s->prof_n] = ProfRec{kind, flops, bytes, 0.0};
             s->prof_n++;
         }
         if (e != cudaSuccess) { err = e; where = what; }
@@ -803,6 +822,12 @@ codec_status plan_call(codec_state_t* s, const int32_t* n_frames, const int32_t*
         L.ntiles64[lvl] = t64[Bc];
         L.ntiles128[lvl] = t128[Bc];
     }
+    {
+        int* q16 = P + s->off_q16;
+        q16[0] = 0;
+        for (int b = 0; b < Bc; b++) q16[b + 1] = q16[b] + (cf[b + 1] - cf[b] + 15) / 16;
+        L.nq16 = q16[Bc];
+    }
     if (cudaMemcpyAsync(s->plan_d, P, sizeof(int) * s->plan_ints, cudaMemcpyHostToDevice, cs) != cudaSuccess)
         return CODEC_ERR_CUDA;
     if (cudaEventRecord(s->plan_ev[i], cs) != cudaSuccess) return CODEC_ERR_CUDA;
@@ -811,6 +836,7 @@ codec_status plan_call(codec_state_t* s, const int32_t* n_frames, const int32_t*
                     reinterpret_cast<const long long*>(D + s->off_pos0), D + s->off_bidx};
     L.tc64 = D + s->off_tc64;
     L.tc128 = D + s->off_tc128;
+    L.q16 = D + s->off_q16;
     L.frames = total;
     L.Bc = Bc;
     L.slot_h.assign(slot, slot + Bc);
@@ -857,7 +883,7 @@ codec_status decode_impl(codec_state_t* s, const int32_t* codes, const int32_t* 
         const size_t per_layer = (size_t)S * s->R * g.d;
         L.run(CODEC_KERNEL_ATTENTION, attn_flops, attn_bytes, "attention", [&] {
             return launch_swa(s->q, s->o, s->kring + per_layer * l, s->vring + per_layer * l, g.d, g.heads,
-                              g.window, s->R, L.pv, rows0, cs);
+                              g.window, s->R, L.pv, L.q16, L.nq16, cs);
         });
         L.gemm(W.o, s->o, L0d, 0, s->h, L0d, g.d, 1, s->h, EPI_RESID, 1.f, 0, "out-proj");
         L.run(CODEC_KERNEL_RMSNORM, norm_flops, norm_bytes, "rmsnorm 2",

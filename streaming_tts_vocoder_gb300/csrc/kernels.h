@@ -23,8 +23,9 @@ cudaError_t launch_gemm_simt(const GemmArgs& a, PlanView plan, int n_row_tiles, 
 cudaError_t launch_rms_norm(const float* x, Layout xl, const float* g, float eps, float* y, Layout yl,
                             int d, PlanView plan, int total_rows, cudaStream_t s);
 
+// qcum: [B + 1] cumulative blocks of 16 queries per batch entry.
 cudaError_t launch_swa(const float* q, float* o, const float* kring, const float* vring, int d,
-                       int heads, int window, int ring_R, PlanView plan, int total_rows,
+                       int heads, int window, int ring_R, PlanView plan, const int* qcum, int n_qblocks,
                        cudaStream_t s);
 
 cudaError_t launch_final_conv(const float* x, Layout xl, int C, const float* w, const float* bias,

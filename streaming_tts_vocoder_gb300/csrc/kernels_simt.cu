@@ -186,97 +186,132 @@ cudaError_t launch_rms_norm(const float* x, Layout xl, const float* g, float eps
 }
 
 // ---------------------------------------------- sliding-window attention --
-// One warp per (query row, head).  Query at absolute position p attends the
-// keys of positions max(0, p - W + 1) .. p, read from the stream's ring
-// (position p lives in ring row p mod R).  Lane i scores keys lo + i, lo + 32 +
-// i, ...; max and denominator go through a fixed butterfly, the value sum runs
-// over the keys in position order, so a query's result depends only on its
-// position and the keys, never on the chunking (blixt/phonon "Speed" item 7
-// ring; item 11 softmax with max subtraction).
+// A block takes up to 16 consecutive queries of one stream and one head,
+// stages the keys and values of every position they can see (at most
+// 16 + W - 1 rows, read from the stream's ring: position p lives in ring row
+// p mod R) in shared memory, and gives each warp two queries.  Query at
+// absolute position p attends positions max(0, p - W + 1) .. p.  Lane i
+// scores keys lo + i, lo + 32 + i, ...; max and denominator go through a
+// fixed butterfly and the value sum runs over the keys in position order, so
+// a query's result depends only on its position and the keys, never on the
+// chunking (blixt/phonon "Speed" item 7: ring of keys and values; item 11:
+// softmax with max subtraction).
 constexpr int kSwaMaxW = 128;
-constexpr int kSwaMaxDh = 256;
+constexpr int kSwaMaxDh = 128;
+constexpr int kSwaQ = 16;           // queries per block
 constexpr int kSwaWarps = 8;
 
 __global__ void __launch_bounds__(kSwaWarps * 32) swa_kernel(
     const float* __restrict__ q, float* __restrict__ o, const float* __restrict__ kring,
-    const float* __restrict__ vring, int d, int heads, int W, int R, PlanView plan, int total_rows)
+    const float* __restrict__ vring, int d, int heads, int W, int R, PlanView plan,
+    const int* __restrict__ qcum)
 {
-    __shared__ float sp[kSwaWarps][kSwaMaxW];
-    __shared__ float sq[kSwaWarps][kSwaMaxDh];
-    const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int gw = blockIdx.x * kSwaWarps + wib;
-    const int row = gw / heads, h = gw - row * heads;
-    if (row >= total_rows) return;
-    const int b = find_seg(plan.cf, plan.B, row);
-    const int t = row - __ldg(plan.cf + b);
-    const long long pos = __ldg(plan.pos0 + b) + t;
-    const long long lo = pos - W + 1 > 0 ? pos - W + 1 : 0;
-    const int nk = (int)(pos - lo + 1);
+    extern __shared__ float sm[];
     const int dh = d / heads;
-    const float* qr = q + (long long)row * d + h * dh;
-    for (int c = lane; c < dh; c += 32) sq[wib][c] = qr[c];
-    __syncwarp();
-    const float scale = 1.0f / sqrtf((float)dh);
+    const int ld = dh + 1;                              // padded row: conflict-free column reads
+    const int maxk = kSwaQ + W - 1;
+    float* sk = sm;                                     // [maxk][dh + 1]
+    float* sv = sk + maxk * ld;                         // [maxk][dh + 1]
+    float* sq = sv + maxk * ld;                         // [kSwaWarps][dh]
+    float* sp = sq + kSwaWarps * dh;                    // [kSwaWarps][W]
+    const int h = blockIdx.y;
+    const int blk = blockIdx.x;
+    const int b = find_seg(qcum, plan.B, blk);
+    const int n = __ldg(plan.cf + b + 1) - __ldg(plan.cf + b);
+    const int tq0 = (blk - __ldg(qcum + b)) * kSwaQ;
+    const int nq = min(kSwaQ, n - tq0);
+    const long long p0 = __ldg(plan.pos0 + b) + tq0;   // position of the block's first query
+    const long long kstart = p0 - W + 1 > 0 ? p0 - W + 1 : 0;
+    const int nk = (int)(p0 + nq - kstart);             // keys the block's queries can see
     const long long slot_base = (long long)__ldg(plan.slot + b) * R;
-    const float* kb = kring + h * dh;
-    const float* vb = vring + h * dh;
-    float sc[kSwaMaxW / 32];
-    float m = -INFINITY;
-#pragma unroll
-    for (int u = 0; u < kSwaMaxW / 32; u++) {
-        const int i = lane + 32 * u;
-        sc[u] = -INFINITY;
-        if (i < nk) {
-            const float* kr = kb + (slot_base + ((lo + i) & (R - 1))) * d;
-            float dot = 0.f;
-            for (int c = 0; c < dh; c++) dot = fmaf(sq[wib][c], __ldg(kr + c), dot);
-            sc[u] = dot * scale;
-            m = fmaxf(m, sc[u]);
-        }
+    for (int i = threadIdx.x; i < nk * dh; i += blockDim.x) {
+        const int r = i / dh, c = i - r * dh;
+        const long long row = (slot_base + ((kstart + r) & (R - 1))) * d + h * dh + c;
+        sk[r * ld + c] = __ldg(kring + row);
+        sv[r * ld + c] = __ldg(vring + row);
     }
+    __syncthreads();
+    const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const float scale = 1.0f / sqrtf((float)dh);
+    const long long row0 = (long long)__ldg(plan.cf + b) + tq0;
+    for (int qi = wib; qi < nq; qi += kSwaWarps) {
+        const long long pos = p0 + qi;
+        const long long lo = pos - W + 1 > 0 ? pos - W + 1 : 0;
+        const int nkq = (int)(pos - lo + 1);
+        const int off = (int)(lo - kstart);             // smem row of key lo
+        const float* qr = q + (row0 + qi) * d + h * dh;
+        for (int c = lane; c < dh; c += 32) sq[wib * dh + c] = qr[c];
+        __syncwarp();
+        float sc[kSwaMaxW / 32];
+        float m = -INFINITY;
 #pragma unroll
-    for (int off = 16; off; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-    float z = 0.f;
-#pragma unroll
-    for (int u = 0; u < kSwaMaxW / 32; u++) {
-        const int i = lane + 32 * u;
-        if (i < nk) {
-            const float p = expf(sc[u] - m);
-            sp[wib][i] = p;
-            z += p;
+        for (int u = 0; u < kSwaMaxW / 32; u++) {
+            const int i = lane + 32 * u;
+            sc[u] = -INFINITY;
+            if (i < nkq) {
+                const float* kr = sk + (off + i) * ld;
+                float dot = 0.f;
+                for (int c = 0; c < dh; c++) dot = fmaf(sq[wib * dh + c], kr[c], dot);
+                sc[u] = dot * scale;
+                m = fmaxf(m, sc[u]);
+            }
         }
-    }
 #pragma unroll
-    for (int off = 16; off; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
-    __syncwarp();
-    const float inv_z = 1.0f / z;
-    for (int c = lane; c < dh; c += 32) {
-        float acc = 0.f;
-        for (int i = 0; i < nk; i++)
-            acc = fmaf(sp[wib][i], __ldg(vb + (slot_base + ((lo + i) & (R - 1))) * d + c), acc);
-        o[(long long)row * d + h * dh + c] = acc * inv_z;
+        for (int sh = 16; sh; sh >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, sh));
+        float z = 0.f;
+#pragma unroll
+        for (int u = 0; u < kSwaMaxW / 32; u++) {
+            const int i = lane + 32 * u;
+            if (i < nkq) {
+                const float pe = expf(sc[u] - m);
+                sp[wib * W + i] = pe;
+                z += pe;
+            }
+        }
+#pragma unroll
+        for (int sh = 16; sh; sh >>= 1) z += __shfl_xor_sync(0xffffffffu, z, sh);
+        __syncwarp();
+        const float inv_z = 1.0f / z;
+        for (int c = lane; c < dh; c += 32) {
+            float acc = 0.f;
+            for (int i = 0; i < nkq; i++) acc = fmaf(sp[wib * W + i], sv[(off + i) * ld + c], acc);
+            o[(row0 + qi) * d + h * dh + c] = acc * inv_z;
+        }
+        __syncwarp();
     }
 }
 
 cudaError_t launch_swa(const float* q, float* o, const float* kring, const float* vring, int d,
-                       int heads, int window, int ring_R, PlanView plan, int total_rows,
+                       int heads, int window, int ring_R, PlanView plan, const int* qcum, int n_qblocks,
                        cudaStream_t s)
 {
-    if (total_rows <= 0) return cudaSuccess;
-    const long long warps = (long long)total_rows * heads;
-    swa_kernel<<<(unsigned)((warps + kSwaWarps - 1) / kSwaWarps), kSwaWarps * 32, 0, s>>>(
-        q, o, kring, vring, d, heads, window, ring_R, plan, total_rows);
+    if (n_qblocks <= 0) return cudaSuccess;
+    const int dh = d / heads;
+    if (dh > kSwaMaxDh || window > kSwaMaxW) return cudaErrorInvalidValue;
+    const int maxk = kSwaQ + window - 1;
+    const size_t smem = sizeof(float) * (2 * (size_t)maxk * (dh + 1) + (size_t)kSwaWarps * dh + (size_t)kSwaWarps * window);
+    static size_t configured = 0;
+    if (smem > 48 * 1024 && smem > configured) {
+        cudaError_t e = cudaFuncSetAttribute(swa_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        configured = smem;
+    }
+    swa_kernel<<<dim3(n_qblocks, heads), kSwaWarps * 32, smem, s>>>(q, o, kring, vring, d, heads, window, ring_R,
+                                                                    plan, qcum);
     return cudaGetLastError();
 }
 
 // ------------------------------------------------ final Snake-conv-tanh --
-// y[t] = tanh(b + sum_j sum_c w[j][c] snake(x[t - (k-1) + j][c])), C -> 1.
-// A 128-row tile plus its k-1 history rows is staged in shared memory with
-// Snake applied once per element (row stride C + 1 against bank conflicts);
-// each thread then produces one sample.  Bandwidth-bound: one input row in,
-// one sample out (blixt/phonon "Open work": a direct kernel for the last
-// convolution with 1 output channel).
+// y[t] = tanh(b + sum_j p_j[t - (k-1) + j]), p_j[r] = sum_c w[j][c] snake(x[r][c]),
+// C -> 1.  One thread per input row computes that row's k partial dot
+// products (its channels read once, Snake applied once per element) into
+// shared memory; then one thread per output row sums its k partials in tap
+// order.  A block covers 128 output rows and the k-1 history rows before
+// them.  Bandwidth-bound: one input row in, one sample out (blixt/phonon
+// "Open work": a direct kernel for the last convolution with 1 output
+// channel).
 constexpr int kFinalTile = 128;
+constexpr int kFinalMaxK = 16;
 
 __global__ void __launch_bounds__(kFinalTile) final_conv_kernel(
     const float* __restrict__ x, Layout xl, int C, const float* __restrict__ w,
@@ -286,34 +321,51 @@ __global__ void __launch_bounds__(kFinalTile) final_conv_kernel(
     const int* __restrict__ tcum)
 {
     extern __shared__ float sm[];
-    const int ld = C + 1;
-    float* sa = sm;                                   // [kFinalTile + k - 1][C + 1]
-    float* sw = sm + (kFinalTile + k - 1) * ld;       // [k][C]
+    float* sw = sm;                                   // [k][C] weights
+    float* sa = sm + k * C;                           // [C] alpha, [C] 1/alpha
+    float* sp = sa + 2 * C;                           // [kFinalTile + k - 1][k] partials
     const int tile = blockIdx.x;
     const int b = find_seg(tcum, plan.B, tile);
     const int seg_rows = (__ldg(plan.cf + b + 1) - __ldg(plan.cf + b)) * xl.r;
     const int t0 = (tile - __ldg(tcum + b)) * kFinalTile;
     const int nrows = min(kFinalTile, seg_rows - t0);
     const long long base = seg_base(xl, plan.cf, b) + t0 - (k - 1);
-    const int rows = nrows + k - 1;
-    for (int i = threadIdx.x; i < rows * C; i += blockDim.x) {
-        const int r = i / C, c = i - r * C;
-        sa[r * ld + c] = snake_f(__ldg(x + (base + r) * C + c), __ldg(alpha + c), __ldg(inv_alpha + c));
-    }
     for (int i = threadIdx.x; i < k * C; i += blockDim.x) sw[i] = __ldg(w + i);
+    for (int i = threadIdx.x; i < C; i += blockDim.x) {
+        sa[i] = __ldg(alpha + i);
+        sa[C + i] = __ldg(inv_alpha + i);
+    }
+    __syncthreads();
+    const int rows = nrows + k - 1;
+    for (int r = threadIdx.x; r < rows; r += blockDim.x) {
+        float part[kFinalMaxK];
+#pragma unroll
+        for (int j = 0; j < kFinalMaxK; j++) part[j] = 0.f;
+        const float4* xr = reinterpret_cast<const float4*>(x + (base + r) * C);
+        for (int c4 = 0; c4 < (C >> 2); c4++) {
+            const float4 v = __ldg(xr + c4);
+            const float e[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int u = 0; u < 4; u++) {
+                const int c = 4 * c4 + u;
+                const float s = snake_f(e[u], sa[c], sa[C + c]);
+#pragma unroll
+                for (int j = 0; j < kFinalMaxK; j++)
+                    if (j < k) part[j] = fmaf(sw[j * C + c], s, part[j]);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kFinalMaxK; j++)
+            if (j < k) sp[r * k + j] = part[j];
+    }
     __syncthreads();
     const int m = threadIdx.x;
     if (m < nrows) {
-        float acc = 0.f;
-        for (int j = 0; j < k; j++) {
-            const float* ar = sa + (m + j) * ld;
-            const float* wr = sw + j * C;
-            for (int c = 0; c < C; c++) acc = fmaf(wr[c], ar[c], acc);
-        }
-        const float y = acc + __ldg(bias);
+        float acc = __ldg(bias);
+        for (int j = 0; j < k; j++) acc += sp[(m + j) * k + j];
         const long long idx = (long long)__ldg(bidx + b) * audio_ld + t0 + m;
-        audio[idx] = tanhf(y);
-        if (pre_tanh) pre_tanh[idx] = y;
+        audio[idx] = tanhf(acc);
+        if (pre_tanh) pre_tanh[idx] = acc;
     }
 }
 
@@ -323,10 +375,14 @@ cudaError_t launch_final_conv(const float* x, Layout xl, int C, const float* w, 
                               int n_row_tiles, cudaStream_t s)
 {
     if (n_row_tiles <= 0) return cudaSuccess;
-    const size_t smem = sizeof(float) * ((size_t)(kFinalTile + k - 1) * (C + 1) + (size_t)k * C);
-    cudaError_t e = cudaFuncSetAttribute(final_conv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return e;
+    if (k > kFinalMaxK) return cudaErrorInvalidValue;
+    const size_t smem = sizeof(float) * ((size_t)k * C + 2 * (size_t)C + (size_t)(kFinalTile + k - 1) * k);
+    static size_t configured = 0;
+    if (smem > 48 * 1024 && smem > configured) {
+        cudaError_t e = cudaFuncSetAttribute(final_conv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        configured = smem;
+    }
     final_conv_kernel<<<n_row_tiles, kFinalTile, smem, s>>>(x, xl, C, w, bias, alpha, inv_alpha, k,
                                                             audio, pre_tanh, audio_ld, plan,
                                                             plan.bidx, tcum);

@@ -12,30 +12,31 @@
 // by more than 10x on random weights.  The tensor core adds each MMA's
 // products to the fp32 accumulator with truncation, not rounding; over the
 // hundreds of k-steps of a long conv that bias alone costs about 20x in the
-// output error.  So the hi*hi products go to one TMEM accumulator and the two
-// cross terms (about 2^-11 of its size) to a second one, and a tile's k-loop
-// is cut into chunks of 16 k-steps: each chunk starts from a zero
-// accumulator, and the epilogue folds every chunk into per-row fp32 sums in
-// registers with rounded adds, in chunk order.  The truncation then acts on
-// 16-step partial sums only, and the GEMM is about as accurate as an fp32 FMA
-// loop.
+// output error.  So a tile's k-loop is cut into chunks of 8 k-steps: each
+// chunk starts from a zero accumulator, and the epilogue folds every chunk
+// into per-row fp32 sums in registers with rounded adds, in chunk order.  The
+// truncation then acts on 8-step partial sums only, and the GEMM is about as
+// accurate as an fp32 FMA loop.
 //
 // Implicit GEMM: output row t of stream segment b takes, for tap j, the
 // input row base(b) + t - shift_j, so a k-block is one TMA box at a shifted
 // row coordinate; the [history | chunk] rows in front of each segment supply
-// the causal left context, and a tile never crosses a stream segment.
+// the causal left context, and an M-tile never crosses a stream segment.
 //
-// Roles (320 threads, one CTA per SM, persistent over tiles):
-//   warp 0     TMA producer (one thread)
-//   warp 1     TMEM allocator and MMA issuer (one thread)
-//   warps 2-9  epilogue in two groups of four: warp w reads TMEM lanes
-//              32 (w % 4) .. +31, group (w - 2) / 4 takes the even or the odd
-//              32-column slices of the tile
-// Two TMEM buffers, each a (main, cross) accumulator pair of at most 128
-// columns, alternate between chunks, so the epilogue drains one while the MMA
-// fills the other.  Every wait is bounded: when one expires
-// the CTA raises a flag, stops, drains its copies and MMAs, frees TMEM and
-// returns.
+// Tiles: a CTA computes two 128-row M-tiles against one N-tile of at most 128
+// columns, so every B (weight) tile brought into shared memory feeds two
+// MMAs; operand traffic from L2, not the tensor pipe, bounds this kernel.
+//
+// Roles (384 threads in three warpgroups, one CTA per SM, persistent):
+//   warpgroup 0  warp 0: TMA producer (one thread); warp 1: TMEM allocator
+//                and MMA issuer (one thread); gives registers away
+//   warpgroup 1  epilogue of M-tile 0 of the pair
+//   warpgroup 2  epilogue of M-tile 1
+// A warp of an epilogue warpgroup reads TMEM lanes 32 (w % 4) .. +31 of its
+// M-tile's accumulator.  Two TMEM buffers (2 M-tiles x 128 columns each)
+// alternate between chunks, so the epilogue drains one while the MMA fills
+// the other.  Every wait is bounded: when one expires the CTA raises a flag,
+// stops, drains its copies and MMAs, frees TMEM and returns.
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 
@@ -52,17 +53,18 @@ namespace {
 
 constexpr int kBM = 128;
 constexpr int kBK = 32;              // fp16 per k-block: 64-byte rows, 64-byte swizzle
-constexpr int kThreads = 320;             // 10 warps
+constexpr int kThreads = 384;        // 3 warpgroups
 constexpr int kEpiWarps = 8;
-constexpr int kMaxBN = 128;            // 2 buffers x (main + cross) x 128 columns = 512
+constexpr int kMaxBN = 128;          // 2 buffers x 2 M-tiles x 128 columns = 512
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSpinLimit = 1u << 25;
 constexpr int kSmemBudget = 220 * 1024;
-constexpr uint32_t kAPlaneBytes = kBM * kBK * 2;   // 8 KB
-constexpr int kChunkKb = 8;          // 8 k-blocks = 256 of K = 16 MMA k-steps per TMEM chunk
+constexpr uint32_t kAPlaneBytes = kBM * kBK * 2;   // 8 KB: one M-tile, one plane
+constexpr int kChunkKb = 4;          // 4 k-blocks = 128 of K = 8 MMA k-steps per TMEM chunk
 
 struct TcParams {
     int n_row_tiles;
+    int n_pairs;        // ceil(n_row_tiles / 2)
     int n_tiles_n;
     int BN;
     int nkb;            // k-blocks: ntaps * Cin / kBK
@@ -70,10 +72,9 @@ struct TcParams {
     int stages;
     uint32_t b_stride;  // bytes of one B plane in a stage (1024-aligned)
     uint32_t stage_bytes;
-    uint32_t tx_bytes;  // bytes the four TMA loads of a stage deliver
+    uint32_t tx_bytes;  // bytes the six TMA loads of a stage deliver
     uint32_t idesc;
-    uint32_t cross_off;   // TMEM column of the cross-term accumulator within a buffer
-    uint32_t buf_cols;    // TMEM columns per buffer (main + cross)
+    uint32_t buf_cols;    // TMEM columns per buffer: 2 M-tiles x round32(BN)
     int chunk_kb;         // k-blocks accumulated in TMEM before the epilogue folds them in
     float unscale;
     int* err;
@@ -173,9 +174,9 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar)
                  : "memory");
 }
 
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v)
+// 32 consecutive columns of this warp's 32 lanes, no wait (pair with tmem_wait_ld).
+__device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, uint32_t* r)
 {
-    uint32_t r[32];
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
         "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
@@ -185,10 +186,9 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v)
           "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
           "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[i]);
 }
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v)
 {
@@ -230,6 +230,23 @@ __device__ __forceinline__ TileRows tile_rows(const GemmArgs& a, const PlanView&
 __device__ __forceinline__ void epi_store32(const GemmArgs& a, const PlanView& plan, int b, int t,
                                             long long out_row, int n0, int count, const float* v, float unscale)
 {
+    if (a.epi == EPI_QKV && count == 32 && (a.d & 31) == 0) {
+        // the 32 columns lie in one of q, K, V: q row, or the stream's ring row
+        float4* dst;
+        if (n0 < a.d) {
+            dst = reinterpret_cast<float4*>(a.out + out_row * a.d + n0);
+        } else {
+            const long long pos = __ldg(plan.pos0 + b) + t;
+            const long long rr = (long long)__ldg(plan.slot + b) * a.ring_R + (pos & (a.ring_R - 1));
+            dst = n0 < 2 * a.d ? reinterpret_cast<float4*>(a.kring + rr * a.d + (n0 - a.d))
+                               : reinterpret_cast<float4*>(a.vring + rr * a.d + (n0 - 2 * a.d));
+        }
+#pragma unroll
+        for (int q = 0; q < 8; q++)
+            dst[q] = make_float4(v[4 * q] * unscale, v[4 * q + 1] * unscale, v[4 * q + 2] * unscale,
+                                 v[4 * q + 3] * unscale);
+        return;
+    }
     const bool vec = count == 32 && a.epi != EPI_QKV && ((out_row * a.out_C + n0) & 3) == 0 &&
                      (a.bias == nullptr || (n0 % a.bias_mod) + 32 <= a.bias_mod);
     if (!vec) {
@@ -244,35 +261,44 @@ __device__ __forceinline__ void epi_store32(const GemmArgs& a, const PlanView& p
     const float* bias = a.bias ? a.bias + (n0 % a.bias_mod) : nullptr;
     const bool has_res = a.epi == EPI_RESID || a.epi == EPI_MRF_FIRST || a.epi == EPI_MRF_ADD || a.epi == EPI_MRF_LAST;
     const bool has_old = a.epi == EPI_MRF_ADD || a.epi == EPI_MRF_LAST;
+    // every load of the 32 columns is in flight before the first use
+    float4 r[8], o[8];
 #pragma unroll
-    for (int half = 0; half < 2; half++) {
-        // loads of this half first (memory-level parallelism), then the math
-        float4 r[4], o[4];
+    for (int q = 0; q < 8; q++) {
+        if (has_res) r[q] = r4[q];
+        if (has_old) o[q] = o4[q];
+    }
 #pragma unroll
-        for (int q = 0; q < 4; q++) {
-            if (has_res) r[q] = r4[half * 4 + q];
-            if (has_old) o[q] = o4[half * 4 + q];
+    for (int q = 0; q < 8; q++) {
+        float y[4];
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+            y[e] = v[4 * q + e] * unscale + (bias ? __ldg(bias + 4 * q + e) : 0.f);
+            if (a.epi == EPI_GELU) y[e] = gelu_f(y[e]);
         }
-#pragma unroll
-        for (int q = 0; q < 4; q++) {
-            const int i0 = half * 16 + 4 * q;
-            float y[4];
-#pragma unroll
-            for (int e = 0; e < 4; e++) {
-                y[e] = v[i0 + e] * unscale + (bias ? __ldg(bias + i0 + e) : 0.f);
-                if (a.epi == EPI_GELU) y[e] = gelu_f(y[e]);
-            }
-            if (has_res) {
-                y[0] = r[q].x + y[0]; y[1] = r[q].y + y[1]; y[2] = r[q].z + y[2]; y[3] = r[q].w + y[3];
-            }
-            if (has_old) {
-                y[0] = o[q].x + y[0]; y[1] = o[q].y + y[1]; y[2] = o[q].z + y[2]; y[3] = o[q].w + y[3];
-                if (a.epi == EPI_MRF_LAST) {
-                    y[0] *= a.scale; y[1] *= a.scale; y[2] *= a.scale; y[3] *= a.scale;
-                }
-            }
-            o4[half * 4 + q] = make_float4(y[0], y[1], y[2], y[3]);
+        if (has_res) {
+            y[0] = r[q].x + y[0]; y[1] = r[q].y + y[1]; y[2] = r[q].z + y[2]; y[3] = r[q].w + y[3];
         }
+        if (has_old) {
+            y[0] = o[q].x + y[0]; y[1] = o[q].y + y[1]; y[2] = o[q].z + y[2]; y[3] = o[q].w + y[3];
+            if (a.epi == EPI_MRF_LAST) {
+                y[0] *= a.scale; y[1] *= a.scale; y[2] *= a.scale; y[3] *= a.scale;
+            }
+        }
+        o4[q] = make_float4(y[0], y[1], y[2], y[3]);
+    }
+}
+
+// Pull the lines this row's epilogue will read (residual, earlier MRF sum)
+// towards L2 while the tile's MMAs run.
+__device__ __forceinline__ void epi_prefetch(const GemmArgs& a, long long out_row, int n0, int ncols)
+{
+    const bool has_res = a.epi == EPI_RESID || a.epi == EPI_MRF_FIRST || a.epi == EPI_MRF_ADD || a.epi == EPI_MRF_LAST;
+    const bool has_old = a.epi == EPI_MRF_ADD || a.epi == EPI_MRF_LAST;
+    const long long idx = out_row * a.out_C + n0;
+    for (int c = 0; c < ncols; c += 32) {
+        if (has_res) asm volatile("prefetch.global.L2 [%0];" ::"l"(a.res + idx + c));
+        if (has_old) asm volatile("prefetch.global.L2 [%0];" ::"l"(a.out + idx + c));
     }
 }
 
@@ -316,15 +342,19 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const int total_tiles = p.n_row_tiles * p.n_tiles_n;
+    const int total_tiles = p.n_pairs * p.n_tiles_n;
+    const int wg = warp >> 2;
 
-    if (warp == 0) {
-        if (lane == 0) {
+    if (wg == 0) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 40;" ::: "memory");
+        if (warp == 0 && lane == 0) {
             // ---------------------------------------------------- producer --
             int it = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
-                const TileRows tr = tile_rows(a, plan, tile / p.n_tiles_n);
+                const int pair = tile / p.n_tiles_n;
+                const TileRows t0 = tile_rows(a, plan, 2 * pair);
+                const TileRows t1 = 2 * pair + 1 < p.n_row_tiles ? tile_rows(a, plan, 2 * pair + 1) : t0;
                 const int n0 = (tile % p.n_tiles_n) * p.BN;
                 for (int kb = 0; kb < p.nkb; kb++, it++) {
                     const int s = it % p.stages;
@@ -332,13 +362,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(
                     if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag)) { ok = false; break; }
                     const int j = kb / p.cin_blocks;
                     const int c0 = (kb - j * p.cin_blocks) * kBK;
-                    const int row = (int)(tr.in_base - a.shift[j]);
+                    const int row0 = (int)(t0.in_base - a.shift[j]);
+                    const int row1 = (int)(t1.in_base - a.shift[j]);
                     uint8_t* st = smem + (size_t)s * p.stage_bytes;
                     mbar_expect_tx(&full[s], p.tx_bytes);
-                    tma_load_2d(st, &ma_hi, &full[s], c0, row);
-                    tma_load_2d(st + kAPlaneBytes, &ma_lo, &full[s], c0, row);
-                    tma_load_2d(st + 2 * kAPlaneBytes, &mb_hi, &full[s], kb * kBK, n0);
-                    tma_load_2d(st + 2 * kAPlaneBytes + p.b_stride, &mb_lo, &full[s], kb * kBK, n0);
+                    tma_load_2d(st, &ma_hi, &full[s], c0, row0);
+                    tma_load_2d(st + kAPlaneBytes, &ma_lo, &full[s], c0, row0);
+                    tma_load_2d(st + 2 * kAPlaneBytes, &ma_hi, &full[s], c0, row1);
+                    tma_load_2d(st + 3 * kAPlaneBytes, &ma_lo, &full[s], c0, row1);
+                    tma_load_2d(st + 4 * kAPlaneBytes, &mb_hi, &full[s], kb * kBK, n0);
+                    tma_load_2d(st + 4 * kAPlaneBytes + p.b_stride, &mb_lo, &full[s], kb * kBK, n0);
                 }
             }
             // drain: every stage's last armed load has landed before exit
@@ -346,9 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(
                 const int last = s + ((it - 1 - s) / p.stages) * p.stages;
                 mbar_drain(&full[s], (uint32_t)(last / p.stages) & 1u);
             }
-        }
-    } else if (warp == 1) {
-        if (lane == 0) {
+        } else if (warp == 1 && lane == 0) {
             // --------------------------------------------------- MMA issue --
             // The k-loop of a tile is cut into chunks of chunk_kb k-blocks; each
             // chunk accumulates from zero into one of the two TMEM buffers,
@@ -362,8 +393,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(
                     const uint32_t aph = (uint32_t)(chunk_it >> 1) & 1u;
                     if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t d_main = tmem_base + (uint32_t)acc * p.buf_cols;
-                    const uint32_t d_cross = d_main + p.cross_off;
+                    const uint32_t d0 = tmem_base + (uint32_t)acc * p.buf_cols;
+                    const uint32_t d1 = d0 + (p.buf_cols >> 1);
                     const int kb1 = min(p.nkb, kb0 + p.chunk_kb);
                     for (int kb = kb0; kb < kb1; kb++, it++) {
                         const int s = it % p.stages;
@@ -371,17 +402,22 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(
                         if (!mbar_wait(&full[s], ph, abort_flag)) { ok = false; break; }
                         tc_fence_after();
                         const uint32_t sa = smem_u32(smem + (size_t)s * p.stage_bytes);
-                        const uint64_t dah = sdesc_sw64(sa);
-                        const uint64_t dal = sdesc_sw64(sa + kAPlaneBytes);
-                        const uint64_t dbh = sdesc_sw64(sa + 2 * kAPlaneBytes);
-                        const uint64_t dbl = sdesc_sw64(sa + 2 * kAPlaneBytes + p.b_stride);
+                        const uint64_t a0h = sdesc_sw64(sa);
+                        const uint64_t a0l = sdesc_sw64(sa + kAPlaneBytes);
+                        const uint64_t a1h = sdesc_sw64(sa + 2 * kAPlaneBytes);
+                        const uint64_t a1l = sdesc_sw64(sa + 3 * kAPlaneBytes);
+                        const uint64_t bh = sdesc_sw64(sa + 4 * kAPlaneBytes);
+                        const uint64_t bl = sdesc_sw64(sa + 4 * kAPlaneBytes + p.b_stride);
 #pragma unroll
                         for (int k = 0; k < kBK / 16; k++) {
                             const uint64_t o = (uint64_t)((k * 32) >> 4);
                             const uint32_t accum = (kb != kb0 || k != 0) ? 1u : 0u;
-                            mma_f16(d_main, dah + o, dbh + o, p.idesc, accum);
-                            mma_f16(d_cross, dah + o, dbl + o, p.idesc, accum);
-                            mma_f16(d_cross, dal + o, dbh + o, p.idesc, 1u);
+                            mma_f16(d0, a0h + o, bh + o, p.idesc, accum);
+                            mma_f16(d1, a1h + o, bh + o, p.idesc, accum);
+                            mma_f16(d0, a0h + o, bl + o, p.idesc, 1u);
+                            mma_f16(d1, a1h + o, bl + o, p.idesc, 1u);
+                            mma_f16(d0, a0l + o, bh + o, p.idesc, 1u);
+                            mma_f16(d1, a1l + o, bh + o, p.idesc, 1u);
                         }
                         mma_commit(&empty[s]);
                     }
@@ -394,19 +430,28 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(
             mbar_drain(drain, 0);
         }
     } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 232;" ::: "memory");
         // ------------------------------------------------------ epilogue --
-        // Thread (warp w, lane l) owns output row 32 (w % 4) + l of the tile and
-        // keeps the sums of its group's (at most 2 x 32) columns in registers
-        // across the chunks.
+        // Warpgroup 1 + g finishes M-tile g of the pair; thread (warp w, lane
+        // l) owns row 32 (w % 4) + l and keeps its <= 128 column sums in
+        // registers across the chunks.
+        const int g = wg - 1;
         const int q = warp & 3;
-        const int eg = (warp - 2) >> 2;
         const int m = q * 32 + lane;
         int chunk_it = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
-            float sum[64];
+            const int mt = 2 * (tile / p.n_tiles_n) + g;
+            const int n0 = (tile % p.n_tiles_n) * p.BN;
+            if (mt < p.n_row_tiles) {
+                const TileRows tr = tile_rows(a, plan, mt);
+                if (m < tr.nrows)
+                    epi_prefetch(a, seg_base(a.out_l, plan.cf, tr.b) + (long long)(tr.t0 + m) * a.out_step, n0,
+                                 min(p.BN, a.N - n0));
+            }
+            float sum[kMaxBN];
 #pragma unroll
-            for (int i = 0; i < 64; i++) sum[i] = 0.f;
+            for (int i = 0; i < kMaxBN; i++) sum[i] = 0.f;
             for (int kb0 = 0; kb0 < p.nkb; kb0 += p.chunk_kb, chunk_it++) {
                 const int acc = chunk_it & 1;
                 const uint32_t aph = (uint32_t)(chunk_it >> 1) & 1u;
@@ -416,20 +461,17 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(
                 w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
                 if (!w_ok) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)acc * p.buf_cols;
+                const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)acc * p.buf_cols +
+                                           (uint32_t)g * (p.buf_cols >> 1);
+                // 32-column batches: one x32 load, one wait
 #pragma unroll
-                for (int h = 0; h < 2; h++) {
-                    const int c = (2 * h + eg) * 32;
+                for (int c = 0; c < kMaxBN; c += 32) {
                     if (c < p.BN) {
+                        uint32_t r[32];
+                        tmem_ld32_async(lane_base + (uint32_t)c, r);
+                        tmem_wait_ld();
 #pragma unroll
-                        for (int g = 0; g < 2; g++) {
-                            float v[16], x[16];
-                            tmem_ld16(lane_base + (uint32_t)(c + 16 * g), v);
-                            tmem_ld16(lane_base + p.cross_off + (uint32_t)(c + 16 * g), x);
-#pragma unroll
-                            for (int i = 0; i < 16; i++)
-                                sum[h * 32 + 16 * g + i] = __fadd_rn(sum[h * 32 + 16 * g + i], __fadd_rn(v[i], x[i]));
-                        }
+                        for (int i = 0; i < 32; i++) sum[c + i] = __fadd_rn(sum[c + i], __uint_as_float(r[i]));
                     }
                 }
                 tc_fence_before();
@@ -437,21 +479,17 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(
                 if (lane == 0) mbar_arrive(&tempty[acc]);
             }
             if (!ok) break;
-            const TileRows tr = tile_rows(a, plan, tile / p.n_tiles_n);
-            const int n0 = (tile % p.n_tiles_n) * p.BN;
+            if (mt >= p.n_row_tiles) continue;
+            const TileRows tr = tile_rows(a, plan, mt);
             if (m < tr.nrows) {
                 const int t = tr.t0 + m;
                 const long long out_row = seg_base(a.out_l, plan.cf, tr.b) + (long long)t * a.out_step;
 #pragma unroll
-                for (int h = 0; h < 2; h++) {
-                    const int c = (2 * h + eg) * 32;
+                for (int c = 0; c < kMaxBN; c += 32) {
                     if (c < p.BN) {
                         int count = min(32, p.BN - c);
                         count = min(count, a.N - (n0 + c));
-                        float v[32];
-#pragma unroll
-                        for (int i = 0; i < 32; i++) v[i] = sum[h * 32 + i];
-                        if (count > 0) epi_store32(a, plan, tr.b, t, out_row, n0 + c, count, v, p.unscale);
+                        if (count > 0) epi_store32(a, plan, tr.b, t, out_row, n0 + c, count, sum + c, p.unscale);
                     }
                 }
             }
@@ -468,6 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(
     }
     if (threadIdx.x == 0 && *abort_flag) atomicExch(p.err, 1);
 }
+
 // hi = fp16(a), lo = fp16(a - hi), a = Snake(x) or x; four channels per thread.
 __global__ void tc_prep_kernel(const float4* __restrict__ x, const float* __restrict__ alpha,
                                const float* __restrict__ inv_alpha, long long n4, int cin4,
@@ -599,20 +638,22 @@ cudaError_t launch_tc_gemm(const GemmArgs& a, const TcWeights& w, PlanView plan,
     if (!make_map(&ma_lo, scratch->a_lo, (uint64_t)a.Cin, (uint64_t)a_rows, kBK, kBM)) return cudaErrorInvalidValue;
     TcParams p;
     p.n_row_tiles = n_row_tiles;
+    p.n_pairs = (n_row_tiles + 1) / 2;
     p.n_tiles_n = w.n_tiles;
     p.BN = w.BN;
     p.cin_blocks = a.Cin / kBK;
     p.nkb = a.ntaps * p.cin_blocks;
     p.b_stride = round1024((uint32_t)w.BN * kBK * 2);
-    p.stage_bytes = 2 * kAPlaneBytes + 2 * p.b_stride;
-    p.tx_bytes = 2 * kAPlaneBytes + 2 * (uint32_t)w.BN * kBK * 2;
+    p.stage_bytes = 4 * kAPlaneBytes + 2 * p.b_stride;
+    p.tx_bytes = 4 * kAPlaneBytes + 2 * (uint32_t)w.BN * kBK * 2;
     const int extra = 1024 + 256;
     p.stages = std::min(8, (kSmemBudget - extra) / (int)p.stage_bytes);
     if (p.stages < 2) return cudaErrorInvalidValue;
     p.idesc = idesc_f16(kBM, w.BN);
-    p.cross_off = (uint32_t)((w.BN + 31) / 32 * 32);
-    p.buf_cols = 2 * p.cross_off;
-    p.chunk_kb = kChunkKb;
+    p.buf_cols = 2 * (uint32_t)((w.BN + 31) / 32 * 32);
+    // a short k-loop (<= 12 k-blocks, 24 k-steps) accumulates in one chunk;
+    // longer ones are cut every kChunkKb k-blocks
+    p.chunk_kb = p.nkb <= 12 ? p.nkb : kChunkKb;
     p.unscale = w.unscale;
     p.err = scratch->err;
     const size_t smem = (size_t)p.stages * p.stage_bytes + extra;
@@ -622,7 +663,7 @@ cudaError_t launch_tc_gemm(const GemmArgs& a, const TcWeights& w, PlanView plan,
         if (e != cudaSuccess) return e;
         configured = 1;
     }
-    const int tiles = n_row_tiles * w.n_tiles;
+    const int tiles = p.n_pairs * w.n_tiles;
     const int grid = std::min(tiles, num_sms > 0 ? num_sms : 152);
     tc_gemm_kernel<<<grid, kThreads, smem, s>>>(ma_hi, ma_lo, w.map_hi, w.map_lo, a, plan, p);
     return cudaGetLastError();
