@@ -23,19 +23,22 @@
 // row coordinate; the [history | chunk] rows in front of each segment supply
 // the causal left context, and an M-tile never crosses a stream segment.
 //
-// Tiles: a CTA computes two 128-row M-tiles against one N-tile of at most 128
-// columns, so every B (weight) tile brought into shared memory feeds two
-// MMAs; operand traffic from L2, not the tensor pipe, bounds this kernel.
+// Tiles: an M-tile is 128 rows.  For N > 128 a CTA tile is one M-tile by an
+// N-tile of up to 256 columns (one MMA of N = 256 per k-step and pass); for
+// N <= 128 it is two M-tiles sharing the N-tile, so each B (weight) tile in
+// shared memory still feeds 256 x N outputs.  With three passes the MMAs
+// read shared memory about as fast as it can deliver, and the TMA writes into
+// it compete for the same bandwidth, so the large tile matters more here than
+// for a single-pass GEMM.
 //
 // Roles (384 threads in three warpgroups, one CTA per SM, persistent):
 //   warpgroup 0  warp 0: TMA producer (one thread); warp 1: TMEM allocator
 //                and MMA issuer (one thread); gives registers away
-//   warpgroup 1  epilogue of M-tile 0 of the pair
-//   warpgroup 2  epilogue of M-tile 1
-// A warp of an epilogue warpgroup reads TMEM lanes 32 (w % 4) .. +31 of its
-// M-tile's accumulator.  Two TMEM buffers (2 M-tiles x 128 columns each)
-// alternate between chunks, so the epilogue drains one while the MMA fills
-// the other.  Every wait is bounded: when one expires the CTA raises a flag,
+//   warpgroups 1, 2  epilogue: with two M-tiles, warpgroup 1 + g takes
+//                M-tile g; with one, it takes columns 128 g .. 128 g + 127
+// A warp of an epilogue warpgroup reads TMEM lanes 32 (w % 4) .. +31.  Two
+// TMEM buffers of 256 columns alternate between chunks, so the epilogue
+// drains one while the MMA fills the other.  Every wait is bounded: when one expires the CTA raises a flag,
 // stops, drains its copies and MMAs, frees TMEM and returns.
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
@@ -55,7 +58,8 @@ constexpr int kBM = 128;
 constexpr int kBK = 32;              // fp16 per k-block: 64-byte rows, 64-byte swizzle
 constexpr int kThreads = 384;        // 3 warpgroups
 constexpr int kEpiWarps = 8;
-constexpr int kMaxBN = 128;          // 2 buffers x 2 M-tiles x 128 columns = 512
+constexpr int kMaxBN = 256;          // 2 buffers x 256 columns = 512
+constexpr int kEpiCols = 128;        // columns one epilogue thread sums
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSpinLimit = 1u << 25;
 constexpr int kSmemBudget = 220 * 1024;
@@ -64,7 +68,8 @@ constexpr int kChunkKb = 4;          // 4 k-blocks = 128 of K = 8 MMA k-steps pe
 
 struct TcParams {
     int n_row_tiles;
-    int n_pairs;        // ceil(n_row_tiles / 2)
+    int mtiles;         // M-tiles per CTA tile: 2 when BN <= 128, else 1
+    int n_mgroups;      // ceil(n_row_tiles / mtiles)
     int n_tiles_n;
     int BN;
     int nkb;            // k-blocks: ntaps * Cin / kBK
@@ -72,9 +77,10 @@ struct TcParams {
     int stages;
     uint32_t b_stride;  // bytes of one B plane in a stage (1024-aligned)
     uint32_t stage_bytes;
-    uint32_t tx_bytes;  // bytes the six TMA loads of a stage deliver
+    uint32_t tx_bytes;  // bytes the TMA loads of a stage deliver
     uint32_t idesc;
-    uint32_t buf_cols;    // TMEM columns per buffer: 2 M-tiles x round32(BN)
+    uint32_t buf_cols;    // TMEM columns per buffer: mtiles x round32(BN) <= 256
+    uint32_t mt_cols;     // TMEM column offset between the M-tiles of a buffer
     int chunk_kb;         // k-blocks accumulated in TMEM before the epilogue folds them in
     float unscale;
     int* err;
@@ -247,8 +253,7 @@ __device__ __forceinline__ void epi_store32(const GemmArgs& a, const PlanView& p
                                  v[4 * q + 3] * unscale);
         return;
     }
-    const bool vec = count == 32 && a.epi != EPI_QKV && ((out_row * a.out_C + n0) & 3) == 0 &&
-                     (a.bias == nullptr || (n0 % a.bias_mod) + 32 <= a.bias_mod);
+    const bool vec = count == 32 && a.epi != EPI_QKV && ((out_row * a.out_C + n0) & 3) == 0;
     if (!vec) {
 #pragma unroll
         for (int i = 0; i < 32; i++)
@@ -258,9 +263,11 @@ __device__ __forceinline__ void epi_store32(const GemmArgs& a, const PlanView& p
     const long long idx = out_row * a.out_C + n0;
     float4* o4 = reinterpret_cast<float4*>(a.out + idx);
     const float4* r4 = reinterpret_cast<const float4*>(a.res ? a.res + idx : a.out + idx);
-    const float* bias = a.bias ? a.bias + (n0 % a.bias_mod) : nullptr;
     const bool has_res = a.epi == EPI_RESID || a.epi == EPI_MRF_FIRST || a.epi == EPI_MRF_ADD || a.epi == EPI_MRF_LAST;
     const bool has_old = a.epi == EPI_MRF_ADD || a.epi == EPI_MRF_LAST;
+    // bias[n % bias_mod], walked with a wrapping index (the phase GEMM of a
+    // transposed conv repeats its bias every Cout columns)
+    int bi = a.bias ? n0 % a.bias_mod : 0;
     // every load of the 32 columns is in flight before the first use
     float4 r[8], o[8];
 #pragma unroll
@@ -273,7 +280,11 @@ __device__ __forceinline__ void epi_store32(const GemmArgs& a, const PlanView& p
         float y[4];
 #pragma unroll
         for (int e = 0; e < 4; e++) {
-            y[e] = v[4 * q + e] * unscale + (bias ? __ldg(bias + 4 * q + e) : 0.f);
+            y[e] = v[4 * q + e] * unscale;
+            if (a.bias) {
+                y[e] += __ldg(a.bias + bi);
+                bi = (bi + 1 == a.bias_mod) ? 0 : bi + 1;
+            }
             if (a.epi == EPI_GELU) y[e] = gelu_f(y[e]);
         }
         if (has_res) {
@@ -342,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const int total_tiles = p.n_pairs * p.n_tiles_n;
+    const int total_tiles = p.n_mgroups * p.n_tiles_n;
     const int wg = warp >> 2;
 
     if (wg == 0) {
@@ -352,9 +363,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(
             int it = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
-                const int pair = tile / p.n_tiles_n;
-                const TileRows t0 = tile_rows(a, plan, 2 * pair);
-                const TileRows t1 = 2 * pair + 1 < p.n_row_tiles ? tile_rows(a, plan, 2 * pair + 1) : t0;
+                const int mg = tile / p.n_tiles_n;
+                const TileRows t0 = tile_rows(a, plan, p.mtiles * mg);
+                const TileRows t1 =
+                    (p.mtiles == 2 && 2 * mg + 1 < p.n_row_tiles) ? tile_rows(a, plan, 2 * mg + 1) : t0;
                 const int n0 = (tile % p.n_tiles_n) * p.BN;
                 for (int kb = 0; kb < p.nkb; kb++, it++) {
                     const int s = it % p.stages;
@@ -368,10 +380,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(
                     mbar_expect_tx(&full[s], p.tx_bytes);
                     tma_load_2d(st, &ma_hi, &full[s], c0, row0);
                     tma_load_2d(st + kAPlaneBytes, &ma_lo, &full[s], c0, row0);
-                    tma_load_2d(st + 2 * kAPlaneBytes, &ma_hi, &full[s], c0, row1);
-                    tma_load_2d(st + 3 * kAPlaneBytes, &ma_lo, &full[s], c0, row1);
-                    tma_load_2d(st + 4 * kAPlaneBytes, &mb_hi, &full[s], kb * kBK, n0);
-                    tma_load_2d(st + 4 * kAPlaneBytes + p.b_stride, &mb_lo, &full[s], kb * kBK, n0);
+                    if (p.mtiles == 2) {
+                        tma_load_2d(st + 2 * kAPlaneBytes, &ma_hi, &full[s], c0, row1);
+                        tma_load_2d(st + 3 * kAPlaneBytes, &ma_lo, &full[s], c0, row1);
+                    }
+                    uint8_t* sb = st + 2 * p.mtiles * kAPlaneBytes;
+                    tma_load_2d(sb, &mb_hi, &full[s], kb * kBK, n0);
+                    tma_load_2d(sb + p.b_stride, &mb_lo, &full[s], kb * kBK, n0);
                 }
             }
             // drain: every stage's last armed load has landed before exit
@@ -393,8 +408,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(
                     const uint32_t aph = (uint32_t)(chunk_it >> 1) & 1u;
                     if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t d0 = tmem_base + (uint32_t)acc * p.buf_cols;
-                    const uint32_t d1 = d0 + (p.buf_cols >> 1);
+                    const uint32_t d0 = tmem_base + (uint32_t)acc * (uint32_t)kMaxBN;
+                    const uint32_t d1 = d0 + p.mt_cols;
                     const int kb1 = min(p.nkb, kb0 + p.chunk_kb);
                     for (int kb = kb0; kb < kb1; kb++, it++) {
                         const int s = it % p.stages;
@@ -406,18 +421,30 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(
                         const uint64_t a0l = sdesc_sw64(sa + kAPlaneBytes);
                         const uint64_t a1h = sdesc_sw64(sa + 2 * kAPlaneBytes);
                         const uint64_t a1l = sdesc_sw64(sa + 3 * kAPlaneBytes);
-                        const uint64_t bh = sdesc_sw64(sa + 4 * kAPlaneBytes);
-                        const uint64_t bl = sdesc_sw64(sa + 4 * kAPlaneBytes + p.b_stride);
+                        const uint32_t sb = sa + 2 * (uint32_t)p.mtiles * kAPlaneBytes;
+                        const uint64_t bh = sdesc_sw64(sb);
+                        const uint64_t bl = sdesc_sw64(sb + p.b_stride);
+                        if (p.mtiles == 2) {
 #pragma unroll
-                        for (int k = 0; k < kBK / 16; k++) {
-                            const uint64_t o = (uint64_t)((k * 32) >> 4);
-                            const uint32_t accum = (kb != kb0 || k != 0) ? 1u : 0u;
-                            mma_f16(d0, a0h + o, bh + o, p.idesc, accum);
-                            mma_f16(d1, a1h + o, bh + o, p.idesc, accum);
-                            mma_f16(d0, a0h + o, bl + o, p.idesc, 1u);
-                            mma_f16(d1, a1h + o, bl + o, p.idesc, 1u);
-                            mma_f16(d0, a0l + o, bh + o, p.idesc, 1u);
-                            mma_f16(d1, a1l + o, bh + o, p.idesc, 1u);
+                            for (int k = 0; k < kBK / 16; k++) {
+                                const uint64_t o = (uint64_t)((k * 32) >> 4);
+                                const uint32_t accum = (kb != kb0 || k != 0) ? 1u : 0u;
+                                mma_f16(d0, a0h + o, bh + o, p.idesc, accum);
+                                mma_f16(d1, a1h + o, bh + o, p.idesc, accum);
+                                mma_f16(d0, a0h + o, bl + o, p.idesc, 1u);
+                                mma_f16(d1, a1h + o, bl + o, p.idesc, 1u);
+                                mma_f16(d0, a0l + o, bh + o, p.idesc, 1u);
+                                mma_f16(d1, a1l + o, bh + o, p.idesc, 1u);
+                            }
+                        } else {
+#pragma unroll
+                            for (int k = 0; k < kBK / 16; k++) {
+                                const uint64_t o = (uint64_t)((k * 32) >> 4);
+                                const uint32_t accum = (kb != kb0 || k != 0) ? 1u : 0u;
+                                mma_f16(d0, a0h + o, bh + o, p.idesc, accum);
+                                mma_f16(d0, a0h + o, bl + o, p.idesc, 1u);
+                                mma_f16(d0, a0l + o, bh + o, p.idesc, 1u);
+                            }
                         }
                         mma_commit(&empty[s]);
                     }
@@ -432,26 +459,31 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 232;" ::: "memory");
         // ------------------------------------------------------ epilogue --
-        // Warpgroup 1 + g finishes M-tile g of the pair; thread (warp w, lane
-        // l) owns row 32 (w % 4) + l and keeps its <= 128 column sums in
+        // With two M-tiles, warpgroup 1 + g finishes M-tile g; with one, it
+        // finishes columns 128 g .. 128 g + 127.  Thread (warp w, lane l)
+        // owns row 32 (w % 4) + l and keeps its <= 128 column sums in
         // registers across the chunks.
         const int g = wg - 1;
+        const int my_mt = p.mtiles == 2 ? g : 0;
+        const int col0 = p.mtiles == 2 ? 0 : g * kEpiCols;
+        const int ncol = max(0, min(kEpiCols, p.BN - col0));
         const int q = warp & 3;
         const int m = q * 32 + lane;
         int chunk_it = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
-            const int mt = 2 * (tile / p.n_tiles_n) + g;
-            const int n0 = (tile % p.n_tiles_n) * p.BN;
-            if (mt < p.n_row_tiles) {
+            const int mt = p.mtiles * (tile / p.n_tiles_n) + my_mt;
+            const int n0 = (tile % p.n_tiles_n) * p.BN + col0;
+            const int nvalid = min(ncol, a.N - n0);
+            if (mt < p.n_row_tiles && nvalid > 0) {
                 const TileRows tr = tile_rows(a, plan, mt);
                 if (m < tr.nrows)
                     epi_prefetch(a, seg_base(a.out_l, plan.cf, tr.b) + (long long)(tr.t0 + m) * a.out_step, n0,
-                                 min(p.BN, a.N - n0));
+                                 nvalid);
             }
-            float sum[kMaxBN];
+            float sum[kEpiCols];
 #pragma unroll
-            for (int i = 0; i < kMaxBN; i++) sum[i] = 0.f;
+            for (int i = 0; i < kEpiCols; i++) sum[i] = 0.f;
             for (int kb0 = 0; kb0 < p.nkb; kb0 += p.chunk_kb, chunk_it++) {
                 const int acc = chunk_it & 1;
                 const uint32_t aph = (uint32_t)(chunk_it >> 1) & 1u;
@@ -461,12 +493,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(
                 w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
                 if (!w_ok) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)acc * p.buf_cols +
-                                           (uint32_t)g * (p.buf_cols >> 1);
+                const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)acc * (uint32_t)kMaxBN +
+                                           (uint32_t)my_mt * p.mt_cols + (uint32_t)col0;
                 // 32-column batches: one x32 load, one wait
 #pragma unroll
-                for (int c = 0; c < kMaxBN; c += 32) {
-                    if (c < p.BN) {
+                for (int c = 0; c < kEpiCols; c += 32) {
+                    if (c < ncol) {
                         uint32_t r[32];
                         tmem_ld32_async(lane_base + (uint32_t)c, r);
                         tmem_wait_ld();
@@ -479,16 +511,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(
                 if (lane == 0) mbar_arrive(&tempty[acc]);
             }
             if (!ok) break;
-            if (mt >= p.n_row_tiles) continue;
+            if (mt >= p.n_row_tiles || nvalid <= 0) continue;
             const TileRows tr = tile_rows(a, plan, mt);
             if (m < tr.nrows) {
                 const int t = tr.t0 + m;
                 const long long out_row = seg_base(a.out_l, plan.cf, tr.b) + (long long)t * a.out_step;
 #pragma unroll
-                for (int c = 0; c < kMaxBN; c += 32) {
-                    if (c < p.BN) {
-                        int count = min(32, p.BN - c);
-                        count = min(count, a.N - (n0 + c));
+                for (int c = 0; c < kEpiCols; c += 32) {
+                    if (c < nvalid) {
+                        const int count = min(32, nvalid - c);
                         if (count > 0) epi_store32(a, plan, tr.b, t, out_row, n0 + c, count, sum + c, p.unscale);
                     }
                 }
@@ -593,8 +624,13 @@ bool tc_pack_weights(const float* wkn, int ntaps, int Cin, int N, TcWeights* out
     out->hi = dh;
     out->lo = dl;
     out->unscale = std::ldexp(1.0f, -e);
-    const int nt = (N + kMaxBN - 1) / kMaxBN;
-    out->BN = ((N + nt - 1) / nt + 15) / 16 * 16;
+    // N-tile: a multiple of 32 up to 256 that pads N least (ties: the wider)
+    int best = 32;
+    for (int bn = 32; bn <= kMaxBN; bn += 32) {
+        const int pad = (N + bn - 1) / bn * bn, best_pad = (N + best - 1) / best * best;
+        if (pad < best_pad || (pad == best_pad && bn > best)) best = bn;
+    }
+    out->BN = best;
     out->n_tiles = (N + out->BN - 1) / out->BN;
     if (!make_map(&out->map_hi, dh, K, (uint64_t)N, kBK, (uint32_t)out->BN)) return false;
     if (!make_map(&out->map_lo, dl, K, (uint64_t)N, kBK, (uint32_t)out->BN)) return false;
@@ -638,19 +674,21 @@ cudaError_t launch_tc_gemm(const GemmArgs& a, const TcWeights& w, PlanView plan,
     if (!make_map(&ma_lo, scratch->a_lo, (uint64_t)a.Cin, (uint64_t)a_rows, kBK, kBM)) return cudaErrorInvalidValue;
     TcParams p;
     p.n_row_tiles = n_row_tiles;
-    p.n_pairs = (n_row_tiles + 1) / 2;
+    p.mtiles = w.BN <= 128 ? 2 : 1;
+    p.n_mgroups = (n_row_tiles + p.mtiles - 1) / p.mtiles;
     p.n_tiles_n = w.n_tiles;
     p.BN = w.BN;
     p.cin_blocks = a.Cin / kBK;
     p.nkb = a.ntaps * p.cin_blocks;
     p.b_stride = round1024((uint32_t)w.BN * kBK * 2);
-    p.stage_bytes = 4 * kAPlaneBytes + 2 * p.b_stride;
-    p.tx_bytes = 4 * kAPlaneBytes + 2 * (uint32_t)w.BN * kBK * 2;
+    p.stage_bytes = 2 * (uint32_t)p.mtiles * kAPlaneBytes + 2 * p.b_stride;
+    p.tx_bytes = 2 * (uint32_t)p.mtiles * kAPlaneBytes + 2 * (uint32_t)w.BN * kBK * 2;
     const int extra = 1024 + 256;
     p.stages = std::min(8, (kSmemBudget - extra) / (int)p.stage_bytes);
     if (p.stages < 2) return cudaErrorInvalidValue;
     p.idesc = idesc_f16(kBM, w.BN);
-    p.buf_cols = 2 * (uint32_t)((w.BN + 31) / 32 * 32);
+    p.mt_cols = (uint32_t)((w.BN + 31) / 32 * 32);
+    p.buf_cols = (uint32_t)p.mtiles * p.mt_cols;
     // a short k-loop (<= 12 k-blocks, 24 k-steps) accumulates in one chunk;
     // longer ones are cut every kChunkKb k-blocks
     p.chunk_kb = p.nkb <= 12 ? p.nkb : kChunkKb;
@@ -663,7 +701,7 @@ cudaError_t launch_tc_gemm(const GemmArgs& a, const TcWeights& w, PlanView plan,
         if (e != cudaSuccess) return e;
         configured = 1;
     }
-    const int tiles = p.n_pairs * w.n_tiles;
+    const int tiles = p.n_mgroups * w.n_tiles;
     const int grid = std::min(tiles, num_sms > 0 ? num_sms : 152);
     tc_gemm_kernel<<<grid, kThreads, smem, s>>>(ma_hi, ma_lo, w.map_hi, w.map_lo, a, plan, p);
     return cudaGetLastError();
