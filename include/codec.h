@@ -197,6 +197,27 @@ CODEC_API codec_status codec_decode_chunk_host(codec_state_t* state, const int32
                                      const int32_t* n_frames, const int32_t* stream_ids, int32_t B,
                                      int32_t T_max, float* audio_host, void* stream);
 
+/*
+ * One causal dilated Conv1d on the tensor-core fp16x3 path, outside the
+ * decoder: y[t] = bias + sum_j sum_ci W[co][ci][j] a[H + t - (k-1-j) dil][ci],
+ * a = Snake_alpha(x) when alpha is given, else x, H = (k-1) dil.  The same
+ * operand split, tcgen05 GEMM and chunked accumulation as the decoder's convs;
+ * for verification of that kernel and for callers composing their own layers.
+ *   x     device float [H + T][Cin], the H history rows first
+ *   w     device float [Cout][Cin][k] (PyTorch Conv1d layout)
+ *   bias  device float [Cout] or NULL;  alpha device float [Cin] or NULL
+ *   y     device float [T][Cout]
+ * Uses the state's scratch, so it needs a state of a CODEC_PRECISION_FP16X3
+ * codec (else CODEC_ERR_CONFIG) and is ordered with that state's other work on
+ * the same stream.  Requires Cin % 32 == 0, Cout % 16 == 0, T >= 1,
+ * 1 <= k <= 16, dilation >= 1, Cin <= 4096 when alpha is given
+ * (CODEC_ERR_ARG); (H + T) * Cin and Cout * Cin * k within the scratch the
+ * state sized for its decoder (CODEC_ERR_CAPACITY).
+ */
+CODEC_API codec_status codec_state_conv1d(codec_state_t* state, const float* x, int32_t T, int32_t Cin,
+                                          const float* w, const float* bias, const float* alpha, int32_t Cout,
+                                          int32_t k, int32_t dilation, float* y, void* stream);
+
 /* Frames decoded and sticky error bits of one slot.  Synchronises stream
  * (host-blocking).  Errors: CODEC_ERR_NULL, CODEC_ERR_ARG, CODEC_ERR_CUDA. */
 CODEC_API codec_status codec_state_query(codec_state_t* state, int32_t stream_id, codec_stream_info* info,

@@ -97,6 +97,7 @@ def _lib():
             "codec_state_last_launches": (i32, [_P]),
             "codec_status_string": (ctypes.c_char_p, [i32]),
             "codec_profile_begin": (i32, [_P, i32]),
+            "codec_state_conv1d": (i32, [_P, _P, i32, i32, _P, _P, _P, i32, i32, i32, _P, _P]),
             "codec_profile_end": (i32, [_P, ctypes.POINTER(KernelStatsC), _P]),
             "codec_profile_launches": (i32, [_P, ctypes.POINTER(LaunchRecordC), i32, ctypes.POINTER(i32)]),
         }
@@ -253,6 +254,15 @@ class CodecState:
         ids_p = None if ids is None else ids.ctypes.data_as(_I32P)
         _check(_lib().codec_decode_chunk_host(self._h, _ptr(codes), nf.ctypes.data_as(_I32P), ids_p, B, T_max,
                                               _ptr(audio), _stream_handle(stream)), "codec_decode_chunk_host")
+
+    def conv1d(self, x, w, y, bias=None, alpha=None, dilation=1, stream=None):
+        """codec_state_conv1d: x [(k-1) dil + T][Cin], w [Cout][Cin][k], y [T][Cout]
+        (contiguous float32 CUDA tensors); bias [Cout], alpha [Cin] optional."""
+        Cout, Cin, k = w.shape
+        T = y.shape[0]
+        opt = lambda t: None if t is None else _ptr(t)
+        _check(_lib().codec_state_conv1d(self._h, _ptr(x), T, Cin, _ptr(w), opt(bias), opt(alpha), Cout, k,
+                                         dilation, _ptr(y), _stream_handle(stream)), "codec_state_conv1d")
 
     def query(self, stream_id: int, stream=None):
         info = StreamInfoC()

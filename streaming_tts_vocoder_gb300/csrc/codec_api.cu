@@ -514,9 +514,12 @@ codec_status codec_state_create(codec_t* c, int32_t n_streams, codec_state_t** o
     s->audio_d = dev_alloc<float>(A, (size_t)S * g.max_chunk_frames * c->spf, st);
     if (st == CODEC_OK && g.precision == CODEC_PRECISION_FP16X3) {
         // operand planes for the widest tensor-core input: (contraction, input level, prefixed?)
-        size_t elems = 0;
+        size_t elems = 0, b_elems = 0;
         auto need = [&](const Contraction& C, int lvl, bool pref) {
-            if (C.use_tc) elems = std::max(elems, rows(lvl, pref) * (size_t)C.Cin);
+            if (C.use_tc) {
+                elems = std::max(elems, rows(lvl, pref) * (size_t)C.Cin);
+                b_elems = std::max(b_elems, (size_t)C.K * C.N);
+            }
         };
         need(c->pre, 0, true);
         for (const LayerW& L : c->layers) {
@@ -531,7 +534,7 @@ codec_status codec_state_create(codec_t* c, int32_t n_streams, codec_state_t** o
             for (int j = 0; j < g.n_rb; j++)
                 for (int i = 0; i < g.n_dil; i++) need(c->rb[c->rb_index(si, j, i)], g.n_up + 1 + si, true);
         }
-        if (!tc_scratch_alloc(&s->tc_scratch, std::max<size_t>(elems, 4), A)) st = CODEC_ERR_OOM;
+        if (!tc_scratch_alloc(&s->tc_scratch, std::max<size_t>(elems, 4), b_elems, A)) st = CODEC_ERR_OOM;
     }
     if (st == CODEC_OK && cudaDeviceSynchronize() != cudaSuccess) st = CODEC_ERR_CUDA;
     if (st != CODEC_OK) {
@@ -647,6 +650,22 @@ codec_status codec_state_reset(codec_state_t* s, const int32_t* ids, int32_t n, 
         return CODEC_ERR_CUDA;
     for (int i : list) s->frames_h[i] = 0;
     return CODEC_OK;
+}
+
+codec_status codec_state_conv1d(codec_state_t* s, const float* x, int32_t T, int32_t Cin, const float* w,
+                                const float* bias, const float* alpha, int32_t Cout, int32_t k, int32_t dilation,
+                                float* y, void* stream)
+{
+    if (!s || !x || !w || !y) return CODEC_ERR_NULL;
+    if (!s->tc_scratch.op.words) return CODEC_ERR_CONFIG;
+    const int r = run_tc_conv1d(s->tc_scratch.op, x, T, Cin, w, bias, alpha, Cout, k, dilation, y, s->c->num_sms,
+                                (cudaStream_t)stream);
+    switch (r) {
+    case OP_OK: return CODEC_OK;
+    case OP_BAD_ARG: return CODEC_ERR_ARG;
+    case OP_TOO_BIG: return CODEC_ERR_CAPACITY;
+    default: return CODEC_ERR_CUDA;
+    }
 }
 
 codec_status codec_state_query(codec_state_t* s, int32_t id, codec_stream_info* info, void* stream)

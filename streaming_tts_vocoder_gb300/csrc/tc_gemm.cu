@@ -83,6 +83,7 @@ struct TcParams {
     uint32_t mt_cols;     // TMEM column offset between the M-tiles of a buffer
     int chunk_kb;         // k-blocks accumulated in TMEM before the epilogue folds them in
     float unscale;
+    const float* unscale_dev;   // when set, the accumulator scale is read from here
     int* err;
 };
 
@@ -354,6 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const int total_tiles = p.n_mgroups * p.n_tiles_n;
+    const float unscale = p.unscale_dev ? *p.unscale_dev : p.unscale;
     const int wg = warp >> 2;
 
     if (wg == 0) {
@@ -520,7 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(
                 for (int c = 0; c < kEpiCols; c += 32) {
                     if (c < nvalid) {
                         const int count = min(32, nvalid - c);
-                        if (count > 0) epi_store32(a, plan, tr.b, t, out_row, n0 + c, count, sum + c, p.unscale);
+                        if (count > 0) epi_store32(a, plan, tr.b, t, out_row, n0 + c, count, sum + c, unscale);
                     }
                 }
             }
@@ -595,6 +597,17 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer
 
 uint32_t round1024(uint32_t x) { return (x + 1023u) & ~1023u; }
 
+// N-tile: a multiple of 32 up to 256 that pads N least (ties: the wider).
+int pick_bn(int N)
+{
+    int best = 32;
+    for (int bn = 32; bn <= kMaxBN; bn += 32) {
+        const int pad = (N + bn - 1) / bn * bn, best_pad = (N + best - 1) / best * best;
+        if (pad < best_pad || (pad == best_pad && bn > best)) best = bn;
+    }
+    return best;
+}
+
 }  // namespace
 
 bool tc_eligible(int Cin, int N) { return Cin >= kBK && Cin % kBK == 0 && N >= 16 && N % 16 == 0; }
@@ -624,21 +637,22 @@ bool tc_pack_weights(const float* wkn, int ntaps, int Cin, int N, TcWeights* out
     out->hi = dh;
     out->lo = dl;
     out->unscale = std::ldexp(1.0f, -e);
-    // N-tile: a multiple of 32 up to 256 that pads N least (ties: the wider)
-    int best = 32;
-    for (int bn = 32; bn <= kMaxBN; bn += 32) {
-        const int pad = (N + bn - 1) / bn * bn, best_pad = (N + best - 1) / best * best;
-        if (pad < best_pad || (pad == best_pad && bn > best)) best = bn;
-    }
-    out->BN = best;
+    out->BN = pick_bn(N);
     out->n_tiles = (N + out->BN - 1) / out->BN;
     if (!make_map(&out->map_hi, dh, K, (uint64_t)N, kBK, (uint32_t)out->BN)) return false;
     if (!make_map(&out->map_lo, dl, K, (uint64_t)N, kBK, (uint32_t)out->BN)) return false;
     return true;
 }
 
-bool tc_scratch_alloc(TcScratch* s, size_t elems, std::vector<void*>& allocs)
+bool tc_scratch_alloc(TcScratch* s, size_t elems, size_t b_elems, std::vector<void*>& allocs)
 {
+    s->op.b_elems = b_elems;
+    for (void** q : {&s->op.b_hi, &s->op.b_lo}) {
+        if (cudaMalloc(q, std::max<size_t>(b_elems, 1) * sizeof(__half)) != cudaSuccess) return false;
+        allocs.push_back(*q);
+    }
+    if (cudaMalloc(&s->op.words, kOpWords * sizeof(int)) != cudaSuccess) return false;
+    allocs.push_back(s->op.words);
     if (cudaMalloc(&s->a_hi, elems * sizeof(__half)) != cudaSuccess) return false;
     allocs.push_back(s->a_hi);
     if (cudaMalloc(&s->a_lo, elems * sizeof(__half)) != cudaSuccess) return false;
@@ -647,6 +661,10 @@ bool tc_scratch_alloc(TcScratch* s, size_t elems, std::vector<void*>& allocs)
     allocs.push_back(s->err);
     if (cudaMemset(s->err, 0, sizeof(int)) != cudaSuccess) return false;
     s->elems = elems;
+    s->op.a_hi = s->a_hi;
+    s->op.a_lo = s->a_lo;
+    s->op.a_elems = elems;
+    s->op.err = s->err;
     return true;
 }
 
@@ -665,13 +683,16 @@ cudaError_t launch_tc_prep(const float* x, const float* alpha, const float* inv_
     return cudaGetLastError();
 }
 
-cudaError_t launch_tc_gemm(const GemmArgs& a, const TcWeights& w, PlanView plan, int n_row_tiles,
-                           const TcScratch* scratch, long long a_rows, int num_sms, cudaStream_t s)
+namespace {
+
+cudaError_t tc_gemm_core(const GemmArgs& a, const TcWeights& w, const float* unscale_dev, PlanView plan,
+                         int n_row_tiles, const void* a_hi, const void* a_lo, long long a_rows, int* err,
+                         int num_sms, cudaStream_t s)
 {
     if (n_row_tiles <= 0) return cudaSuccess;
     alignas(64) CUtensorMap ma_hi, ma_lo;
-    if (!make_map(&ma_hi, scratch->a_hi, (uint64_t)a.Cin, (uint64_t)a_rows, kBK, kBM)) return cudaErrorInvalidValue;
-    if (!make_map(&ma_lo, scratch->a_lo, (uint64_t)a.Cin, (uint64_t)a_rows, kBK, kBM)) return cudaErrorInvalidValue;
+    if (!make_map(&ma_hi, a_hi, (uint64_t)a.Cin, (uint64_t)a_rows, kBK, kBM)) return cudaErrorInvalidValue;
+    if (!make_map(&ma_lo, a_lo, (uint64_t)a.Cin, (uint64_t)a_rows, kBK, kBM)) return cudaErrorInvalidValue;
     TcParams p;
     p.n_row_tiles = n_row_tiles;
     p.mtiles = w.BN <= 128 ? 2 : 1;
@@ -693,7 +714,8 @@ cudaError_t launch_tc_gemm(const GemmArgs& a, const TcWeights& w, PlanView plan,
     // longer ones are cut every kChunkKb k-blocks
     p.chunk_kb = p.nkb <= 12 ? p.nkb : kChunkKb;
     p.unscale = w.unscale;
-    p.err = scratch->err;
+    p.unscale_dev = unscale_dev;
+    p.err = err;
     const size_t smem = (size_t)p.stages * p.stage_bytes + extra;
     static int configured = 0;
     if (!configured) {
@@ -705,6 +727,135 @@ cudaError_t launch_tc_gemm(const GemmArgs& a, const TcWeights& w, PlanView plan,
     const int grid = std::min(tiles, num_sms > 0 ? num_sms : 152);
     tc_gemm_kernel<<<grid, kThreads, smem, s>>>(ma_hi, ma_lo, w.map_hi, w.map_lo, a, plan, p);
     return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_tc_gemm(const GemmArgs& a, const TcWeights& w, PlanView plan, int n_row_tiles,
+                           const TcScratch* scratch, long long a_rows, int num_sms, cudaStream_t s)
+{
+    return tc_gemm_core(a, w, nullptr, plan, n_row_tiles, scratch->a_hi, scratch->a_lo, a_rows, scratch->err,
+                        num_sms, s);
+}
+
+// ------------------------------------------------------- standalone conv --
+// One causal dilated Conv1d through the same prep + tcgen05 kernels, with the
+// weights packed on the device and every scratch array (operand planes, the
+// one-segment plan, the weight scale) in the memory TcOpScratch points to.
+
+namespace {
+
+// word layout of TcOpScratch::words: plan (8 ints), weight |max| bits, the
+// accumulator scale, then 1/alpha for up to kOpMaxCin channels
+constexpr int kOpPlan = 0, kOpWmax = 8, kOpUnscale = 9, kOpInvAlpha = 16;
+
+__global__ void op_setup_kernel(int* words, int T, const float* __restrict__ alpha, int Cin)
+{
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i == 0) {
+        long long* pos0 = reinterpret_cast<long long*>(words + kOpPlan);
+        pos0[0] = 0;                         // words 0, 1
+        words[kOpPlan + 2] = 0;              // cf = {0, T}
+        words[kOpPlan + 3] = T;
+        words[kOpPlan + 4] = 0;              // slot
+        words[kOpPlan + 5] = 0;              // bidx
+        words[kOpPlan + 6] = 0;              // 128-row tiles = {0, ceil(T / 128)}
+        words[kOpPlan + 7] = (T + kBM - 1) / kBM;
+        words[kOpWmax] = 0;
+    }
+    if (alpha && i < Cin) reinterpret_cast<float*>(words + kOpInvAlpha)[i] = 1.0f / alpha[i];
+}
+
+__global__ void op_wmax_kernel(const float* __restrict__ w, long long n, unsigned* __restrict__ out)
+{
+    unsigned m = 0;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
+        m = max(m, __float_as_uint(fabsf(w[i])));      // non-negative floats order like their bits
+#pragma unroll
+    for (int o = 16; o; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if ((threadIdx.x & 31) == 0) atomicMax(out, m);
+}
+
+// w [Cout][Cin][k] -> planes [Cout][k Cin] (tap-major K) of w * 2^e, e from |w|max
+__global__ void op_wpack_kernel(const float* __restrict__ w, int Cout, int Cin, int k, int* words,
+                                __half* __restrict__ hi, __half* __restrict__ lo)
+{
+    const float mx = __uint_as_float(static_cast<unsigned>(words[kOpWmax]));
+    const int e = mx > 0.f ? -(int)floorf(log2f(mx)) : 0;
+    const float scale = ldexpf(1.0f, e);
+    const long long K = (long long)k * Cin, n = (long long)Cout * K;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+        const long long co = i / K, kk = i - co * K;
+        const long long j = kk / Cin, ci = kk - j * Cin;
+        const float v = w[(co * Cin + ci) * k + j] * scale;
+        const __half h = __float2half_rn(v);
+        hi[i] = h;
+        lo[i] = __float2half_rn(v - __half2float(h));
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0) reinterpret_cast<float*>(words)[kOpUnscale] = ldexpf(1.0f, -e);
+}
+
+}  // namespace
+
+int run_tc_conv1d(const TcOpScratch& sc, const float* x, int T, int Cin, const float* w,
+                                const float* bias, const float* alpha, int Cout, int k, int dil, float* y,
+                                int num_sms, cudaStream_t s)
+{
+    if (T < 1 || k < 1 || k > kMaxTaps || dil < 1 || !tc_eligible(Cin, Cout)) return OP_BAD_ARG;
+    if (alpha && Cin > kOpMaxCin) return OP_BAD_ARG;
+    const long long H = (long long)(k - 1) * dil;
+    const long long rows = H + T;
+    const long long K = (long long)k * Cin;
+    if ((size_t)(rows * Cin) > sc.a_elems || (size_t)(K * Cout) > sc.b_elems) return OP_TOO_BIG;
+    if (rows > (1LL << 30)) return OP_TOO_BIG;
+    int* words = sc.words;
+    const float* inv_alpha = reinterpret_cast<const float*>(words + kOpInvAlpha);
+    op_setup_kernel<<<(std::max(Cin, 1) + 255) / 256, 256, 0, s>>>(words, T, alpha, Cin);
+    if (cudaGetLastError() != cudaSuccess) return OP_CUDA;
+    const long long wn = K * Cout;
+    const int wblocks = (int)std::min<long long>((wn + 255) / 256, 152LL * 8);
+    op_wmax_kernel<<<wblocks, 256, 0, s>>>(w, wn, reinterpret_cast<unsigned*>(words + kOpWmax));
+    op_wpack_kernel<<<wblocks, 256, 0, s>>>(w, Cout, Cin, k, words, static_cast<__half*>(sc.b_hi),
+                                            static_cast<__half*>(sc.b_lo));
+    if (cudaGetLastError() != cudaSuccess) return OP_CUDA;
+    TcScratch as;
+    as.a_hi = sc.a_hi;
+    as.a_lo = sc.a_lo;
+    as.elems = sc.a_elems;
+    as.err = sc.err;
+    if (launch_tc_prep(x, alpha, alpha ? inv_alpha : nullptr, rows, Cin, &as, s) != cudaSuccess) return OP_CUDA;
+    TcWeights tw;
+    tw.hi = sc.b_hi;
+    tw.lo = sc.b_lo;
+    tw.BN = pick_bn(Cout);
+    tw.n_tiles = (Cout + tw.BN - 1) / tw.BN;
+    if (!make_map(&tw.map_hi, sc.b_hi, (uint64_t)K, (uint64_t)Cout, kBK, (uint32_t)tw.BN)) return OP_CUDA;
+    if (!make_map(&tw.map_lo, sc.b_lo, (uint64_t)K, (uint64_t)Cout, kBK, (uint32_t)tw.BN)) return OP_CUDA;
+    GemmArgs a{};
+    a.in = x;
+    a.in_l = Layout{1, (int)H};
+    a.Cin = Cin;
+    a.ntaps = k;
+    for (int j = 0; j < k; j++) a.shift[j] = (k - 1 - j) * dil;
+    a.N = Cout;
+    a.K = (int)K;
+    a.bias = bias;
+    a.bias_mod = Cout;
+    a.out = y;
+    a.out_l = Layout{1, 0};
+    a.out_C = Cout;
+    a.out_step = 1;
+    a.epi = EPI_STORE;
+    a.scale = 1.f;
+    a.tcum = words + kOpPlan + 6;
+    a.bm = kBM;
+    PlanView plan{1, words + kOpPlan + 2, words + kOpPlan + 4, reinterpret_cast<const long long*>(words + kOpPlan),
+                  words + kOpPlan + 5};
+    const int n_row_tiles = (T + kBM - 1) / kBM;
+    if (tc_gemm_core(a, tw, reinterpret_cast<const float*>(words) + kOpUnscale, plan, n_row_tiles, sc.a_hi, sc.a_lo,
+                     rows, sc.err, num_sms, s) != cudaSuccess)
+        return OP_CUDA;
+    return OP_OK;
 }
 
 }  // namespace codec

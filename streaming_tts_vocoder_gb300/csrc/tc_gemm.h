@@ -22,6 +22,21 @@ struct TcWeights {
     int n_tiles = 0;
 };
 
+// Scratch of one standalone tensor-core conv: operand planes, and kOpWords
+// words for its one-segment plan, weight scale and 1/alpha.
+constexpr int kOpMaxCin = 4096;
+constexpr int kOpWords = 16 + kOpMaxCin;
+struct TcOpScratch {
+    void* a_hi = nullptr;
+    void* a_lo = nullptr;
+    size_t a_elems = 0;
+    void* b_hi = nullptr;
+    void* b_lo = nullptr;
+    size_t b_elems = 0;
+    int* words = nullptr;
+    int* err = nullptr;
+};
+
 // Per-state scratch for the A-operand planes (Snake applied, split into fp16
 // hi and lo), big enough for the widest input of any contraction, plus the
 // sticky flag a kernel sets when one of its bounded waits expires.
@@ -30,12 +45,13 @@ struct TcScratch {
     void* a_lo = nullptr;
     size_t elems = 0;
     int* err = nullptr;
+    TcOpScratch op;       // the same planes plus weight planes for codec_state_conv1d
 };
 
 bool tc_eligible(int Cin, int N);
 bool tc_pack_weights(const float* wkn, int ntaps, int Cin, int N, TcWeights* out,
                      std::vector<void*>& allocs);
-bool tc_scratch_alloc(TcScratch* s, size_t elems, std::vector<void*>& allocs);
+bool tc_scratch_alloc(TcScratch* s, size_t elems, size_t b_elems, std::vector<void*>& allocs);
 
 // A-operand planes of rows x Cin: hi = fp16(a), lo = fp16(a - hi) with
 // a = Snake(x) when alpha is given, else x.
@@ -44,5 +60,12 @@ cudaError_t launch_tc_prep(const float* x, const float* alpha, const float* inv_
 // The GEMM over the planes prepared by launch_tc_prep (a_rows rows).
 cudaError_t launch_tc_gemm(const GemmArgs& a, const TcWeights& w, PlanView plan, int n_row_tiles,
                            const TcScratch* scratch, long long a_rows, int num_sms, cudaStream_t s);
+
+// y = conv(Snake_alpha(x)) + bias for one sequence: x [(k-1) dil + T][Cin]
+// (history rows first), w [Cout][Cin][k], y [T][Cout], all device fp32;
+// alpha and bias may be null.  Returns one of OP_*.
+enum { OP_OK = 0, OP_BAD_ARG = 1, OP_TOO_BIG = 2, OP_CUDA = 3 };
+int run_tc_conv1d(const TcOpScratch& sc, const float* x, int T, int Cin, const float* w, const float* bias,
+                  const float* alpha, int Cout, int k, int dil, float* y, int num_sms, cudaStream_t s);
 
 }  // namespace codec
