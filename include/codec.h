@@ -218,6 +218,30 @@ CODEC_API codec_status codec_state_conv1d(codec_state_t* state, const float* x, 
                                           const float* w, const float* bias, const float* alpha, int32_t Cout,
                                           int32_t k, int32_t dilation, float* y, void* stream);
 
+/*
+ * codec_state_conv1d without any device allocation, for callers that cannot
+ * allocate at the point of use: a real-time audio thread (cudaMalloc can block
+ * for an unbounded time and synchronises the device), a host application
+ * whose GPU memory is owned by its own pool allocator, an embedding handed
+ * only input and output buffers.  The pages have no counterpart of this entry
+ * point; it is a service of this library.
+ *
+ * Same computation, arguments, layouts and argument errors as
+ * codec_state_conv1d, but no codec or state: the caller passes the inputs and
+ * the output, and the scratch (operand planes, plan, weight scale) lives in
+ * one 32 MiB device array of the library, which every GPU that loads the
+ * library keeps until the process exits.  Limits: (H + T) * Cin <= 4,194,304
+ * and Cout * Cin * k <= 4,194,304, else CODEC_ERR_CAPACITY with nothing
+ * enqueued.  The first call on a device looks up the array's device address
+ * on the current device (no allocation); make that first call before any
+ * stream capture.  All calls on a device share the array and it keeps the
+ * last call's contents (each call rewrites what it reads): calls that
+ * overlap on the GPU, on different streams or threads, race on it.
+ */
+CODEC_API codec_status codec_conv1d_noalloc(const float* x, int32_t T, int32_t Cin, const float* w,
+                                            const float* bias, const float* alpha, int32_t Cout, int32_t k,
+                                            int32_t dilation, float* y, void* stream);
+
 /* Frames decoded and sticky error bits of one slot.  Synchronises stream
  * (host-blocking).  Errors: CODEC_ERR_NULL, CODEC_ERR_ARG, CODEC_ERR_CUDA. */
 CODEC_API codec_status codec_state_query(codec_state_t* state, int32_t stream_id, codec_stream_info* info,

@@ -98,6 +98,7 @@ def _lib():
             "codec_status_string": (ctypes.c_char_p, [i32]),
             "codec_profile_begin": (i32, [_P, i32]),
             "codec_state_conv1d": (i32, [_P, _P, i32, i32, _P, _P, _P, i32, i32, i32, _P, _P]),
+            "codec_conv1d_noalloc": (i32, [_P, i32, i32, _P, _P, _P, i32, i32, i32, _P, _P]),
             "codec_profile_end": (i32, [_P, ctypes.POINTER(KernelStatsC), _P]),
             "codec_profile_launches": (i32, [_P, ctypes.POINTER(LaunchRecordC), i32, ctypes.POINTER(i32)]),
         }
@@ -161,6 +162,17 @@ def _stream_handle(stream):
         import torch
         stream = torch.cuda.current_stream()
     return ctypes.c_void_p(stream.cuda_stream)
+
+
+def conv1d_noalloc(x, w, y, bias=None, alpha=None, dilation=1, stream=None):
+    """codec_conv1d_noalloc: the tensor-core causal conv with no device
+    allocation (the library's fixed scratch array); same arguments as
+    CodecState.conv1d."""
+    Cout, Cin, k = w.shape
+    T = y.shape[0]
+    opt = lambda t: None if t is None else _ptr(t)
+    _check(_lib().codec_conv1d_noalloc(_ptr(x), T, Cin, _ptr(w), opt(bias), opt(alpha), Cout, k, dilation,
+                                       _ptr(y), _stream_handle(stream)), "codec_conv1d_noalloc")
 
 
 class Codec:
