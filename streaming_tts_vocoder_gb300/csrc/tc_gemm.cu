@@ -12,11 +12,11 @@
 // by more than 10x on random weights.  The tensor core adds each MMA's
 // products to the fp32 accumulator with truncation, not rounding; over the
 // hundreds of k-steps of a long conv that bias alone costs about 20x in the
-// output error.  So a tile's k-loop is cut into chunks of 8 k-steps: each
+// output error.  So a tile's k-loop is cut into chunks of 16 k-steps: each
 // chunk starts from a zero accumulator, and the epilogue folds every chunk
 // into per-row fp32 sums in registers with rounded adds, in chunk order.  The
-// truncation then acts on 8-step partial sums only, and the GEMM is about as
-// accurate as an fp32 FMA loop.
+// truncation then acts on 16-step partial sums only, and the decoder's output
+// error stays within a small factor of an fp32 FMA loop's.
 //
 // Implicit GEMM: output row t of stream segment b takes, for tap j, the
 // input row base(b) + t - shift_j, so a k-block is one TMA box at a shifted
@@ -36,10 +36,11 @@
 //                and MMA issuer (one thread); gives registers away
 //   warpgroups 1, 2  epilogue: with two M-tiles, warpgroup 1 + g takes
 //                M-tile g; with one, it takes columns 128 g .. 128 g + 127
-// A warp of an epilogue warpgroup reads TMEM lanes 32 (w % 4) .. +31.  Two
-// TMEM buffers of 256 columns alternate between chunks, so the epilogue
-// drains one while the MMA fills the other.  Every wait is bounded: when one expires the CTA raises a flag,
-// stops, drains its copies and MMAs, frees TMEM and returns.
+// A warp of an epilogue warpgroup reads TMEM lanes 32 (w % 4) .. +31.  Two to
+// four TMEM buffers (as many as fit in 512 columns) rotate between chunks, so
+// the epilogue drains one while the MMA fills the next.  Every wait is
+// bounded: when one expires the CTA raises a flag, stops, drains its copies
+// and MMAs, frees TMEM and returns.
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 
@@ -60,11 +61,12 @@ constexpr int kThreads = 384;        // 3 warpgroups
 constexpr int kEpiWarps = 8;
 constexpr int kMaxBN = 256;          // 2 buffers x 256 columns = 512
 constexpr int kEpiCols = 128;        // columns one epilogue thread sums
+constexpr int kMaxBufs = 4;          // TMEM chunk buffers
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSpinLimit = 1u << 25;
 constexpr int kSmemBudget = 220 * 1024;
 constexpr uint32_t kAPlaneBytes = kBM * kBK * 2;   // 8 KB: one M-tile, one plane
-constexpr int kChunkKb = 4;          // 4 k-blocks = 128 of K = 8 MMA k-steps per TMEM chunk
+constexpr int kChunkKb = 8;          // 8 k-blocks = 256 of K = 16 MMA k-steps per TMEM chunk
 
 struct TcParams {
     int n_row_tiles;
@@ -81,6 +83,7 @@ struct TcParams {
     uint32_t idesc;
     uint32_t buf_cols;    // TMEM columns per buffer: mtiles x round32(BN) <= 256
     uint32_t mt_cols;     // TMEM column offset between the M-tiles of a buffer
+    int nbuf;             // TMEM buffers (512 / buf_cols, at most kMaxBufs)
     int chunk_kb;         // k-blocks accumulated in TMEM before the epilogue folds them in
     float unscale;
     const float* unscale_dev;   // when set, the accumulator scale is read from here
@@ -325,8 +328,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(
     uint64_t* full = bars;
     uint64_t* empty = bars + p.stages;
     uint64_t* tfull = bars + 2 * p.stages;
-    uint64_t* tempty = tfull + 2;
-    uint64_t* drain = tempty + 2;
+    uint64_t* tempty = tfull + kMaxBufs;
+    uint64_t* drain = tempty + kMaxBufs;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -336,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
-        for (int i = 0; i < 2; i++) {
+        for (int i = 0; i < p.nbuf; i++) {
             mbar_init(&tfull[i], 1);
             mbar_init(&tempty[i], kEpiWarps);
         }
@@ -406,11 +409,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(
             bool ok = true;
             for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
                 for (int kb0 = 0; kb0 < p.nkb && ok; kb0 += p.chunk_kb, chunk_it++) {
-                    const int acc = chunk_it & 1;
-                    const uint32_t aph = (uint32_t)(chunk_it >> 1) & 1u;
+                    const int acc = chunk_it % p.nbuf;
+                    const uint32_t aph = (uint32_t)(chunk_it / p.nbuf) & 1u;
                     if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t d0 = tmem_base + (uint32_t)acc * (uint32_t)kMaxBN;
+                    const uint32_t d0 = tmem_base + (uint32_t)acc * p.buf_cols;
                     const uint32_t d1 = d0 + p.mt_cols;
                     const int kb1 = min(p.nkb, kb0 + p.chunk_kb);
                     for (int kb = kb0; kb < kb1; kb++, it++) {
@@ -487,15 +490,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(
 #pragma unroll
             for (int i = 0; i < kEpiCols; i++) sum[i] = 0.f;
             for (int kb0 = 0; kb0 < p.nkb; kb0 += p.chunk_kb, chunk_it++) {
-                const int acc = chunk_it & 1;
-                const uint32_t aph = (uint32_t)(chunk_it >> 1) & 1u;
+                const int acc = chunk_it % p.nbuf;
+                const uint32_t aph = (uint32_t)(chunk_it / p.nbuf) & 1u;
                 // one lane polls, the warp follows its verdict (tcgen05.ld needs a converged warp)
                 int w_ok = 1;
                 if (lane == 0) w_ok = mbar_wait(&tfull[acc], aph, abort_flag) ? 1 : 0;
                 w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
                 if (!w_ok) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)acc * (uint32_t)kMaxBN +
+                const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)acc * p.buf_cols +
                                            (uint32_t)my_mt * p.mt_cols + (uint32_t)col0;
                 // 32-column batches: one x32 load, one wait
 #pragma unroll
@@ -704,12 +707,13 @@ cudaError_t tc_gemm_core(const GemmArgs& a, const TcWeights& w, const float* uns
     p.b_stride = round1024((uint32_t)w.BN * kBK * 2);
     p.stage_bytes = 2 * (uint32_t)p.mtiles * kAPlaneBytes + 2 * p.b_stride;
     p.tx_bytes = 2 * (uint32_t)p.mtiles * kAPlaneBytes + 2 * (uint32_t)w.BN * kBK * 2;
-    const int extra = 1024 + 256;
+    const int extra = 1024 + 512;
     p.stages = std::min(8, (kSmemBudget - extra) / (int)p.stage_bytes);
     if (p.stages < 2) return cudaErrorInvalidValue;
     p.idesc = idesc_f16(kBM, w.BN);
     p.mt_cols = (uint32_t)((w.BN + 31) / 32 * 32);
     p.buf_cols = (uint32_t)p.mtiles * p.mt_cols;
+    p.nbuf = std::min<int>(kMaxBufs, (int)(kTmemCols / p.buf_cols));
     // a short k-loop (<= 12 k-blocks, 24 k-steps) accumulates in one chunk;
     // longer ones are cut every kChunkKb k-blocks
     p.chunk_kb = p.nkb <= 12 ? p.nkb : kChunkKb;
