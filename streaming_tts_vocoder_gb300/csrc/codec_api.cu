@@ -534,7 +534,9 @@ codec_status codec_state_create(codec_t* c, int32_t n_streams, codec_state_t** o
             for (int j = 0; j < g.n_rb; j++)
                 for (int i = 0; i < g.n_dil; i++) need(c->rb[c->rb_index(si, j, i)], g.n_up + 1 + si, true);
         }
-        if (!tc_scratch_alloc(&s->tc_scratch, std::max<size_t>(elems, 4), b_elems, A)) st = CODEC_ERR_OOM;
+        // split-GEMM partials: 64 M floats (256 MB)
+        if (!tc_scratch_alloc(&s->tc_scratch, std::max<size_t>(elems, 4), b_elems, size_t(64) << 20, A))
+            st = CODEC_ERR_OOM;
     }
     if (st == CODEC_OK && cudaDeviceSynchronize() != cudaSuccess) st = CODEC_ERR_CUDA;
     if (st != CODEC_OK) {
@@ -770,9 +772,12 @@ struct Launcher {
             run(CODEC_KERNEL_OPERAND_PREP, 0.0, 8.0 * (double)arows * C.Cin, what, [&] {
                 return launch_tc_prep(in, C.alpha, C.inv_alpha, arows, C.Cin, &s->tc_scratch, cs);
             });
+            int extra = 0;
             run(CODEC_KERNEL_GEMM_TC, flops, bytes, what, [&] {
-                return launch_tc_gemm(a, C.tc, pv, ntiles128[in_lvl], &s->tc_scratch, arows, s->c->num_sms, cs);
+                return launch_tc_gemm(a, C.tc, pv, ntiles128[in_lvl], &s->tc_scratch, arows, s->c->num_sms, cs,
+                                      &extra);
             });
+            launches += extra > 1 ? extra - 1 : 0;   // the split reduction, timed with its GEMM
         } else {
             a.tcum = tc64 + (size_t)in_lvl * S1;
             a.bm = 64;

@@ -85,6 +85,10 @@ struct TcParams {
     uint32_t mt_cols;     // TMEM column offset between the M-tiles of a buffer
     int nbuf;             // TMEM buffers (512 / buf_cols, at most kMaxBufs)
     int chunk_kb;         // k-blocks accumulated in TMEM before the epilogue folds them in
+    int n_chunks;         // chunks of a tile's k-loop
+    int n_splits;         // CTA tiles per output tile along K (1: fold in registers)
+    int cps;              // chunks per split
+    float* ws;            // n_splits > 1: chunk partials [n_chunks][n_row_tiles][128][N]
     float unscale;
     const float* unscale_dev;   // when set, the accumulator scale is read from here
     int* err;
@@ -253,15 +257,15 @@ __device__ __forceinline__ void epi_store32(const GemmArgs& a, const PlanView& p
         }
 #pragma unroll
         for (int q = 0; q < 8; q++)
-            dst[q] = make_float4(v[4 * q] * unscale, v[4 * q + 1] * unscale, v[4 * q + 2] * unscale,
-                                 v[4 * q + 3] * unscale);
+            dst[q] = make_float4(__fmul_rn(v[4 * q], unscale), __fmul_rn(v[4 * q + 1], unscale),
+                                 __fmul_rn(v[4 * q + 2], unscale), __fmul_rn(v[4 * q + 3], unscale));
         return;
     }
     const bool vec = count == 32 && a.epi != EPI_QKV && ((out_row * a.out_C + n0) & 3) == 0;
     if (!vec) {
 #pragma unroll
         for (int i = 0; i < 32; i++)
-            if (i < count) gemm_store(a, plan, b, t, out_row, n0 + i, v[i] * unscale);
+            if (i < count) gemm_store(a, plan, b, t, out_row, n0 + i, __fmul_rn(v[i], unscale));
         return;
     }
     const long long idx = out_row * a.out_C + n0;
@@ -284,9 +288,9 @@ __device__ __forceinline__ void epi_store32(const GemmArgs& a, const PlanView& p
         float y[4];
 #pragma unroll
         for (int e = 0; e < 4; e++) {
-            y[e] = v[4 * q + e] * unscale;
+            y[e] = __fmul_rn(v[4 * q + e], unscale);
             if (a.bias) {
-                y[e] += __ldg(a.bias + bi);
+                y[e] = __fadd_rn(y[e], __ldg(a.bias + bi));
                 bi = (bi + 1 == a.bias_mod) ? 0 : bi + 1;
             }
             if (a.epi == EPI_GELU) y[e] = gelu_f(y[e]);
@@ -357,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const int total_tiles = p.n_mgroups * p.n_tiles_n;
+    const int total_tiles = p.n_mgroups * p.n_tiles_n * p.n_splits;
     const float unscale = p.unscale_dev ? *p.unscale_dev : p.unscale;
     const int wg = warp >> 2;
 
@@ -368,12 +372,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(
             int it = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
-                const int mg = tile / p.n_tiles_n;
+                const int sp = tile % p.n_splits, mn = tile / p.n_splits;
+                const int mg = mn / p.n_tiles_n;
                 const TileRows t0 = tile_rows(a, plan, p.mtiles * mg);
                 const TileRows t1 =
                     (p.mtiles == 2 && 2 * mg + 1 < p.n_row_tiles) ? tile_rows(a, plan, 2 * mg + 1) : t0;
-                const int n0 = (tile % p.n_tiles_n) * p.BN;
-                for (int kb = 0; kb < p.nkb; kb++, it++) {
+                const int n0 = (mn % p.n_tiles_n) * p.BN;
+                const int kb_lo = sp * p.cps * p.chunk_kb, kb_hi = min(p.nkb, kb_lo + p.cps * p.chunk_kb);
+                for (int kb = kb_lo; kb < kb_hi; kb++, it++) {
                     const int s = it % p.stages;
                     const uint32_t ph = (uint32_t)(it / p.stages) & 1u;
                     if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag)) { ok = false; break; }
@@ -408,7 +414,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(
             int it = 0, chunk_it = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
-                for (int kb0 = 0; kb0 < p.nkb && ok; kb0 += p.chunk_kb, chunk_it++) {
+                const int sp = tile % p.n_splits;
+                const int kb_lo = sp * p.cps * p.chunk_kb, kb_hi = min(p.nkb, kb_lo + p.cps * p.chunk_kb);
+                for (int kb0 = kb_lo; kb0 < kb_hi && ok; kb0 += p.chunk_kb, chunk_it++) {
                     const int acc = chunk_it % p.nbuf;
                     const uint32_t aph = (uint32_t)(chunk_it / p.nbuf) & 1u;
                     if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag)) { ok = false; break; }
@@ -477,10 +485,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(
         int chunk_it = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
-            const int mt = p.mtiles * (tile / p.n_tiles_n) + my_mt;
-            const int n0 = (tile % p.n_tiles_n) * p.BN + col0;
+            const int sp = tile % p.n_splits, mn = tile / p.n_splits;
+            const int kb_lo = sp * p.cps * p.chunk_kb, kb_hi = min(p.nkb, kb_lo + p.cps * p.chunk_kb);
+            const int mt = p.mtiles * (mn / p.n_tiles_n) + my_mt;
+            const int n0 = (mn % p.n_tiles_n) * p.BN + col0;
             const int nvalid = min(ncol, a.N - n0);
-            if (mt < p.n_row_tiles && nvalid > 0) {
+            if (p.n_splits == 1 && mt < p.n_row_tiles && nvalid > 0) {
                 const TileRows tr = tile_rows(a, plan, mt);
                 if (m < tr.nrows)
                     epi_prefetch(a, seg_base(a.out_l, plan.cf, tr.b) + (long long)(tr.t0 + m) * a.out_step, n0,
@@ -489,7 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(
             float sum[kEpiCols];
 #pragma unroll
             for (int i = 0; i < kEpiCols; i++) sum[i] = 0.f;
-            for (int kb0 = 0; kb0 < p.nkb; kb0 += p.chunk_kb, chunk_it++) {
+            for (int kb0 = kb_lo; kb0 < kb_hi; kb0 += p.chunk_kb, chunk_it++) {
                 const int acc = chunk_it % p.nbuf;
                 const uint32_t aph = (uint32_t)(chunk_it / p.nbuf) & 1u;
                 // one lane polls, the warp follows its verdict (tcgen05.ld needs a converged warp)
@@ -501,14 +511,24 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(
                 const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)acc * p.buf_cols +
                                            (uint32_t)my_mt * p.mt_cols + (uint32_t)col0;
                 // 32-column batches: one x32 load, one wait
+                // split tiles hand each chunk's partial to the reduce kernel
+                float* wrow = nullptr;
+                if (p.n_splits > 1 && mt < p.n_row_tiles)
+                    wrow = p.ws + (((size_t)(kb0 / p.chunk_kb) * p.n_row_tiles + mt) * kBM + m) * a.N + n0;
 #pragma unroll
                 for (int c = 0; c < kEpiCols; c += 32) {
                     if (c < ncol) {
                         uint32_t r[32];
                         tmem_ld32_async(lane_base + (uint32_t)c, r);
                         tmem_wait_ld();
+                        if (p.n_splits == 1) {
 #pragma unroll
-                        for (int i = 0; i < 32; i++) sum[c + i] = __fadd_rn(sum[c + i], __uint_as_float(r[i]));
+                            for (int i = 0; i < 32; i++) sum[c + i] = __fadd_rn(sum[c + i], __uint_as_float(r[i]));
+                        } else if (wrow && c < nvalid) {
+#pragma unroll
+                            for (int i = 0; i < 32; i++)
+                                if (c + i < nvalid) wrow[c + i] = __uint_as_float(r[i]);
+                        }
                     }
                 }
                 tc_fence_before();
@@ -516,7 +536,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(
                 if (lane == 0) mbar_arrive(&tempty[acc]);
             }
             if (!ok) break;
-            if (mt >= p.n_row_tiles || nvalid <= 0) continue;
+            if (p.n_splits > 1 || mt >= p.n_row_tiles || nvalid <= 0) continue;
             const TileRows tr = tile_rows(a, plan, mt);
             if (m < tr.nrows) {
                 const int t = tr.t0 + m;
@@ -541,6 +561,34 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(
                      : "memory");
     }
     if (threadIdx.x == 0 && *abort_flag) atomicExch(p.err, 1);
+}
+
+// Split tiles: fold the chunk partials of each output in chunk order with
+// rounded adds, exactly as the unsplit epilogue folds them in registers, then
+// run the same epilogue.  One thread per (row, 32 columns).
+__global__ void __launch_bounds__(kBM) tc_reduce_kernel(const GemmArgs a, const PlanView plan, const float* __restrict__ ws,
+                                                        int n_chunks, int n_row_tiles, float unscale,
+                                                        const float* __restrict__ unscale_dev)
+{
+    const int mt = blockIdx.x;
+    const int n0 = blockIdx.y * 32;
+    const int m = threadIdx.x;
+    const TileRows tr = tile_rows(a, plan, mt);
+    if (m >= tr.nrows) return;
+    const int count = min(32, a.N - n0);
+    const float us = unscale_dev ? *unscale_dev : unscale;
+    float sum[32];
+#pragma unroll
+    for (int i = 0; i < 32; i++) sum[i] = 0.f;
+    for (int c = 0; c < n_chunks; c++) {
+        const float* src = ws + (((size_t)c * n_row_tiles + mt) * kBM + m) * a.N + n0;
+#pragma unroll
+        for (int i = 0; i < 32; i++)
+            if (i < count) sum[i] = __fadd_rn(sum[i], src[i]);
+    }
+    const int t = tr.t0 + m;
+    const long long out_row = seg_base(a.out_l, plan.cf, tr.b) + (long long)t * a.out_step;
+    epi_store32(a, plan, tr.b, t, out_row, n0, count, sum, us);
 }
 
 // hi = fp16(a), lo = fp16(a - hi), a = Snake(x) or x; four channels per thread.
@@ -647,8 +695,13 @@ bool tc_pack_weights(const float* wkn, int ntaps, int Cin, int N, TcWeights* out
     return true;
 }
 
-bool tc_scratch_alloc(TcScratch* s, size_t elems, size_t b_elems, std::vector<void*>& allocs)
+bool tc_scratch_alloc(TcScratch* s, size_t elems, size_t b_elems, size_t ws_floats, std::vector<void*>& allocs)
 {
+    if (ws_floats) {
+        if (cudaMalloc(&s->ws, ws_floats * sizeof(float)) != cudaSuccess) return false;
+        allocs.push_back(s->ws);
+        s->ws_floats = ws_floats;
+    }
     s->op.b_elems = b_elems;
     for (void** q : {&s->op.b_hi, &s->op.b_lo}) {
         if (cudaMalloc(q, std::max<size_t>(b_elems, 1) * sizeof(__half)) != cudaSuccess) return false;
@@ -690,7 +743,7 @@ namespace {
 
 cudaError_t tc_gemm_core(const GemmArgs& a, const TcWeights& w, const float* unscale_dev, PlanView plan,
                          int n_row_tiles, const void* a_hi, const void* a_lo, long long a_rows, int* err,
-                         int num_sms, cudaStream_t s)
+                         int num_sms, cudaStream_t s, float* ws, size_t ws_floats, int* launches)
 {
     if (n_row_tiles <= 0) return cudaSuccess;
     alignas(64) CUtensorMap ma_hi, ma_lo;
@@ -717,6 +770,25 @@ cudaError_t tc_gemm_core(const GemmArgs& a, const TcWeights& w, const float* uns
     // a short k-loop (<= 12 k-blocks, 24 k-steps) accumulates in one chunk;
     // longer ones are cut every kChunkKb k-blocks
     p.chunk_kb = p.nkb <= 12 ? p.nkb : kChunkKb;
+    p.n_chunks = (p.nkb + p.chunk_kb - 1) / p.chunk_kb;
+    // Too few tiles to fill the GPU: split the k-loop over CTAs by whole
+    // chunks.  The reduce kernel folds the chunk partials in the same order
+    // as the unsplit epilogue, so splitting never changes a result's bits.
+    p.n_splits = 1;
+    p.cps = p.n_chunks;
+    p.ws = nullptr;
+    {
+        const int sms = num_sms > 0 ? num_sms : 152;
+        const int tiles = ((n_row_tiles + p.mtiles - 1) / p.mtiles) * w.n_tiles;
+        const size_t need = (size_t)p.n_chunks * n_row_tiles * kBM * a.N;
+        if (ws && tiles < sms / 2 && p.n_chunks >= 2 && need <= ws_floats) {
+            int ns = std::min(p.n_chunks, (sms + tiles - 1) / tiles);
+            p.cps = (p.n_chunks + ns - 1) / ns;
+            p.n_splits = (p.n_chunks + p.cps - 1) / p.cps;
+            if (p.n_splits > 1) p.ws = ws;
+            else p.cps = p.n_chunks;
+        }
+    }
     p.unscale = w.unscale;
     p.unscale_dev = unscale_dev;
     p.err = err;
@@ -727,19 +799,25 @@ cudaError_t tc_gemm_core(const GemmArgs& a, const TcWeights& w, const float* uns
         if (e != cudaSuccess) return e;
         configured = 1;
     }
-    const int tiles = p.n_mgroups * w.n_tiles;
+    const int tiles = p.n_mgroups * w.n_tiles * p.n_splits;
     const int grid = std::min(tiles, num_sms > 0 ? num_sms : 152);
     tc_gemm_kernel<<<grid, kThreads, smem, s>>>(ma_hi, ma_lo, w.map_hi, w.map_lo, a, plan, p);
+    cudaError_t e = cudaGetLastError();
+    if (launches) (*launches)++;
+    if (e != cudaSuccess || p.n_splits == 1) return e;
+    tc_reduce_kernel<<<dim3(n_row_tiles, (a.N + 31) / 32), kBM, 0, s>>>(a, plan, p.ws, p.n_chunks, n_row_tiles,
+                                                                        p.unscale, unscale_dev);
+    if (launches) (*launches)++;
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_tc_gemm(const GemmArgs& a, const TcWeights& w, PlanView plan, int n_row_tiles,
-                           const TcScratch* scratch, long long a_rows, int num_sms, cudaStream_t s)
+                           const TcScratch* scratch, long long a_rows, int num_sms, cudaStream_t s, int* launches)
 {
     return tc_gemm_core(a, w, nullptr, plan, n_row_tiles, scratch->a_hi, scratch->a_lo, a_rows, scratch->err,
-                        num_sms, s);
+                        num_sms, s, scratch->ws, scratch->ws_floats, launches);
 }
 
 // ------------------------------------------------------- standalone conv --
@@ -857,7 +935,7 @@ int run_tc_conv1d(const TcOpScratch& sc, const float* x, int T, int Cin, const f
                   words + kOpPlan + 5};
     const int n_row_tiles = (T + kBM - 1) / kBM;
     if (tc_gemm_core(a, tw, reinterpret_cast<const float*>(words) + kOpUnscale, plan, n_row_tiles, sc.a_hi, sc.a_lo,
-                     rows, sc.err, num_sms, s) != cudaSuccess)
+                     rows, sc.err, num_sms, s, nullptr, 0, nullptr) != cudaSuccess)
         return OP_CUDA;
     return OP_OK;
 }

@@ -45,21 +45,26 @@ struct TcScratch {
     void* a_lo = nullptr;
     size_t elems = 0;
     int* err = nullptr;
+    float* ws = nullptr;  // chunk partials of split GEMMs
+    size_t ws_floats = 0;
     TcOpScratch op;       // the same planes plus weight planes for codec_state_conv1d
 };
 
 bool tc_eligible(int Cin, int N);
 bool tc_pack_weights(const float* wkn, int ntaps, int Cin, int N, TcWeights* out,
                      std::vector<void*>& allocs);
-bool tc_scratch_alloc(TcScratch* s, size_t elems, size_t b_elems, std::vector<void*>& allocs);
+bool tc_scratch_alloc(TcScratch* s, size_t elems, size_t b_elems, size_t ws_floats, std::vector<void*>& allocs);
 
 // A-operand planes of rows x Cin: hi = fp16(a), lo = fp16(a - hi) with
 // a = Snake(x) when alpha is given, else x.
 cudaError_t launch_tc_prep(const float* x, const float* alpha, const float* inv_alpha, long long rows, int Cin,
                            TcScratch* scratch, cudaStream_t s);
-// The GEMM over the planes prepared by launch_tc_prep (a_rows rows).
+// The GEMM over the planes prepared by launch_tc_prep (a_rows rows); when it
+// has too few tiles for the GPU it also launches the split reduction.
+// *launches is incremented per kernel launched.
 cudaError_t launch_tc_gemm(const GemmArgs& a, const TcWeights& w, PlanView plan, int n_row_tiles,
-                           const TcScratch* scratch, long long a_rows, int num_sms, cudaStream_t s);
+                           const TcScratch* scratch, long long a_rows, int num_sms, cudaStream_t s,
+                           int* launches);
 
 // y = conv(Snake_alpha(x)) + bias for one sequence: x [(k-1) dil + T][Cin]
 // (history rows first), w [Cout][Cin][k], y [T][Cout], all device fp32;
