@@ -1,0 +1,66 @@
+"""The multi-GPU path of bench.py on CPU: two gloo ranks stand in for two
+replicas.  Streams shard across replicas with no exchange, so the only
+cross-rank steps are the barrier around the timed region and the max of the
+ranks' times; the job rate is every rank's units over the slowest rank's
+time.  Also: the reference arm does no work on ranks other than 0."""
+from __future__ import annotations
+
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank(rank, world, port, out):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        bench.barrier(world)
+        local_ms = 100.0 * (rank + 1)                      # rank 1 is the slow replica
+        ms = bench.max_over_ranks(local_ms, world)
+        rate = bench.job_throughput(1280.0, ms, world)
+        bench.barrier(world)
+        out.put((rank, ms, rate))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_replicas_take_the_slowest_time():
+    world, port = 2, _free_port()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_rank, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in range(world))
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, ms, rate in res:
+        assert ms == 200.0                                 # every rank sees the max
+        assert rate == pytest.approx(2 * 1280.0 / 0.2)     # both replicas' audio over the slowest time
+
+
+def test_single_process_is_identity():
+    assert bench.max_over_ranks(12.5, 1) == 12.5
+    assert bench.job_throughput(100.0, 500.0, 1) == pytest.approx(200.0)
+
+
+def test_reference_arm_idle_on_other_ranks(monkeypatch):
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+
+    class Args:
+        decoder, steps, warmup = "tiny", 1, 0
+
+    assert bench.run_reference(Args()) == 0
