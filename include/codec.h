@@ -247,6 +247,15 @@ CODEC_API codec_status codec_conv1d_noalloc(const float* x, int32_t T, int32_t C
 CODEC_API codec_status codec_state_query(codec_state_t* state, int32_t stream_id, codec_stream_info* info,
                                void* stream);
 
+/* Graph replay (on by default): a decode call whose shape (the per-stream
+ * frame counts, T_max) and buffers (codes, audio, pre_tanh) match an earlier
+ * call replays that call's captured CUDA graph instead of launching its
+ * kernels one by one; a shape is captured the second time it is seen.  Results are the
+ * same either way.  enable = 0 turns replay off and frees the graphs (it
+ * synchronises the device).  Calls made while codec_profile_begin is active
+ * launch directly.  Errors: CODEC_ERR_NULL, CODEC_ERR_CUDA. */
+CODEC_API codec_status codec_state_set_graphs(codec_state_t* state, int32_t enable);
+
 /* Number of stream slots of a state. */
 CODEC_API int32_t codec_state_streams(const codec_state_t* state);
 

@@ -97,6 +97,7 @@ def _lib():
             "codec_state_last_launches": (i32, [_P]),
             "codec_status_string": (ctypes.c_char_p, [i32]),
             "codec_profile_begin": (i32, [_P, i32]),
+            "codec_state_set_graphs": (i32, [_P, i32]),
             "codec_state_conv1d": (i32, [_P, _P, i32, i32, _P, _P, _P, i32, i32, i32, _P, _P]),
             "codec_conv1d_noalloc": (i32, [_P, i32, i32, _P, _P, _P, i32, i32, i32, _P, _P]),
             "codec_profile_end": (i32, [_P, ctypes.POINTER(KernelStatsC), _P]),
@@ -281,6 +282,9 @@ class CodecState:
         _check(_lib().codec_state_query(self._h, stream_id, ctypes.byref(info), _stream_handle(stream)),
                "codec_state_query")
         return int(info.frames_decoded), int(info.error_bits)
+
+    def set_graphs(self, enable: bool):
+        _check(_lib().codec_state_set_graphs(self._h, 1 if enable else 0), "codec_state_set_graphs")
 
     def profile_begin(self, max_records: int = 65536):
         _check(_lib().codec_profile_begin(self._h, max_records), "codec_profile_begin")

@@ -33,6 +33,9 @@ cudaError_t launch_final_conv(const float* x, Layout xl, int C, const float* w, 
                               float* pre_tanh, long long audio_ld, PlanView plan, const int* tcum,
                               int n_row_tiles, cudaStream_t s);
 
+// Sets the kernels' shared-memory carve-outs; called once per codec.
+cudaError_t configure_simt_kernels();
+
 cudaError_t launch_hist_fill(const HistDesc* d, int nd, PlanView plan, cudaStream_t s);
 cudaError_t launch_hist_commit(const HistDesc* d, int nd, PlanView plan, const int* n_frames,
                                long long* frames, cudaStream_t s);

@@ -200,6 +200,7 @@ constexpr int kSwaMaxW = 128;
 constexpr int kSwaMaxDh = 128;
 constexpr int kSwaQ = 16;           // queries per block
 constexpr int kSwaWarps = 8;
+constexpr int kSwaMaxSmem = 160 * 1024;
 
 __global__ void __launch_bounds__(kSwaWarps * 32) swa_kernel(
     const float* __restrict__ q, float* __restrict__ o, const float* __restrict__ kring,
@@ -290,12 +291,7 @@ cudaError_t launch_swa(const float* q, float* o, const float* kring, const float
     if (dh > kSwaMaxDh || window > kSwaMaxW) return cudaErrorInvalidValue;
     const int maxk = kSwaQ + window - 1;
     const size_t smem = sizeof(float) * (2 * (size_t)maxk * (dh + 1) + (size_t)kSwaWarps * dh + (size_t)kSwaWarps * window);
-    static size_t configured = 0;
-    if (smem > 48 * 1024 && smem > configured) {
-        cudaError_t e = cudaFuncSetAttribute(swa_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        configured = smem;
-    }
+    if (smem > (size_t)kSwaMaxSmem) return cudaErrorInvalidValue;
     swa_kernel<<<dim3(n_qblocks, heads), kSwaWarps * 32, smem, s>>>(q, o, kring, vring, d, heads, window, ring_R,
                                                                     plan, qcum);
     return cudaGetLastError();
@@ -312,6 +308,7 @@ cudaError_t launch_swa(const float* q, float* o, const float* kring, const float
 // channel).
 constexpr int kFinalTile = 128;
 constexpr int kFinalMaxK = 16;
+constexpr int kFinalMaxSmem = 160 * 1024;
 
 __global__ void __launch_bounds__(kFinalTile) final_conv_kernel(
     const float* __restrict__ x, Layout xl, int C, const float* __restrict__ w,
@@ -377,12 +374,7 @@ cudaError_t launch_final_conv(const float* x, Layout xl, int C, const float* w, 
     if (n_row_tiles <= 0) return cudaSuccess;
     if (k > kFinalMaxK) return cudaErrorInvalidValue;
     const size_t smem = sizeof(float) * ((size_t)k * C + 2 * (size_t)C + (size_t)(kFinalTile + k - 1) * k);
-    static size_t configured = 0;
-    if (smem > 48 * 1024 && smem > configured) {
-        cudaError_t e = cudaFuncSetAttribute(final_conv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        configured = smem;
-    }
+    if (smem > (size_t)kFinalMaxSmem) return cudaErrorInvalidValue;
     final_conv_kernel<<<n_row_tiles, kFinalTile, smem, s>>>(x, xl, C, w, bias, alpha, inv_alpha, k,
                                                             audio, pre_tanh, audio_ld, plan,
                                                             plan.bidx, tcum);
@@ -456,6 +448,13 @@ cudaError_t launch_state_reset(const HistDesc* d, int nd, const int* slots, int 
     if (n_slots <= 0) return cudaSuccess;
     state_reset_kernel<<<dim3(nd + 1, n_slots), 256, 0, s>>>(d, nd, slots, frames, err_words);
     return cudaGetLastError();
+}
+
+cudaError_t configure_simt_kernels()
+{
+    cudaError_t e = cudaFuncSetAttribute(swa_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSwaMaxSmem);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(final_conv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kFinalMaxSmem);
 }
 
 }  // namespace codec

@@ -490,6 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(
             const int mt = p.mtiles * (mn / p.n_tiles_n) + my_mt;
             const int n0 = (mn % p.n_tiles_n) * p.BN + col0;
             const int nvalid = min(ncol, a.N - n0);
+            const int tile_nrows = mt < p.n_row_tiles ? tile_rows(a, plan, mt).nrows : 0;
             if (p.n_splits == 1 && mt < p.n_row_tiles && nvalid > 0) {
                 const TileRows tr = tile_rows(a, plan, mt);
                 if (m < tr.nrows)
@@ -513,7 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(
                 // 32-column batches: one x32 load, one wait
                 // split tiles hand each chunk's partial to the reduce kernel
                 float* wrow = nullptr;
-                if (p.n_splits > 1 && mt < p.n_row_tiles)
+                if (p.n_splits > 1 && mt < p.n_row_tiles && m < tile_nrows)
                     wrow = p.ws + (((size_t)(kb0 / p.chunk_kb) * p.n_row_tiles + mt) * kBM + m) * a.N + n0;
 #pragma unroll
                 for (int c = 0; c < kEpiCols; c += 32) {
@@ -565,30 +566,46 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(
 
 // Split tiles: fold the chunk partials of each output in chunk order with
 // rounded adds, exactly as the unsplit epilogue folds them in registers, then
-// run the same epilogue.  One thread per (row, 32 columns).
-__global__ void __launch_bounds__(kBM) tc_reduce_kernel(const GemmArgs a, const PlanView plan, const float* __restrict__ ws,
-                                                        int n_chunks, int n_row_tiles, float unscale,
-                                                        const float* __restrict__ unscale_dev)
+// apply the same per-element epilogue.  One thread per (row, 4 columns); the
+// partial loads of several chunks are in flight at once.
+constexpr int kReduceRows = 32;
+__global__ void __launch_bounds__(kReduceRows * 8) tc_reduce_kernel(const GemmArgs a, const PlanView plan,
+                                                                   const float* __restrict__ ws, int n_chunks,
+                                                                   int n_row_tiles, float unscale,
+                                                                   const float* __restrict__ unscale_dev)
 {
     const int mt = blockIdx.x;
-    const int n0 = blockIdx.y * 32;
-    const int m = threadIdx.x;
+    const int m = blockIdx.z * kReduceRows + (threadIdx.x >> 3);
+    const int n = (blockIdx.y * 8 + (threadIdx.x & 7)) * 4;
     const TileRows tr = tile_rows(a, plan, mt);
-    if (m >= tr.nrows) return;
-    const int count = min(32, a.N - n0);
+    if (m >= tr.nrows || n >= a.N) return;
     const float us = unscale_dev ? *unscale_dev : unscale;
-    float sum[32];
+    const size_t stride = (size_t)n_row_tiles * kBM * a.N;
+    const float* src = ws + ((size_t)mt * kBM + m) * a.N + n;
+    float sum[4] = {0.f, 0.f, 0.f, 0.f};
+    const bool v4 = n + 4 <= a.N && (a.N & 3) == 0;
+    int c = 0;
+    if (v4) {
+        for (; c + 4 <= n_chunks; c += 4) {
+            float4 p[4];
 #pragma unroll
-    for (int i = 0; i < 32; i++) sum[i] = 0.f;
-    for (int c = 0; c < n_chunks; c++) {
-        const float* src = ws + (((size_t)c * n_row_tiles + mt) * kBM + m) * a.N + n0;
+            for (int u = 0; u < 4; u++) p[u] = __ldg(reinterpret_cast<const float4*>(src + (size_t)(c + u) * stride));
 #pragma unroll
-        for (int i = 0; i < 32; i++)
-            if (i < count) sum[i] = __fadd_rn(sum[i], src[i]);
+            for (int u = 0; u < 4; u++) {
+                sum[0] = __fadd_rn(sum[0], p[u].x);
+                sum[1] = __fadd_rn(sum[1], p[u].y);
+                sum[2] = __fadd_rn(sum[2], p[u].z);
+                sum[3] = __fadd_rn(sum[3], p[u].w);
+            }
+        }
     }
+    for (; c < n_chunks; c++)
+        for (int e = 0; e < 4; e++)
+            if (n + e < a.N) sum[e] = __fadd_rn(sum[e], __ldg(src + (size_t)c * stride + e));
     const int t = tr.t0 + m;
     const long long out_row = seg_base(a.out_l, plan.cf, tr.b) + (long long)t * a.out_step;
-    epi_store32(a, plan, tr.b, t, out_row, n0, count, sum, us);
+    for (int e = 0; e < 4; e++)
+        if (n + e < a.N) gemm_store(a, plan, tr.b, t, out_row, n + e, __fmul_rn(sum[e], us));
 }
 
 // hi = fp16(a), lo = fp16(a - hi), a = Snake(x) or x; four channels per thread.
@@ -660,6 +677,11 @@ int pick_bn(int N)
 }
 
 }  // namespace
+
+cudaError_t tc_configure()
+{
+    return cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
+}
 
 bool tc_eligible(int Cin, int N) { return Cin >= kBK && Cin % kBK == 0 && N >= 16 && N % 16 == 0; }
 
@@ -793,20 +815,14 @@ cudaError_t tc_gemm_core(const GemmArgs& a, const TcWeights& w, const float* uns
     p.unscale_dev = unscale_dev;
     p.err = err;
     const size_t smem = (size_t)p.stages * p.stage_bytes + extra;
-    static int configured = 0;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
-        if (e != cudaSuccess) return e;
-        configured = 1;
-    }
     const int tiles = p.n_mgroups * w.n_tiles * p.n_splits;
     const int grid = std::min(tiles, num_sms > 0 ? num_sms : 152);
     tc_gemm_kernel<<<grid, kThreads, smem, s>>>(ma_hi, ma_lo, w.map_hi, w.map_lo, a, plan, p);
     cudaError_t e = cudaGetLastError();
     if (launches) (*launches)++;
     if (e != cudaSuccess || p.n_splits == 1) return e;
-    tc_reduce_kernel<<<dim3(n_row_tiles, (a.N + 31) / 32), kBM, 0, s>>>(a, plan, p.ws, p.n_chunks, n_row_tiles,
-                                                                        p.unscale, unscale_dev);
+    tc_reduce_kernel<<<dim3(n_row_tiles, (a.N + 31) / 32, kBM / kReduceRows), kReduceRows * 8, 0, s>>>(
+        a, plan, p.ws, p.n_chunks, n_row_tiles, p.unscale, unscale_dev);
     if (launches) (*launches)++;
     return cudaGetLastError();
 }

@@ -50,6 +50,8 @@ struct TcScratch {
     TcOpScratch op;       // the same planes plus weight planes for codec_state_conv1d
 };
 
+// Sets the GEMM kernel's shared-memory carve-out; called once per codec.
+cudaError_t tc_configure();
 bool tc_eligible(int Cin, int N);
 bool tc_pack_weights(const float* wkn, int ntaps, int Cin, int N, TcWeights* out,
                      std::vector<void*>& allocs);
