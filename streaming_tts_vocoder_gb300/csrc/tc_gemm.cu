@@ -773,7 +773,14 @@ cudaError_t tc_gemm_core(const GemmArgs& a, const TcWeights& w, const float* uns
     if (!make_map(&ma_lo, a_lo, (uint64_t)a.Cin, (uint64_t)a_rows, kBK, kBM)) return cudaErrorInvalidValue;
     TcParams p;
     p.n_row_tiles = n_row_tiles;
-    p.mtiles = w.BN <= 128 ? 2 : 1;
+    // two M-tiles share each B tile when N is narrow, unless pairing would
+    // leave SMs idle (few rows: latency matters more than B traffic).  Each
+    // M-tile's MMAs are the same either way, so the pairing never changes a
+    // result's bits.
+    {
+        const int sms = num_sms > 0 ? num_sms : 152;
+        p.mtiles = (w.BN <= 128 && ((n_row_tiles + 1) / 2) * w.n_tiles >= sms) ? 2 : 1;
+    }
     p.n_mgroups = (n_row_tiles + p.mtiles - 1) / p.mtiles;
     p.n_tiles_n = w.n_tiles;
     p.BN = w.BN;
