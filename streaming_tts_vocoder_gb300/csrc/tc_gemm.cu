@@ -64,7 +64,8 @@ constexpr int kEpiCols = 128;        // columns one epilogue thread sums
 constexpr int kMaxBufs = 4;          // TMEM chunk buffers
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSpinLimit = 1u << 25;
-constexpr int kSmemBudget = 220 * 1024;
+constexpr int kSmemBudget = 227 * 1024;   // the opt-in maximum per CTA
+constexpr int kStageOutBytes = kEpiWarps * 32 * 32 * 4;   // one 32 x 32 fp32 block per epilogue warp
 constexpr uint32_t kAPlaneBytes = kBM * kBK * 2;   // 8 KB: one M-tile, one plane
 constexpr int kChunkKb = 8;          // 8 k-blocks = 256 of K = 16 MMA k-steps per TMEM chunk
 
@@ -240,72 +241,70 @@ __device__ __forceinline__ TileRows tile_rows(const GemmArgs& a, const PlanView&
     return r;
 }
 
-// 32 consecutive output columns n0 .. n0+31 of one row (count of them valid).
-__device__ __forceinline__ void epi_store32(const GemmArgs& a, const PlanView& plan, int b, int t,
-                                            long long out_row, int n0, int count, const float* v, float unscale)
+// The epilogue leaves TMEM with one row per thread (32 rows x 32 columns per
+// warp and load).  Written to global memory that way, every warp access
+// touches 32 rows, 16 bytes each; so each 32 x 32 block first goes through
+// shared memory, and the global loads and stores then cover four rows of 128
+// contiguous bytes per warp access.  The 16-byte chunks of a staged row are
+// XOR-swizzled by the row so that the row-wise writes and the column-quad
+// reads are both free of bank conflicts.
+__device__ __forceinline__ void stage_put(float4* stg, int lane, const float* v)
 {
-    if (a.epi == EPI_QKV && count == 32 && (a.d & 31) == 0) {
-        // the 32 columns lie in one of q, K, V: q row, or the stream's ring row
-        float4* dst;
-        if (n0 < a.d) {
-            dst = reinterpret_cast<float4*>(a.out + out_row * a.d + n0);
-        } else {
-            const long long pos = __ldg(plan.pos0 + b) + t;
-            const long long rr = (long long)__ldg(plan.slot + b) * a.ring_R + (pos & (a.ring_R - 1));
-            dst = n0 < 2 * a.d ? reinterpret_cast<float4*>(a.kring + rr * a.d + (n0 - a.d))
-                               : reinterpret_cast<float4*>(a.vring + rr * a.d + (n0 - 2 * a.d));
-        }
 #pragma unroll
-        for (int q = 0; q < 8; q++)
-            dst[q] = make_float4(__fmul_rn(v[4 * q], unscale), __fmul_rn(v[4 * q + 1], unscale),
-                                 __fmul_rn(v[4 * q + 2], unscale), __fmul_rn(v[4 * q + 3], unscale));
-        return;
+    for (int j = 0; j < 8; j++)
+        stg[lane * 8 + (j ^ (lane & 7))] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+}
+
+__device__ __forceinline__ float4 stage_get(const float4* stg, int r, int cq)
+{
+    return stg[r * 8 + (cq ^ (r & 7))];
+}
+
+// Destination of four consecutive output columns n .. n+3 of output row t
+// (row out_row of the output layout), or null when they cannot be moved as
+// one aligned float4 (fewer than four valid, or a misaligned row).
+__device__ __forceinline__ float* epi_dst4(const GemmArgs& a, const PlanView& plan, int b, int t,
+                                           long long out_row, int n, int cnt)
+{
+    if (cnt < 4) return nullptr;
+    if (a.epi == EPI_QKV) {
+        if (a.d & 3) return nullptr;
+        if (n < a.d) return a.out + out_row * a.d + n;
+        const long long pos = __ldg(plan.pos0 + b) + t;
+        const long long rr = (long long)__ldg(plan.slot + b) * a.ring_R + (pos & (a.ring_R - 1));
+        return n < 2 * a.d ? a.kring + rr * a.d + (n - a.d) : a.vring + rr * a.d + (n - 2 * a.d);
     }
-    const bool vec = count == 32 && a.epi != EPI_QKV && ((out_row * a.out_C + n0) & 3) == 0;
-    if (!vec) {
-#pragma unroll
-        for (int i = 0; i < 32; i++)
-            if (i < count) gemm_store(a, plan, b, t, out_row, n0 + i, __fmul_rn(v[i], unscale));
-        return;
-    }
-    const long long idx = out_row * a.out_C + n0;
-    float4* o4 = reinterpret_cast<float4*>(a.out + idx);
-    const float4* r4 = reinterpret_cast<const float4*>(a.res ? a.res + idx : a.out + idx);
-    const bool has_res = a.epi == EPI_RESID || a.epi == EPI_MRF_FIRST || a.epi == EPI_MRF_ADD || a.epi == EPI_MRF_LAST;
-    const bool has_old = a.epi == EPI_MRF_ADD || a.epi == EPI_MRF_LAST;
-    // bias[n % bias_mod], walked with a wrapping index (the phase GEMM of a
-    // transposed conv repeats its bias every Cout columns)
-    int bi = a.bias ? n0 % a.bias_mod : 0;
-    // every load of the 32 columns is in flight before the first use
-    float4 r[8], o[8];
-#pragma unroll
-    for (int q = 0; q < 8; q++) {
-        if (has_res) r[q] = r4[q];
-        if (has_old) o[q] = o4[q];
-    }
-#pragma unroll
-    for (int q = 0; q < 8; q++) {
-        float y[4];
-#pragma unroll
-        for (int e = 0; e < 4; e++) {
-            y[e] = __fmul_rn(v[4 * q + e], unscale);
-            if (a.bias) {
-                y[e] = __fadd_rn(y[e], __ldg(a.bias + bi));
-                bi = (bi + 1 == a.bias_mod) ? 0 : bi + 1;
-            }
-            if (a.epi == EPI_GELU) y[e] = gelu_f(y[e]);
-        }
-        if (has_res) {
-            y[0] = r[q].x + y[0]; y[1] = r[q].y + y[1]; y[2] = r[q].z + y[2]; y[3] = r[q].w + y[3];
-        }
-        if (has_old) {
-            y[0] = o[q].x + y[0]; y[1] = o[q].y + y[1]; y[2] = o[q].z + y[2]; y[3] = o[q].w + y[3];
-            if (a.epi == EPI_MRF_LAST) {
-                y[0] *= a.scale; y[1] *= a.scale; y[2] *= a.scale; y[3] *= a.scale;
-            }
-        }
-        o4[q] = make_float4(y[0], y[1], y[2], y[3]);
-    }
+    const long long idx = out_row * a.out_C + n;
+    return (idx & 3) ? nullptr : a.out + idx;
+}
+
+// The per-element epilogue of the modes that read nothing back (store,
+// GELU, q/K/V scatter): sum x unscale + bias, then GELU.
+__device__ __forceinline__ float epi_plain(const GemmArgs& a, float v, float bias, float unscale)
+{
+    float y = __fmul_rn(v, unscale);
+    if (a.bias) y = __fadd_rn(y, bias);
+    if (a.epi == EPI_GELU) y = gelu_f(y);
+    return y;
+}
+
+// The same for the modes that add the residual r (and the earlier MRF sum o).
+__device__ __forceinline__ float epi_resid(const GemmArgs& a, float v, float bias, float r, float o, float unscale)
+{
+    float y = __fmul_rn(v, unscale);
+    if (a.bias) y = __fadd_rn(y, bias);
+    y = r + y;
+    if (a.epi == EPI_MRF_ADD) y = o + y;
+    if (a.epi == EPI_MRF_LAST) y = (o + y) * a.scale;
+    return y;
+}
+
+// Columns that cannot move as one aligned float4: element by element.
+__device__ __noinline__ void epi_store_slow(const GemmArgs& a, const PlanView& plan, int b, int t, long long out_row,
+                                            int n, int cnt, float4 v, float unscale)
+{
+    const float ve[4] = {v.x, v.y, v.z, v.w};
+    for (int e = 0; e < cnt && e < 4; e++) gemm_store(a, plan, b, t, out_row, n + e, __fmul_rn(ve[e], unscale));
 }
 
 // Pull the lines this row's epilogue will read (residual, earlier MRF sum)
@@ -328,7 +327,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)p.stages * p.stage_bytes);
+    float4* stage_out = reinterpret_cast<float4*>(smem + (size_t)p.stages * p.stage_bytes);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)p.stages * p.stage_bytes + kStageOutBytes);
     uint64_t* full = bars;
     uint64_t* empty = bars + p.stages;
     uint64_t* tfull = bars + 2 * p.stages;
@@ -482,6 +482,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(
         const int ncol = max(0, min(kEpiCols, p.BN - col0));
         const int q = warp & 3;
         const int m = q * 32 + lane;
+        const int cq = lane & 7;        // column quad of the transposed pass
+        float4* stg = stage_out + (warp - 4) * 256;
+        const bool has_res = a.epi == EPI_RESID || a.epi == EPI_MRF_FIRST || a.epi == EPI_MRF_ADD || a.epi == EPI_MRF_LAST;
+        const bool has_old = a.epi == EPI_MRF_ADD || a.epi == EPI_MRF_LAST;
         int chunk_it = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
@@ -490,13 +494,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(
             const int mt = p.mtiles * (mn / p.n_tiles_n) + my_mt;
             const int n0 = (mn % p.n_tiles_n) * p.BN + col0;
             const int nvalid = min(ncol, a.N - n0);
-            const int tile_nrows = mt < p.n_row_tiles ? tile_rows(a, plan, mt).nrows : 0;
-            if (p.n_splits == 1 && mt < p.n_row_tiles && nvalid > 0) {
-                const TileRows tr = tile_rows(a, plan, mt);
-                if (m < tr.nrows)
-                    epi_prefetch(a, seg_base(a.out_l, plan.cf, tr.b) + (long long)(tr.t0 + m) * a.out_step, n0,
-                                 nvalid);
-            }
+            TileRows tr{0, 0, 0, 0};
+            if (mt < p.n_row_tiles) tr = tile_rows(a, plan, mt);
+            const long long out_base = mt < p.n_row_tiles ? seg_base(a.out_l, plan.cf, tr.b) : 0;
+            if (p.n_splits == 1 && nvalid > 0 && m < tr.nrows)
+                epi_prefetch(a, out_base + (long long)(tr.t0 + m) * a.out_step, n0, nvalid);
             float sum[kEpiCols];
 #pragma unroll
             for (int i = 0; i < kEpiCols; i++) sum[i] = 0.f;
@@ -511,11 +513,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(
                 tc_fence_after();
                 const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)acc * p.buf_cols +
                                            (uint32_t)my_mt * p.mt_cols + (uint32_t)col0;
-                // 32-column batches: one x32 load, one wait
-                // split tiles hand each chunk's partial to the reduce kernel
-                float* wrow = nullptr;
-                if (p.n_splits > 1 && mt < p.n_row_tiles && m < tile_nrows)
-                    wrow = p.ws + (((size_t)(kb0 / p.chunk_kb) * p.n_row_tiles + mt) * kBM + m) * a.N + n0;
+                // split tiles hand each chunk's partial to the reduce kernel:
+                // partials [chunk][row tile][128][N]
+                float* wtile = p.n_splits > 1
+                                   ? p.ws + ((size_t)(kb0 / p.chunk_kb) * p.n_row_tiles + mt) * kBM * a.N + n0
+                                   : nullptr;
 #pragma unroll
                 for (int c = 0; c < kEpiCols; c += 32) {
                     if (c < ncol) {
@@ -525,10 +527,19 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(
                         if (p.n_splits == 1) {
 #pragma unroll
                             for (int i = 0; i < 32; i++) sum[c + i] = __fadd_rn(sum[c + i], __uint_as_float(r[i]));
-                        } else if (wrow && c < nvalid) {
+                        } else if (c < nvalid && mt < p.n_row_tiles) {
+                            stage_put(stg, lane, reinterpret_cast<const float*>(r));
+                            __syncwarp();
+                            if (c + 4 * cq < nvalid) {
 #pragma unroll
-                            for (int i = 0; i < 32; i++)
-                                if (c + i < nvalid) wrow[c + i] = __uint_as_float(r[i]);
+                                for (int i = 0; i < 8; i++) {
+                                    const int mr = q * 32 + 4 * i + (lane >> 3);
+                                    if (mr < tr.nrows)
+                                        *reinterpret_cast<float4*>(wtile + (size_t)mr * a.N + c + 4 * cq) =
+                                            stage_get(stg, 4 * i + (lane >> 3), cq);
+                                }
+                            }
+                            __syncwarp();
                         }
                     }
                 }
@@ -538,17 +549,87 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(
             }
             if (!ok) break;
             if (p.n_splits > 1 || mt >= p.n_row_tiles || nvalid <= 0) continue;
-            const TileRows tr = tile_rows(a, plan, mt);
-            if (m < tr.nrows) {
-                const int t = tr.t0 + m;
-                const long long out_row = seg_base(a.out_l, plan.cf, tr.b) + (long long)t * a.out_step;
+            // Transposed pass, one 32-column slice at a time: lane takes column
+            // quad cq of rows 4 i + lane / 8.  The loop is not unrolled (its
+            // body is long); the slice's sums are always sum[0..31], the rest
+            // move down by 32 after each slice.
+            const bool vec_ok = a.epi == EPI_QKV ? (a.d & 3) == 0 : (a.out_C & 3) == 0;
+#pragma unroll 1
+            for (int c = 0; c < nvalid; c += 32) {
+                stage_put(stg, lane, sum);
+                __syncwarp();
+                const int n = n0 + c + 4 * cq;
+                const int cnt = min(4, nvalid - c - 4 * cq);
+                float bias4[4] = {0.f, 0.f, 0.f, 0.f};
+                if (a.bias && cnt > 0) {
+                    int bi = n % a.bias_mod;
 #pragma unroll
-                for (int c = 0; c < kEpiCols; c += 32) {
-                    if (c < nvalid) {
-                        const int count = min(32, nvalid - c);
-                        if (count > 0) epi_store32(a, plan, tr.b, t, out_row, n0 + c, count, sum + c, unscale);
+                    for (int e = 0; e < 4; e++) {
+                        if (e < cnt) bias4[e] = __ldg(a.bias + bi);
+                        bi = (bi + 1 == a.bias_mod) ? 0 : bi + 1;
                     }
                 }
+                if (cnt == 4 && vec_ok && has_res) {
+                    // every load of the slice is in flight before the first store
+                    float4 rv[8], ov[8];
+                    long long off[8];
+#pragma unroll
+                    for (int i = 0; i < 8; i++) {
+                        const int mr = q * 32 + 4 * i + (lane >> 3);
+                        off[i] = -1;
+                        rv[i] = ov[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        if (mr < tr.nrows) {
+                            off[i] = (out_base + (long long)(tr.t0 + mr) * a.out_step) * a.out_C + n;
+                            rv[i] = *reinterpret_cast<const float4*>((a.res ? a.res : a.out) + off[i]);
+                            if (has_old) ov[i] = *reinterpret_cast<const float4*>(a.out + off[i]);
+                        }
+                    }
+#pragma unroll
+                    for (int i = 0; i < 8; i++) {
+                        if (off[i] >= 0) {
+                            const float4 v = stage_get(stg, 4 * i + (lane >> 3), cq);
+                            float4 y;
+                            y.x = epi_resid(a, v.x, bias4[0], rv[i].x, ov[i].x, unscale);
+                            y.y = epi_resid(a, v.y, bias4[1], rv[i].y, ov[i].y, unscale);
+                            y.z = epi_resid(a, v.z, bias4[2], rv[i].z, ov[i].z, unscale);
+                            y.w = epi_resid(a, v.w, bias4[3], rv[i].w, ov[i].w, unscale);
+                            *reinterpret_cast<float4*>(a.out + off[i]) = y;
+                        }
+                    }
+                } else if (cnt == 4 && vec_ok) {
+#pragma unroll 2
+                    for (int i = 0; i < 8; i++) {
+                        const int r = 4 * i + (lane >> 3);
+                        const int mr = q * 32 + r;
+                        if (mr < tr.nrows) {
+                            const int t = tr.t0 + mr;
+                            const float4 v = stage_get(stg, r, cq);
+                            float4 y;
+                            y.x = epi_plain(a, v.x, bias4[0], unscale);
+                            y.y = epi_plain(a, v.y, bias4[1], unscale);
+                            y.z = epi_plain(a, v.z, bias4[2], unscale);
+                            y.w = epi_plain(a, v.w, bias4[3], unscale);
+                            const long long orow = out_base + (long long)t * a.out_step;
+                            float* dst = epi_dst4(a, plan, tr.b, t, orow, n, cnt);
+                            if (dst) *reinterpret_cast<float4*>(dst) = y;
+                            else epi_store_slow(a, plan, tr.b, t, orow, n, cnt, v, unscale);
+                        }
+                    }
+                } else if (cnt > 0) {
+#pragma unroll 1
+                    for (int i = 0; i < 8; i++) {
+                        const int r = 4 * i + (lane >> 3);
+                        const int mr = q * 32 + r;
+                        if (mr < tr.nrows) {
+                            const int t = tr.t0 + mr;
+                            epi_store_slow(a, plan, tr.b, t, out_base + (long long)t * a.out_step, n, cnt,
+                                           stage_get(stg, r, cq), unscale);
+                        }
+                    }
+                }
+                __syncwarp();
+#pragma unroll
+                for (int j = 0; j < kEpiCols - 32; j++) sum[j] = sum[j + 32];
             }
         }
     }
@@ -789,7 +870,7 @@ cudaError_t tc_gemm_core(const GemmArgs& a, const TcWeights& w, const float* uns
     p.b_stride = round1024((uint32_t)w.BN * kBK * 2);
     p.stage_bytes = 2 * (uint32_t)p.mtiles * kAPlaneBytes + 2 * p.b_stride;
     p.tx_bytes = 2 * (uint32_t)p.mtiles * kAPlaneBytes + 2 * (uint32_t)w.BN * kBK * 2;
-    const int extra = 1024 + 512;
+    const int extra = 1024 + 512 + kStageOutBytes;
     p.stages = std::min(8, (kSmemBudget - extra) / (int)p.stage_bytes);
     if (p.stages < 2) return cudaErrorInvalidValue;
     p.idesc = idesc_f16(kBM, w.BN);
