@@ -61,6 +61,8 @@ extern "C" codec_status codec_conv1d_noalloc(const float* x, int32_t T, int32_t 
             if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return CODEC_ERR_CUDA;
             int sms = 0;
             if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return CODEC_ERR_CUDA;
+            // the GEMM's shared-memory size and register split, as codec_create sets them
+            if (tc_configure() != cudaSuccess) return CODEC_ERR_CUDA;
             g_dev[dev].base = static_cast<unsigned char*>(p);
             g_dev[dev].sms = sms;
         }
