@@ -689,27 +689,52 @@ __global__ void __launch_bounds__(kReduceRows * 8) tc_reduce_kernel(const GemmAr
         if (n + e < a.N) gemm_store(a, plan, tr.b, t, out_row, n + e, __fmul_rn(sum[e], us));
 }
 
-// hi = fp16(a), lo = fp16(a - hi), a = Snake(x) or x; four channels per thread.
-__global__ void tc_prep_kernel(const float4* __restrict__ x, const float* __restrict__ alpha,
-                               const float* __restrict__ inv_alpha, long long n4, int cin4,
-                               __half2* __restrict__ hi, __half2* __restrict__ lo)
+// hi = fp16(a), lo = fp16(a - hi), a = Snake(x) or x; eight consecutive
+// channels (32 bytes in, 16 out per plane) per thread and one unit per
+// thread, so every load of the grid can be in flight at once.  The Snake
+// parameters are read as float4 when aligned (4 loads per thread, not 16).
+__global__ void __launch_bounds__(256) tc_prep_kernel(const float4* __restrict__ x, const float* __restrict__ alpha,
+                                                      const float* __restrict__ inv_alpha, bool vec_alpha,
+                                                      unsigned units, unsigned cin8, uint4* __restrict__ hi,
+                                                      uint4* __restrict__ lo)
 {
-    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4; i += (long long)gridDim.x * blockDim.x) {
-        float4 v = x[i];
-        if (alpha) {
-            const int c = (int)(i % cin4) * 4;
-            v.x = snake_f(v.x, __ldg(alpha + c), __ldg(inv_alpha + c));
-            v.y = snake_f(v.y, __ldg(alpha + c + 1), __ldg(inv_alpha + c + 1));
-            v.z = snake_f(v.z, __ldg(alpha + c + 2), __ldg(inv_alpha + c + 2));
-            v.w = snake_f(v.w, __ldg(alpha + c + 3), __ldg(inv_alpha + c + 3));
+    const unsigned u = blockIdx.x * 256u + threadIdx.x;
+    if (u >= units) return;
+    const float4 p0 = __ldg(x + 2 * (size_t)u), p1 = __ldg(x + 2 * (size_t)u + 1);
+    float v[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+    if (alpha) {
+        const unsigned c = (u % cin8) * 8u;
+        float al[8], ia[8];
+        if (vec_alpha) {
+            const float4 a0 = __ldg(reinterpret_cast<const float4*>(alpha + c));
+            const float4 a1 = __ldg(reinterpret_cast<const float4*>(alpha + c) + 1);
+            const float4 i0 = __ldg(reinterpret_cast<const float4*>(inv_alpha + c));
+            const float4 i1 = __ldg(reinterpret_cast<const float4*>(inv_alpha + c) + 1);
+            al[0] = a0.x; al[1] = a0.y; al[2] = a0.z; al[3] = a0.w;
+            al[4] = a1.x; al[5] = a1.y; al[6] = a1.z; al[7] = a1.w;
+            ia[0] = i0.x; ia[1] = i0.y; ia[2] = i0.z; ia[3] = i0.w;
+            ia[4] = i1.x; ia[5] = i1.y; ia[6] = i1.z; ia[7] = i1.w;
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; e++) {
+                al[e] = __ldg(alpha + c + e);
+                ia[e] = __ldg(inv_alpha + c + e);
+            }
         }
-        const __half hx = __float2half_rn(v.x), hy = __float2half_rn(v.y);
-        const __half hz = __float2half_rn(v.z), hw = __float2half_rn(v.w);
-        hi[2 * i] = __halves2half2(hx, hy);
-        hi[2 * i + 1] = __halves2half2(hz, hw);
-        lo[2 * i] = __halves2half2(__float2half_rn(v.x - __half2float(hx)), __float2half_rn(v.y - __half2float(hy)));
-        lo[2 * i + 1] = __halves2half2(__float2half_rn(v.z - __half2float(hz)), __float2half_rn(v.w - __half2float(hw)));
+#pragma unroll
+        for (int e = 0; e < 8; e++) v[e] = snake_f(v[e], al[e], ia[e]);
     }
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int e = 0; e < 4; e++) {
+        const __half h0 = __float2half_rn(v[2 * e]), h1 = __float2half_rn(v[2 * e + 1]);
+        const __half l0 = __float2half_rn(v[2 * e] - __half2float(h0));
+        const __half l1 = __float2half_rn(v[2 * e + 1] - __half2float(h1));
+        h[e] = (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
+        l[e] = (uint32_t)__half_as_ushort(l0) | ((uint32_t)__half_as_ushort(l1) << 16);
+    }
+    hi[u] = make_uint4(h[0], h[1], h[2], h[3]);
+    lo[u] = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
@@ -832,13 +857,12 @@ cudaError_t launch_tc_prep(const float* x, const float* alpha, const float* inv_
 {
     const long long n = rows * Cin;
     if (n <= 0) return cudaSuccess;
-    if ((size_t)n > scratch->elems) return cudaErrorInvalidValue;
-    const long long n4 = n / 4;
-    const int threads = 256;
-    const long long blocks = std::min<long long>((n4 + threads - 1) / threads, 152LL * 16);
-    tc_prep_kernel<<<(unsigned)blocks, threads, 0, s>>>(reinterpret_cast<const float4*>(x), alpha, inv_alpha, n4,
-                                                         Cin / 4, reinterpret_cast<__half2*>(scratch->a_hi),
-                                                         reinterpret_cast<__half2*>(scratch->a_lo));
+    if ((size_t)n > scratch->elems || Cin % 8 != 0 || n / 8 >= (1LL << 32)) return cudaErrorInvalidValue;
+    const unsigned units = (unsigned)(n / 8);
+    const bool vec_alpha = alpha && ((reinterpret_cast<uintptr_t>(alpha) | reinterpret_cast<uintptr_t>(inv_alpha)) & 15) == 0;
+    tc_prep_kernel<<<(units + 255) / 256, 256, 0, s>>>(reinterpret_cast<const float4*>(x), alpha, inv_alpha, vec_alpha,
+                                                       units, (unsigned)(Cin / 8), static_cast<uint4*>(scratch->a_hi),
+                                                       static_cast<uint4*>(scratch->a_lo));
     return cudaGetLastError();
 }
 
