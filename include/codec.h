@@ -66,7 +66,15 @@ typedef enum codec_precision {
      * tcgen05 tensor cores with both operands split into fp16 hi + lo parts and
      * three MMAs (hi*hi + hi*lo + lo*hi) accumulated in fp32 in TMEM; the rest
      * on CUDA cores in fp32. */
-    CODEC_PRECISION_FP16X3 = 1
+    CODEC_PRECISION_FP16X3 = 1,
+    /* The same contractions in a single fp16 pass (hi*hi only: both operands
+     * rounded to fp16, fp32 accumulation).  Faster, but approximate: on the
+     * random-weight decoders it misses the 1e-3 waveform bound of the other
+     * two modes (its error against the fp64 reference is reported, not
+     * bounded).  The reduced-precision decoder mode of the vllm-omni "Edge TTS
+     * design" page, section 1.5 (quality row: no lower than fp16 for the
+     * decoder). */
+    CODEC_PRECISION_FP16 = 2
 } codec_precision;
 
 /*
@@ -207,7 +215,7 @@ CODEC_API codec_status codec_decode_chunk_host(codec_state_t* state, const int32
  *   w     device float [Cout][Cin][k] (PyTorch Conv1d layout)
  *   bias  device float [Cout] or NULL;  alpha device float [Cin] or NULL
  *   y     device float [T][Cout]
- * Uses the state's scratch, so it needs a state of a CODEC_PRECISION_FP16X3
+ * Uses the state's scratch, so it needs a state of a tensor-core
  * codec (else CODEC_ERR_CONFIG) and is ordered with that state's other work on
  * the same stream.  Requires Cin % 32 == 0, Cout % 16 == 0, T >= 1,
  * 1 <= k <= 16, dilation >= 1, Cin <= 4096 when alpha is given

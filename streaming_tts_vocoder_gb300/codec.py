@@ -19,6 +19,7 @@ HEADER = PKG.parent / "include" / "codec.h"
 
 PRECISION_FP32 = 0
 PRECISION_FP16X3 = 1
+PRECISION_FP16 = 2       # single fp16 pass: approximate, outside the parity bound
 STREAM_ERR_BAD_CODE = 1
 
 STATUS = {0: "CODEC_OK", 1: "CODEC_ERR_NULL", 2: "CODEC_ERR_CONFIG", 3: "CODEC_ERR_WEIGHTS",

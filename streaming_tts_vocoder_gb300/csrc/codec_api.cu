@@ -159,7 +159,9 @@ bool cfg_valid(const codec_config* c)
     if (c->final_k < 1 || c->final_k > kMaxTaps) return false;
     if (!(c->rms_eps > 0.f)) return false;
     if (c->max_streams < 1 || c->max_chunk_frames < 1 || c->max_batch_frames < c->max_chunk_frames) return false;
-    if (c->precision != CODEC_PRECISION_FP32 && c->precision != CODEC_PRECISION_FP16X3) return false;
+    if (c->precision != CODEC_PRECISION_FP32 && c->precision != CODEC_PRECISION_FP16X3 &&
+        c->precision != CODEC_PRECISION_FP16)
+        return false;
     long long spf = 1;
     for (int u = 0; u < c->n_up; u++) spf *= c->up_s;
     for (int s = 0; s < c->n_stages; s++) spf *= c->strides[s];
@@ -228,9 +230,10 @@ void finish_contraction(codec_s* c, Contraction& C, const std::vector<float>& wk
         C.alpha = dev_upload(c->allocs, alpha, (size_t)C.Cin, st);
         C.inv_alpha = dev_upload(c->allocs, inv.data(), inv.size(), st);
     }
-    C.use_tc = c->cfg.precision == CODEC_PRECISION_FP16X3 && tc_eligible(C.Cin, C.N);
+    C.use_tc = c->cfg.precision != CODEC_PRECISION_FP32 && tc_eligible(C.Cin, C.N);
     if (C.use_tc && st == CODEC_OK) {
-        if (!tc_pack_weights(wkn.data(), C.ntaps, C.Cin, C.N, &C.tc, c->allocs)) st = CODEC_ERR_OOM;
+        const int passes = c->cfg.precision == CODEC_PRECISION_FP16 ? 1 : 3;
+        if (!tc_pack_weights(wkn.data(), C.ntaps, C.Cin, C.N, passes, &C.tc, c->allocs)) st = CODEC_ERR_OOM;
     }
 }
 
@@ -532,7 +535,7 @@ codec_status codec_state_create(codec_t* c, int32_t n_streams, codec_state_t** o
     }
     s->codes_d = dev_alloc<int>(A, (size_t)S * g.Q * g.max_chunk_frames, st);
     s->audio_d = dev_alloc<float>(A, (size_t)S * g.max_chunk_frames * c->spf, st);
-    if (st == CODEC_OK && g.precision == CODEC_PRECISION_FP16X3) {
+    if (st == CODEC_OK && g.precision != CODEC_PRECISION_FP32) {
         // operand planes for the widest tensor-core input: (contraction, input level, prefixed?)
         size_t elems = 0, b_elems = 0;
         auto need = [&](const Contraction& C, int lvl, bool pref) {
@@ -806,7 +809,7 @@ struct Launcher {
             a.bm = 128;
             const long long arows = il.P ? rows_pref(in_lvl, il) : rows(in_lvl);
             run(CODEC_KERNEL_OPERAND_PREP, 0.0, 8.0 * (double)arows * C.Cin, what, [&] {
-                return launch_tc_prep(in, C.alpha, C.inv_alpha, arows, C.Cin, &s->tc_scratch, cs);
+                return launch_tc_prep(in, C.alpha, C.inv_alpha, arows, C.Cin, &s->tc_scratch, C.tc.passes == 3, cs);
             });
             int extra = 0;
             run(CODEC_KERNEL_GEMM_TC, flops, bytes, what, [&] {

@@ -77,6 +77,7 @@ struct TcParams {
     int BN;
     int nkb;            // k-blocks: ntaps * Cin / kBK
     int cin_blocks;     // Cin / kBK
+    int ntaps;
     int stages;
     uint32_t b_stride;  // bytes of one B plane in a stage (1024-aligned)
     uint32_t stage_bytes;
@@ -158,6 +159,11 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
             smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
         : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map)
+{
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -320,6 +326,10 @@ __device__ __forceinline__ void epi_prefetch(const GemmArgs& a, long long out_ro
     }
 }
 
+// kPasses: 3 for the hi/lo split (hi*hi + hi*lo + lo*hi), 1 for a single
+// fp16 pass over the hi planes only.  A compile-time parameter: the copy and
+// MMA loops stay branch-free.
+template <int kPasses>
 __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(
     const __grid_constant__ CUtensorMap ma_hi, const __grid_constant__ CUtensorMap ma_lo,
     const __grid_constant__ CUtensorMap mb_hi, const __grid_constant__ CUtensorMap mb_lo, const GemmArgs a,
@@ -338,6 +348,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // stage layout: A planes (M-tile g, plane pl) at (g NP + pl) x 8 KB, then the B planes
+    constexpr int NP = kPasses == 3 ? 2 : 1;
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.stages; s++) {
             mbar_init(&full[s], 1);
@@ -369,74 +381,93 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(
         asm volatile("setmaxnreg.dec.sync.aligned.u32 40;" ::: "memory");
         if (warp == 0 && lane == 0) {
             // ---------------------------------------------------- producer --
-            int it = 0;
+            // One thread: every dependent instruction costs its full latency,
+            // so the k-loop keeps its indices by increments (no division).
+            prefetch_tensormap(&ma_hi);
+            prefetch_tensormap(&mb_hi);
+            if (NP == 2) {
+                prefetch_tensormap(&ma_lo);
+                prefetch_tensormap(&mb_lo);
+            }
+            int it = 0, s = 0;
+            uint32_t ph = 0;
+            uint8_t* st = smem;
             bool ok = true;
             for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
                 const int sp = tile % p.n_splits, mn = tile / p.n_splits;
                 const int mg = mn / p.n_tiles_n;
-                const TileRows t0 = tile_rows(a, plan, p.mtiles * mg);
-                const TileRows t1 =
-                    (p.mtiles == 2 && 2 * mg + 1 < p.n_row_tiles) ? tile_rows(a, plan, 2 * mg + 1) : t0;
+                const long long in0 = tile_rows(a, plan, p.mtiles * mg).in_base;
+                const long long in1 =
+                    (p.mtiles == 2 && 2 * mg + 1 < p.n_row_tiles) ? tile_rows(a, plan, 2 * mg + 1).in_base : in0;
                 const int n0 = (mn % p.n_tiles_n) * p.BN;
                 const int kb_lo = sp * p.cps * p.chunk_kb, kb_hi = min(p.nkb, kb_lo + p.cps * p.chunk_kb);
-                for (int kb = kb_lo; kb < kb_hi; kb++, it++) {
-                    const int s = it % p.stages;
-                    const uint32_t ph = (uint32_t)(it / p.stages) & 1u;
+                // k-block kb = tap j x cin_blocks + channel block cb
+                int j = kb_lo / p.cin_blocks, cb = kb_lo - j * p.cin_blocks;
+                int row0 = (int)(in0 - a.shift[j]), row1 = (int)(in1 - a.shift[j]);
+                for (int kb = kb_lo; kb < kb_hi; kb++) {
                     if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag)) { ok = false; break; }
-                    const int j = kb / p.cin_blocks;
-                    const int c0 = (kb - j * p.cin_blocks) * kBK;
-                    const int row0 = (int)(t0.in_base - a.shift[j]);
-                    const int row1 = (int)(t1.in_base - a.shift[j]);
-                    uint8_t* st = smem + (size_t)s * p.stage_bytes;
+                    const int c0 = cb * kBK;
                     mbar_expect_tx(&full[s], p.tx_bytes);
                     tma_load_2d(st, &ma_hi, &full[s], c0, row0);
-                    tma_load_2d(st + kAPlaneBytes, &ma_lo, &full[s], c0, row0);
+                    if (NP == 2) tma_load_2d(st + kAPlaneBytes, &ma_lo, &full[s], c0, row0);
                     if (p.mtiles == 2) {
-                        tma_load_2d(st + 2 * kAPlaneBytes, &ma_hi, &full[s], c0, row1);
-                        tma_load_2d(st + 3 * kAPlaneBytes, &ma_lo, &full[s], c0, row1);
+                        tma_load_2d(st + NP * kAPlaneBytes, &ma_hi, &full[s], c0, row1);
+                        if (NP == 2) tma_load_2d(st + 3 * kAPlaneBytes, &ma_lo, &full[s], c0, row1);
                     }
-                    uint8_t* sb = st + 2 * p.mtiles * kAPlaneBytes;
+                    uint8_t* sb = st + NP * p.mtiles * kAPlaneBytes;
                     tma_load_2d(sb, &mb_hi, &full[s], kb * kBK, n0);
-                    tma_load_2d(sb + p.b_stride, &mb_lo, &full[s], kb * kBK, n0);
+                    if (NP == 2) tma_load_2d(sb + p.b_stride, &mb_lo, &full[s], kb * kBK, n0);
+                    it++;
+                    st += p.stage_bytes;
+                    if (++s == p.stages) {
+                        s = 0;
+                        ph ^= 1u;
+                        st = smem;
+                    }
+                    if (++cb == p.cin_blocks) {
+                        cb = 0;
+                        if (++j < p.ntaps) {
+                            row0 = (int)(in0 - a.shift[j]);
+                            row1 = (int)(in1 - a.shift[j]);
+                        }
+                    }
                 }
             }
             // drain: every stage's last armed load has landed before exit
-            for (int s = 0; s < p.stages && s < it; s++) {
-                const int last = s + ((it - 1 - s) / p.stages) * p.stages;
-                mbar_drain(&full[s], (uint32_t)(last / p.stages) & 1u);
+            for (int q = 0; q < p.stages && q < it; q++) {
+                const int last = q + ((it - 1 - q) / p.stages) * p.stages;
+                mbar_drain(&full[q], (uint32_t)(last / p.stages) & 1u);
             }
         } else if (warp == 1 && lane == 0) {
             // --------------------------------------------------- MMA issue --
             // The k-loop of a tile is cut into chunks of chunk_kb k-blocks; each
-            // chunk accumulates from zero into one of the two TMEM buffers,
-            // which the epilogue folds into rounded fp32 sums while the next
-            // chunk runs.
-            int it = 0, chunk_it = 0;
+            // chunk accumulates from zero into one of the TMEM buffers, which
+            // the epilogue folds into rounded fp32 sums while the next chunk
+            // runs.  Indices by increments, as in the producer.
+            int s = 0, acc = 0;
+            uint32_t ph = 0, aph = 0;
+            const uint32_t smem0 = smem_u32(smem);
+            uint32_t sa = smem0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
                 const int sp = tile % p.n_splits;
                 const int kb_lo = sp * p.cps * p.chunk_kb, kb_hi = min(p.nkb, kb_lo + p.cps * p.chunk_kb);
-                for (int kb0 = kb_lo; kb0 < kb_hi && ok; kb0 += p.chunk_kb, chunk_it++) {
-                    const int acc = chunk_it % p.nbuf;
-                    const uint32_t aph = (uint32_t)(chunk_it / p.nbuf) & 1u;
+                for (int kb0 = kb_lo; kb0 < kb_hi && ok; kb0 += p.chunk_kb) {
                     if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t d0 = tmem_base + (uint32_t)acc * p.buf_cols;
                     const uint32_t d1 = d0 + p.mt_cols;
                     const int kb1 = min(p.nkb, kb0 + p.chunk_kb);
-                    for (int kb = kb0; kb < kb1; kb++, it++) {
-                        const int s = it % p.stages;
-                        const uint32_t ph = (uint32_t)(it / p.stages) & 1u;
+                    for (int kb = kb0; kb < kb1; kb++) {
                         if (!mbar_wait(&full[s], ph, abort_flag)) { ok = false; break; }
                         tc_fence_after();
-                        const uint32_t sa = smem_u32(smem + (size_t)s * p.stage_bytes);
+                        // descriptors of the stage's planes: one base plus constant steps
                         const uint64_t a0h = sdesc_sw64(sa);
-                        const uint64_t a0l = sdesc_sw64(sa + kAPlaneBytes);
-                        const uint64_t a1h = sdesc_sw64(sa + 2 * kAPlaneBytes);
-                        const uint64_t a1l = sdesc_sw64(sa + 3 * kAPlaneBytes);
-                        const uint32_t sb = sa + 2 * (uint32_t)p.mtiles * kAPlaneBytes;
-                        const uint64_t bh = sdesc_sw64(sb);
-                        const uint64_t bl = sdesc_sw64(sb + p.b_stride);
+                        const uint64_t a0l = a0h + (kAPlaneBytes >> 4);
+                        const uint64_t a1h = a0h + ((NP * kAPlaneBytes) >> 4);
+                        const uint64_t a1l = a0h + ((3 * kAPlaneBytes) >> 4);
+                        const uint64_t bh = a0h + ((NP * (uint32_t)p.mtiles * kAPlaneBytes) >> 4);
+                        const uint64_t bl = bh + (p.b_stride >> 4);
                         if (p.mtiles == 2) {
 #pragma unroll
                             for (int k = 0; k < kBK / 16; k++) {
@@ -444,10 +475,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(
                                 const uint32_t accum = (kb != kb0 || k != 0) ? 1u : 0u;
                                 mma_f16(d0, a0h + o, bh + o, p.idesc, accum);
                                 mma_f16(d1, a1h + o, bh + o, p.idesc, accum);
-                                mma_f16(d0, a0h + o, bl + o, p.idesc, 1u);
-                                mma_f16(d1, a1h + o, bl + o, p.idesc, 1u);
-                                mma_f16(d0, a0l + o, bh + o, p.idesc, 1u);
-                                mma_f16(d1, a1l + o, bh + o, p.idesc, 1u);
+                                if (kPasses == 3) {
+                                    mma_f16(d0, a0h + o, bl + o, p.idesc, 1u);
+                                    mma_f16(d1, a1h + o, bl + o, p.idesc, 1u);
+                                    mma_f16(d0, a0l + o, bh + o, p.idesc, 1u);
+                                    mma_f16(d1, a1l + o, bh + o, p.idesc, 1u);
+                                }
                             }
                         } else {
 #pragma unroll
@@ -455,14 +488,26 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(
                                 const uint64_t o = (uint64_t)((k * 32) >> 4);
                                 const uint32_t accum = (kb != kb0 || k != 0) ? 1u : 0u;
                                 mma_f16(d0, a0h + o, bh + o, p.idesc, accum);
-                                mma_f16(d0, a0h + o, bl + o, p.idesc, 1u);
-                                mma_f16(d0, a0l + o, bh + o, p.idesc, 1u);
+                                if (kPasses == 3) {
+                                    mma_f16(d0, a0h + o, bl + o, p.idesc, 1u);
+                                    mma_f16(d0, a0l + o, bh + o, p.idesc, 1u);
+                                }
                             }
                         }
                         mma_commit(&empty[s]);
+                        sa += p.stage_bytes;
+                        if (++s == p.stages) {
+                            s = 0;
+                            ph ^= 1u;
+                            sa = smem0;
+                        }
                     }
                     if (!ok) break;
                     mma_commit(&tfull[acc]);
+                    if (++acc == p.nbuf) {
+                        acc = 0;
+                        aph ^= 1u;
+                    }
                 }
             }
             // all issued MMAs complete before TMEM is released
@@ -696,7 +741,7 @@ __global__ void __launch_bounds__(kReduceRows * 8) tc_reduce_kernel(const GemmAr
 __global__ void __launch_bounds__(256) tc_prep_kernel(const float4* __restrict__ x, const float* __restrict__ alpha,
                                                       const float* __restrict__ inv_alpha, bool vec_alpha,
                                                       unsigned units, unsigned cin8, uint4* __restrict__ hi,
-                                                      uint4* __restrict__ lo)
+                                                      uint4* __restrict__ lo /* null: hi only */)
 {
     const unsigned u = blockIdx.x * 256u + threadIdx.x;
     if (u >= units) return;
@@ -734,7 +779,7 @@ __global__ void __launch_bounds__(256) tc_prep_kernel(const float4* __restrict__
         l[e] = (uint32_t)__half_as_ushort(l0) | ((uint32_t)__half_as_ushort(l1) << 16);
     }
     hi[u] = make_uint4(h[0], h[1], h[2], h[3]);
-    lo[u] = make_uint4(l[0], l[1], l[2], l[3]);
+    if (lo) lo[u] = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
@@ -786,13 +831,19 @@ int pick_bn(int N)
 
 cudaError_t tc_configure()
 {
-    return cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
+    for (const void* k : {(const void*)tc_gemm_kernel<1>, (const void*)tc_gemm_kernel<3>}) {
+        const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 bool tc_eligible(int Cin, int N) { return Cin >= kBK && Cin % kBK == 0 && N >= 16 && N % 16 == 0; }
 
-bool tc_pack_weights(const float* wkn, int ntaps, int Cin, int N, TcWeights* out, std::vector<void*>& allocs)
+bool tc_pack_weights(const float* wkn, int ntaps, int Cin, int N, int passes, TcWeights* out,
+                     std::vector<void*>& allocs)
 {
+    out->passes = passes;
     const size_t K = (size_t)ntaps * Cin;
     float mx = 0.f;
     for (size_t i = 0; i < K * (size_t)N; i++) mx = std::fmax(mx, std::fabs(wkn[i]));
@@ -853,7 +904,7 @@ bool tc_scratch_alloc(TcScratch* s, size_t elems, size_t b_elems, size_t ws_floa
 }
 
 cudaError_t launch_tc_prep(const float* x, const float* alpha, const float* inv_alpha, long long rows, int Cin,
-                           TcScratch* scratch, cudaStream_t s)
+                           TcScratch* scratch, bool with_lo, cudaStream_t s)
 {
     const long long n = rows * Cin;
     if (n <= 0) return cudaSuccess;
@@ -862,7 +913,7 @@ cudaError_t launch_tc_prep(const float* x, const float* alpha, const float* inv_
     const bool vec_alpha = alpha && ((reinterpret_cast<uintptr_t>(alpha) | reinterpret_cast<uintptr_t>(inv_alpha)) & 15) == 0;
     tc_prep_kernel<<<(units + 255) / 256, 256, 0, s>>>(reinterpret_cast<const float4*>(x), alpha, inv_alpha, vec_alpha,
                                                        units, (unsigned)(Cin / 8), static_cast<uint4*>(scratch->a_hi),
-                                                       static_cast<uint4*>(scratch->a_lo));
+                                                       with_lo ? static_cast<uint4*>(scratch->a_lo) : nullptr);
     return cudaGetLastError();
 }
 
@@ -890,10 +941,12 @@ cudaError_t tc_gemm_core(const GemmArgs& a, const TcWeights& w, const float* uns
     p.n_tiles_n = w.n_tiles;
     p.BN = w.BN;
     p.cin_blocks = a.Cin / kBK;
+    p.ntaps = a.ntaps;
     p.nkb = a.ntaps * p.cin_blocks;
+    const uint32_t np = w.passes == 3 ? 2u : 1u;   // planes per operand in a stage
     p.b_stride = round1024((uint32_t)w.BN * kBK * 2);
-    p.stage_bytes = 2 * (uint32_t)p.mtiles * kAPlaneBytes + 2 * p.b_stride;
-    p.tx_bytes = 2 * (uint32_t)p.mtiles * kAPlaneBytes + 2 * (uint32_t)w.BN * kBK * 2;
+    p.stage_bytes = np * (uint32_t)p.mtiles * kAPlaneBytes + np * p.b_stride;
+    p.tx_bytes = np * (uint32_t)p.mtiles * kAPlaneBytes + np * (uint32_t)w.BN * kBK * 2;
     const int extra = 1024 + 512 + kStageOutBytes;
     p.stages = std::min(8, (kSmemBudget - extra) / (int)p.stage_bytes);
     if (p.stages < 2) return cudaErrorInvalidValue;
@@ -929,7 +982,10 @@ cudaError_t tc_gemm_core(const GemmArgs& a, const TcWeights& w, const float* uns
     const size_t smem = (size_t)p.stages * p.stage_bytes + extra;
     const int tiles = p.n_mgroups * w.n_tiles * p.n_splits;
     const int grid = std::min(tiles, num_sms > 0 ? num_sms : 152);
-    tc_gemm_kernel<<<grid, kThreads, smem, s>>>(ma_hi, ma_lo, w.map_hi, w.map_lo, a, plan, p);
+    if (w.passes == 3)
+        tc_gemm_kernel<3><<<grid, kThreads, smem, s>>>(ma_hi, ma_lo, w.map_hi, w.map_lo, a, plan, p);
+    else
+        tc_gemm_kernel<1><<<grid, kThreads, smem, s>>>(ma_hi, ma_lo, w.map_hi, w.map_lo, a, plan, p);
     cudaError_t e = cudaGetLastError();
     if (launches) (*launches)++;
     if (e != cudaSuccess || p.n_splits == 1) return e;
@@ -1033,8 +1089,9 @@ int run_tc_conv1d(const TcOpScratch& sc, const float* x, int T, int Cin, const f
     as.a_lo = sc.a_lo;
     as.elems = sc.a_elems;
     as.err = sc.err;
-    if (launch_tc_prep(x, alpha, alpha ? inv_alpha : nullptr, rows, Cin, &as, s) != cudaSuccess) return OP_CUDA;
+    if (launch_tc_prep(x, alpha, alpha ? inv_alpha : nullptr, rows, Cin, &as, true, s) != cudaSuccess) return OP_CUDA;
     TcWeights tw;
+    tw.passes = 3;
     tw.hi = sc.b_hi;
     tw.lo = sc.b_lo;
     tw.BN = pick_bn(Cout);

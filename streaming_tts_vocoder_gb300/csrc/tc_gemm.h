@@ -18,8 +18,9 @@ struct TcWeights {
     void* hi = nullptr;      // __half [N][K]
     void* lo = nullptr;
     float unscale = 1.f;     // 2^-e, applied to the accumulator
-    int BN = 0;              // N tile (multiple of 16, <= 128)
+    int BN = 0;              // N tile (multiple of 32, <= 256)
     int n_tiles = 0;
+    int passes = 3;          // 3: hi*hi + hi*lo + lo*hi; 1: hi*hi only (single fp16 pass)
 };
 
 // Scratch of one standalone tensor-core conv: operand planes, and kOpWords
@@ -53,14 +54,14 @@ struct TcScratch {
 // Sets the GEMM kernel's shared-memory carve-out; called once per codec.
 cudaError_t tc_configure();
 bool tc_eligible(int Cin, int N);
-bool tc_pack_weights(const float* wkn, int ntaps, int Cin, int N, TcWeights* out,
+bool tc_pack_weights(const float* wkn, int ntaps, int Cin, int N, int passes, TcWeights* out,
                      std::vector<void*>& allocs);
 bool tc_scratch_alloc(TcScratch* s, size_t elems, size_t b_elems, size_t ws_floats, std::vector<void*>& allocs);
 
-// A-operand planes of rows x Cin: hi = fp16(a), lo = fp16(a - hi) with
-// a = Snake(x) when alpha is given, else x.
+// A-operand planes of rows x Cin: hi = fp16(a), lo = fp16(a - hi) (lo only
+// when with_lo) with a = Snake(x) when alpha is given, else x.
 cudaError_t launch_tc_prep(const float* x, const float* alpha, const float* inv_alpha, long long rows, int Cin,
-                           TcScratch* scratch, cudaStream_t s);
+                           TcScratch* scratch, bool with_lo, cudaStream_t s);
 // The GEMM over the planes prepared by launch_tc_prep (a_rows rows); when it
 // has too few tiles for the GPU it also launches the split reduction.
 // *launches is incremented per kernel launched.
