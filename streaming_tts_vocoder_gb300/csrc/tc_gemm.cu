@@ -79,7 +79,6 @@ struct TcParams {
     int cin_blocks;     // Cin / kBK
     int ntaps;
     int stages;
-    uint32_t b_stride;  // bytes of one B plane in a stage (1024-aligned)
     uint32_t stage_bytes;
     uint32_t tx_bytes;  // bytes the TMA loads of a stage deliver
     uint32_t idesc;
@@ -176,6 +175,16 @@ __device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr)
 {
     return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(512 >> 4) << 32) |
            ((uint64_t)1 << 46) | ((uint64_t)4 << 61);
+}
+
+// The same with 128-byte swizzle: rows of 128 bytes (a k-block's 32 hi then
+// 32 lo values), 8-row groups 1024 bytes apart.  A k-step's operand starts
+// 32 bytes further per 16 elements inside the row (hi at 0 / 32, lo at 64 /
+// 96); the MMA takes the swizzle phase from the address bits.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr)
+{
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
 __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
@@ -329,11 +338,15 @@ __device__ __forceinline__ void epi_prefetch(const GemmArgs& a, long long out_ro
 // kPasses: 3 for the hi/lo split (hi*hi + hi*lo + lo*hi), 1 for a single
 // fp16 pass over the hi planes only.  A compile-time parameter: the copy and
 // MMA loops stay branch-free.
+//   3 passes: ma / mb map the interleaved operands ([rows][Cin/32][32 hi | 32
+//   lo], [N][K/32][32 hi | 32 lo]); a stage holds per M-tile one 128 x 128-byte
+//   A box and one BN x 128-byte B box, 128-byte swizzled: a k-block's hi and
+//   lo parts arrive in the same TMA row, half the copies of separate planes.
+//   1 pass: the hi planes alone in 64-byte rows, 64-byte swizzled.
 template <int kPasses>
-__global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(
-    const __grid_constant__ CUtensorMap ma_hi, const __grid_constant__ CUtensorMap ma_lo,
-    const __grid_constant__ CUtensorMap mb_hi, const __grid_constant__ CUtensorMap mb_lo, const GemmArgs a,
-    const PlanView plan, const TcParams p)
+__global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_constant__ CUtensorMap ma,
+                                                              const __grid_constant__ CUtensorMap mb,
+                                                              const GemmArgs a, const PlanView plan, const TcParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -348,8 +361,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // stage layout: A planes (M-tile g, plane pl) at (g NP + pl) x 8 KB, then the B planes
-    constexpr int NP = kPasses == 3 ? 2 : 1;
+    // stage layout: A box of M-tile g at g x kABox, then the B box
+    constexpr uint32_t kRow = kPasses == 3 ? 128u : 64u;      // bytes per operand row in a stage
+    constexpr uint32_t kABox = kBM * kRow;                    // one M-tile's A box
+    constexpr int kBoxK = kPasses == 3 ? 2 * kBK : kBK;       // box width in elements
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.stages; s++) {
             mbar_init(&full[s], 1);
@@ -383,12 +398,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(
             // ---------------------------------------------------- producer --
             // One thread: every dependent instruction costs its full latency,
             // so the k-loop keeps its indices by increments (no division).
-            prefetch_tensormap(&ma_hi);
-            prefetch_tensormap(&mb_hi);
-            if (NP == 2) {
-                prefetch_tensormap(&ma_lo);
-                prefetch_tensormap(&mb_lo);
-            }
+            prefetch_tensormap(&ma);
+            prefetch_tensormap(&mb);
             int it = 0, s = 0;
             uint32_t ph = 0;
             uint8_t* st = smem;
@@ -406,17 +417,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(
                 int row0 = (int)(in0 - a.shift[j]), row1 = (int)(in1 - a.shift[j]);
                 for (int kb = kb_lo; kb < kb_hi; kb++) {
                     if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag)) { ok = false; break; }
-                    const int c0 = cb * kBK;
+                    const int c0 = cb * kBoxK;
                     mbar_expect_tx(&full[s], p.tx_bytes);
-                    tma_load_2d(st, &ma_hi, &full[s], c0, row0);
-                    if (NP == 2) tma_load_2d(st + kAPlaneBytes, &ma_lo, &full[s], c0, row0);
-                    if (p.mtiles == 2) {
-                        tma_load_2d(st + NP * kAPlaneBytes, &ma_hi, &full[s], c0, row1);
-                        if (NP == 2) tma_load_2d(st + 3 * kAPlaneBytes, &ma_lo, &full[s], c0, row1);
-                    }
-                    uint8_t* sb = st + NP * p.mtiles * kAPlaneBytes;
-                    tma_load_2d(sb, &mb_hi, &full[s], kb * kBK, n0);
-                    if (NP == 2) tma_load_2d(sb + p.b_stride, &mb_lo, &full[s], kb * kBK, n0);
+                    tma_load_2d(st, &ma, &full[s], c0, row0);
+                    if (p.mtiles == 2) tma_load_2d(st + kABox, &ma, &full[s], c0, row1);
+                    tma_load_2d(st + p.mtiles * kABox, &mb, &full[s], kb * kBoxK, n0);
                     it++;
                     st += p.stage_bytes;
                     if (++s == p.stages) {
@@ -461,13 +466,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(
                     for (int kb = kb0; kb < kb1; kb++) {
                         if (!mbar_wait(&full[s], ph, abort_flag)) { ok = false; break; }
                         tc_fence_after();
-                        // descriptors of the stage's planes: one base plus constant steps
-                        const uint64_t a0h = sdesc_sw64(sa);
-                        const uint64_t a0l = a0h + (kAPlaneBytes >> 4);
-                        const uint64_t a1h = a0h + ((NP * kAPlaneBytes) >> 4);
-                        const uint64_t a1l = a0h + ((3 * kAPlaneBytes) >> 4);
-                        const uint64_t bh = a0h + ((NP * (uint32_t)p.mtiles * kAPlaneBytes) >> 4);
-                        const uint64_t bl = bh + (p.b_stride >> 4);
+                        // descriptors of the stage's boxes: one base plus constant
+                        // steps; in three-pass mode the lo part of a row sits 64
+                        // bytes after its hi part
+                        const uint64_t a0h = kPasses == 3 ? sdesc_sw128(sa) : sdesc_sw64(sa);
+                        const uint64_t a0l = a0h + (64 >> 4);
+                        const uint64_t a1h = a0h + (kABox >> 4);
+                        const uint64_t a1l = a1h + (64 >> 4);
+                        const uint64_t bh = a0h + (((uint32_t)p.mtiles * kABox) >> 4);
+                        const uint64_t bl = bh + (64 >> 4);
                         if (p.mtiles == 2) {
 #pragma unroll
                             for (int k = 0; k < kBK / 16; k++) {
@@ -738,17 +745,20 @@ __global__ void __launch_bounds__(kReduceRows * 8) tc_reduce_kernel(const GemmAr
 // channels (32 bytes in, 16 out per plane) per thread and one unit per
 // thread, so every load of the grid can be in flight at once.  The Snake
 // parameters are read as float4 when aligned (4 loads per thread, not 16).
+// interleaved: [rows][Cin / 32][32 hi | 32 lo] (three-pass mode: a 32-channel
+// k-block of a row is one 128-byte TMA row); else the hi plane [rows][Cin].
 __global__ void __launch_bounds__(256) tc_prep_kernel(const float4* __restrict__ x, const float* __restrict__ alpha,
                                                       const float* __restrict__ inv_alpha, bool vec_alpha,
                                                       unsigned units, unsigned cin8, uint4* __restrict__ hi,
-                                                      uint4* __restrict__ lo /* null: hi only */)
+                                                      bool interleaved)
 {
     const unsigned u = blockIdx.x * 256u + threadIdx.x;
     if (u >= units) return;
     const float4 p0 = __ldg(x + 2 * (size_t)u), p1 = __ldg(x + 2 * (size_t)u + 1);
     float v[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+    const unsigned c8 = u % cin8;
     if (alpha) {
-        const unsigned c = (u % cin8) * 8u;
+        const unsigned c = c8 * 8u;
         float al[8], ia[8];
         if (vec_alpha) {
             const float4 a0 = __ldg(reinterpret_cast<const float4*>(alpha + c));
@@ -778,8 +788,15 @@ __global__ void __launch_bounds__(256) tc_prep_kernel(const float4* __restrict__
         h[e] = (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
         l[e] = (uint32_t)__half_as_ushort(l0) | ((uint32_t)__half_as_ushort(l1) << 16);
     }
-    hi[u] = make_uint4(h[0], h[1], h[2], h[3]);
-    if (lo) lo[u] = make_uint4(l[0], l[1], l[2], l[3]);
+    if (interleaved) {
+        // [rows][Cin / 32][32 hi | 32 lo]: unit u = (row, c8) lands at
+        // 2 u - (c8 % 4) (hi) and 4 units further (lo)
+        const size_t at = 2 * (size_t)u - (c8 & 3u);
+        hi[at] = make_uint4(h[0], h[1], h[2], h[3]);
+        hi[at + 4] = make_uint4(l[0], l[1], l[2], l[3]);
+    } else {
+        hi[u] = make_uint4(h[0], h[1], h[2], h[3]);
+    }
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
@@ -808,8 +825,10 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer
     cuuint64_t strides[1] = {inner * 2};
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t estr[2] = {1, 1};
+    // 64-element (128-byte) boxes take the 128-byte swizzle, 32-element ones the 64-byte one
+    const CUtensorMapSwizzle sw = box_inner * 2 == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -849,28 +868,32 @@ bool tc_pack_weights(const float* wkn, int ntaps, int Cin, int N, int passes, Tc
     for (size_t i = 0; i < K * (size_t)N; i++) mx = std::fmax(mx, std::fabs(wkn[i]));
     const int e = mx > 0.f ? -(int)std::floor(std::log2(mx)) : 0;
     const float scale = std::ldexp(1.0f, e);
-    std::vector<__half> hi(K * N), lo(K * N);
+    // passes == 3: one [N][2K] buffer, each 32-wide k-block stored as its 32 hi
+    // then its 32 lo values (one 128-byte TMA row per k-block and n); passes
+    // == 1: the hi plane [N][K] alone
+    const size_t KP = passes == 3 ? 2 * K : K;
+    std::vector<__half> pl(KP * N);
     for (int n = 0; n < N; n++)
         for (size_t k = 0; k < K; k++) {
             const float w = wkn[k * N + n] * scale;
             const __half h = __float2half_rn(w);
-            hi[(size_t)n * K + k] = h;
-            lo[(size_t)n * K + k] = __float2half_rn(w - __half2float(h));
+            if (passes == 3) {
+                const size_t at = (size_t)n * KP + (k / kBK) * (2 * kBK) + (k % kBK);
+                pl[at] = h;
+                pl[at + kBK] = __float2half_rn(w - __half2float(h));
+            } else {
+                pl[(size_t)n * KP + k] = h;
+            }
         }
-    void *dh = nullptr, *dl = nullptr;
-    if (cudaMalloc(&dh, hi.size() * sizeof(__half)) != cudaSuccess) return false;
+    void* dh = nullptr;
+    if (cudaMalloc(&dh, pl.size() * sizeof(__half)) != cudaSuccess) return false;
     allocs.push_back(dh);
-    if (cudaMalloc(&dl, lo.size() * sizeof(__half)) != cudaSuccess) return false;
-    allocs.push_back(dl);
-    if (cudaMemcpy(dh, hi.data(), hi.size() * sizeof(__half), cudaMemcpyHostToDevice) != cudaSuccess) return false;
-    if (cudaMemcpy(dl, lo.data(), lo.size() * sizeof(__half), cudaMemcpyHostToDevice) != cudaSuccess) return false;
+    if (cudaMemcpy(dh, pl.data(), pl.size() * sizeof(__half), cudaMemcpyHostToDevice) != cudaSuccess) return false;
     out->hi = dh;
-    out->lo = dl;
     out->unscale = std::ldexp(1.0f, -e);
     out->BN = pick_bn(N);
     out->n_tiles = (N + out->BN - 1) / out->BN;
-    if (!make_map(&out->map_hi, dh, K, (uint64_t)N, kBK, (uint32_t)out->BN)) return false;
-    if (!make_map(&out->map_lo, dl, K, (uint64_t)N, kBK, (uint32_t)out->BN)) return false;
+    if (!make_map(&out->map_hi, dh, KP, (uint64_t)N, passes == 3 ? 2 * kBK : kBK, (uint32_t)out->BN)) return false;
     return true;
 }
 
@@ -881,17 +904,17 @@ bool tc_scratch_alloc(TcScratch* s, size_t elems, size_t b_elems, size_t ws_floa
         allocs.push_back(s->ws);
         s->ws_floats = ws_floats;
     }
+    // each operand's two planes in one block (lo right after hi): the
+    // three-pass layout interleaves them over the whole block
     s->op.b_elems = b_elems;
-    for (void** q : {&s->op.b_hi, &s->op.b_lo}) {
-        if (cudaMalloc(q, std::max<size_t>(b_elems, 1) * sizeof(__half)) != cudaSuccess) return false;
-        allocs.push_back(*q);
-    }
+    if (cudaMalloc(&s->op.b_hi, 2 * std::max<size_t>(b_elems, 1) * sizeof(__half)) != cudaSuccess) return false;
+    allocs.push_back(s->op.b_hi);
+    s->op.b_lo = static_cast<__half*>(s->op.b_hi) + std::max<size_t>(b_elems, 1);
     if (cudaMalloc(&s->op.words, kOpWords * sizeof(int)) != cudaSuccess) return false;
     allocs.push_back(s->op.words);
-    if (cudaMalloc(&s->a_hi, elems * sizeof(__half)) != cudaSuccess) return false;
+    if (cudaMalloc(&s->a_hi, 2 * elems * sizeof(__half)) != cudaSuccess) return false;
     allocs.push_back(s->a_hi);
-    if (cudaMalloc(&s->a_lo, elems * sizeof(__half)) != cudaSuccess) return false;
-    allocs.push_back(s->a_lo);
+    s->a_lo = static_cast<__half*>(s->a_hi) + elems;
     if (cudaMalloc(&s->err, sizeof(int)) != cudaSuccess) return false;
     allocs.push_back(s->err);
     if (cudaMemset(s->err, 0, sizeof(int)) != cudaSuccess) return false;
@@ -913,20 +936,22 @@ cudaError_t launch_tc_prep(const float* x, const float* alpha, const float* inv_
     const bool vec_alpha = alpha && ((reinterpret_cast<uintptr_t>(alpha) | reinterpret_cast<uintptr_t>(inv_alpha)) & 15) == 0;
     tc_prep_kernel<<<(units + 255) / 256, 256, 0, s>>>(reinterpret_cast<const float4*>(x), alpha, inv_alpha, vec_alpha,
                                                        units, (unsigned)(Cin / 8), static_cast<uint4*>(scratch->a_hi),
-                                                       with_lo ? static_cast<uint4*>(scratch->a_lo) : nullptr);
+                                                       with_lo);
     return cudaGetLastError();
 }
 
 namespace {
 
 cudaError_t tc_gemm_core(const GemmArgs& a, const TcWeights& w, const float* unscale_dev, PlanView plan,
-                         int n_row_tiles, const void* a_hi, const void* a_lo, long long a_rows, int* err,
+                         int n_row_tiles, const void* a_planes, long long a_rows, int* err,
                          int num_sms, cudaStream_t s, float* ws, size_t ws_floats, int* launches)
 {
     if (n_row_tiles <= 0) return cudaSuccess;
-    alignas(64) CUtensorMap ma_hi, ma_lo;
-    if (!make_map(&ma_hi, a_hi, (uint64_t)a.Cin, (uint64_t)a_rows, kBK, kBM)) return cudaErrorInvalidValue;
-    if (!make_map(&ma_lo, a_lo, (uint64_t)a.Cin, (uint64_t)a_rows, kBK, kBM)) return cudaErrorInvalidValue;
+    // A: the interleaved [rows][2 Cin] operand (three passes) or the hi plane
+    alignas(64) CUtensorMap ma;
+    const int box_k = w.passes == 3 ? 2 * kBK : kBK;
+    const uint64_t a_inner = (uint64_t)a.Cin * (w.passes == 3 ? 2 : 1);
+    if (!make_map(&ma, a_planes, a_inner, (uint64_t)a_rows, box_k, kBM)) return cudaErrorInvalidValue;
     TcParams p;
     p.n_row_tiles = n_row_tiles;
     // two M-tiles share each B tile when N is narrow, unless pairing would
@@ -943,10 +968,10 @@ cudaError_t tc_gemm_core(const GemmArgs& a, const TcWeights& w, const float* uns
     p.cin_blocks = a.Cin / kBK;
     p.ntaps = a.ntaps;
     p.nkb = a.ntaps * p.cin_blocks;
-    const uint32_t np = w.passes == 3 ? 2u : 1u;   // planes per operand in a stage
-    p.b_stride = round1024((uint32_t)w.BN * kBK * 2);
-    p.stage_bytes = np * (uint32_t)p.mtiles * kAPlaneBytes + np * p.b_stride;
-    p.tx_bytes = np * (uint32_t)p.mtiles * kAPlaneBytes + np * (uint32_t)w.BN * kBK * 2;
+    // operand rows in a stage: 128 bytes (a k-block's hi and lo) or 64 (hi only)
+    const uint32_t row = w.passes == 3 ? 128u : 64u;
+    p.stage_bytes = (uint32_t)p.mtiles * kBM * row + round1024((uint32_t)w.BN * row);
+    p.tx_bytes = (uint32_t)p.mtiles * kBM * row + (uint32_t)w.BN * row;
     const int extra = 1024 + 512 + kStageOutBytes;
     p.stages = std::min(8, (kSmemBudget - extra) / (int)p.stage_bytes);
     if (p.stages < 2) return cudaErrorInvalidValue;
@@ -983,9 +1008,9 @@ cudaError_t tc_gemm_core(const GemmArgs& a, const TcWeights& w, const float* uns
     const int tiles = p.n_mgroups * w.n_tiles * p.n_splits;
     const int grid = std::min(tiles, num_sms > 0 ? num_sms : 152);
     if (w.passes == 3)
-        tc_gemm_kernel<3><<<grid, kThreads, smem, s>>>(ma_hi, ma_lo, w.map_hi, w.map_lo, a, plan, p);
+        tc_gemm_kernel<3><<<grid, kThreads, smem, s>>>(ma, w.map_hi, a, plan, p);
     else
-        tc_gemm_kernel<1><<<grid, kThreads, smem, s>>>(ma_hi, ma_lo, w.map_hi, w.map_lo, a, plan, p);
+        tc_gemm_kernel<1><<<grid, kThreads, smem, s>>>(ma, w.map_hi, a, plan, p);
     cudaError_t e = cudaGetLastError();
     if (launches) (*launches)++;
     if (e != cudaSuccess || p.n_splits == 1) return e;
@@ -1000,7 +1025,7 @@ cudaError_t tc_gemm_core(const GemmArgs& a, const TcWeights& w, const float* uns
 cudaError_t launch_tc_gemm(const GemmArgs& a, const TcWeights& w, PlanView plan, int n_row_tiles,
                            const TcScratch* scratch, long long a_rows, int num_sms, cudaStream_t s, int* launches)
 {
-    return tc_gemm_core(a, w, nullptr, plan, n_row_tiles, scratch->a_hi, scratch->a_lo, a_rows, scratch->err,
+    return tc_gemm_core(a, w, nullptr, plan, n_row_tiles, scratch->a_hi, a_rows, scratch->err,
                         num_sms, s, scratch->ws, scratch->ws_floats, launches);
 }
 
@@ -1042,9 +1067,10 @@ __global__ void op_wmax_kernel(const float* __restrict__ w, long long n, unsigne
     if ((threadIdx.x & 31) == 0) atomicMax(out, m);
 }
 
-// w [Cout][Cin][k] -> planes [Cout][k Cin] (tap-major K) of w * 2^e, e from |w|max
+// w [Cout][Cin][k] -> w * 2^e (e from |w|max), K = k Cin tap-major, in the
+// three-pass layout [Cout][K / 32][32 hi | 32 lo]
 __global__ void op_wpack_kernel(const float* __restrict__ w, int Cout, int Cin, int k, int* words,
-                                __half* __restrict__ hi, __half* __restrict__ lo)
+                                __half* __restrict__ out)
 {
     const float mx = __uint_as_float(static_cast<unsigned>(words[kOpWmax]));
     const int e = mx > 0.f ? -(int)floorf(log2f(mx)) : 0;
@@ -1055,8 +1081,9 @@ __global__ void op_wpack_kernel(const float* __restrict__ w, int Cout, int Cin, 
         const long long j = kk / Cin, ci = kk - j * Cin;
         const float v = w[(co * Cin + ci) * k + j] * scale;
         const __half h = __float2half_rn(v);
-        hi[i] = h;
-        lo[i] = __float2half_rn(v - __half2float(h));
+        const long long at = co * 2 * K + (kk / kBK) * (2 * kBK) + (kk % kBK);
+        out[at] = h;
+        out[at + kBK] = __float2half_rn(v - __half2float(h));
     }
     if (blockIdx.x == 0 && threadIdx.x == 0) reinterpret_cast<float*>(words)[kOpUnscale] = ldexpf(1.0f, -e);
 }
@@ -1081,8 +1108,7 @@ int run_tc_conv1d(const TcOpScratch& sc, const float* x, int T, int Cin, const f
     const long long wn = K * Cout;
     const int wblocks = (int)std::min<long long>((wn + 255) / 256, 152LL * 8);
     op_wmax_kernel<<<wblocks, 256, 0, s>>>(w, wn, reinterpret_cast<unsigned*>(words + kOpWmax));
-    op_wpack_kernel<<<wblocks, 256, 0, s>>>(w, Cout, Cin, k, words, static_cast<__half*>(sc.b_hi),
-                                            static_cast<__half*>(sc.b_lo));
+    op_wpack_kernel<<<wblocks, 256, 0, s>>>(w, Cout, Cin, k, words, static_cast<__half*>(sc.b_hi));
     if (cudaGetLastError() != cudaSuccess) return OP_CUDA;
     TcScratch as;
     as.a_hi = sc.a_hi;
@@ -1093,11 +1119,9 @@ int run_tc_conv1d(const TcOpScratch& sc, const float* x, int T, int Cin, const f
     TcWeights tw;
     tw.passes = 3;
     tw.hi = sc.b_hi;
-    tw.lo = sc.b_lo;
     tw.BN = pick_bn(Cout);
     tw.n_tiles = (Cout + tw.BN - 1) / tw.BN;
-    if (!make_map(&tw.map_hi, sc.b_hi, (uint64_t)K, (uint64_t)Cout, kBK, (uint32_t)tw.BN)) return OP_CUDA;
-    if (!make_map(&tw.map_lo, sc.b_lo, (uint64_t)K, (uint64_t)Cout, kBK, (uint32_t)tw.BN)) return OP_CUDA;
+    if (!make_map(&tw.map_hi, sc.b_hi, (uint64_t)(2 * K), (uint64_t)Cout, 2 * kBK, (uint32_t)tw.BN)) return OP_CUDA;
     GemmArgs a{};
     a.in = x;
     a.in_l = Layout{1, (int)H};
@@ -1119,7 +1143,7 @@ int run_tc_conv1d(const TcOpScratch& sc, const float* x, int T, int Cin, const f
     PlanView plan{1, words + kOpPlan + 2, words + kOpPlan + 4, reinterpret_cast<const long long*>(words + kOpPlan),
                   words + kOpPlan + 5};
     const int n_row_tiles = (T + kBM - 1) / kBM;
-    if (tc_gemm_core(a, tw, reinterpret_cast<const float*>(words) + kOpUnscale, plan, n_row_tiles, sc.a_hi, sc.a_lo,
+    if (tc_gemm_core(a, tw, reinterpret_cast<const float*>(words) + kOpUnscale, plan, n_row_tiles, sc.a_hi,
                      rows, sc.err, num_sms, s, nullptr, 0, nullptr) != cudaSuccess)
         return OP_CUDA;
     return OP_OK;

@@ -13,10 +13,8 @@ namespace codec {
 // Weight planes of one contraction for the tensor cores: B = W^T, K-major
 // [N][K], scaled by 2^e (max |W 2^e| in [1, 2)) and split into fp16 hi and lo.
 struct TcWeights {
-    CUtensorMap map_hi;          // CUtensorMap is itself 64-byte aligned
-    CUtensorMap map_lo;
-    void* hi = nullptr;      // __half [N][K]
-    void* lo = nullptr;
+    CUtensorMap map_hi;      // over `hi` (CUtensorMap is itself 64-byte aligned)
+    void* hi = nullptr;      // passes 3: __half [N][K / 32][32 hi | 32 lo]; passes 1: __half [N][K] (hi)
     float unscale = 1.f;     // 2^-e, applied to the accumulator
     int BN = 0;              // N tile (multiple of 32, <= 256)
     int n_tiles = 0;
@@ -28,10 +26,10 @@ struct TcWeights {
 constexpr int kOpMaxCin = 4096;
 constexpr int kOpWords = 16 + kOpMaxCin;
 struct TcOpScratch {
-    void* a_hi = nullptr;
+    void* a_hi = nullptr;     // 2 a_elems fp16 from here on: a_lo == a_hi + a_elems
     void* a_lo = nullptr;
     size_t a_elems = 0;
-    void* b_hi = nullptr;
+    void* b_hi = nullptr;     // 2 b_elems fp16 from here on: b_lo == b_hi + b_elems
     void* b_lo = nullptr;
     size_t b_elems = 0;
     int* words = nullptr;
@@ -42,8 +40,8 @@ struct TcOpScratch {
 // hi and lo), big enough for the widest input of any contraction, plus the
 // sticky flag a kernel sets when one of its bounded waits expires.
 struct TcScratch {
-    void* a_hi = nullptr;
-    void* a_lo = nullptr;
+    void* a_hi = nullptr;     // 2 elems fp16 from here on (a_lo == a_hi + elems): the three-pass
+    void* a_lo = nullptr;     // layout interleaves hi and lo over all of it, the one-pass mode uses hi
     size_t elems = 0;
     int* err = nullptr;
     float* ws = nullptr;  // chunk partials of split GEMMs
