@@ -69,6 +69,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true", help="skip the cpu_baseline oracle timing")
     ap.add_argument("--first-audio-runs", type=int, default=100)
+    ap.add_argument("--profile-call", default=None, metavar="S,CH,REPS",
+                    help="profiling aid: REPS fixed decode calls of S streams x CH frames (graphs off), no timing")
     return ap.parse_args()
 
 
@@ -404,10 +406,35 @@ def run_ours(args):
     return 0
 
 
+def run_profile_call(args):
+    """A fixed launch sequence for ncu: REPS identical calls of S streams x CH
+    frames each, CUDA graphs off, so that launch i of a kernel is the same
+    layer in every call."""
+    S, CH, REPS = (int(v) for v in args.profile_call.split(","))
+    import torch
+    from streaming_tts_vocoder_gb300 import codec as C
+    cfg = qwen3_config() if args.decoder == "qwen3" else tiny_config()
+    blob = pack_blob(cfg, make_weights(cfg, 0))
+    prec = {"fp16x3": C.PRECISION_FP16X3, "fp16": C.PRECISION_FP16, "fp32": C.PRECISION_FP32}[args.precision]
+    cod = C.Codec(cfg, blob, max_streams=S, max_chunk_frames=CH, max_batch_frames=S * CH, precision=prec)
+    st = cod.state()
+    st.set_graphs(False)
+    dev = torch.device("cuda")
+    codes = torch.from_numpy(np.stack([make_codes(cfg, CH, 1000 + s) for s in range(S)])).to(dev)
+    audio = torch.empty(S, CH * cod.samples_per_frame, device=dev)
+    for _ in range(REPS):
+        st.decode(codes, [CH] * S, audio)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_call": [S, CH, REPS], "mean_abs": float(audio.abs().mean())}))
+    return 0
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
+    if args.profile_call:
+        return run_profile_call(args)
     return run_ours(args)
 
 
