@@ -69,6 +69,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true", help="skip the cpu_baseline oracle timing")
     ap.add_argument("--first-audio-runs", type=int, default=100)
+    ap.add_argument("--schedule", action="store_true",
+                    help="latency of streaming chunk schedules (time to first audio, per-chunk latency, "
+                         "playback gaps) for carried-state and recompute decoding, instead of the throughput line")
     ap.add_argument("--profile-call", default=None, metavar="S,CH,REPS",
                     help="profiling aid: REPS fixed decode calls of S streams x CH frames (graphs off), no timing")
     return ap.parse_args()
@@ -429,12 +432,102 @@ def run_profile_call(args):
     return 0
 
 
+def playback_gaps(lats_ms, frames, frame_ms):
+    """Chunks decoded back to back (chunk i ready after the sum of the first
+    i + 1 latencies) and played as soon as ready: the silence before each
+    chunk after the first, in ms."""
+    ready, queued_until, gaps = 0.0, None, []
+    for lat, n in zip(lats_ms, frames):
+        ready += lat
+        if queued_until is None:
+            queued_until = ready + n * frame_ms
+        else:
+            gaps.append(max(0.0, ready - queued_until))
+            queued_until = max(queued_until, ready) + n * frame_ms
+    return gaps
+
+
+SCHEDULES = {
+    # frames per call, repeated until the stream's frames are used up
+    "1_then_25": [1] + [25] * 100,
+    "ramp_4_4_8_16_25": [4, 4, 8, 16] + [25] * 100,
+    "doubling_1_2_4_8": [1, 2, 4, 8] + [8] * 400,
+    "fixed_25": [25] * 100,
+}
+
+
+def run_schedule(args):
+    """Streaming latency of one stream under a chunk schedule, codes all
+    available up front (the decode cost alone).  carried: the decoder keeps
+    its conv histories and K/V window across calls.  recompute: every call
+    re-decodes up to 72 frames of left context from an empty state and keeps
+    only the new frames' audio (the server mode the pages describe).  A call
+    of n frames gives n x 80 ms of audio; playback stalls when the next chunk
+    is ready after the audio before it ran out."""
+    import torch
+    from streaming_tts_vocoder_gb300 import codec as C
+    cfg = qwen3_config() if args.decoder == "qwen3" else tiny_config()
+    blob = pack_blob(cfg, make_weights(cfg, 0))
+    prec = {"fp16x3": C.PRECISION_FP16X3, "fp16": C.PRECISION_FP16, "fp32": C.PRECISION_FP32}[args.precision]
+    ctx = 72
+    F = 250
+    cod = C.Codec(cfg, blob, max_streams=1, max_chunk_frames=ctx + 25, precision=prec)
+    st = cod.state()
+    dev = torch.device("cuda")
+    stream = torch.cuda.current_stream()
+    codes = make_codes(cfg, F, 1000)
+    spf = cod.samples_per_frame
+    frame_ms = 1e3 / FRAME_RATE_HZ
+    out = {"metric": "streaming chunk latency, one stream", "decoder": args.decoder, "precision": args.precision,
+           "frames": F, "frame_ms": frame_ms, "context_frames_recompute": ctx, "schedules": {}}
+    for name, sched in SCHEDULES.items():
+        for mode in ("carried", "recompute"):
+            lat_runs = []
+            for rep in range(3):                 # first pass warms the graph cache; keep the last
+                st.reset([0], stream=stream)
+                torch.cuda.synchronize()
+                t, lats, sizes = 0, [], []
+                for n in sched:
+                    if t >= F:
+                        break
+                    n = min(n, F - t)
+                    lo = max(0, t - ctx) if mode == "recompute" else t
+                    seg = codes[:, lo:t + n]
+                    c = torch.from_numpy(np.ascontiguousarray(seg)).reshape(1, cfg.Q, seg.shape[1]).to(dev)
+                    a = torch.empty(1, seg.shape[1] * spf, device=dev)
+                    if mode == "recompute":
+                        st.reset([0], stream=stream)
+                    torch.cuda.synchronize()
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    st.decode(c, [seg.shape[1]], a, stream_ids=[0], stream=stream)
+                    e1.record(stream)
+                    e1.synchronize()
+                    lats.append(e0.elapsed_time(e1))
+                    sizes.append(n)
+                    t += n
+                lat_runs.append((lats, sizes))
+            lats, sizes = lat_runs[-1]
+            gaps = playback_gaps(lats, sizes, frame_ms)
+            out["schedules"][f"{name}/{mode}"] = {
+                "ttfa_ms": lats[0], "calls": len(lats),
+                "chunk_latency_ms_p50": float(np.percentile(lats, 50)),
+                "chunk_latency_ms_p95": float(np.percentile(lats, 95)),
+                "playback_gap_ms_total": float(sum(gaps)),
+                "playback_gap_ms_p95": float(np.percentile(gaps, 95)) if gaps else 0.0,
+                "decode_ms_total": float(sum(lats)), "audio_ms": float(sum(sizes) * frame_ms)}
+    print(json.dumps(out))
+    return 0
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
     if args.profile_call:
         return run_profile_call(args)
+    if args.schedule:
+        return run_schedule(args)
     return run_ours(args)
 
 

@@ -64,3 +64,11 @@ def test_reference_arm_idle_on_other_ranks(monkeypatch):
         decoder, steps, warmup = "tiny", 1, 0
 
     assert bench.run_reference(Args()) == 0
+
+
+def test_playback_gaps():
+    # 80 ms frames: a 1-frame chunk ready at 10 ms plays until 90 ms; the next
+    # (ready at 10 + 100 = 110 ms) leaves a 20 ms gap; the third is ready at
+    # 115 ms while the second plays until 110 + 2 x 80 = 270 ms: no gap
+    assert bench.playback_gaps([10.0, 100.0, 5.0], [1, 2, 1], 80.0) == [20.0, 0.0]
+    assert bench.playback_gaps([1.0], [25], 80.0) == []
