@@ -807,14 +807,17 @@ struct Launcher {
         if (C.use_tc) {
             a.tcum = tc128 + (size_t)in_lvl * S1;
             a.bm = 128;
+            // dense single-tap contractions tile all streams' rows back to back
+            // (the transformer linears: 1600 rows of 64 streams are 13 tiles, not 64)
+            a.dense = (il.P == 0 && ol.P == 0 && C.ntaps == 1 && out_step == 1) ? 1 : 0;
+            const int n_row_tiles = a.dense ? (int)((rows(in_lvl) + 127) / 128) : ntiles128[in_lvl];
             const long long arows = il.P ? rows_pref(in_lvl, il) : rows(in_lvl);
             run(CODEC_KERNEL_OPERAND_PREP, 0.0, 8.0 * (double)arows * C.Cin, what, [&] {
                 return launch_tc_prep(in, C.alpha, C.inv_alpha, arows, C.Cin, &s->tc_scratch, C.tc.passes == 3, cs);
             });
             int extra = 0;
             run(CODEC_KERNEL_GEMM_TC, flops, bytes, what, [&] {
-                return launch_tc_gemm(a, C.tc, pv, ntiles128[in_lvl], &s->tc_scratch, arows, s->c->num_sms, cs,
-                                      &extra);
+                return launch_tc_gemm(a, C.tc, pv, n_row_tiles, &s->tc_scratch, arows, s->c->num_sms, cs, &extra);
             });
             launches += extra > 1 ? extra - 1 : 0;   // the split reduction, timed with its GEMM
         } else {

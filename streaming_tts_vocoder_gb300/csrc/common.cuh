@@ -74,6 +74,10 @@ struct GemmArgs {
     // tiling
     const int* tcum;         // [B + 1] cumulative row tiles of the input level
     int bm;
+    // 1: input and output dense (P = 0), one tap, out_step 1 - row tiles run
+    // over all segments' rows back to back (tile mt = rows 128 mt ...), since
+    // no row reads another row; the q/K/V scatter finds each row's segment.
+    int dense;
 };
 
 __device__ __forceinline__ int find_seg(const int* cum, int B, int x)
@@ -120,6 +124,10 @@ __device__ __forceinline__ void gemm_store(const GemmArgs& a, const PlanView& pl
         if (n < a.d) {
             a.out[out_row * a.d + n] = v;
         } else {
+            if (b < 0) {            // dense tiling: t is the row over all segments
+                b = find_seg(plan.cf, plan.B, t);
+                t -= __ldg(plan.cf + b);
+            }
             const long long pos = __ldg(plan.pos0 + b) + t;
             const long long rr = (long long)__ldg(plan.slot + b) * a.ring_R + (pos & (a.ring_R - 1));
             if (n < 2 * a.d) a.kring[rr * a.d + (n - a.d)] = v;

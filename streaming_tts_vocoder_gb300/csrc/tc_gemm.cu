@@ -248,6 +248,14 @@ struct TileRows {
 __device__ __forceinline__ TileRows tile_rows(const GemmArgs& a, const PlanView& plan, int mt)
 {
     TileRows r;
+    if (a.dense) {
+        const int total = __ldg(plan.cf + plan.B) * a.in_l.r;
+        r.b = -1;
+        r.t0 = mt * kBM;
+        r.nrows = min(kBM, total - r.t0);
+        r.in_base = r.t0;
+        return r;
+    }
     r.b = find_seg(a.tcum, plan.B, mt);
     const int seg_rows = (__ldg(plan.cf + r.b + 1) - __ldg(plan.cf + r.b)) * a.in_l.r;
     r.t0 = (mt - __ldg(a.tcum + r.b)) * kBM;
@@ -285,6 +293,10 @@ __device__ __forceinline__ float* epi_dst4(const GemmArgs& a, const PlanView& pl
     if (a.epi == EPI_QKV) {
         if (a.d & 3) return nullptr;
         if (n < a.d) return a.out + out_row * a.d + n;
+        if (b < 0) {                // dense tiling: t is the row over all segments
+            b = find_seg(plan.cf, plan.B, t);
+            t -= __ldg(plan.cf + b);
+        }
         const long long pos = __ldg(plan.pos0 + b) + t;
         const long long rr = (long long)__ldg(plan.slot + b) * a.ring_R + (pos & (a.ring_R - 1));
         return n < 2 * a.d ? a.kring + rr * a.d + (n - a.d) : a.vring + rr * a.d + (n - 2 * a.d);
@@ -548,7 +560,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
             const int nvalid = min(ncol, a.N - n0);
             TileRows tr{0, 0, 0, 0};
             if (mt < p.n_row_tiles) tr = tile_rows(a, plan, mt);
-            const long long out_base = mt < p.n_row_tiles ? seg_base(a.out_l, plan.cf, tr.b) : 0;
+            const long long out_base = (mt < p.n_row_tiles && !a.dense) ? seg_base(a.out_l, plan.cf, tr.b) : 0;
             if (p.n_splits == 1 && nvalid > 0 && m < tr.nrows)
                 epi_prefetch(a, out_base + (long long)(tr.t0 + m) * a.out_step, n0, nvalid);
             float sum[kEpiCols];
@@ -736,7 +748,7 @@ __global__ void __launch_bounds__(kReduceRows * 8) tc_reduce_kernel(const GemmAr
         for (int e = 0; e < 4; e++)
             if (n + e < a.N) sum[e] = __fadd_rn(sum[e], __ldg(src + (size_t)c * stride + e));
     const int t = tr.t0 + m;
-    const long long out_row = seg_base(a.out_l, plan.cf, tr.b) + (long long)t * a.out_step;
+    const long long out_row = (a.dense ? 0 : seg_base(a.out_l, plan.cf, tr.b)) + (long long)t * a.out_step;
     for (int e = 0; e < 4; e++)
         if (n + e < a.N) gemm_store(a, plan, tr.b, t, out_row, n + e, __fmul_rn(sum[e], us));
 }
@@ -990,15 +1002,30 @@ cudaError_t tc_gemm_core(const GemmArgs& a, const TcWeights& w, const float* uns
     p.cps = p.n_chunks;
     p.ws = nullptr;
     {
+        // Pick the split count that minimises waves / splits, the time of the
+        // busiest CTA in units of a whole tile's k-loop: with few tiles (a
+        // one-frame call) it spreads every tile over many CTAs; with a little
+        // over one wave (1600 rows of a transformer linear: 156 tiles on 152
+        // SMs) it evens out the second wave.  A split pays for its partials'
+        // round trip and the reduction, so it must win by more than 10 %.
         const int sms = num_sms > 0 ? num_sms : 152;
         const int tiles = ((n_row_tiles + p.mtiles - 1) / p.mtiles) * w.n_tiles;
         const size_t need = (size_t)p.n_chunks * n_row_tiles * kBM * a.N;
-        if (ws && tiles < sms / 2 && p.n_chunks >= 2 && need <= ws_floats) {
-            int ns = std::min(p.n_chunks, (sms + tiles - 1) / tiles);
-            p.cps = (p.n_chunks + ns - 1) / ns;
+        if (ws && p.n_chunks >= 2 && need <= ws_floats && tiles < 4 * sms) {
+            double best = (double)((tiles + sms - 1) / sms);
+            int best_cps = p.n_chunks;
+            for (int ns = 2; ns <= p.n_chunks; ns++) {
+                const int cps = (p.n_chunks + ns - 1) / ns;
+                const int nsplit = (p.n_chunks + cps - 1) / cps;
+                const double t = (double)((tiles * nsplit + sms - 1) / sms) * cps / p.n_chunks;
+                if (t < best * 0.9) {
+                    best = t;
+                    best_cps = cps;
+                }
+            }
+            p.cps = best_cps;
             p.n_splits = (p.n_chunks + p.cps - 1) / p.cps;
             if (p.n_splits > 1) p.ws = ws;
-            else p.cps = p.n_chunks;
         }
     }
     p.unscale = w.unscale;
