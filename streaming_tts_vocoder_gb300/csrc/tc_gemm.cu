@@ -1,9 +1,9 @@
 // Tensor-core implicit GEMM for the decoder's dense contractions (causal and
 // dilated Conv1d, the transposed convs in their phase-GEMM form, the
-// transformer linears) on sm_103a: TMA loads of 128 x 32 operand tiles into
-// 64-byte-swizzled shared memory, tcgen05.mma issued by one thread with the
-// fp32 accumulator in TMEM, and an epilogue that reads TMEM back with
-// tcgen05.ld and applies bias / residual / MRF average / GELU / ring scatter.
+// transformer linears) on sm_103a: TMA loads of 32-channel k-blocks into
+// swizzled shared memory, tcgen05.mma issued by one thread with the fp32
+// accumulator in TMEM, and an epilogue that reads TMEM back with tcgen05.ld
+// and applies bias / residual / MRF average / GELU / ring scatter.
 //
 // Precision: each operand is split into fp16 hi + lo parts (x = hi + lo to
 // about 22 bits) and every k-step issues hi*hi + hi*lo + lo*hi, so the result
@@ -18,18 +18,23 @@
 // truncation then acts on 16-step partial sums only, and the decoder's output
 // error stays within a small factor of an fp32 FMA loop's.
 //
+// Operand layout: in the three-pass mode a k-block's hi and lo halves share
+// one 128-byte row ([rows][Cin/32][32 hi | 32 lo], the same for the weights),
+// so one 128-byte-swizzled TMA box brings both; the kernel is bound by its
+// copies as much as by its MMAs, and a copy costs about one cycle per row.
+// The single-pass mode reads the hi plane alone in 64-byte rows.
+//
 // Implicit GEMM: output row t of stream segment b takes, for tap j, the
 // input row base(b) + t - shift_j, so a k-block is one TMA box at a shifted
 // row coordinate; the [history | chunk] rows in front of each segment supply
-// the causal left context, and an M-tile never crosses a stream segment.
+// the causal left context, and an M-tile never crosses a stream segment,
+// except for dense single-tap contractions (the transformer linears), whose
+// M-tiles run over all segments' rows back to back.
 //
 // Tiles: an M-tile is 128 rows.  For N > 128 a CTA tile is one M-tile by an
 // N-tile of up to 256 columns (one MMA of N = 256 per k-step and pass); for
 // N <= 128 it is two M-tiles sharing the N-tile, so each B (weight) tile in
-// shared memory still feeds 256 x N outputs.  With three passes the MMAs
-// read shared memory about as fast as it can deliver, and the TMA writes into
-// it compete for the same bandwidth, so the large tile matters more here than
-// for a single-pass GEMM.
+// shared memory still feeds 256 x N outputs.
 //
 // Roles (384 threads in three warpgroups, one CTA per SM, persistent):
 //   warpgroup 0  warp 0: TMA producer (one thread); warp 1: TMEM allocator
