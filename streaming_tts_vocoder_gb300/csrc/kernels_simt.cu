@@ -310,6 +310,10 @@ constexpr int kFinalTile = 128;
 constexpr int kFinalMaxK = 16;
 constexpr int kFinalMaxSmem = 160 * 1024;
 
+// KP: taps padded to 8 or 16.  The weights sit in shared memory as [C][KP]
+// (zero beyond k) and are read as float4s, the Snake parameters as float2s,
+// so a channel costs its Snake, KP/4 + 1 shared loads and KP FMAs.
+template <int KP>
 __global__ void __launch_bounds__(kFinalTile) final_conv_kernel(
     const float* __restrict__ x, Layout xl, int C, const float* __restrict__ w,
     const float* __restrict__ bias, const float* __restrict__ alpha,
@@ -317,27 +321,28 @@ __global__ void __launch_bounds__(kFinalTile) final_conv_kernel(
     float* __restrict__ pre_tanh, long long audio_ld, PlanView plan, const int* __restrict__ bidx,
     const int* __restrict__ tcum)
 {
-    extern __shared__ float sm[];
-    float* sw = sm;                                   // [k][C] weights
-    float* sa = sm + k * C;                           // [C] alpha, [C] 1/alpha
-    float* sp = sa + 2 * C;                           // [kFinalTile + k - 1][k] partials
+    extern __shared__ float4 sm4[];
+    float4* sw = sm4;                                                   // [C][KP / 4]
+    float2* sa = reinterpret_cast<float2*>(sm4 + (size_t)C * (KP / 4)); // [C] (alpha, 1/alpha)
+    float* sp = reinterpret_cast<float*>(sa + C);                       // [kFinalTile + k - 1][k] partials
     const int tile = blockIdx.x;
     const int b = find_seg(tcum, plan.B, tile);
     const int seg_rows = (__ldg(plan.cf + b + 1) - __ldg(plan.cf + b)) * xl.r;
     const int t0 = (tile - __ldg(tcum + b)) * kFinalTile;
     const int nrows = min(kFinalTile, seg_rows - t0);
     const long long base = seg_base(xl, plan.cf, b) + t0 - (k - 1);
-    for (int i = threadIdx.x; i < k * C; i += blockDim.x) sw[i] = __ldg(w + i);
-    for (int i = threadIdx.x; i < C; i += blockDim.x) {
-        sa[i] = __ldg(alpha + i);
-        sa[C + i] = __ldg(inv_alpha + i);
+    float* swf = reinterpret_cast<float*>(sw);
+    for (int i = threadIdx.x; i < KP * C; i += blockDim.x) {
+        const int c = i / KP, j = i - c * KP;
+        swf[i] = j < k ? __ldg(w + (size_t)j * C + c) : 0.f;
     }
+    for (int i = threadIdx.x; i < C; i += blockDim.x) sa[i] = make_float2(__ldg(alpha + i), __ldg(inv_alpha + i));
     __syncthreads();
     const int rows = nrows + k - 1;
     for (int r = threadIdx.x; r < rows; r += blockDim.x) {
-        float part[kFinalMaxK];
+        float part[KP];
 #pragma unroll
-        for (int j = 0; j < kFinalMaxK; j++) part[j] = 0.f;
+        for (int j = 0; j < KP; j++) part[j] = 0.f;
         const float4* xr = reinterpret_cast<const float4*>(x + (base + r) * C);
         for (int c4 = 0; c4 < (C >> 2); c4++) {
             const float4 v = __ldg(xr + c4);
@@ -345,14 +350,20 @@ __global__ void __launch_bounds__(kFinalTile) final_conv_kernel(
 #pragma unroll
             for (int u = 0; u < 4; u++) {
                 const int c = 4 * c4 + u;
-                const float s = snake_f(e[u], sa[c], sa[C + c]);
+                const float2 al = sa[c];
+                const float sn = snake_f(e[u], al.x, al.y);
 #pragma unroll
-                for (int j = 0; j < kFinalMaxK; j++)
-                    if (j < k) part[j] = fmaf(sw[j * C + c], s, part[j]);
+                for (int q = 0; q < KP / 4; q++) {
+                    const float4 wq = sw[c * (KP / 4) + q];
+                    part[4 * q] = fmaf(wq.x, sn, part[4 * q]);
+                    part[4 * q + 1] = fmaf(wq.y, sn, part[4 * q + 1]);
+                    part[4 * q + 2] = fmaf(wq.z, sn, part[4 * q + 2]);
+                    part[4 * q + 3] = fmaf(wq.w, sn, part[4 * q + 3]);
+                }
             }
         }
 #pragma unroll
-        for (int j = 0; j < kFinalMaxK; j++)
+        for (int j = 0; j < KP; j++)
             if (j < k) sp[r * k + j] = part[j];
     }
     __syncthreads();
@@ -373,11 +384,15 @@ cudaError_t launch_final_conv(const float* x, Layout xl, int C, const float* w, 
 {
     if (n_row_tiles <= 0) return cudaSuccess;
     if (k > kFinalMaxK) return cudaErrorInvalidValue;
-    const size_t smem = sizeof(float) * ((size_t)k * C + 2 * (size_t)C + (size_t)(kFinalTile + k - 1) * k);
+    const int KP = k <= 8 ? 8 : 16;
+    const size_t smem = sizeof(float) * ((size_t)KP * C + 2 * (size_t)C + (size_t)(kFinalTile + k - 1) * k);
     if (smem > (size_t)kFinalMaxSmem) return cudaErrorInvalidValue;
-    final_conv_kernel<<<n_row_tiles, kFinalTile, smem, s>>>(x, xl, C, w, bias, alpha, inv_alpha, k,
-                                                            audio, pre_tanh, audio_ld, plan,
-                                                            plan.bidx, tcum);
+    if (KP == 8)
+        final_conv_kernel<8><<<n_row_tiles, kFinalTile, smem, s>>>(x, xl, C, w, bias, alpha, inv_alpha, k, audio,
+                                                                    pre_tanh, audio_ld, plan, plan.bidx, tcum);
+    else
+        final_conv_kernel<16><<<n_row_tiles, kFinalTile, smem, s>>>(x, xl, C, w, bias, alpha, inv_alpha, k, audio,
+                                                                     pre_tanh, audio_ld, plan, plan.bidx, tcum);
     return cudaGetLastError();
 }
 
@@ -454,7 +469,9 @@ cudaError_t configure_simt_kernels()
 {
     cudaError_t e = cudaFuncSetAttribute(swa_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSwaMaxSmem);
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(final_conv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kFinalMaxSmem);
+    e = cudaFuncSetAttribute(final_conv_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kFinalMaxSmem);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(final_conv_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kFinalMaxSmem);
 }
 
 }  // namespace codec
