@@ -74,6 +74,9 @@ def parse():
                          "playback gaps) for carried-state and recompute decoding, instead of the throughput line")
     ap.add_argument("--profile-call", default=None, metavar="S,CH,REPS",
                     help="profiling aid: REPS fixed decode calls of S streams x CH frames (graphs off), no timing")
+    ap.add_argument("--layer-times", default=None, metavar="S,CH",
+                    help="per-launch CUDA-event times of one decode call of S streams x CH frames from an empty "
+                         "state (graphs off), labelled by layer, one JSON line")
     return ap.parse_args()
 
 
@@ -432,6 +435,60 @@ def run_profile_call(args):
     return 0
 
 
+def layer_labels(cfg):
+    """Names of the decoder's launches in call order (an operand prep carries
+    the name of the GEMM it feeds)."""
+    names = ["history fill", "codebook gather", "pre-conv"]
+    for l in range(cfg.layers):
+        names += [f"L{l} rmsnorm 1", f"L{l} qkv", f"L{l} attention", f"L{l} out-proj", f"L{l} rmsnorm 2",
+                  f"L{l} mlp 1", f"L{l} mlp 2"]
+    names += ["final rmsnorm"] + [f"latent up {u}" for u in range(len(cfg.up_channels))]
+    for s in range(len(cfg.strides)):
+        names.append(f"stage {s} convT")
+        for k in cfg.rb_kernels:
+            for d in cfg.dilations:
+                names.append(f"stage {s} rb k{k} d{d}")
+    return names + ["final conv", "history commit"]
+
+
+def run_layer_times(args):
+    """Per-launch CUDA-event times of one decode call (the third of three
+    identical calls from an empty state, graphs off), labelled by layer."""
+    S, CH = (int(v) for v in args.layer_times.split(","))
+    import torch
+    from streaming_tts_vocoder_gb300 import codec as C
+    cfg = qwen3_config() if args.decoder == "qwen3" else tiny_config()
+    blob = pack_blob(cfg, make_weights(cfg, 0))
+    prec = {"fp16x3": C.PRECISION_FP16X3, "fp16": C.PRECISION_FP16, "fp32": C.PRECISION_FP32}[args.precision]
+    cod = C.Codec(cfg, blob, max_streams=S, max_chunk_frames=CH, max_batch_frames=S * CH, precision=prec)
+    st = cod.state()
+    st.set_graphs(False)
+    dev = torch.device("cuda")
+    codes = torch.from_numpy(np.stack([make_codes(cfg, CH, 1000 + s) for s in range(S)])).to(dev)
+    audio = torch.empty(S, CH * cod.samples_per_frame, device=dev)
+    for _ in range(3):
+        st.reset()
+        torch.cuda.synchronize()
+        st.profile_begin()
+        st.decode(codes, [CH] * S, audio)
+        st.profile_end()
+    names = iter(layer_labels(cfg))
+    rows, cur = [], None
+    for kind, ms, flops, nbytes in st.profile_launches():
+        if kind == "operand_prep":
+            cur = cur or next(names)
+            name = cur
+        else:
+            name = cur or next(names)
+            cur = None
+        rows.append({"layer": name, "kernel": kind, "us": round(ms * 1e3, 2),
+                     "tflops": round(flops / ms / 1e9, 1) if ms and flops else None,
+                     "gbs": round(nbytes / ms / 1e6, 1) if ms and nbytes else None})
+    print(json.dumps({"layer_times": [S, CH], "decoder": args.decoder, "precision": args.precision,
+                      "total_us": round(sum(r["us"] for r in rows), 1), "launches": rows}))
+    return 0
+
+
 def playback_gaps(lats_ms, frames, frame_ms):
     """Chunks decoded back to back (chunk i ready after the sum of the first
     i + 1 latencies) and played as soon as ready: the silence before each
@@ -526,6 +583,8 @@ def main():
         return run_reference(args)
     if args.profile_call:
         return run_profile_call(args)
+    if args.layer_times:
+        return run_layer_times(args)
     if args.schedule:
         return run_schedule(args)
     return run_ours(args)
