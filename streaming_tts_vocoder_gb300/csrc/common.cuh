@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace codec {
 
 constexpr int kMaxTaps = 16;
@@ -89,6 +91,36 @@ __device__ __forceinline__ int find_seg(const int* cum, int B, int x)
         if (__ldg(cum + mid) <= x) lo = mid; else hi = mid - 1;
     }
     return lo;
+}
+
+// Programmatic dependent launch.  The decoder's kernels are launched with
+// programmatic stream serialisation, so a kernel may start (and do set-up that
+// touches no global memory) while its predecessor in the stream still runs.
+// pdl_wait() returns once every prerequisite grid has completed and its memory
+// operations are visible (at once when there is none): every kernel calls it
+// before its first global memory access and before any of its threads can
+// exit, so a kernel's completion still implies its predecessors'.  Then
+// pdl_launch() lets the kernel's own successor begin launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Enqueue kernel<<<grid, block, smem, s>>>(args...) with programmatic stream
+// serialisation (see pdl_wait).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args&&... args)
+{
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 // Snake, x + sin(a x)^2 / a, with explicit roundings so every kernel that

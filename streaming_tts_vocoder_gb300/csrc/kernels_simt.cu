@@ -19,6 +19,8 @@ __global__ void __launch_bounds__(128) rvq_gather_kernel(
     PlanView plan, const int* __restrict__ bidx, float* __restrict__ e, Layout el,
     unsigned* __restrict__ err_words)
 {
+    pdl_wait();
+    pdl_launch();
     __shared__ int sc[64];
     __shared__ int sbad;
     const int row = blockIdx.x;
@@ -55,8 +57,8 @@ cudaError_t launch_rvq_gather(const float* cb, int Q, int V, int E, const int* c
                               int total_rows, cudaStream_t s)
 {
     if (total_rows <= 0) return cudaSuccess;
-    rvq_gather_kernel<<<total_rows, 128, 0, s>>>(cb, Q, V, E, codes, T_max, plan, plan.bidx, e,
-                                                 el, err_words);
+    launch_pdl(rvq_gather_kernel, dim3(total_rows), dim3(128), 0, s, cb, Q, V, E, codes, T_max, plan, plan.bidx,
+               e, el, err_words);
     return cudaGetLastError();
 }
 
@@ -70,6 +72,8 @@ constexpr int SB_M = 64, SB_N = 64, SB_K = 16;
 
 __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmArgs a, PlanView plan)
 {
+    pdl_wait();
+    pdl_launch();
     __shared__ float As[SB_K][SB_M + 4];
     __shared__ float Bs[SB_K][SB_N + 4];
     const int tile = blockIdx.x;
@@ -141,7 +145,7 @@ cudaError_t launch_gemm_simt(const GemmArgs& a, PlanView plan, int n_row_tiles, 
 {
     if (n_row_tiles <= 0) return cudaSuccess;
     dim3 grid(n_row_tiles, (a.N + SB_N - 1) / SB_N);
-    gemm_simt_kernel<<<grid, 256, 0, s>>>(a, plan);
+    launch_pdl(gemm_simt_kernel, dim3(grid), dim3(256), 0, s, a, plan);
     return cudaGetLastError();
 }
 
@@ -152,6 +156,8 @@ __global__ void rms_norm_kernel(const float* __restrict__ x, Layout xl, const fl
                                 float eps, float* __restrict__ y, Layout yl, int d, PlanView plan,
                                 int total_rows)
 {
+    pdl_wait();
+    pdl_launch();
     const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (row >= total_rows) return;
@@ -180,8 +186,8 @@ cudaError_t launch_rms_norm(const float* x, Layout xl, const float* g, float eps
 {
     if (total_rows <= 0) return cudaSuccess;
     const int threads = 256, rows_per_block = threads / 32;
-    rms_norm_kernel<<<(total_rows + rows_per_block - 1) / rows_per_block, threads, 0, s>>>(
-        x, xl, g, eps, y, yl, d, plan, total_rows);
+    launch_pdl(rms_norm_kernel, dim3((total_rows + rows_per_block - 1) / rows_per_block), dim3(threads), 0, s,
+               x, xl, g, eps, y, yl, d, plan, total_rows);
     return cudaGetLastError();
 }
 
@@ -207,6 +213,8 @@ __global__ void __launch_bounds__(kSwaWarps * 32) swa_kernel(
     const float* __restrict__ vring, int d, int heads, int W, int R, PlanView plan,
     const int* __restrict__ qcum)
 {
+    pdl_wait();
+    pdl_launch();
     extern __shared__ float sm[];
     const int dh = d / heads;
     const int ld = dh + 1;                              // padded row: conflict-free column reads
@@ -292,8 +300,8 @@ cudaError_t launch_swa(const float* q, float* o, const float* kring, const float
     const int maxk = kSwaQ + window - 1;
     const size_t smem = sizeof(float) * (2 * (size_t)maxk * (dh + 1) + (size_t)kSwaWarps * dh + (size_t)kSwaWarps * window);
     if (smem > (size_t)kSwaMaxSmem) return cudaErrorInvalidValue;
-    swa_kernel<<<dim3(n_qblocks, heads), kSwaWarps * 32, smem, s>>>(q, o, kring, vring, d, heads, window, ring_R,
-                                                                    plan, qcum);
+    launch_pdl(swa_kernel, dim3(n_qblocks, heads), dim3(kSwaWarps * 32), smem, s, q, o, kring, vring, d, heads,
+               window, ring_R, plan, qcum);
     return cudaGetLastError();
 }
 
@@ -321,6 +329,8 @@ __global__ void __launch_bounds__(kFinalTile) final_conv_kernel(
     float* __restrict__ pre_tanh, long long audio_ld, PlanView plan, const int* __restrict__ bidx,
     const int* __restrict__ tcum)
 {
+    pdl_wait();
+    pdl_launch();
     extern __shared__ float4 sm4[];
     float4* sw = sm4;                                                   // [C][KP / 4]
     float2* sa = reinterpret_cast<float2*>(sm4 + (size_t)C * (KP / 4)); // [C] (alpha, 1/alpha)
@@ -388,11 +398,11 @@ cudaError_t launch_final_conv(const float* x, Layout xl, int C, const float* w, 
     const size_t smem = sizeof(float) * ((size_t)KP * C + 2 * (size_t)C + (size_t)(kFinalTile + k - 1) * k);
     if (smem > (size_t)kFinalMaxSmem) return cudaErrorInvalidValue;
     if (KP == 8)
-        final_conv_kernel<8><<<n_row_tiles, kFinalTile, smem, s>>>(x, xl, C, w, bias, alpha, inv_alpha, k, audio,
-                                                                    pre_tanh, audio_ld, plan, plan.bidx, tcum);
+        launch_pdl(final_conv_kernel<8>, dim3(n_row_tiles), dim3(kFinalTile), smem, s, x, xl, C, w, bias, alpha,
+                   inv_alpha, k, audio, pre_tanh, audio_ld, plan, plan.bidx, tcum);
     else
-        final_conv_kernel<16><<<n_row_tiles, kFinalTile, smem, s>>>(x, xl, C, w, bias, alpha, inv_alpha, k, audio,
-                                                                     pre_tanh, audio_ld, plan, plan.bidx, tcum);
+        launch_pdl(final_conv_kernel<16>, dim3(n_row_tiles), dim3(kFinalTile), smem, s, x, xl, C, w, bias, alpha,
+                   inv_alpha, k, audio, pre_tanh, audio_ld, plan, plan.bidx, tcum);
     return cudaGetLastError();
 }
 
@@ -403,6 +413,8 @@ cudaError_t launch_final_conv(const float* x, Layout xl, int C, const float* w, 
 // stage's last rows to its front).  One block per (tensor, batch entry).
 __global__ void hist_fill_kernel(const HistDesc* __restrict__ dsc, PlanView plan)
 {
+    pdl_wait();
+    pdl_launch();
     const HistDesc h = dsc[blockIdx.x];
     const int b = blockIdx.y;
     if (h.H == 0) return;
@@ -416,6 +428,8 @@ __global__ void hist_fill_kernel(const HistDesc* __restrict__ dsc, PlanView plan
 __global__ void hist_commit_kernel(const HistDesc* __restrict__ dsc, PlanView plan,
                                    long long* __restrict__ frames)
 {
+    pdl_wait();
+    pdl_launch();
     const HistDesc h = dsc[blockIdx.x];
     const int b = blockIdx.y;
     const int n = __ldg(plan.cf + b + 1) - __ldg(plan.cf + b);
@@ -431,6 +445,8 @@ __global__ void hist_commit_kernel(const HistDesc* __restrict__ dsc, PlanView pl
 __global__ void state_reset_kernel(const HistDesc* __restrict__ dsc, int nd, const int* __restrict__ slots,
                                    long long* __restrict__ frames, unsigned* __restrict__ err_words)
 {
+    pdl_wait();
+    pdl_launch();
     const int slot = slots[blockIdx.y];
     if ((int)blockIdx.x == nd) {
         if (threadIdx.x == 0) { frames[slot] = 0; err_words[slot] = 0u; }
@@ -445,7 +461,7 @@ __global__ void state_reset_kernel(const HistDesc* __restrict__ dsc, int nd, con
 cudaError_t launch_hist_fill(const HistDesc* d, int nd, PlanView plan, cudaStream_t s)
 {
     if (nd <= 0 || plan.B <= 0) return cudaSuccess;
-    hist_fill_kernel<<<dim3(nd, plan.B), 256, 0, s>>>(d, plan);
+    launch_pdl(hist_fill_kernel, dim3(nd, plan.B), dim3(256), 0, s, d, plan);
     return cudaGetLastError();
 }
 
@@ -453,7 +469,7 @@ cudaError_t launch_hist_commit(const HistDesc* d, int nd, PlanView plan, const i
                                long long* frames, cudaStream_t s)
 {
     if (nd <= 0 || plan.B <= 0) return cudaSuccess;
-    hist_commit_kernel<<<dim3(nd, plan.B), 256, 0, s>>>(d, plan, frames);
+    launch_pdl(hist_commit_kernel, dim3(nd, plan.B), dim3(256), 0, s, d, plan, frames);
     return cudaGetLastError();
 }
 

@@ -404,6 +404,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // the set-up above touches shared memory and TMEM only; global memory
+    // written by earlier kernels is read from here on
+    pdl_wait();
+    pdl_launch();
     const uint32_t tmem_base = *tmem_slot;
     const int total_tiles = p.n_mgroups * p.n_tiles_n * p.n_splits;
     const float unscale = p.unscale_dev ? *p.unscale_dev : p.unscale;
@@ -724,6 +728,8 @@ __global__ void __launch_bounds__(kReduceRows * 8) tc_reduce_kernel(const GemmAr
                                                                    int n_row_tiles, float unscale,
                                                                    const float* __restrict__ unscale_dev)
 {
+    pdl_wait();
+    pdl_launch();
     const int mt = blockIdx.x;
     const int m = blockIdx.z * kReduceRows + (threadIdx.x >> 3);
     const int n = (blockIdx.y * 8 + (threadIdx.x & 7)) * 4;
@@ -769,6 +775,8 @@ __global__ void __launch_bounds__(256) tc_prep_kernel(const float4* __restrict__
                                                       unsigned units, unsigned cin8, uint4* __restrict__ hi,
                                                       bool interleaved)
 {
+    pdl_wait();
+    pdl_launch();
     const unsigned u = blockIdx.x * 256u + threadIdx.x;
     if (u >= units) return;
     const float4 p0 = __ldg(x + 2 * (size_t)u), p1 = __ldg(x + 2 * (size_t)u + 1);
@@ -951,9 +959,9 @@ cudaError_t launch_tc_prep(const float* x, const float* alpha, const float* inv_
     if ((size_t)n > scratch->elems || Cin % 8 != 0 || n / 8 >= (1LL << 32)) return cudaErrorInvalidValue;
     const unsigned units = (unsigned)(n / 8);
     const bool vec_alpha = alpha && ((reinterpret_cast<uintptr_t>(alpha) | reinterpret_cast<uintptr_t>(inv_alpha)) & 15) == 0;
-    tc_prep_kernel<<<(units + 255) / 256, 256, 0, s>>>(reinterpret_cast<const float4*>(x), alpha, inv_alpha, vec_alpha,
-                                                       units, (unsigned)(Cin / 8), static_cast<uint4*>(scratch->a_hi),
-                                                       with_lo);
+    launch_pdl(tc_prep_kernel, dim3((units + 255) / 256), dim3(256), 0, s, reinterpret_cast<const float4*>(x),
+               alpha, inv_alpha, vec_alpha, units, (unsigned)(Cin / 8), static_cast<uint4*>(scratch->a_hi),
+               with_lo);
     return cudaGetLastError();
 }
 
@@ -1040,14 +1048,14 @@ cudaError_t tc_gemm_core(const GemmArgs& a, const TcWeights& w, const float* uns
     const int tiles = p.n_mgroups * w.n_tiles * p.n_splits;
     const int grid = std::min(tiles, num_sms > 0 ? num_sms : 152);
     if (w.passes == 3)
-        tc_gemm_kernel<3><<<grid, kThreads, smem, s>>>(ma, w.map_hi, a, plan, p);
+        launch_pdl(tc_gemm_kernel<3>, dim3(grid), dim3(kThreads), smem, s, ma, w.map_hi, a, plan, p);
     else
-        tc_gemm_kernel<1><<<grid, kThreads, smem, s>>>(ma, w.map_hi, a, plan, p);
+        launch_pdl(tc_gemm_kernel<1>, dim3(grid), dim3(kThreads), smem, s, ma, w.map_hi, a, plan, p);
     cudaError_t e = cudaGetLastError();
     if (launches) (*launches)++;
     if (e != cudaSuccess || p.n_splits == 1) return e;
-    tc_reduce_kernel<<<dim3(n_row_tiles, (a.N + 31) / 32, kBM / kReduceRows), kReduceRows * 8, 0, s>>>(
-        a, plan, p.ws, p.n_chunks, n_row_tiles, p.unscale, unscale_dev);
+    launch_pdl(tc_reduce_kernel, dim3(n_row_tiles, (a.N + 31) / 32, kBM / kReduceRows), dim3(kReduceRows * 8), 0,
+               s, a, plan, p.ws, p.n_chunks, n_row_tiles, p.unscale, unscale_dev);
     if (launches) (*launches)++;
     return cudaGetLastError();
 }
