@@ -74,6 +74,9 @@ def parse():
                          "playback gaps) for carried-state and recompute decoding, instead of the throughput line")
     ap.add_argument("--profile-call", default=None, metavar="S,CH,REPS",
                     help="profiling aid: REPS fixed decode calls of S streams x CH frames (graphs off), no timing")
+    ap.add_argument("--workload", choices=["decoder", "istft"], default="decoder",
+                    help="istft: the streaming iSTFT head alone (Vocos-shaped: n_fft 1024, hop 256, 24 kHz), "
+                         "--streams streams x 10 chunks of 94 frames")
     ap.add_argument("--layer-times", default=None, metavar="S,CH",
                     help="per-launch CUDA-event times of one decode call of S streams x CH frames from an empty "
                          "state (graphs off), labelled by layer, one JSON line")
@@ -489,6 +492,80 @@ def run_layer_times(args):
     return 0
 
 
+def run_istft(args):
+    """Throughput of the streaming iSTFT head on one GPU: S streams, each 10
+    chunks of 94 frames (about 1 s of audio per chunk at hop 256, 24 kHz),
+    spectra resident in HBM; the roofline is the call's algorithmic bytes
+    (spectra in, audio out, carried frames read and written) over its
+    CUDA-event time against the measured copy bandwidth."""
+    import torch
+    from streaming_tts_vocoder_gb300 import codec as C
+    from streaming_tts_vocoder_gb300.synthetic import make_istft_spec
+    n_fft, hop, sr, CH, NCH = 1024, 256, 24000, 94, 10
+    S = args.streams
+    nb = n_fft // 2 + 1
+    ist = C.Istft(n_fft, hop, mag_clip=100.0, max_streams=S, max_chunk_frames=CH)
+    dev = torch.device("cuda")
+    stream = torch.cuda.current_stream()
+    spec = torch.from_numpy(np.stack([make_istft_spec(n_fft, CH * NCH, 2000 + s) for s in range(S)])).to(dev)
+    chunks = [spec[:, c * CH:(c + 1) * CH].contiguous() for c in range(NCH)]
+    audio = torch.empty(S, CH * hop, device=dev)
+    flush = torch.empty(64 << 20, dtype=torch.float32, device=dev)     # 256 MB > L2, written between steps
+
+    def step():
+        ist.reset(stream=stream)
+        for c in range(NCH):
+            ist.decode(chunks[c], [CH] * S, audio, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    clk = ClockSampler(torch.cuda.current_device())
+    clk.start()
+    total = 0.0
+    for _ in range(args.steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step()
+        e1.record(stream)
+        e1.synchronize()
+        total += e0.elapsed_time(e1)
+    clocks = clk.stop()
+    ms = total / args.steps
+    audio_s = S * CH * NCH * hop / sr
+    frames = S * CH * NCH
+    taps = n_fft // hop
+    alg = frames * (2 * nb * 4 + hop * 4) + NCH * S * 2 * (taps - 1) * n_fft * 4
+    pk, pk_src = peaks()
+    achieved = alg / (ms / 1e3) / 1e9
+    cpu = None
+    if not args.no_cpu:
+        from oracle import istft as O
+        sample = make_istft_spec(n_fft, CH, 2000).astype(np.float64)
+        t0 = time.perf_counter()
+        reps = 0
+        while time.perf_counter() - t0 < 5.0:
+            O.IstftStream(n_fft, hop, 100.0).decode(sample)
+            reps += 1
+        dt = time.perf_counter() - t0
+        cpu = {"value": reps * CH * hop / sr / dt, "unit": "audio-s/s", "cores": 1, "kind": "oracle",
+               "sample": f"one stream x {CH} frames, repeated for {dt:.1f} s"}
+    print(json.dumps({
+        "metric": "iSTFT head audio-sec/sec", "value": audio_s / (ms / 1e3), "unit": "audio-s/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded log-magnitudes and phases)",
+        "config": {"workload": f"{S} streams x {NCH} chunks of {CH} frames, Vocos-shaped iSTFT head",
+                   "n_fft": n_fft, "hop": hop, "sample_rate": sr, "l2": "a 256 MB buffer is written before each step"},
+        "frames_per_s": frames / (ms / 1e3),
+        "roofline": {"bound": "hbm", "kernel": "istft call (frame, overlap-add, commit kernels)",
+                     "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
+                     "traffic": None, "peak_note": f"{pk_src} copy bandwidth",
+                     "algorithmic_bytes_per_frame": alg / frames},
+        "gpu_launches": args.steps * NCH * 3 + args.steps, "clocks": clocks, "cpu_baseline": cpu}))
+    return 0
+
+
 def playback_gaps(lats_ms, frames, frame_ms):
     """Chunks decoded back to back (chunk i ready after the sum of the first
     i + 1 latencies) and played as soon as ready: the silence before each
@@ -585,6 +662,8 @@ def main():
         return run_profile_call(args)
     if args.layer_times:
         return run_layer_times(args)
+    if args.workload == "istft":
+        return run_istft(args)
     if args.schedule:
         return run_schedule(args)
     return run_ours(args)

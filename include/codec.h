@@ -317,6 +317,62 @@ CODEC_API codec_status codec_profile_launches(codec_state_t* state, codec_launch
                                               int32_t* n_out);
 
 /* Static description of a status code. */
+/*
+ * Streaming iSTFT head: the last step of the iSTFT-head vocoders the pages
+ * list (F5-TTS's Vocos, "Vocos -> iSTFT"; CosyVoice2's and Chatterbox's HiFT,
+ * "F0 -> NSF source, iSTFT"; Kokoro's iSTFTNet generator, whose iSTFT the Core
+ * AI Kokoro note runs as a transposed convolution of stride 5 from 11 channels
+ * to 1, i.e. n_fft 20 and hop 5).  Independent of codec_t.
+ *
+ * A frame holds n_bins = n_fft / 2 + 1 log-magnitudes L[k], then n_bins phases
+ * p[k] in radians.  X[k] = min(exp(L[k]), mag_clip) * (cos p[k] + i sin p[k])
+ * (no clip when mag_clip <= 0); the frame's signal is the inverse real DFT of
+ * X (the imaginary parts of the DC and Nyquist bins are ignored) times the
+ * periodic Hann window w[m] = sin^2(pi m / n_fft); frames are overlap-added at
+ * hop and the sum is divided by the stationary window-square envelope
+ * E[n mod hop] = sum_j w[(n mod hop) + j hop]^2.  Streaming is causal: frames
+ * before a stream's start are zero, and frame t completes samples
+ * [t hop, (t + 1) hop), so a call of n frames returns n * hop samples; each
+ * stream carries its last n_fft / hop - 1 windowed frames.
+ *
+ * Limits: n_fft even, 4 <= n_fft <= 4096, hop >= 1 dividing n_fft.  Power-of-
+ * two n_fft uses a radix-2 FFT in shared memory, other sizes a direct DFT.
+ */
+typedef struct codec_istft_config {
+    int32_t n_fft;
+    int32_t hop;
+    float mag_clip;            /* magnitudes above this are clipped; <= 0: no clip */
+    int32_t max_streams;       /* stream slots */
+    int32_t max_chunk_frames;  /* frames per stream and call */
+} codec_istft_config;
+
+typedef struct codec_istft_s codec_istft_t;
+
+/* All device memory (per-slot carried frames, the per-call frame scratch,
+ * the envelope, the plan) is allocated here on the current device; every slot
+ * starts reset.  CODEC_ERR_CONFIG for limits outside the above. */
+CODEC_API codec_status codec_istft_create(const codec_istft_config* cfg, codec_istft_t** out);
+
+/* Synchronises the device, then frees everything. */
+CODEC_API void codec_istft_destroy(codec_istft_t* istft);
+
+/* Clears the carried frames of stream_ids (host, n ids; NULL: all slots),
+ * stream-ordered on `stream`. */
+CODEC_API codec_status codec_istft_reset(codec_istft_t* istft, const int32_t* stream_ids, int32_t n,
+                                         void* stream);
+
+/* One chunk for B streams.  spec: device float [B][T_max][2 n_bins] (batch
+ * entry b's frames 0 .. n_frames[b] - 1 are read); n_frames: host [B], each in
+ * 0 .. T_max; stream_ids: host [B] distinct slots, or NULL for 0 .. B-1;
+ * audio: device float [B][T_max hop], entry b's first n_frames[b] hop samples
+ * are written.  The caller owns spec and audio and keeps them alive until
+ * `stream` passes the call.  Argument errors (B > max_streams, T_max >
+ * max_chunk_frames, repeated ids, n_frames out of range) return before
+ * anything is enqueued. */
+CODEC_API codec_status codec_istft_decode(codec_istft_t* istft, const float* spec, const int32_t* n_frames,
+                                          const int32_t* stream_ids, int32_t B, int32_t T_max, float* audio,
+                                          void* stream);
+
 CODEC_API const char* codec_status_string(codec_status status);
 
 #ifdef __cplusplus

@@ -63,6 +63,11 @@ class LaunchRecordC(ctypes.Structure):
                 ("flops", ctypes.c_double), ("bytes", ctypes.c_double)]
 
 
+class IstftConfigC(ctypes.Structure):
+    _fields_ = [("n_fft", ctypes.c_int32), ("hop", ctypes.c_int32), ("mag_clip", ctypes.c_float),
+                ("max_streams", ctypes.c_int32), ("max_chunk_frames", ctypes.c_int32)]
+
+
 class StreamInfoC(ctypes.Structure):
     _fields_ = [("frames_decoded", ctypes.c_int64), ("error_bits", ctypes.c_uint32),
                 ("reserved", ctypes.c_int32)]
@@ -103,6 +108,10 @@ def _lib():
             "codec_conv1d_noalloc": (i32, [_P, i32, i32, _P, _P, _P, i32, i32, i32, _P, _P]),
             "codec_profile_end": (i32, [_P, ctypes.POINTER(KernelStatsC), _P]),
             "codec_profile_launches": (i32, [_P, ctypes.POINTER(LaunchRecordC), i32, ctypes.POINTER(i32)]),
+            "codec_istft_create": (i32, [ctypes.POINTER(IstftConfigC), ctypes.POINTER(_P)]),
+            "codec_istft_destroy": (None, [_P]),
+            "codec_istft_reset": (i32, [_P, _I32P, i32, _P]),
+            "codec_istft_decode": (i32, [_P, _P, _I32P, _I32P, i32, i32, _P, _P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(l, name)
@@ -175,6 +184,52 @@ def conv1d_noalloc(x, w, y, bias=None, alpha=None, dilation=1, stream=None):
     opt = lambda t: None if t is None else _ptr(t)
     _check(_lib().codec_conv1d_noalloc(_ptr(x), T, Cin, _ptr(w), opt(bias), opt(alpha), Cout, k, dilation,
                                        _ptr(y), _stream_handle(stream)), "codec_conv1d_noalloc")
+
+
+class Istft:
+    """codec_istft_*: the streaming iSTFT head (log-magnitude / phase frames in,
+    hop samples per frame out), with per-slot carried frames."""
+
+    def __init__(self, n_fft: int, hop: int, mag_clip: float = 0.0, max_streams: int = 1,
+                 max_chunk_frames: int = 64):
+        c = IstftConfigC(n_fft, hop, mag_clip, max_streams, max_chunk_frames)
+        h = _P()
+        _check(_lib().codec_istft_create(ctypes.byref(c), ctypes.byref(h)), "codec_istft_create")
+        self._h = h
+        self.n_fft, self.hop, self.n_bins = n_fft, hop, n_fft // 2 + 1
+
+    def close(self):
+        if getattr(self, "_h", None):
+            _lib().codec_istft_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        self.close()
+
+    def reset(self, stream_ids=None, stream=None):
+        if stream_ids is None:
+            _check(_lib().codec_istft_reset(self._h, None, 0, _stream_handle(stream)), "codec_istft_reset")
+        else:
+            ids = np.ascontiguousarray(stream_ids, dtype=np.int32)
+            _check(_lib().codec_istft_reset(self._h, ids.ctypes.data_as(_I32P), ids.size, _stream_handle(stream)),
+                   "codec_istft_reset")
+
+    def decode(self, spec, n_frames, audio, stream_ids=None, stream=None):
+        """spec: contiguous float32 CUDA [B][T_max][2 n_bins]; audio: contiguous
+        float32 CUDA [B][T_max hop]; n_frames and stream_ids: host sequences of
+        length B."""
+        B, T_max, width = spec.shape
+        nf = np.ascontiguousarray(n_frames, dtype=np.int32)
+        ids = None if stream_ids is None else np.ascontiguousarray(stream_ids, dtype=np.int32)
+        if nf.size != B or (ids is not None and ids.size != B):
+            raise ValueError("n_frames / stream_ids must have one entry per batch row")
+        if width != 2 * self.n_bins or not (spec.is_cuda and spec.is_contiguous() and str(spec.dtype) == "torch.float32"):
+            raise ValueError(f"spec must be a contiguous float32 CUDA tensor [B][T_max][{2 * self.n_bins}]")
+        if not (audio.is_cuda and audio.is_contiguous() and audio.numel() >= B * T_max * self.hop):
+            raise ValueError("audio must be a contiguous float32 CUDA tensor of B * T_max * hop values")
+        ids_p = None if ids is None else ids.ctypes.data_as(_I32P)
+        _check(_lib().codec_istft_decode(self._h, _ptr(spec), nf.ctypes.data_as(_I32P), ids_p, B, T_max,
+                                         _ptr(audio), _stream_handle(stream)), "codec_istft_decode")
 
 
 class Codec:

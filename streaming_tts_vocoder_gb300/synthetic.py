@@ -215,3 +215,14 @@ def staggered_schedule(n_streams: int, frames: int, chunk: int = 25):
             ticks.append(tick)
         t0 += chunk
     return ticks
+
+
+def make_istft_spec(n_fft: int, frames: int, seed: int, logmag_mean: float = -1.0,
+                    logmag_std: float = 1.0) -> np.ndarray:
+    """Seeded iSTFT-head input [frames][2 (n_fft / 2 + 1)] float32: log-magnitudes
+    N(logmag_mean, logmag_std), then phases U[-pi, pi)."""
+    nb = n_fft // 2 + 1
+    rng = np.random.default_rng(seed)
+    lm = rng.normal(logmag_mean, logmag_std, (frames, nb))
+    ph = rng.uniform(-np.pi, np.pi, (frames, nb))
+    return np.concatenate([lm, ph], axis=1).astype(np.float32)
