@@ -349,8 +349,10 @@ typedef struct codec_istft_config {
 typedef struct codec_istft_s codec_istft_t;
 
 /* All device memory (per-slot carried frames, the per-call frame scratch,
- * the envelope, the plan) is allocated here on the current device; every slot
- * starts reset.  CODEC_ERR_CONFIG for limits outside the above. */
+ * the envelope and twiddle tables, the plan) is allocated here on the current
+ * device; every slot starts reset.  CODEC_ERR_CONFIG for limits outside the
+ * above.  A codec_istft_t is used by one host thread at a time, and its calls
+ * go to one stream at a time (they share the plan and the frame scratch). */
 CODEC_API codec_status codec_istft_create(const codec_istft_config* cfg, codec_istft_t** out);
 
 /* Synchronises the device, then frees everything. */

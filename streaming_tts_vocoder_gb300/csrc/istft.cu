@@ -4,17 +4,20 @@
 // window-square envelope, causal, with each stream's last n_fft / hop - 1
 // windowed frames carried between calls.
 //
-// Three kernels per call, all over the call's packed frames (stream segments
-// back to back, as the decoder packs them):
+// Two kernels per call, over the call's packed frames (stream segments back
+// to back, as the decoder packs them):
 //   istft_frame_kernel   one block per frame: spectrum in shared memory,
 //                        Hermitian completion, inverse FFT (radix-2 Stockham
 //                        for power-of-two n_fft, a direct DFT otherwise),
 //                        window; the windowed frame goes to a scratch row
-//   istft_ola_kernel     one thread per output sample: the n_fft / hop frames
-//                        covering it (scratch rows, or carried frames for
-//                        frames before the chunk), newest first, / envelope
-//   istft_commit_kernel  one block per stream: the last n_fft / hop - 1
-//                        windowed frames become the carried frames
+//   istft_ola_kernel     y = 0: one thread per output sample, the n_fft / hop
+//                        frames covering it (scratch rows, or carried frames
+//                        for frames before the chunk), newest first, over the
+//                        envelope; y = 1: the last n_fft / hop - 1 windowed
+//                        frames become the carried frames
+// The carried frames of a slot live in two buffers used in turn (the host
+// keeps which one is current), so the same launch can read the old ones and
+// write the new ones.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -37,13 +40,15 @@ struct IstftPlan {
     const int* cf;      // [B + 1] cumulative frames
     const int* slot;    // [B]
     const int* bidx;    // [B] row in the caller's spec / audio arrays
+    const int* cur;     // [B] the slot's current carried-frame buffer (0 or 1)
 };
 
 // Frame f of the call (global index over all segments): block per frame.
 // Shared memory: two n_fft complex buffers and the n_fft twiddles
-// exp(+2 pi i j / n_fft).
-__global__ void istft_frame_kernel(const float* __restrict__ spec, IstftPlan plan, int T_max, int n_fft, int log2n,
-                                   float mag_clip, float* __restrict__ frames)
+// exp(+2 pi i j / n_fft), copied from the table made at create.
+__global__ void istft_frame_kernel(const float* __restrict__ spec, const float2* __restrict__ twiddles,
+                                   IstftPlan plan, int T_max, int n_fft, int log2n, float mag_clip,
+                                   float* __restrict__ frames)
 {
     extern __shared__ float2 sh[];
     float2* a = sh;
@@ -54,11 +59,7 @@ __global__ void istft_frame_kernel(const float* __restrict__ spec, IstftPlan pla
     const int t = f - __ldg(plan.cf + seg);
     const int nb = n_fft / 2 + 1;
     const float* row = spec + ((size_t)__ldg(plan.bidx + seg) * T_max + t) * (size_t)(2 * nb);
-    for (int j = threadIdx.x; j < n_fft; j += blockDim.x) {
-        float s, c;
-        sincospif(2.0f * (float)j / (float)n_fft, &s, &c);
-        tw[j] = make_float2(c, s);
-    }
+    for (int j = threadIdx.x; j < n_fft; j += blockDim.x) tw[j] = __ldg(twiddles + j);
     // X[k] for k <= n_fft / 2 and its Hermitian mirror; the imaginary parts of
     // the DC and Nyquist bins do not enter the real inverse transform
     for (int k = threadIdx.x; k < nb; k += blockDim.x) {
@@ -122,52 +123,54 @@ __global__ void istft_frame_kernel(const float* __restrict__ spec, IstftPlan pla
     }
 }
 
-// Output sample u of the call (global over all segments' samples).
-__global__ void istft_ola_kernel(const float* __restrict__ frames, const float* __restrict__ state,
+// blockIdx.y == 0: output sample u of the call (global over all segments'
+// samples).  blockIdx.y == 1: element (segment, i, m) of the new carried
+// frames, carried frame i = frame n - (taps - 1) + i of the chunk (n its
+// frames), from the scratch rows or, for a chunk shorter than that, from the
+// old carried frames; written to the slot's other buffer.
+__global__ void istft_ola_kernel(const float* __restrict__ frames, float* __restrict__ state,
                                  const float* __restrict__ env, IstftPlan plan, int n_fft, int hop, int T_max,
-                                 long long total_samples, float* __restrict__ audio)
+                                 long long total_samples, long long state_per_buf, float* __restrict__ audio)
 {
     const long long u = blockIdx.x * (long long)blockDim.x + threadIdx.x;
-    if (u >= total_samples) return;
     const int taps = n_fft / hop;
-    const int fg = (int)(u / hop);
-    const int p = (int)(u - (long long)fg * hop);
-    const int seg = find_seg(plan.cf, plan.B, fg);
-    const int f0 = __ldg(plan.cf + seg);
-    const int t = fg - f0;
-    const float* carried = state + (size_t)__ldg(plan.slot + seg) * (taps - 1) * n_fft;
-    float y = 0.f;
-    for (int j = 0; j < taps; j++) {
-        const int tj = t - j;
-        const float* fr = tj >= 0 ? frames + (size_t)(f0 + tj) * n_fft : carried + (size_t)(tj + taps - 1) * n_fft;
-        y += __ldg(fr + p + j * hop);
-    }
-    audio[((size_t)__ldg(plan.bidx + seg) * T_max + t) * hop + p] = __fdiv_rn(y, __ldg(env + p));
-}
-
-// Block per batch entry: carried frame i becomes frame n - (taps - 1) + i of
-// this chunk (n its frames), taken from the scratch rows or, when the chunk
-// is shorter than that, from a later carried frame (read before it is
-// overwritten: frames are moved in ascending i).
-__global__ void istft_commit_kernel(const float* __restrict__ frames, float* __restrict__ state, IstftPlan plan,
-                                    int n_fft, int hop)
-{
-    const int taps = n_fft / hop;
-    const int seg = blockIdx.x;
-    const int f0 = __ldg(plan.cf + seg);
-    const int n = __ldg(plan.cf + seg + 1) - f0;
-    float* carried = state + (size_t)__ldg(plan.slot + seg) * (taps - 1) * n_fft;
-    for (int i = 0; i < taps - 1; i++) {
+    const long long per_slot = (long long)(taps - 1) * n_fft;
+    if (blockIdx.y == 0) {
+        if (u >= total_samples) return;
+        const int fg = (int)(u / hop);
+        const int p = (int)(u - (long long)fg * hop);
+        const int seg = find_seg(plan.cf, plan.B, fg);
+        const int f0 = __ldg(plan.cf + seg);
+        const int t = fg - f0;
+        const float* carried = state + __ldg(plan.cur + seg) * state_per_buf + __ldg(plan.slot + seg) * per_slot;
+        float y = 0.f;
+        for (int j = 0; j < taps; j++) {
+            const int tj = t - j;
+            const float* fr = tj >= 0 ? frames + (size_t)(f0 + tj) * n_fft : carried + (size_t)(tj + taps - 1) * n_fft;
+            y += fr[p + j * hop];
+        }
+        audio[((size_t)__ldg(plan.bidx + seg) * T_max + t) * hop + p] = __fdiv_rn(y, __ldg(env + p));
+    } else {
+        if (u >= (long long)plan.B * per_slot) return;
+        const int seg = (int)(u / per_slot);
+        const long long e = u - (long long)seg * per_slot;
+        const int i = (int)(e / n_fft), m = (int)(e - (long long)i * n_fft);
+        const int f0 = __ldg(plan.cf + seg);
+        const int n = __ldg(plan.cf + seg + 1) - f0;
+        const int c = __ldg(plan.cur + seg);
+        const long long slot_off = __ldg(plan.slot + seg) * per_slot;
         const int tj = n - (taps - 1) + i;
-        const float* src = tj >= 0 ? frames + (size_t)(f0 + tj) * n_fft : carried + (size_t)(tj + taps - 1) * n_fft;
-        for (int m = threadIdx.x; m < n_fft; m += blockDim.x) carried[(size_t)i * n_fft + m] = src[m];
-        __syncthreads();
+        const float v = tj >= 0 ? frames[(size_t)(f0 + tj) * n_fft + m]
+                                : state[c * state_per_buf + slot_off + (long long)(tj + taps - 1) * n_fft + m];
+        state[(1 - c) * state_per_buf + slot_off + e] = v;
     }
 }
 
-__global__ void istft_reset_kernel(float* __restrict__ state, const int* __restrict__ slots, int per_slot)
+// Both carried-frame buffers of the listed slots (blockIdx.y: the buffer).
+__global__ void istft_reset_kernel(float* __restrict__ state, const int* __restrict__ slots, int per_slot,
+                                   long long state_per_buf)
 {
-    float* s = state + (size_t)__ldg(slots + blockIdx.x) * per_slot;
+    float* s = state + blockIdx.y * state_per_buf + (size_t)__ldg(slots + blockIdx.x) * per_slot;
     for (int m = threadIdx.x; m < per_slot; m += blockDim.x) s[m] = 0.f;
 }
 
@@ -181,7 +184,9 @@ struct codec_istft_s {
     codec_istft_config cfg{};
     int taps = 0, nb = 0, log2n = 0, threads = 0;
     size_t smem = 0;
-    float* state = nullptr;     // [slots][taps - 1][n_fft]
+    float* state = nullptr;     // [2][slots][taps - 1][n_fft]: two buffers used in turn
+    std::vector<int> cur;       // per slot: the buffer holding its current carried frames
+    float2* twiddles = nullptr; // [n_fft] exp(+2 pi i j / n_fft)
     float* frames = nullptr;    // [max_streams * max_chunk_frames][n_fft]
     float* env = nullptr;       // [hop]
     int* slots_d = nullptr;     // reset list
@@ -248,11 +253,13 @@ codec_status codec_istft_create(const codec_istft_config* cfg, codec_istft_t** o
     }
     bool ok = true;
     const size_t S = (size_t)c.max_streams;
-    s->state = istft_alloc<float>(s, S * (s->taps - 1) * c.n_fft, ok);
+    s->state = istft_alloc<float>(s, 2 * S * (s->taps - 1) * c.n_fft, ok);
+    s->twiddles = istft_alloc<float2>(s, c.n_fft, ok);
+    s->cur.assign(S, 0);
     s->frames = istft_alloc<float>(s, S * c.max_chunk_frames * c.n_fft, ok);
     s->env = istft_alloc<float>(s, c.hop, ok);
     s->slots_d = istft_alloc<int>(s, S, ok);
-    s->plan_ints = (int)(3 * S + 1);
+    s->plan_ints = (int)(4 * S + 1);
     s->plan_d = istft_alloc<int>(s, s->plan_ints, ok);
     for (int i = 0; i < kPlanRing && ok; i++) {
         if (cudaMallocHost(&s->plan_h[i], sizeof(int) * s->plan_ints) != cudaSuccess) ok = false;
@@ -272,8 +279,14 @@ codec_status codec_istft_create(const codec_istft_config* cfg, codec_istft_t** o
         }
         env[p] = (float)e;
     }
+    std::vector<float2> tw(c.n_fft);
+    for (int j = 0; j < c.n_fft; j++) {
+        const double a = 2.0 * M_PI * (double)j / (double)c.n_fft;
+        tw[j] = make_float2((float)std::cos(a), (float)std::sin(a));
+    }
     if (cudaMemcpy(s->env, env.data(), sizeof(float) * c.hop, cudaMemcpyHostToDevice) != cudaSuccess ||
-        (s->taps > 1 && cudaMemset(s->state, 0, sizeof(float) * S * (s->taps - 1) * c.n_fft) != cudaSuccess) ||
+        cudaMemcpy(s->twiddles, tw.data(), sizeof(float2) * c.n_fft, cudaMemcpyHostToDevice) != cudaSuccess ||
+        (s->taps > 1 && cudaMemset(s->state, 0, sizeof(float) * 2 * S * (s->taps - 1) * c.n_fft) != cudaSuccess) ||
         cudaDeviceSynchronize() != cudaSuccess) {
         istft_free(s);
         return CODEC_ERR_CUDA;
@@ -317,7 +330,8 @@ codec_status codec_istft_reset(codec_istft_t* s, const int32_t* ids, int32_t n, 
             cudaSuccess ||
         cudaEventRecord(s->plan_ev[i], cs) != cudaSuccess)
         return CODEC_ERR_CUDA;
-    istft_reset_kernel<<<(unsigned)list.size(), 256, 0, cs>>>(s->state, s->slots_d, per_slot);
+    istft_reset_kernel<<<dim3((unsigned)list.size(), 2), 256, 0, cs>>>(s->state, s->slots_d, per_slot,
+                                                                        (long long)S * per_slot);
     return cudaGetLastError() == cudaSuccess ? CODEC_OK : CODEC_ERR_CUDA;
 }
 
@@ -343,12 +357,14 @@ codec_status codec_istft_decode(codec_istft_t* s, const float* spec, const int32
     int* cf = s->plan_h[i];
     int* slot = cf + S + 1;
     int* bidx = slot + S;
+    int* cur = bidx + S;
     int Bc = 0;
     cf[0] = 0;
     for (int b = 0; b < B; b++) {
         if (n_frames[b] == 0) continue;
         slot[Bc] = ids ? ids[b] : b;
         bidx[Bc] = b;
+        cur[Bc] = s->cur[slot[Bc]];
         cf[Bc + 1] = cf[Bc] + n_frames[b];
         Bc++;
     }
@@ -357,13 +373,15 @@ codec_status codec_istft_decode(codec_istft_t* s, const float* spec, const int32
     if (cudaMemcpyAsync(s->plan_d, cf, sizeof(int) * s->plan_ints, cudaMemcpyHostToDevice, cs) != cudaSuccess ||
         cudaEventRecord(s->plan_ev[i], cs) != cudaSuccess)
         return CODEC_ERR_CUDA;
-    const IstftPlan plan{Bc, s->plan_d, s->plan_d + S + 1, s->plan_d + 2 * S + 1};
-    istft_frame_kernel<<<total, s->threads, s->smem, cs>>>(spec, plan, T_max, c.n_fft, s->log2n, c.mag_clip,
-                                                           s->frames);
+    const IstftPlan plan{Bc, s->plan_d, s->plan_d + S + 1, s->plan_d + 2 * S + 1, s->plan_d + 3 * S + 1};
+    istft_frame_kernel<<<total, s->threads, s->smem, cs>>>(spec, s->twiddles, plan, T_max, c.n_fft, s->log2n,
+                                                           c.mag_clip, s->frames);
     const long long samples = (long long)total * c.hop;
-    istft_ola_kernel<<<(unsigned)((samples + 255) / 256), 256, 0, cs>>>(s->frames, s->state, s->env, plan, c.n_fft,
-                                                                      c.hop, T_max, samples, audio);
-    if (s->taps > 1)
-        istft_commit_kernel<<<Bc, 256, 0, cs>>>(s->frames, s->state, plan, c.n_fft, c.hop);
+    const long long per_slot = (long long)(s->taps - 1) * c.n_fft;
+    const long long work = std::max(samples, (long long)Bc * per_slot);
+    istft_ola_kernel<<<dim3((unsigned)((work + 255) / 256), s->taps > 1 ? 2 : 1), 256, 0, cs>>>(
+        s->frames, s->state, s->env, plan, c.n_fft, c.hop, T_max, samples, (long long)S * per_slot, audio);
+    // the new carried frames are in the other buffer from here on
+    for (int b = 0; b < Bc; b++) s->cur[slot[b]] ^= 1;
     return cudaGetLastError() == cudaSuccess ? CODEC_OK : CODEC_ERR_CUDA;
 }
