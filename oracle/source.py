@@ -11,7 +11,8 @@ rate fs, H harmonics, amplitude A, voiced when F0 > threshold):
   * the frame's F0 is held for its upp samples (nearest upsampling);
   * the per-sample phase increment in cycles is quantised to 2^-32:
     D = rint(F0 * (2^32 / fs)) as an integer (2^32 / fs in float64, round half
-    to even), so that the phase is an exact integer running sum;
+    to even; F0 clamped to [0, fs / 2]), so that the phase is an exact integer
+    running sum;
   * the phase of sample n is P[n] = (P[-1] + sum_{m <= n} D[m]) mod 2^32 (the
     increment of sample n included), carried between chunks; harmonic h has
     phase h P[n] mod 2^32;
@@ -34,14 +35,19 @@ TWO32 = 4294967296
 
 
 def phase_increments(f0: np.ndarray, fs: float) -> np.ndarray:
-    """D = rint(F0 * (2^32 / fs)) per frame, as int64 (float64 arithmetic)."""
-    scale = np.float64(TWO32) / np.float64(fs)
-    return np.rint(np.asarray(f0, dtype=np.float32).astype(np.float64) * scale).astype(np.int64)
+    """D = rint(min(max(F0, 0), fs / 2) * (2^32 / fs)) per frame, as int64
+    (float64 arithmetic; fs is the float32 configuration value)."""
+    fs64 = np.float64(np.float32(fs))
+    scale = np.float64(TWO32) / fs64
+    f = np.clip(np.asarray(f0, dtype=np.float32).astype(np.float64), 0.0, fs64 / 2)
+    return np.rint(f * scale).astype(np.int64)
 
 
 class SineSource:
     def __init__(self, upp: int, fs: float, harmonics: int, amplitude: float, threshold: float = 0.0):
-        self.upp, self.fs, self.H, self.A, self.thr = upp, fs, harmonics, amplitude, threshold
+        # amplitude, threshold and fs are float32 configuration values
+        self.upp, self.fs, self.H = upp, fs, harmonics
+        self.A, self.thr = float(np.float32(amplitude)), np.float32(threshold)
         self.phase = 0            # P[-1], an integer in [0, 2^32)
 
     def reset(self):
