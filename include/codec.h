@@ -375,6 +375,78 @@ CODEC_API codec_status codec_istft_decode(codec_istft_t* istft, const float* spe
                                           const int32_t* stream_ids, int32_t B, int32_t T_max, float* audio,
                                           void* stream);
 
+/*
+ * Harmonic sine source: the hn-NSF excitation of the iSTFT-head vocoders (the
+ * Core AI Kokoro note: "har = STFT(SineGen(f0_upsamp(F0)))"; HiFT's "F0 -> NSF
+ * source").  Per stream and F0 frame (Hz), held for upp samples:
+ * D = rint(min(max(F0, 0), fs / 2) * (2^32 / fs)) is the phase increment per
+ * sample in units of 2^-32 cycle (float64 arithmetic, round half to even);
+ * the phase P[n] = (P[n - 1] + D) mod 2^32 is an exact integer running sum,
+ * carried between calls (0 after reset); output
+ * out[n][h - 1] = amplitude * sin(2 pi (h P[n] mod 2^32) / 2^32) for
+ * h = 1 .. harmonics where F0 > voiced_threshold, else 0.
+ * Limits: 1 <= upp <= 65536, 1 <= harmonics <= 16, sample_rate > 0.
+ */
+typedef struct codec_sine_config {
+    int32_t upp;               /* samples per F0 frame */
+    float sample_rate;
+    int32_t harmonics;
+    float amplitude;
+    float voiced_threshold;
+    int32_t max_streams;
+    int32_t max_chunk_frames;
+} codec_sine_config;
+
+typedef struct codec_sine_s codec_sine_t;
+
+/* Allocates the per-slot phases and the per-call plan and frame scratch on
+ * the current device, all slots reset.  One host thread and one stream at a
+ * time per object. */
+CODEC_API codec_status codec_sine_create(const codec_sine_config* cfg, codec_sine_t** out);
+CODEC_API void codec_sine_destroy(codec_sine_t* sine);
+/* Phases of stream_ids (host, n; NULL: all) back to 0, stream-ordered. */
+CODEC_API codec_status codec_sine_reset(codec_sine_t* sine, const int32_t* stream_ids, int32_t n, void* stream);
+/* f0: device float [B][T_max] (entry b's first n_frames[b] frames read);
+ * n_frames, stream_ids: host [B] (ids distinct, NULL: 0 .. B-1); out: device
+ * float [B][T_max upp][harmonics], entry b's first n_frames[b] upp rows
+ * written.  Argument errors return before anything is enqueued. */
+CODEC_API codec_status codec_sine_decode(codec_sine_t* sine, const float* f0, const int32_t* n_frames,
+                                         const int32_t* stream_ids, int32_t B, int32_t T_max, float* out,
+                                         void* stream);
+
+/*
+ * Streaming analysis STFT (the "STFT" of the same excitation path): frame t
+ * of a stream covers its input samples [(t + 1) hop - n_fft, (t + 1) hop)
+ * (zeros before the stream's start), times the periodic Hann window
+ * w[m] = sin^2(pi m / n_fft); X_t[k] = sum_m w[m] x[m] exp(-2 pi i k m /
+ * n_fft), k = 0 .. n_fft / 2.  Every hop of input yields one frame; each
+ * stream carries its last n_fft - hop input samples.  Fed to the iSTFT head
+ * (as log|X| and arg X) it returns the input delayed by n_fft - hop samples.
+ * Limits as for the iSTFT head.
+ */
+typedef struct codec_stft_config {
+    int32_t n_fft;
+    int32_t hop;
+    int32_t max_streams;
+    int32_t max_chunk_frames;  /* hops (frames) per stream and call */
+} codec_stft_config;
+
+typedef struct codec_stft_s codec_stft_t;
+
+/* Allocates the per-slot input history (two buffers used in turn), the
+ * twiddle table and the plan on the current device, all slots reset.  One
+ * host thread and one stream at a time per object. */
+CODEC_API codec_status codec_stft_create(const codec_stft_config* cfg, codec_stft_t** out);
+CODEC_API void codec_stft_destroy(codec_stft_t* stft);
+CODEC_API codec_status codec_stft_reset(codec_stft_t* stft, const int32_t* stream_ids, int32_t n, void* stream);
+/* x: device float [B][T_max hop] (entry b's first n_frames[b] hop samples
+ * read); n_frames: host [B], hops per entry, 0 .. T_max; stream_ids as above;
+ * spec: device float [B][T_max][2 (n_fft / 2 + 1)], per frame the real parts
+ * then the imaginary parts; entry b's first n_frames[b] frames written. */
+CODEC_API codec_status codec_stft_decode(codec_stft_t* stft, const float* x, const int32_t* n_frames,
+                                         const int32_t* stream_ids, int32_t B, int32_t T_max, float* spec,
+                                         void* stream);
+
 CODEC_API const char* codec_status_string(codec_status status);
 
 #ifdef __cplusplus

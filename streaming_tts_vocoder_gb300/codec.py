@@ -68,6 +68,17 @@ class IstftConfigC(ctypes.Structure):
                 ("max_streams", ctypes.c_int32), ("max_chunk_frames", ctypes.c_int32)]
 
 
+class SineConfigC(ctypes.Structure):
+    _fields_ = [("upp", ctypes.c_int32), ("sample_rate", ctypes.c_float), ("harmonics", ctypes.c_int32),
+                ("amplitude", ctypes.c_float), ("voiced_threshold", ctypes.c_float),
+                ("max_streams", ctypes.c_int32), ("max_chunk_frames", ctypes.c_int32)]
+
+
+class StftConfigC(ctypes.Structure):
+    _fields_ = [("n_fft", ctypes.c_int32), ("hop", ctypes.c_int32), ("max_streams", ctypes.c_int32),
+                ("max_chunk_frames", ctypes.c_int32)]
+
+
 class StreamInfoC(ctypes.Structure):
     _fields_ = [("frames_decoded", ctypes.c_int64), ("error_bits", ctypes.c_uint32),
                 ("reserved", ctypes.c_int32)]
@@ -112,6 +123,14 @@ def _lib():
             "codec_istft_destroy": (None, [_P]),
             "codec_istft_reset": (i32, [_P, _I32P, i32, _P]),
             "codec_istft_decode": (i32, [_P, _P, _I32P, _I32P, i32, i32, _P, _P]),
+            "codec_sine_create": (i32, [ctypes.POINTER(SineConfigC), ctypes.POINTER(_P)]),
+            "codec_sine_destroy": (None, [_P]),
+            "codec_sine_reset": (i32, [_P, _I32P, i32, _P]),
+            "codec_sine_decode": (i32, [_P, _P, _I32P, _I32P, i32, i32, _P, _P]),
+            "codec_stft_create": (i32, [ctypes.POINTER(StftConfigC), ctypes.POINTER(_P)]),
+            "codec_stft_destroy": (None, [_P]),
+            "codec_stft_reset": (i32, [_P, _I32P, i32, _P]),
+            "codec_stft_decode": (i32, [_P, _P, _I32P, _I32P, i32, i32, _P, _P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(l, name)
@@ -230,6 +249,76 @@ class Istft:
         ids_p = None if ids is None else ids.ctypes.data_as(_I32P)
         _check(_lib().codec_istft_decode(self._h, _ptr(spec), nf.ctypes.data_as(_I32P), ids_p, B, T_max,
                                          _ptr(audio), _stream_handle(stream)), "codec_istft_decode")
+
+
+class _Streamed:
+    """Shared marshalling of the per-stream ops (create / reset / decode / destroy)."""
+    _prefix = ""
+
+    def _create(self, cfg):
+        h = _P()
+        _check(getattr(_lib(), self._prefix + "create")(ctypes.byref(cfg), ctypes.byref(h)), self._prefix + "create")
+        self._h = h
+
+    def close(self):
+        if getattr(self, "_h", None):
+            getattr(_lib(), self._prefix + "destroy")(self._h)
+            self._h = None
+
+    def __del__(self):
+        self.close()
+
+    def reset(self, stream_ids=None, stream=None):
+        fn = getattr(_lib(), self._prefix + "reset")
+        if stream_ids is None:
+            _check(fn(self._h, None, 0, _stream_handle(stream)), self._prefix + "reset")
+        else:
+            ids = np.ascontiguousarray(stream_ids, dtype=np.int32)
+            _check(fn(self._h, ids.ctypes.data_as(_I32P), ids.size, _stream_handle(stream)), self._prefix + "reset")
+
+    def _decode(self, inp, n_frames, out, stream_ids, stream, in_per_frame, out_per_frame):
+        B, T_max = inp.shape[0], inp.shape[1] if inp.dim() > 1 else 1
+        nf = np.ascontiguousarray(n_frames, dtype=np.int32)
+        ids = None if stream_ids is None else np.ascontiguousarray(stream_ids, dtype=np.int32)
+        if nf.size != B or (ids is not None and ids.size != B):
+            raise ValueError("n_frames / stream_ids must have one entry per batch row")
+        for t, per in ((inp, in_per_frame), (out, out_per_frame)):
+            if not (t.is_cuda and t.is_contiguous() and str(t.dtype) == "torch.float32"):
+                raise ValueError("arguments must be contiguous float32 CUDA tensors")
+        if inp.numel() != B * T_max * in_per_frame or out.numel() < B * T_max * out_per_frame:
+            raise ValueError("tensor sizes do not match the call")
+        ids_p = None if ids is None else ids.ctypes.data_as(_I32P)
+        _check(getattr(_lib(), self._prefix + "decode")(self._h, _ptr(inp), nf.ctypes.data_as(_I32P), ids_p, B,
+                                                        T_max, _ptr(out), _stream_handle(stream)),
+               self._prefix + "decode")
+
+
+class SineSource(_Streamed):
+    """codec_sine_*: harmonic sine source, F0 frames in, [samples][harmonics] out."""
+    _prefix = "codec_sine_"
+
+    def __init__(self, upp: int, sample_rate: float, harmonics: int, amplitude: float = 0.1,
+                 voiced_threshold: float = 0.0, max_streams: int = 1, max_chunk_frames: int = 64):
+        self.upp, self.harmonics = upp, harmonics
+        self._create(SineConfigC(upp, sample_rate, harmonics, amplitude, voiced_threshold, max_streams,
+                                 max_chunk_frames))
+
+    def decode(self, f0, n_frames, out, stream_ids=None, stream=None):
+        """f0: float32 CUDA [B][T_max]; out: float32 CUDA [B][T_max upp][harmonics]."""
+        self._decode(f0, n_frames, out, stream_ids, stream, 1, self.upp * self.harmonics)
+
+
+class Stft(_Streamed):
+    """codec_stft_*: causal analysis STFT, hop samples per frame in, 2 (n_fft / 2 + 1) values per frame out."""
+    _prefix = "codec_stft_"
+
+    def __init__(self, n_fft: int, hop: int, max_streams: int = 1, max_chunk_frames: int = 64):
+        self.n_fft, self.hop, self.n_bins = n_fft, hop, n_fft // 2 + 1
+        self._create(StftConfigC(n_fft, hop, max_streams, max_chunk_frames))
+
+    def decode(self, x, n_frames, spec, stream_ids=None, stream=None):
+        """x: float32 CUDA [B][T_max][hop]; spec: float32 CUDA [B][T_max][2 n_bins]."""
+        self._decode(x, n_frames, spec, stream_ids, stream, self.hop, 2 * self.n_bins)
 
 
 class Codec:

@@ -27,6 +27,7 @@
 
 #include "codec.h"
 #include "common.cuh"
+#include "fft_smem.cuh"
 
 namespace codec {
 
@@ -75,29 +76,7 @@ __global__ void istft_frame_kernel(const float* __restrict__ spec, const float2*
     __syncthreads();
     float2* out = a;
     if (log2n > 0) {
-        // radix-2 Stockham inverse FFT: stage with half-length Ls maps
-        // in[j], in[j + n/2] (j = g Ls + k) to out[2 g Ls + k], out[2 g Ls + k + Ls]
-        float2* in = a;
-        float2* o = b;
-        const int half = n_fft / 2;
-        for (int Ls = 1; Ls < n_fft; Ls <<= 1) {
-            const int tstep = half / Ls;      // twiddle exp(i pi k / Ls) = tw[k * n / (2 Ls)]
-            for (int j = threadIdx.x; j < half; j += blockDim.x) {
-                const int k = j & (Ls - 1);
-                const float2 u = in[j];
-                const float2 v0 = in[j + half];
-                const float2 w = tw[k * tstep];
-                const float2 v = make_float2(v0.x * w.x - v0.y * w.y, v0.x * w.y + v0.y * w.x);
-                const int d = 2 * (j - k) + k;
-                o[d] = make_float2(u.x + v.x, u.y + v.y);
-                o[d + Ls] = make_float2(u.x - v.x, u.y - v.y);
-            }
-            __syncthreads();
-            float2* tmp = in;
-            in = o;
-            o = tmp;
-        }
-        out = in;
+        out = fft_stockham(a, b, tw, n_fft, false);
     } else {
         // direct inverse DFT: x[m] = sum_k X[k] exp(2 pi i k m / n)
         for (int m = threadIdx.x; m < n_fft; m += blockDim.x) {

@@ -226,3 +226,12 @@ def make_istft_spec(n_fft: int, frames: int, seed: int, logmag_mean: float = -1.
     lm = rng.normal(logmag_mean, logmag_std, (frames, nb))
     ph = rng.uniform(-np.pi, np.pi, (frames, nb))
     return np.concatenate([lm, ph], axis=1).astype(np.float32)
+
+
+def make_f0(frames: int, seed: int, voiced_fraction: float = 0.7) -> np.ndarray:
+    """Seeded F0 contour [frames] float32 in Hz: voiced runs with F0 drifting in
+    [80, 400] Hz, unvoiced frames (0 Hz) with probability 1 - voiced_fraction."""
+    rng = np.random.default_rng(seed)
+    f = np.clip(200.0 + np.cumsum(rng.normal(0.0, 8.0, frames)), 80.0, 400.0)
+    f[rng.random(frames) >= voiced_fraction] = 0.0
+    return f.astype(np.float32)
