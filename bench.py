@@ -74,9 +74,11 @@ def parse():
                          "playback gaps) for carried-state and recompute decoding, instead of the throughput line")
     ap.add_argument("--profile-call", default=None, metavar="S,CH,REPS",
                     help="profiling aid: REPS fixed decode calls of S streams x CH frames (graphs off), no timing")
-    ap.add_argument("--workload", choices=["decoder", "istft"], default="decoder",
+    ap.add_argument("--workload", choices=["decoder", "istft", "source"], default="decoder",
                     help="istft: the streaming iSTFT head alone (Vocos-shaped: n_fft 1024, hop 256, 24 kHz), "
-                         "--streams streams x 10 chunks of 94 frames")
+                         "--streams streams x 10 chunks of 94 frames; source: the harmonic sine source (8 "
+                         "harmonics, F0 every 256 samples) and the analysis STFT (n_fft 16, hop 4) on the "
+                         "same streams and chunk lengths")
     ap.add_argument("--layer-times", default=None, metavar="S,CH",
                     help="per-launch CUDA-event times of one decode call of S streams x CH frames from an empty "
                          "state (graphs off), labelled by layer, one JSON line")
@@ -566,6 +568,88 @@ def run_istft(args):
     return 0
 
 
+def timed_steps(step, steps, warmup, stream):
+    """Mean CUDA-event ms of `step` over `steps` runs after `warmup` runs, with
+    a 256 MB buffer written before each timed run (larger than L2)."""
+    import torch
+    flush = torch.empty(64 << 20, dtype=torch.float32, device="cuda")
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    total = 0.0
+    for _ in range(steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step()
+        e1.record(stream)
+        e1.synchronize()
+        total += e0.elapsed_time(e1)
+    return total / steps
+
+
+def run_source(args):
+    """Throughput of the excitation ops on one GPU: S streams x 10 chunks of 94
+    F0 frames (upp 256 at 24 kHz: about 1 s of audio per chunk) through the
+    8-harmonic sine source, and the same amount of 24 kHz signal through the
+    analysis STFT (n_fft 16, hop 4: HiFT-sized).  Rooflines: each op's
+    algorithmic bytes (inputs read, outputs written, carried state) over its
+    CUDA-event time against the measured copy bandwidth."""
+    import torch
+    from streaming_tts_vocoder_gb300 import codec as C
+    from streaming_tts_vocoder_gb300.synthetic import make_f0
+    S, CH, NCH, upp, sr, H, n_fft, hop = args.streams, 94, 10, 256, 24000, 8, 16, 4
+    dev = torch.device("cuda")
+    stream = torch.cuda.current_stream()
+    src = C.SineSource(upp, float(sr), H, amplitude=0.1, max_streams=S, max_chunk_frames=CH)
+    f0 = torch.from_numpy(np.stack([make_f0(CH * NCH, 3000 + s) for s in range(S)])).to(dev)
+    f0c = [f0[:, c * CH:(c + 1) * CH].contiguous() for c in range(NCH)]
+    exc = torch.empty(S, CH * upp, H, device=dev)
+
+    def sine_step():
+        src.reset(stream=stream)
+        for c in range(NCH):
+            src.decode(f0c[c], [CH] * S, exc, stream=stream)
+
+    hops = CH * upp // hop                       # the same audio per chunk through the STFT
+    st = C.Stft(n_fft, hop, max_streams=S, max_chunk_frames=hops)
+    gen = torch.Generator(device="cpu").manual_seed(5)
+    xc = [torch.randn(S, hops, hop, generator=gen).to(dev) for _ in range(NCH)]
+    nb = n_fft // 2 + 1
+    spec = torch.empty(S, hops, 2 * nb, device=dev)
+
+    def stft_step():
+        st.reset(stream=stream)
+        for c in range(NCH):
+            st.decode(xc[c], [hops] * S, spec, stream=stream)
+
+    warm = max(3, args.warmup)
+    clk = ClockSampler(torch.cuda.current_device())
+    clk.start()
+    ms_sine = timed_steps(sine_step, args.steps, warm, stream)
+    ms_stft = timed_steps(stft_step, args.steps, warm, stream)
+    clocks = clk.stop()
+    audio_s = S * CH * NCH * upp / sr
+    pk, pk_src = peaks()
+    b_sine = S * NCH * (CH * 4 + CH * upp * H * 4)
+    b_stft = S * NCH * (hops * hop * 4 + hops * 2 * nb * 4 + 2 * (n_fft - hop) * 4)
+    roof = lambda b, ms, name: {"bound": "hbm", "kernel": name, "achieved": b / (ms / 1e3) / 1e9,
+                                "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": b / (ms / 1e3) / 1e9 / pk["hbm_gbs"],
+                                "traffic": None, "peak_note": f"{pk_src} copy bandwidth"}
+    print(json.dumps({
+        "metric": "harmonic sine source audio-sec/sec", "value": audio_s / (ms_sine / 1e3), "unit": "audio-s/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": warm, "ms_per_step": ms_sine, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32 (u32 phase)", "data": "synthetic (seeded F0 contours)",
+        "config": {"workload": f"{S} streams x {NCH} chunks of {CH} F0 frames, {H} harmonics, {upp} samples per "
+                               f"frame, {sr} Hz", "l2": "a 256 MB buffer is written before each step"},
+        "roofline": roof(b_sine, ms_sine, "sine source call (scan, output kernels)"),
+        "stft": {"value": audio_s / (ms_stft / 1e3), "unit": "audio-s/s", "ms_per_step": ms_stft,
+                 "config": {"n_fft": n_fft, "hop": hop, "frames_per_chunk": hops},
+                 "roofline": roof(b_stft, ms_stft, "stft call (frame, history kernels)")},
+        "gpu_launches": args.steps * (1 + 2 * NCH) * 2, "clocks": clocks, "cpu_baseline": None}))
+    return 0
+
+
 def playback_gaps(lats_ms, frames, frame_ms):
     """Chunks decoded back to back (chunk i ready after the sum of the first
     i + 1 latencies) and played as soon as ready: the silence before each
@@ -664,6 +748,8 @@ def main():
         return run_layer_times(args)
     if args.workload == "istft":
         return run_istft(args)
+    if args.workload == "source":
+        return run_source(args)
     if args.schedule:
         return run_schedule(args)
     return run_ours(args)

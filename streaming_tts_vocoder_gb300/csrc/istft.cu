@@ -44,61 +44,70 @@ struct IstftPlan {
     const int* cur;     // [B] the slot's current carried-frame buffer (0 or 1)
 };
 
-// Frame f of the call (global index over all segments): block per frame.
-// Shared memory: two n_fft complex buffers and the n_fft twiddles
-// exp(+2 pi i j / n_fft), copied from the table made at create.
+// Frames of the call (global index over all segments), fpb per block, one
+// team of tpf threads each.  Shared memory: the n_fft twiddles exp(+2 pi i j
+// / n_fft), copied from the table made at create, then two n_fft complex
+// buffers per team.  Every thread reaches every barrier; a team past the last
+// frame does no work.
 __global__ void istft_frame_kernel(const float* __restrict__ spec, const float2* __restrict__ twiddles,
-                                   IstftPlan plan, int T_max, int n_fft, int log2n, float mag_clip,
-                                   float* __restrict__ frames)
+                                   IstftPlan plan, int total, int T_max, int n_fft, int log2n, int tpf,
+                                   float mag_clip, float* __restrict__ frames)
 {
     extern __shared__ float2 sh[];
-    float2* a = sh;
-    float2* b = sh + n_fft;
-    float2* tw = sh + 2 * n_fft;
-    const int f = blockIdx.x;
-    const int seg = find_seg(plan.cf, plan.B, f);
-    const int t = f - __ldg(plan.cf + seg);
-    const int nb = n_fft / 2 + 1;
-    const float* row = spec + ((size_t)__ldg(plan.bidx + seg) * T_max + t) * (size_t)(2 * nb);
+    float2* tw = sh;
+    const int team = threadIdx.x / tpf, tid = threadIdx.x - team * tpf;
+    float2* a = sh + n_fft + (size_t)team * 2 * n_fft;
+    float2* b = a + n_fft;
+    const int f = blockIdx.x * (blockDim.x / tpf) + team;
+    const bool valid = f < total;
     for (int j = threadIdx.x; j < n_fft; j += blockDim.x) tw[j] = __ldg(twiddles + j);
-    // X[k] for k <= n_fft / 2 and its Hermitian mirror; the imaginary parts of
-    // the DC and Nyquist bins do not enter the real inverse transform
-    for (int k = threadIdx.x; k < nb; k += blockDim.x) {
-        float mag = expf(__ldg(row + k));
-        if (mag_clip > 0.f) mag = fminf(mag, mag_clip);
-        float s, c;
-        sincosf(__ldg(row + nb + k), &s, &c);
-        float2 x = make_float2(mag * c, mag * s);
-        if (k == 0 || 2 * k == n_fft) x.y = 0.f;
-        a[k] = x;
-        if (k > 0 && 2 * k < n_fft) a[n_fft - k] = make_float2(x.x, -x.y);
+    const int nb = n_fft / 2 + 1;
+    if (valid) {
+        const int seg = find_seg(plan.cf, plan.B, f);
+        const int t = f - __ldg(plan.cf + seg);
+        const float* row = spec + ((size_t)__ldg(plan.bidx + seg) * T_max + t) * (size_t)(2 * nb);
+        // X[k] for k <= n_fft / 2 and its Hermitian mirror; the imaginary parts of
+        // the DC and Nyquist bins do not enter the real inverse transform
+        for (int k = tid; k < nb; k += tpf) {
+            float mag = expf(__ldg(row + k));
+            if (mag_clip > 0.f) mag = fminf(mag, mag_clip);
+            float sn, cs;
+            sincosf(__ldg(row + nb + k), &sn, &cs);
+            float2 x = make_float2(mag * cs, mag * sn);
+            if (k == 0 || 2 * k == n_fft) x.y = 0.f;
+            a[k] = x;
+            if (k > 0 && 2 * k < n_fft) a[n_fft - k] = make_float2(x.x, -x.y);
+        }
     }
     __syncthreads();
     float2* out = a;
     if (log2n > 0) {
-        out = fft_stockham(a, b, tw, n_fft, false);
+        out = fft_stockham(a, b, tw, n_fft, false, tid, tpf);
     } else {
         // direct inverse DFT: x[m] = sum_k X[k] exp(2 pi i k m / n)
-        for (int m = threadIdx.x; m < n_fft; m += blockDim.x) {
-            float re = 0.f;
-            int km = 0;
-            for (int k = 0; k < n_fft; k++) {
-                const float2 x = a[k], w = tw[km];
-                re = fmaf(x.x, w.x, re);
-                re = fmaf(-x.y, w.y, re);
-                km += m;
-                if (km >= n_fft) km -= n_fft;
+        if (valid) {
+            for (int m = tid; m < n_fft; m += tpf) {
+                float re = 0.f;
+                int km = 0;
+                for (int k = 0; k < n_fft; k++) {
+                    const float2 x = a[k], w = tw[km];
+                    re = fmaf(x.x, w.x, re);
+                    re = fmaf(-x.y, w.y, re);
+                    km += m;
+                    if (km >= n_fft) km -= n_fft;
+                }
+                b[m].x = re;
             }
-            b[m].x = re;
         }
         __syncthreads();
         out = b;
     }
+    if (!valid) return;
     float* dst = frames + (size_t)f * n_fft;
     const float inv_n = 1.0f / (float)n_fft;
-    for (int m = threadIdx.x; m < n_fft; m += blockDim.x) {
-        const float s = sinpif((float)m / (float)n_fft);
-        dst[m] = out[m].x * inv_n * (s * s);
+    for (int m = tid; m < n_fft; m += tpf) {
+        const float sv = sinpif((float)m / (float)n_fft);
+        dst[m] = out[m].x * inv_n * (sv * sv);
     }
 }
 
@@ -161,7 +170,7 @@ using namespace codec;
 
 struct codec_istft_s {
     codec_istft_config cfg{};
-    int taps = 0, nb = 0, log2n = 0, threads = 0;
+    int taps = 0, nb = 0, log2n = 0, tpf = 0, fpb = 0;   // threads per frame, frames per block
     size_t smem = 0;
     float* state = nullptr;     // [2][slots][taps - 1][n_fft]: two buffers used in turn
     std::vector<int> cur;       // per slot: the buffer holding its current carried frames
@@ -223,8 +232,9 @@ codec_status codec_istft_create(const codec_istft_config* cfg, codec_istft_t** o
     s->log2n = 0;
     if ((c.n_fft & (c.n_fft - 1)) == 0)
         while ((1 << s->log2n) < c.n_fft) s->log2n++;
-    s->threads = c.n_fft >= 512 ? 256 : 128;
-    s->smem = sizeof(float2) * 3 * (size_t)c.n_fft;
+    s->tpf = fft_team_threads(c.n_fft);
+    s->fpb = std::max(1, 256 / s->tpf);
+    s->smem = sizeof(float2) * (1 + 2 * (size_t)s->fpb) * (size_t)c.n_fft;
     if (cudaFuncSetAttribute(istft_frame_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s->smem) !=
         cudaSuccess) {
         istft_free(s);
@@ -353,8 +363,8 @@ codec_status codec_istft_decode(codec_istft_t* s, const float* spec, const int32
         cudaEventRecord(s->plan_ev[i], cs) != cudaSuccess)
         return CODEC_ERR_CUDA;
     const IstftPlan plan{Bc, s->plan_d, s->plan_d + S + 1, s->plan_d + 2 * S + 1, s->plan_d + 3 * S + 1};
-    istft_frame_kernel<<<total, s->threads, s->smem, cs>>>(spec, s->twiddles, plan, T_max, c.n_fft, s->log2n,
-                                                           c.mag_clip, s->frames);
+    istft_frame_kernel<<<(total + s->fpb - 1) / s->fpb, s->fpb * s->tpf, s->smem, cs>>>(
+        spec, s->twiddles, plan, total, T_max, c.n_fft, s->log2n, s->tpf, c.mag_clip, s->frames);
     const long long samples = (long long)total * c.hop;
     const long long per_slot = (long long)(s->taps - 1) * c.n_fft;
     const long long work = std::max(samples, (long long)Bc * per_slot);

@@ -86,55 +86,66 @@ __global__ void sine_out_kernel(const float* __restrict__ f0, SrcPlan plan, int 
     }
 }
 
-// Frame f of the call: block per frame.  Shared memory: two n_fft complex
-// buffers and the twiddles exp(+2 pi i j / n_fft).
+// Frames of the call, fpb per block, one team of tpf threads each.  Shared
+// memory: the twiddles exp(+2 pi i j / n_fft), then two n_fft complex buffers
+// per team.  Every thread reaches every barrier; a team past the last frame
+// does no work.
 __global__ void stft_frame_kernel(const float* __restrict__ x, const float* __restrict__ hist,
-                                  const float2* __restrict__ twiddles, SrcPlan plan, int T_max, int n_fft, int hop,
-                                  int log2n, long long hist_per_buf, float* __restrict__ spec)
+                                  const float2* __restrict__ twiddles, SrcPlan plan, int total, int T_max,
+                                  int n_fft, int hop, int log2n, int tpf, long long hist_per_buf,
+                                  float* __restrict__ spec)
 {
     extern __shared__ float2 sh[];
-    float2* a = sh;
-    float2* b = sh + n_fft;
-    float2* tw = sh + 2 * n_fft;
-    const int f = blockIdx.x;
-    const int seg = find_seg(plan.cf, plan.B, f);
-    const int t = f - __ldg(plan.cf + seg);
-    const int L = n_fft - hop;
-    const int bi = __ldg(plan.bidx + seg);
-    const float* xr = x + (size_t)bi * T_max * hop;
-    const float* hr = hist + __ldg(plan.cur + seg) * hist_per_buf + (size_t)__ldg(plan.slot + seg) * L;
+    float2* tw = sh;
+    const int team = threadIdx.x / tpf, tid = threadIdx.x - team * tpf;
+    float2* a = sh + n_fft + (size_t)team * 2 * n_fft;
+    float2* b = a + n_fft;
+    const int f = blockIdx.x * (blockDim.x / tpf) + team;
+    const bool valid = f < total;
     for (int j = threadIdx.x; j < n_fft; j += blockDim.x) tw[j] = __ldg(twiddles + j);
-    for (int m = threadIdx.x; m < n_fft; m += blockDim.x) {
-        const int j = t * hop + m;              // position in [history | chunk]
-        const float v = j < L ? __ldg(hr + j) : __ldg(xr + (j - L));
-        const float s = sinpif((float)m / (float)n_fft);
-        a[m] = make_float2(v * (s * s), 0.f);
+    const int L = n_fft - hop;
+    int seg = 0, t = 0, bi = 0;
+    if (valid) {
+        seg = find_seg(plan.cf, plan.B, f);
+        t = f - __ldg(plan.cf + seg);
+        bi = __ldg(plan.bidx + seg);
+        const float* xr = x + (size_t)bi * T_max * hop;
+        const float* hr = hist + __ldg(plan.cur + seg) * hist_per_buf + (size_t)__ldg(plan.slot + seg) * L;
+        for (int m = tid; m < n_fft; m += tpf) {
+            const int j = t * hop + m;              // position in [history | chunk]
+            const float v = j < L ? __ldg(hr + j) : __ldg(xr + (j - L));
+            const float sv = sinpif((float)m / (float)n_fft);
+            a[m] = make_float2(v * (sv * sv), 0.f);
+        }
     }
     __syncthreads();
     const int nb = n_fft / 2 + 1;
     const float2* X;
     if (log2n > 0) {
-        X = fft_stockham(a, b, tw, n_fft, true);
+        X = fft_stockham(a, b, tw, n_fft, true, tid, tpf);
     } else {
         // direct DFT of the bins kept: X[k] = sum_m a[m] exp(-2 pi i k m / n)
-        for (int k = threadIdx.x; k < nb; k += blockDim.x) {
-            float re = 0.f, im = 0.f;
-            int km = 0;
-            for (int m = 0; m < n_fft; m++) {
-                const float v = a[m].x;
-                const float2 w = tw[km];
-                re = fmaf(v, w.x, re);
-                im = fmaf(-v, w.y, im);
-                km += k;
-                if (km >= n_fft) km -= n_fft;
+        if (valid) {
+            for (int k = tid; k < nb; k += tpf) {
+                float re = 0.f, im = 0.f;
+                int km = 0;
+                for (int m = 0; m < n_fft; m++) {
+                    const float v = a[m].x;
+                    const float2 w = tw[km];
+                    re = fmaf(v, w.x, re);
+                    im = fmaf(-v, w.y, im);
+                    km += k;
+                    if (km >= n_fft) km -= n_fft;
+                }
+                b[k] = make_float2(re, im);
             }
-            b[k] = make_float2(re, im);
         }
         __syncthreads();
         X = b;
     }
+    if (!valid) return;
     float* dst = spec + ((size_t)bi * T_max + t) * (size_t)(2 * nb);
-    for (int k = threadIdx.x; k < nb; k += blockDim.x) {
+    for (int k = tid; k < nb; k += tpf) {
         dst[k] = X[k].x;
         dst[nb + k] = X[k].y;
     }
@@ -297,7 +308,7 @@ struct codec_sine_s {
 
 struct codec_stft_s {
     codec_stft_config cfg{};
-    int log2n = 0, threads = 0;
+    int log2n = 0, tpf = 0, fpb = 0;   // threads per frame, frames per block
     size_t smem = 0;
     float* hist = nullptr;         // [2][slots][n_fft - hop]
     float2* twiddles = nullptr;
@@ -414,8 +425,9 @@ codec_status codec_stft_create(const codec_stft_config* cfg, codec_stft_t** out)
     s->cfg = c;
     if ((c.n_fft & (c.n_fft - 1)) == 0)
         while ((1 << s->log2n) < c.n_fft) s->log2n++;
-    s->threads = c.n_fft >= 512 ? 256 : 128;
-    s->smem = sizeof(float2) * 3 * (size_t)c.n_fft;
+    s->tpf = fft_team_threads(c.n_fft);
+    s->fpb = std::max(1, 256 / s->tpf);
+    s->smem = sizeof(float2) * (1 + 2 * (size_t)s->fpb) * (size_t)c.n_fft;
     if (cudaFuncSetAttribute(stft_frame_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s->smem) !=
         cudaSuccess) {
         src_free(s);
@@ -481,8 +493,8 @@ codec_status codec_stft_decode(codec_stft_t* s, const float* x, const int32_t* n
     if (st != CODEC_OK || Bc == 0) return st;
     const long long L = c.n_fft - c.hop;
     const long long per_buf = (long long)c.max_streams * L;
-    stft_frame_kernel<<<total, s->threads, s->smem, cs>>>(x, s->hist, s->twiddles, plan, T_max, c.n_fft, c.hop,
-                                                          s->log2n, per_buf, spec);
+    stft_frame_kernel<<<(total + s->fpb - 1) / s->fpb, s->fpb * s->tpf, s->smem, cs>>>(
+        x, s->hist, s->twiddles, plan, total, T_max, c.n_fft, c.hop, s->log2n, s->tpf, per_buf, spec);
     if (L > 0) {
         const long long work = (long long)Bc * L;
         stft_commit_kernel<<<(unsigned)((work + 255) / 256), 256, 0, cs>>>(x, s->hist, plan, T_max, c.n_fft, c.hop,
