@@ -778,9 +778,11 @@ struct Launcher {
     long long rows(int lvl) const { return frames * s->c->level_r[lvl]; }
     long long rows_pref(int lvl, Layout l) const { return frames * s->c->level_r[lvl] + (long long)Bc * l.P; }
 
+    // from_producer: the operand planes are already in plane block 0, written
+    // by the kernel that produced `in`; otherwise the prep kernel makes them.
     void gemm(const Contraction& C, const float* in, Layout il, int in_lvl, float* out, Layout ol,
               int out_C, int out_step, const float* res, int epi, float scale, int layer_ring,
-              const char* what)
+              const char* what, bool from_producer = false)
     {
         if (err != cudaSuccess) return;
         const int S1 = s->n_slots + 1;
@@ -812,9 +814,11 @@ struct Launcher {
             a.dense = (il.P == 0 && ol.P == 0 && C.ntaps == 1 && out_step == 1) ? 1 : 0;
             const int n_row_tiles = a.dense ? (int)((rows(in_lvl) + 127) / 128) : ntiles128[in_lvl];
             const long long arows = il.P ? rows_pref(in_lvl, il) : rows(in_lvl);
-            run(CODEC_KERNEL_OPERAND_PREP, 0.0, 8.0 * (double)arows * C.Cin, what, [&] {
-                return launch_tc_prep(in, C.alpha, C.inv_alpha, arows, C.Cin, &s->tc_scratch, C.tc.passes == 3, cs);
-            });
+            if (!from_producer)
+                run(CODEC_KERNEL_OPERAND_PREP, 0.0, 8.0 * (double)arows * C.Cin, what, [&] {
+                    return launch_tc_prep(in, C.alpha, C.inv_alpha, arows, C.Cin, &s->tc_scratch, C.tc.passes == 3,
+                                          cs);
+                });
             int extra = 0;
             run(CODEC_KERNEL_GEMM_TC, flops, bytes, what, [&] {
                 return launch_tc_gemm(a, C.tc, pv, n_row_tiles, &s->tc_scratch, arows, s->c->num_sms, cs, &extra);
@@ -937,18 +941,28 @@ void enqueue_decode(codec_state_t* s, Launcher& L, const int32_t* codes, int32_t
     }
     for (int l = 0; l < g.layers; l++) {
         const LayerW& W = c->layers[l];
-        L.run(CODEC_KERNEL_RMSNORM, norm_flops, norm_bytes, "rmsnorm 1",
-              [&] { return launch_rms_norm(s->h, L0d, W.n1, g.rms_eps, s->u, L0d, g.d, L.pv, rows0, cs); });
-        L.gemm(W.qkv, s->u, L0d, 0, s->q, L0d, g.d, 1, nullptr, EPI_QKV, 1.f, l, "qkv");
+        // the norms and the attention feed tensor-core GEMMs only: they write the
+        // GEMM's operand planes themselves (the prep kernel would split the same
+        // values the same way)
+        void* pl = s->tc_scratch.a_hi;
+        const int pil = W.qkv.tc.passes == 3 ? 1 : 0;
+        L.run(CODEC_KERNEL_RMSNORM, norm_flops, norm_bytes, "rmsnorm 1", [&] {
+            return launch_rms_norm(s->h, L0d, W.n1, g.rms_eps, s->u, L0d, g.d, L.pv, rows0, cs,
+                                   W.qkv.use_tc ? pl : nullptr, pil);
+        });
+        L.gemm(W.qkv, s->u, L0d, 0, s->q, L0d, g.d, 1, nullptr, EPI_QKV, 1.f, l, "qkv", W.qkv.use_tc);
         const size_t per_layer = (size_t)S * s->R * g.d;
         L.run(CODEC_KERNEL_ATTENTION, attn_flops, attn_bytes, "attention", [&] {
             return launch_swa(s->q, s->o, s->kring + per_layer * l, s->vring + per_layer * l, g.d, g.heads,
-                              g.window, s->R, L.pv, L.q16, L.nq16, cs);
+                              g.window, s->R, L.pv, L.q16, L.nq16, cs, W.o.use_tc ? pl : nullptr,
+                              W.o.tc.passes == 3 ? 1 : 0);
         });
-        L.gemm(W.o, s->o, L0d, 0, s->h, L0d, g.d, 1, s->h, EPI_RESID, 1.f, 0, "out-proj");
-        L.run(CODEC_KERNEL_RMSNORM, norm_flops, norm_bytes, "rmsnorm 2",
-              [&] { return launch_rms_norm(s->h, L0d, W.n2, g.rms_eps, s->u, L0d, g.d, L.pv, rows0, cs); });
-        L.gemm(W.w1, s->u, L0d, 0, s->f, L0d, g.ffn, 1, nullptr, EPI_GELU, 1.f, 0, "mlp 1");
+        L.gemm(W.o, s->o, L0d, 0, s->h, L0d, g.d, 1, s->h, EPI_RESID, 1.f, 0, "out-proj", W.o.use_tc);
+        L.run(CODEC_KERNEL_RMSNORM, norm_flops, norm_bytes, "rmsnorm 2", [&] {
+            return launch_rms_norm(s->h, L0d, W.n2, g.rms_eps, s->u, L0d, g.d, L.pv, rows0, cs,
+                                   W.w1.use_tc ? pl : nullptr, W.w1.tc.passes == 3 ? 1 : 0);
+        });
+        L.gemm(W.w1, s->u, L0d, 0, s->f, L0d, g.ffn, 1, nullptr, EPI_GELU, 1.f, 0, "mlp 1", W.w1.use_tc);
         L.gemm(W.w2, s->f, L0d, 0, s->h, L0d, g.d, 1, s->h, EPI_RESID, 1.f, 0, "mlp 2");
     }
     L.run(CODEC_KERNEL_RMSNORM, norm_flops, norm_bytes, "final rmsnorm",

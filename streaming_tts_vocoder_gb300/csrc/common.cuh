@@ -2,6 +2,7 @@
 // layout and the small device helpers every kernel uses.
 #pragma once
 
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -121,6 +122,46 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
     cfg.attrs = at;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// A tensor-core GEMM operand written by its producer instead of the prep
+// kernel: value v of column n of `row` split into fp16 hi = fp16(v) and lo =
+// fp16(v - hi), bit for bit as the prep kernel splits it, in the interleaved
+// [rows][C / 32][32 hi | 32 lo] layout (il) or as the hi plane [rows][C].
+__device__ __forceinline__ void plane_store1(void* planes, int il, long long row, int C, int n, float v)
+{
+    __half* p = static_cast<__half*>(planes);
+    const __half h = __float2half_rn(v);
+    if (il) {
+        const long long at = row * 2 * C + (n >> 5) * 64 + (n & 31);
+        p[at] = h;
+        p[at + 32] = __float2half_rn(v - __half2float(h));
+    } else {
+        p[row * C + n] = h;
+    }
+}
+
+// The same for four columns n .. n + 3 (n % 4 == 0): one 8-byte store per plane.
+__device__ __forceinline__ void plane_store4(void* planes, int il, long long row, int C, int n, float4 v)
+{
+    const float e[4] = {v.x, v.y, v.z, v.w};
+    uint32_t hw[2], lw[2];
+#pragma unroll
+    for (int i = 0; i < 2; i++) {
+        const __half h0 = __float2half_rn(e[2 * i]), h1 = __float2half_rn(e[2 * i + 1]);
+        const __half l0 = __float2half_rn(e[2 * i] - __half2float(h0));
+        const __half l1 = __float2half_rn(e[2 * i + 1] - __half2float(h1));
+        hw[i] = (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
+        lw[i] = (uint32_t)__half_as_ushort(l0) | ((uint32_t)__half_as_ushort(l1) << 16);
+    }
+    __half* p = static_cast<__half*>(planes);
+    if (il) {
+        const long long at = row * 2 * C + (n >> 5) * 64 + (n & 31);
+        *reinterpret_cast<uint2*>(p + at) = make_uint2(hw[0], hw[1]);
+        *reinterpret_cast<uint2*>(p + at + 32) = make_uint2(lw[0], lw[1]);
+    } else {
+        *reinterpret_cast<uint2*>(p + row * C + n) = make_uint2(hw[0], hw[1]);
+    }
 }
 
 // Snake, x + sin(a x)^2 / a, with explicit roundings so every kernel that

@@ -20,13 +20,17 @@ cudaError_t launch_rvq_gather(const float* cb, int Q, int V, int E, const int* c
 
 cudaError_t launch_gemm_simt(const GemmArgs& a, PlanView plan, int n_row_tiles, cudaStream_t s);
 
+// planes (optional): write the rows as a tensor-core GEMM's operand planes
+// (interleaved hi/lo when planes_il, else the hi plane) instead of y.
 cudaError_t launch_rms_norm(const float* x, Layout xl, const float* g, float eps, float* y, Layout yl,
-                            int d, PlanView plan, int total_rows, cudaStream_t s);
+                            int d, PlanView plan, int total_rows, cudaStream_t s, void* planes = nullptr,
+                            int planes_il = 1);
 
-// qcum: [B + 1] cumulative blocks of 16 queries per batch entry.
+// qcum: [B + 1] cumulative blocks of 16 queries per batch entry.  planes
+// (optional): the output as operand planes instead of o, as for RMSNorm.
 cudaError_t launch_swa(const float* q, float* o, const float* kring, const float* vring, int d,
                        int heads, int window, int ring_R, PlanView plan, const int* qcum, int n_qblocks,
-                       cudaStream_t s);
+                       cudaStream_t s, void* planes = nullptr, int planes_il = 1);
 
 cudaError_t launch_final_conv(const float* x, Layout xl, int C, const float* w, const float* bias,
                               const float* alpha, const float* inv_alpha, int k, float* audio,

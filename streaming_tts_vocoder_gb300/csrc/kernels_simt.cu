@@ -152,9 +152,11 @@ cudaError_t launch_gemm_simt(const GemmArgs& a, PlanView plan, int n_row_tiles, 
 // --------------------------------------------------------------- RMSNorm --
 // y = x / sqrt(mean(x^2) + eps) * g, one warp per row; the row's sum of
 // squares runs lane-strided then through a fixed butterfly.
+// planes set: the normalised row goes straight into a tensor-core GEMM's
+// operand planes (row of layout yl) instead of y.
 __global__ void rms_norm_kernel(const float* __restrict__ x, Layout xl, const float* __restrict__ g,
                                 float eps, float* __restrict__ y, Layout yl, int d, PlanView plan,
-                                int total_rows)
+                                int total_rows, void* planes, int planes_il)
 {
     pdl_wait();
     pdl_launch();
@@ -164,7 +166,8 @@ __global__ void rms_norm_kernel(const float* __restrict__ x, Layout xl, const fl
     const int b = find_seg(plan.cf, plan.B, row);
     const int t = row - __ldg(plan.cf + b);
     const float4* xr = reinterpret_cast<const float4*>(x + (seg_base(xl, plan.cf, b) + t) * d);
-    float4* yr = reinterpret_cast<float4*>(y + (seg_base(yl, plan.cf, b) + t) * d);
+    const long long yrow = seg_base(yl, plan.cf, b) + t;
+    float4* yr = reinterpret_cast<float4*>(y + yrow * d);
     const int d4 = d >> 2;
     float ss = 0.f;
     for (int c = lane; c < d4; c += 32) {
@@ -177,17 +180,20 @@ __global__ void rms_norm_kernel(const float* __restrict__ x, Layout xl, const fl
     const float4* g4 = reinterpret_cast<const float4*>(g);
     for (int c = lane; c < d4; c += 32) {
         const float4 v = xr[c], w = __ldg(g4 + c);
-        yr[c] = make_float4(v.x * r * w.x, v.y * r * w.y, v.z * r * w.z, v.w * r * w.w);
+        const float4 o = make_float4(v.x * r * w.x, v.y * r * w.y, v.z * r * w.z, v.w * r * w.w);
+        if (planes) plane_store4(planes, planes_il, yrow, d, 4 * c, o);
+        else yr[c] = o;
     }
 }
 
 cudaError_t launch_rms_norm(const float* x, Layout xl, const float* g, float eps, float* y, Layout yl,
-                            int d, PlanView plan, int total_rows, cudaStream_t s)
+                            int d, PlanView plan, int total_rows, cudaStream_t s, void* planes, int planes_il)
 {
+    if (planes && (d % 32 != 0)) return cudaErrorInvalidValue;
     if (total_rows <= 0) return cudaSuccess;
     const int threads = 256, rows_per_block = threads / 32;
     launch_pdl(rms_norm_kernel, dim3((total_rows + rows_per_block - 1) / rows_per_block), dim3(threads), 0, s,
-               x, xl, g, eps, y, yl, d, plan, total_rows);
+               x, xl, g, eps, y, yl, d, plan, total_rows, planes, planes_il);
     return cudaGetLastError();
 }
 
@@ -208,10 +214,12 @@ constexpr int kSwaQ = 16;           // queries per block
 constexpr int kSwaWarps = 8;
 constexpr int kSwaMaxSmem = 160 * 1024;
 
+// planes set: the attention output goes straight into the out-projection's
+// tensor-core operand planes (dense rows) instead of o.
 __global__ void __launch_bounds__(kSwaWarps * 32) swa_kernel(
     const float* __restrict__ q, float* __restrict__ o, const float* __restrict__ kring,
     const float* __restrict__ vring, int d, int heads, int W, int R, PlanView plan,
-    const int* __restrict__ qcum)
+    const int* __restrict__ qcum, void* planes, int planes_il)
 {
     pdl_wait();
     pdl_launch();
@@ -284,7 +292,8 @@ __global__ void __launch_bounds__(kSwaWarps * 32) swa_kernel(
         for (int c = lane; c < dh; c += 32) {
             float acc = 0.f;
             for (int i = 0; i < nkq; i++) acc = fmaf(sp[wib * W + i], sv[(off + i) * ld + c], acc);
-            o[(row0 + qi) * d + h * dh + c] = acc * inv_z;
+            if (planes) plane_store1(planes, planes_il, row0 + qi, d, h * dh + c, acc * inv_z);
+            else o[(row0 + qi) * d + h * dh + c] = acc * inv_z;
         }
         __syncwarp();
     }
@@ -292,16 +301,17 @@ __global__ void __launch_bounds__(kSwaWarps * 32) swa_kernel(
 
 cudaError_t launch_swa(const float* q, float* o, const float* kring, const float* vring, int d,
                        int heads, int window, int ring_R, PlanView plan, const int* qcum, int n_qblocks,
-                       cudaStream_t s)
+                       cudaStream_t s, void* planes, int planes_il)
 {
     if (n_qblocks <= 0) return cudaSuccess;
+    if (planes && (d % 32 != 0)) return cudaErrorInvalidValue;
     const int dh = d / heads;
     if (dh > kSwaMaxDh || window > kSwaMaxW) return cudaErrorInvalidValue;
     const int maxk = kSwaQ + window - 1;
     const size_t smem = sizeof(float) * (2 * (size_t)maxk * (dh + 1) + (size_t)kSwaWarps * dh + (size_t)kSwaWarps * window);
     if (smem > (size_t)kSwaMaxSmem) return cudaErrorInvalidValue;
     launch_pdl(swa_kernel, dim3(n_qblocks, heads), dim3(kSwaWarps * 32), smem, s, q, o, kring, vring, d, heads,
-               window, ring_R, plan, qcum);
+               window, ring_R, plan, qcum, planes, planes_il);
     return cudaGetLastError();
 }
 
