@@ -5,10 +5,9 @@
 // decoder and the iSTFT head do.
 //
 // Sine source, two launches per call:
-//   sine_scan_kernel  one thread per batch entry walks its frames: each
-//                     frame's phase at its start and its increment, and the
-//                     slot's phase after the chunk (read and written by that
-//                     one thread)
+//   sine_scan_kernel  one warp per batch entry: each frame's phase at its
+//                     start and its increment (a warp prefix sum over the
+//                     frames), and the slot's phase after the chunk
 //   sine_out_kernel   one thread per output sample: phase = start + (r + 1)
 //                     increment (unsigned 32-bit wrap = modulo one cycle), the
 //                     harmonics' sines
@@ -45,24 +44,43 @@ struct SrcPlan {
     const int* cur;     // [B] current history buffer (analysis STFT)
 };
 
+// One warp per batch entry: the frames' increments D, 32 frames at a time,
+// and an inclusive warp prefix sum of upp D (unsigned, so modulo one cycle,
+// and exact: the order of the additions cannot change a bit) give each
+// frame's phase at its start; lane 0 stores the slot's phase after the chunk
+// (every lane read the old one first).
 __global__ void sine_scan_kernel(const float* __restrict__ f0, SrcPlan plan, int T_max, double scale,
                                  double f0_max, int upp, unsigned* __restrict__ phase,
                                  unsigned* __restrict__ pstart, unsigned* __restrict__ dinc)
 {
-    const int b = blockIdx.x * blockDim.x + threadIdx.x;
-    if (b >= plan.B) return;
+    const int b = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (b >= plan.B) return;                    // whole warps
     const int c0 = __ldg(plan.cf + b), n = __ldg(plan.cf + b + 1) - c0;
     const float* row = f0 + (size_t)__ldg(plan.bidx + b) * T_max;
     const int sl = __ldg(plan.slot + b);
     unsigned P = phase[sl];
-    for (int i = 0; i < n; i++) {
-        const double f = fmin(fmax((double)__ldg(row + i), 0.0), f0_max);
-        const unsigned D = (unsigned)__double2ull_rn(__dmul_rn(f, scale));
-        pstart[c0 + i] = P;
-        dinc[c0 + i] = D;
-        P += (unsigned)upp * D;
+    for (int base = 0; base < n; base += 32) {
+        const int i = base + lane;
+        unsigned D = 0u;
+        if (i < n) {
+            const double f = fmin(fmax((double)__ldg(row + i), 0.0), f0_max);
+            D = (unsigned)__double2ull_rn(__dmul_rn(f, scale));
+        }
+        const unsigned own = (unsigned)upp * D;
+        unsigned incl = own;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        if (i < n) {
+            pstart[c0 + i] = P + (incl - own);
+            dinc[c0 + i] = D;
+        }
+        P += __shfl_sync(0xffffffffu, incl, 31);
     }
-    phase[sl] = P;
+    if (lane == 0) phase[sl] = P;
 }
 
 __global__ void sine_out_kernel(const float* __restrict__ f0, SrcPlan plan, int T_max, int upp, int H,
@@ -403,8 +421,8 @@ codec_status codec_sine_decode(codec_sine_t* s, const float* f0, const int32_t* 
                                           &total, &slots);
     if (st != CODEC_OK || Bc == 0) return st;
     const double fs = (double)c.sample_rate;
-    sine_scan_kernel<<<(Bc + 127) / 128, 128, 0, cs>>>(f0, plan, T_max, 4294967296.0 / fs, fs / 2, c.upp, s->phase,
-                                                     s->pstart, s->dinc);
+    sine_scan_kernel<<<(Bc + 3) / 4, 128, 0, cs>>>(f0, plan, T_max, 4294967296.0 / fs, fs / 2, c.upp, s->phase,
+                                                   s->pstart, s->dinc);
     const long long samples = (long long)total * c.upp;
     sine_out_kernel<<<(unsigned)((samples + 255) / 256), 256, 0, cs>>>(f0, plan, T_max, c.upp, c.harmonics,
                                                                      c.amplitude, c.voiced_threshold, s->pstart,
