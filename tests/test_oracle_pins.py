@@ -434,3 +434,21 @@ def test_pins_catch_window_off_by_one():
     q, k, v = rnd(T, d), rnd(T, d), rnd(T, d)
     wrong = O.swa(q, k, v, 2, window=5)
     assert relerr(wrong, swa_brute(q, k, v, 2, 4)) > 1e-3
+
+
+def test_oracle_independent_of_thread_count():
+    """Every GPU parity claim compares against the oracle: its output must not
+    depend on how many OpenMP threads compute it (each output's sum runs in
+    one thread, in a fixed order)."""
+    cfg = tiny_config()
+    blob = pack_blob(cfg, make_weights(cfg, 0))
+    codes = make_codes(cfg, 8, 3)
+    n0 = O.max_threads()
+    try:
+        O.set_threads(1)
+        one = O.OracleModel(cfg, blob).decode_full(codes)
+        O.set_threads(max(2, n0))
+        many = O.OracleModel(cfg, blob).decode_full(codes)
+    finally:
+        O.set_threads(n0)
+    assert np.array_equal(one, many)
