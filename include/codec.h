@@ -336,7 +336,7 @@ CODEC_API codec_status codec_profile_launches(codec_state_t* state, codec_launch
  * stream carries its last n_fft / hop - 1 windowed frames.
  *
  * Limits: n_fft even, 4 <= n_fft <= 4096, hop >= 1 dividing n_fft.  Power-of-
- * two n_fft uses a radix-2 FFT in shared memory, other sizes a direct DFT.
+ * two n_fft uses a radix-4 (and radix-2) Stockham FFT in shared memory, other sizes a direct DFT.
  */
 typedef struct codec_istft_config {
     int32_t n_fft;

@@ -7,7 +7,7 @@
 // Two kernels per call, over the call's packed frames (stream segments back
 // to back, as the decoder packs them):
 //   istft_frame_kernel   one block per frame: spectrum in shared memory,
-//                        Hermitian completion, inverse FFT (radix-2 Stockham
+//                        Hermitian completion, inverse FFT (radix-4 Stockham
 //                        for power-of-two n_fft, a direct DFT otherwise),
 //                        window; the windowed frame goes to a scratch row
 //   istft_ola_kernel     y = 0: one thread per output sample, the n_fft / hop

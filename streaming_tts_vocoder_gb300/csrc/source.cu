@@ -14,7 +14,7 @@
 // Analysis STFT, two launches per call:
 //   stft_frame_kernel   one block per frame: n_fft input samples (the carried
 //                       history for those before the chunk), Hann window,
-//                       forward FFT in shared memory (radix-2 Stockham, or a
+//                       forward FFT in shared memory (radix-4 Stockham, or a
 //                       direct DFT for other sizes), n_fft / 2 + 1 bins out
 //   stft_commit_kernel  the new history, into the slot's other buffer
 #include <cuda_runtime.h>
