@@ -138,3 +138,19 @@ def test_planted_mistakes_fail_reconstruction():
     assert np.abs(y[lo:] - s[lo:T * hop]).max() > 0.1
     shifted = O.istft_full(spec, n_fft, hop)
     assert np.abs(shifted[lo + hop:] - s[lo:T * hop - hop]).max() > 0.1
+
+
+def test_page_istft_sizes():
+    """The Core AI note runs Kokoro's iSTFT as a transposed conv of stride 5
+    from 11 channels to 1: n_fft / 2 + 1 = 11 bins at hop 5 is n_fft 20, the
+    size the oracle and the GPU tests use; it reconstructs (above)."""
+    import json
+    from pathlib import Path
+    facts = json.loads((Path(__file__).parent / "golden" / "page_facts.json").read_text())
+    hop = facts["istft_transposed_conv_stride"]["value"]
+    bins = facts["istft_transposed_conv_in_channels"]["value"]
+    n_fft = 2 * (bins - 1)
+    assert (n_fft, hop) == (20, 5) and (20, 5) in CONFIGS
+    assert n_fft % hop == 0 and O.envelope(n_fft, hop).min() > 0
+    # 600 samples per Kokoro frame are 120 iSTFT hops
+    assert facts["kokoro_samples_per_frame"]["value"] % hop == 0
