@@ -197,6 +197,60 @@ CODEC_API codec_status codec_embed_chunk(codec_state_t* state, const int32_t* co
                                const int32_t* stream_ids, int32_t B, int32_t T_max, float* emb,
                                void* stream);
 
+/*
+ * Recompute-mode decode: the server schedule of the vllm-omni "Edge TTS
+ * design" page, section 1.4 (each chunk after the first is decoded "with
+ * 72-frame left ctx"), where a call re-decodes its left context from an empty
+ * state and keeps only the new frames' audio.  For each batch entry b with
+ * n_new[b] > 0, its slot is reset, frames 0 .. n_ctx[b] + n_new[b] - 1 of row b
+ * of codes are decoded from the empty state, and only the audio of the last
+ * n_new[b] frames is written, to samples 0 .. n_new[b] * spf - 1 of row b of
+ * audio (and of pre_tanh, device float of audio's layout, or NULL).  The
+ * context frames' audio is computed and dropped.  Afterwards the slot carries
+ * the state after all n_ctx[b] + n_new[b] frames, so a carried-mode
+ * codec_decode_chunk may follow.  Entries with n_new[b] == 0 are left alone.
+ * With the decoder's exact causality, the kept audio equals the last n_new[b]
+ * frames of a full decode of those n_ctx[b] + n_new[b] frames from reset.
+ *   codes   device int32 [B][Q][T_max]; n_ctx, n_new: host int32 [B], each
+ *           >= 0 with n_ctx[b] + n_new[b] <= min(T_max, max_chunk_frames);
+ *           the sum over entries with n_new[b] > 0 <= max_batch_frames.
+ * Errors as codec_decode_chunk (nothing enqueued, not even the reset). */
+CODEC_API codec_status codec_decode_recompute(codec_state_t* state, const int32_t* codes, const int32_t* n_ctx,
+                                              const int32_t* n_new, const int32_t* stream_ids, int32_t B,
+                                              int32_t T_max, float* audio, float* pre_tanh, void* stream);
+
+/*
+ * Chunk schedules of the streaming orchestrator (vllm-omni "Edge TTS design",
+ * section 2.2 "Orchestrator loop": the measured default of 1 frame then 25,
+ * the codec_chunk_ramp example 4, 4, 8, 16, 25, and codec_chunk_adaptive).
+ * codec_chunk_frames returns the frames of chunk `index` (0 = the first),
+ * given the frames already delivered before it, or 0 for an invalid schedule.
+ *   FIXED     chunk 0: first; later chunks: steady.
+ *   RAMP      chunk i < n_ramp: ramp[i]; later chunks: steady.
+ *   ADAPTIVE  chunk 0: min(first, steady); chunk i >= 1: the audio already
+ *             delivered, in frames, capped at steady (at least 1).  From a
+ *             producer that makes frames at least twice as fast as real time
+ *             (the page measures the server's real-time factor at 0.08-0.10),
+ *             a chunk that long arrives before the audio queued ahead of it
+ *             has played out, so playback started on the first chunk never
+ *             stalls for want of frames.  With first = 4 it gives 4, 4, 8, 16,
+ *             25, the page's example ramp; with first = 1, 1, 1, 2, 4, 8, 16,
+ *             25.  (The page names the adaptive mode without defining it; this
+ *             doubling rule is the reading taken.)
+ */
+#define CODEC_SCHEDULE_FIXED 0
+#define CODEC_SCHEDULE_RAMP 1
+#define CODEC_SCHEDULE_ADAPTIVE 2
+typedef struct codec_chunk_schedule {
+    int32_t kind;       /* CODEC_SCHEDULE_* */
+    int32_t first;      /* FIXED, ADAPTIVE: frames of chunk 0 (>= 1) */
+    int32_t steady;     /* frames of the steady chunks (>= 1; 25 on the server) */
+    int32_t n_ramp;     /* RAMP: entries of ramp (0..8) */
+    int32_t ramp[8];
+} codec_chunk_schedule;
+
+CODEC_API int32_t codec_chunk_frames(const codec_chunk_schedule* schedule, int32_t index, int64_t frames_delivered);
+
 /* Host-buffer form: codes_host int32 [B][Q][T_max] and audio_host float
  * [B][T_max * spf] are host memory (page-locked for asynchronous copies).  The
  * call copies the codes to a state-owned device buffer, decodes, copies the
@@ -235,20 +289,28 @@ CODEC_API codec_status codec_state_conv1d(codec_state_t* state, const float* x, 
  * point; it is a service of this library.
  *
  * Same computation, arguments, layouts and argument errors as
- * codec_state_conv1d, but no codec or state: the caller passes the inputs and
- * the output, and the scratch (operand planes, plan, weight scale) lives in
- * one 32 MiB device array of the library, which every GPU that loads the
- * library keeps until the process exits.  Limits: (H + T) * Cin <= 4,194,304
- * and Cout * Cin * k <= 4,194,304, else CODEC_ERR_CAPACITY with nothing
- * enqueued.  The first call on a device looks up the array's device address
- * on the current device (no allocation); make that first call before any
- * stream capture.  All calls on a device share the array and it keeps the
- * last call's contents (each call rewrites what it reads): calls that
- * overlap on the GPU, on different streams or threads, race on it.
+ * codec_state_conv1d (checked first), but no codec or state: the caller
+ * passes the inputs and the output, and the scratch (operand planes, plan,
+ * weight scale, timeout flag) lives in one 32 MiB device array of the library,
+ * which every GPU that loads the library keeps until the process exits.
+ * Limits: (H + T) * Cin <= 4,194,304 and Cout * Cin * k <= 4,194,304, else
+ * CODEC_ERR_CAPACITY; with either error nothing is enqueued.  The first call
+ * on a device looks up the array's device address on the current device (no
+ * allocation); make that first call before any stream capture.  All calls on
+ * a device share the array and it keeps the last call's contents (each call
+ * rewrites what it reads, and clears the timeout flag on its stream first):
+ * calls that overlap on the GPU, on different streams or threads, race on it.
  */
 CODEC_API codec_status codec_conv1d_noalloc(const float* x, int32_t T, int32_t Cin, const float* w,
                                             const float* bias, const float* alpha, int32_t Cout, int32_t k,
                                             int32_t dilation, float* y, void* stream);
+
+/* Whether the last codec_conv1d_noalloc call on the current device gave up on
+ * one of the tensor-core kernel's bounded waits (its output is then not
+ * valid): *timed_out = 1, else 0.  Synchronises stream first (host-blocking)
+ * and allocates nothing.  Errors: CODEC_ERR_NULL, CODEC_ERR_NO_DEVICE,
+ * CODEC_ERR_CUDA. */
+CODEC_API codec_status codec_conv1d_noalloc_status(int32_t* timed_out, void* stream);
 
 /* Frames decoded and sticky error bits of one slot.  Synchronises stream
  * (host-blocking).  Errors: CODEC_ERR_NULL, CODEC_ERR_ARG, CODEC_ERR_CUDA. */
@@ -263,6 +325,17 @@ CODEC_API codec_status codec_state_query(codec_state_t* state, int32_t stream_id
  * synchronises the device).  Calls made while codec_profile_begin is active
  * launch directly.  Errors: CODEC_ERR_NULL, CODEC_ERR_CUDA. */
 CODEC_API codec_status codec_state_set_graphs(codec_state_t* state, int32_t enable);
+
+/* Bounded waits of the tensor-core kernels for this state's calls (decode and
+ * conv1d): every wait gives up after `polls` polls (0: the default, 2^25), the
+ * kernel then stops cleanly, and codec_state_query reports
+ * CODEC_STREAM_ERR_KERNEL_TIMEOUT until a reset of all slots.  unarrived_wait
+ * != 0 exists to verify that path: each GEMM CTA's first epilogue wait then
+ * targets a barrier that no role ever arrives on, so it runs out after
+ * `polls` polls on any input (results of such calls are not valid).  Drops
+ * the captured graphs (synchronises the device).  Errors: CODEC_ERR_NULL,
+ * CODEC_ERR_CUDA. */
+CODEC_API codec_status codec_state_set_wait_limit(codec_state_t* state, uint32_t polls, int32_t unarrived_wait);
 
 /* Number of stream slots of a state. */
 CODEC_API int32_t codec_state_streams(const codec_state_t* state);
@@ -316,7 +389,6 @@ typedef struct codec_launch_record {
 CODEC_API codec_status codec_profile_launches(codec_state_t* state, codec_launch_record* out, int32_t max_out,
                                               int32_t* n_out);
 
-/* Static description of a status code. */
 /*
  * Streaming iSTFT head: the last step of the iSTFT-head vocoders the pages
  * list (F5-TTS's Vocos, "Vocos -> iSTFT"; CosyVoice2's and Chatterbox's HiFT,
@@ -447,6 +519,7 @@ CODEC_API codec_status codec_stft_decode(codec_stft_t* stft, const float* x, con
                                          const int32_t* stream_ids, int32_t B, int32_t T_max, float* spec,
                                          void* stream);
 
+/* Static description of a status code. */
 CODEC_API const char* codec_status_string(codec_status status);
 
 #ifdef __cplusplus

@@ -21,6 +21,7 @@ PRECISION_FP32 = 0
 PRECISION_FP16X3 = 1
 PRECISION_FP16 = 2       # single fp16 pass: approximate, outside the parity bound
 STREAM_ERR_BAD_CODE = 1
+STREAM_ERR_KERNEL_TIMEOUT = 0x80000000
 
 STATUS = {0: "CODEC_OK", 1: "CODEC_ERR_NULL", 2: "CODEC_ERR_CONFIG", 3: "CODEC_ERR_WEIGHTS",
           4: "CODEC_ERR_ARG", 5: "CODEC_ERR_CAPACITY", 6: "CODEC_ERR_OOM", 7: "CODEC_ERR_CUDA",
@@ -79,6 +80,40 @@ class StftConfigC(ctypes.Structure):
                 ("max_chunk_frames", ctypes.c_int32)]
 
 
+class ChunkScheduleC(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("first", ctypes.c_int32), ("steady", ctypes.c_int32),
+                ("n_ramp", ctypes.c_int32), ("ramp", ctypes.c_int32 * 8)]
+
+
+SCHEDULE_FIXED, SCHEDULE_RAMP, SCHEDULE_ADAPTIVE = 0, 1, 2
+
+
+def chunk_schedule(kind: int, first: int = 1, steady: int = 25, ramp=()) -> ChunkScheduleC:
+    c = ChunkScheduleC()
+    c.kind, c.first, c.steady, c.n_ramp = kind, first, steady, len(ramp)
+    for i, v in enumerate(ramp):
+        c.ramp[i] = v
+    return c
+
+
+def chunk_frames(schedule: ChunkScheduleC, index: int, frames_delivered: int) -> int:
+    """codec_chunk_frames: frames of chunk `index` under the schedule."""
+    return _lib().codec_chunk_frames(ctypes.byref(schedule), index, frames_delivered)
+
+
+def schedule_chunks(schedule: ChunkScheduleC, total_frames: int) -> list:
+    """The chunk sizes the schedule gives for a stream of total_frames."""
+    out, done = [], 0
+    while done < total_frames:
+        n = chunk_frames(schedule, len(out), done)
+        if n <= 0:
+            raise ValueError("invalid chunk schedule")
+        n = min(n, total_frames - done)
+        out.append(n)
+        done += n
+    return out
+
+
 class StreamInfoC(ctypes.Structure):
     _fields_ = [("frames_decoded", ctypes.c_int64), ("error_bits", ctypes.c_uint32),
                 ("reserved", ctypes.c_int32)]
@@ -108,6 +143,8 @@ def _lib():
             "codec_decode_chunk": (i32, [_P, _P, _I32P, _I32P, i32, i32, _P, _P]),
             "codec_decode_chunk_ex": (i32, [_P, _P, _I32P, _I32P, i32, i32, _P, _P, _P]),
             "codec_decode_chunk_host": (i32, [_P, _P, _I32P, _I32P, i32, i32, _P, _P]),
+            "codec_decode_recompute": (i32, [_P, _P, _I32P, _I32P, _I32P, i32, i32, _P, _P, _P]),
+            "codec_chunk_frames": (i32, [ctypes.POINTER(ChunkScheduleC), i32, i64]),
             "codec_embed_chunk": (i32, [_P, _P, _I32P, _I32P, i32, i32, _P, _P]),
             "codec_state_query": (i32, [_P, i32, ctypes.POINTER(StreamInfoC), _P]),
             "codec_state_streams": (i32, [_P]),
@@ -117,6 +154,8 @@ def _lib():
             "codec_state_set_graphs": (i32, [_P, i32]),
             "codec_state_conv1d": (i32, [_P, _P, i32, i32, _P, _P, _P, i32, i32, i32, _P, _P]),
             "codec_conv1d_noalloc": (i32, [_P, i32, i32, _P, _P, _P, i32, i32, i32, _P, _P]),
+            "codec_conv1d_noalloc_status": (i32, [ctypes.POINTER(i32), _P]),
+            "codec_state_set_wait_limit": (i32, [_P, ctypes.c_uint32, i32]),
             "codec_profile_end": (i32, [_P, ctypes.POINTER(KernelStatsC), _P]),
             "codec_profile_launches": (i32, [_P, ctypes.POINTER(LaunchRecordC), i32, ctypes.POINTER(i32)]),
             "codec_istft_create": (i32, [ctypes.POINTER(IstftConfigC), ctypes.POINTER(_P)]),
@@ -144,7 +183,7 @@ def header_functions() -> list:
     """Names of the functions include/codec.h declares."""
     text = HEADER.read_text()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(codec_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(codec_[a-z0-9_]+)\s*\(", text)))
 
 
 def config_c(cfg, max_streams=1, max_chunk_frames=97, max_batch_frames=None,
@@ -194,15 +233,41 @@ def _stream_handle(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
+def _conv1d_shapes(x, w, y, bias, alpha, dilation):
+    """Shape and layout checks shared by both conv entry points' wrappers."""
+    Cout, Cin, k = w.shape
+    T = y.shape[0]
+    for name, t in (("x", x), ("w", w), ("y", y), ("bias", bias), ("alpha", alpha)):
+        if t is not None and not (t.is_cuda and t.is_contiguous() and str(t.dtype) == "torch.float32"):
+            raise ValueError(f"{name} must be a contiguous float32 CUDA tensor")
+    if tuple(x.shape) != ((k - 1) * dilation + T, Cin):
+        raise ValueError(f"x must be [(k-1)*dilation + T][Cin] = [{(k - 1) * dilation + T}][{Cin}], got {tuple(x.shape)}")
+    if tuple(y.shape) != (T, Cout):
+        raise ValueError(f"y must be [T][Cout] = [{T}][{Cout}], got {tuple(y.shape)}")
+    if bias is not None and bias.numel() != Cout:
+        raise ValueError("bias must hold Cout values")
+    if alpha is not None and alpha.numel() != Cin:
+        raise ValueError("alpha must hold Cin values")
+    return T, Cin, Cout, k
+
+
 def conv1d_noalloc(x, w, y, bias=None, alpha=None, dilation=1, stream=None):
     """codec_conv1d_noalloc: the tensor-core causal conv with no device
     allocation (the library's fixed scratch array); same arguments as
     CodecState.conv1d."""
-    Cout, Cin, k = w.shape
-    T = y.shape[0]
+    T, Cin, Cout, k = _conv1d_shapes(x, w, y, bias, alpha, dilation)
     opt = lambda t: None if t is None else _ptr(t)
     _check(_lib().codec_conv1d_noalloc(_ptr(x), T, Cin, _ptr(w), opt(bias), opt(alpha), Cout, k, dilation,
                                        _ptr(y), _stream_handle(stream)), "codec_conv1d_noalloc")
+
+
+def conv1d_noalloc_timed_out(stream=None) -> bool:
+    """codec_conv1d_noalloc_status: whether the last allocation-free conv on the
+    current device gave up on a bounded wait (synchronises the stream)."""
+    flag = ctypes.c_int32()
+    _check(_lib().codec_conv1d_noalloc_status(ctypes.byref(flag), _stream_handle(stream)),
+           "codec_conv1d_noalloc_status")
+    return bool(flag.value)
 
 
 class Istft:
@@ -394,6 +459,25 @@ class CodecState:
                                              _ptr(audio), _ptr(pre_tanh), st)
         _check(s, "codec_decode_chunk")
 
+    def decode_recompute(self, codes, n_ctx, n_new, audio, stream_ids=None, pre_tanh=None, stream=None):
+        """codec_decode_recompute: per entry, reset its slot, decode n_ctx + n_new
+        frames of its codes row and write only the n_new frames' audio."""
+        B, Q, T_max = codes.shape
+        nc = np.ascontiguousarray(n_ctx, dtype=np.int32)
+        nn = np.ascontiguousarray(n_new, dtype=np.int32)
+        ids = None if stream_ids is None else np.ascontiguousarray(stream_ids, dtype=np.int32)
+        if nc.size != B or nn.size != B or (ids is not None and ids.size != B):
+            raise ValueError("n_ctx / n_new / stream_ids must have one entry per batch row")
+        if not (codes.is_cuda and str(codes.dtype) == "torch.int32" and codes.is_contiguous()):
+            raise ValueError("codes must be a contiguous int32 CUDA tensor")
+        if not (audio.is_cuda and audio.is_contiguous() and audio.numel() >= B * T_max * self.codec.samples_per_frame):
+            raise ValueError("audio must be a contiguous float32 CUDA tensor of B * T_max * spf values")
+        ids_p = None if ids is None else ids.ctypes.data_as(_I32P)
+        pt = None if pre_tanh is None else _ptr(pre_tanh)
+        _check(_lib().codec_decode_recompute(self._h, _ptr(codes), nc.ctypes.data_as(_I32P), nn.ctypes.data_as(_I32P),
+                                             ids_p, B, T_max, _ptr(audio), pt, _stream_handle(stream)),
+               "codec_decode_recompute")
+
     def embed(self, codes, n_frames, emb, stream_ids=None, stream=None):
         """Codebook sum only: emb device float32 [sum(n_frames)][E]."""
         B, Q, T_max = codes.shape
@@ -416,8 +500,7 @@ class CodecState:
     def conv1d(self, x, w, y, bias=None, alpha=None, dilation=1, stream=None):
         """codec_state_conv1d: x [(k-1) dil + T][Cin], w [Cout][Cin][k], y [T][Cout]
         (contiguous float32 CUDA tensors); bias [Cout], alpha [Cin] optional."""
-        Cout, Cin, k = w.shape
-        T = y.shape[0]
+        T, Cin, Cout, k = _conv1d_shapes(x, w, y, bias, alpha, dilation)
         opt = lambda t: None if t is None else _ptr(t)
         _check(_lib().codec_state_conv1d(self._h, _ptr(x), T, Cin, _ptr(w), opt(bias), opt(alpha), Cout, k,
                                          dilation, _ptr(y), _stream_handle(stream)), "codec_state_conv1d")
@@ -427,6 +510,13 @@ class CodecState:
         _check(_lib().codec_state_query(self._h, stream_id, ctypes.byref(info), _stream_handle(stream)),
                "codec_state_query")
         return int(info.frames_decoded), int(info.error_bits)
+
+    def set_wait_limit(self, polls: int = 0, unarrived_wait: bool = False):
+        """codec_state_set_wait_limit: polls per bounded wait of the tensor-core
+        kernels (0: default); unarrived_wait makes each GEMM CTA's first
+        epilogue wait run out, to verify the timeout path."""
+        _check(_lib().codec_state_set_wait_limit(self._h, polls, 1 if unarrived_wait else 0),
+               "codec_state_set_wait_limit")
 
     def set_graphs(self, enable: bool):
         _check(_lib().codec_state_set_graphs(self._h, 1 if enable else 0), "codec_state_set_graphs")

@@ -110,7 +110,7 @@ struct codec_state_s {
     TcScratch tc_scratch;
     // plan: device copy and a ring of page-locked host staging copies
     int plan_ints = 0;
-    int off_pos0 = 0, off_cf = 0, off_slot = 0, off_bidx = 0, off_tc64 = 0, off_tc128 = 0, off_q16 = 0;
+    int off_pos0 = 0, off_cf = 0, off_slot = 0, off_bidx = 0, off_tc64 = 0, off_tc128 = 0, off_q16 = 0, off_skip = 0;
     int* plan_d = nullptr;
     static constexpr int kPlanRing = 8;
     int* plan_h[kPlanRing] = {};
@@ -520,7 +520,8 @@ codec_status codec_state_create(codec_t* c, int32_t n_streams, codec_state_t** o
     s->off_tc64 = s->off_bidx + S;
     s->off_tc128 = s->off_tc64 + c->n_levels * (S + 1);
     s->off_q16 = s->off_tc128 + c->n_levels * (S + 1);
-    s->plan_ints = s->off_q16 + (S + 1);
+    s->off_skip = s->off_q16 + (S + 1);
+    s->plan_ints = s->off_skip + S;
     s->plan_d = dev_alloc<int>(A, s->plan_ints, st, true);
     for (int i = 0; i < codec_state_s::kPlanRing && st == CODEC_OK; i++) {
         if (cudaMallocHost(&s->plan_h[i], sizeof(int) * s->plan_ints) != cudaSuccess) st = CODEC_ERR_OOM;
@@ -605,6 +606,22 @@ codec_status codec_state_set_graphs(codec_state_t* s, int32_t enable)
         s->graphs.clear();
         s->seen.clear();
     }
+    return CODEC_OK;
+}
+
+codec_status codec_state_set_wait_limit(codec_state_t* s, uint32_t polls, int32_t unarrived_wait)
+{
+    if (!s) return CODEC_ERR_NULL;
+    TcWaitLimit wl;
+    wl.polls = polls ? polls : kDefaultWaitPolls;
+    wl.unarrived_wait = unarrived_wait ? 1 : 0;
+    // captured graphs hold the old limits in their kernel arguments
+    if (cudaDeviceSynchronize() != cudaSuccess) return CODEC_ERR_CUDA;
+    for (GraphEntry& e : s->graphs) cudaGraphExecDestroy(e.exec);
+    s->graphs.clear();
+    s->seen.clear();
+    s->tc_scratch.wait = wl;
+    s->tc_scratch.op.wait = wl;
     return CODEC_OK;
 }
 
@@ -835,7 +852,7 @@ struct Launcher {
 // Validate a call's batch, build its plan (cumulative frames, slots, tile
 // counts per level) in a page-locked staging buffer and enqueue the upload.
 codec_status plan_call(codec_state_t* s, const int32_t* n_frames, const int32_t* ids, int32_t B,
-                       int32_t T_max, cudaStream_t cs, Launcher& L, int& rows0)
+                       int32_t T_max, cudaStream_t cs, Launcher& L, int& rows0, const int32_t* skip_h = nullptr)
 {
     codec_s* c = s->c;
     const codec_config& g = c->cfg;
@@ -864,6 +881,7 @@ codec_status plan_call(codec_state_t* s, const int32_t* n_frames, const int32_t*
     int* cf = P + s->off_cf;
     int* slot = P + s->off_slot;
     int* bidx = P + s->off_bidx;
+    int* skip = P + s->off_skip;
     int Bc = 0;
     cf[0] = 0;
     for (int b = 0; b < B; b++) {
@@ -871,6 +889,7 @@ codec_status plan_call(codec_state_t* s, const int32_t* n_frames, const int32_t*
         const int id = ids ? ids[b] : b;
         slot[Bc] = id;
         bidx[Bc] = b;
+        skip[Bc] = skip_h ? skip_h[b] : 0;
         pos0[Bc] = s->frames_h[id];
         cf[Bc + 1] = cf[Bc] + n_frames[b];
         Bc++;
@@ -903,7 +922,8 @@ codec_status plan_call(codec_state_t* s, const int32_t* n_frames, const int32_t*
     if (cudaEventRecord(s->plan_ev[i], cs) != cudaSuccess) return CODEC_ERR_CUDA;
     const int* D = s->plan_d;
     L.pv = PlanView{Bc, D + s->off_cf, D + s->off_slot,
-                    reinterpret_cast<const long long*>(D + s->off_pos0), D + s->off_bidx};
+                    reinterpret_cast<const long long*>(D + s->off_pos0), D + s->off_bidx,
+                    skip_h ? D + s->off_skip : nullptr};
     L.tc64 = D + s->off_tc64;
     L.tc128 = D + s->off_tc128;
     L.q16 = D + s->off_q16;
@@ -1001,7 +1021,7 @@ void enqueue_decode(codec_state_t* s, Launcher& L, const int32_t* codes, int32_t
         L.run(CODEC_KERNEL_FINAL_CONV, 2.0 * R * Cl * g.final_k, 4.0 * R * (Cl + (pre_tanh ? 2 : 1)), "final conv",
               [&] {
                   return launch_final_conv(x, lay(xl), Cl, c->out_w, c->out_b, c->out_alpha, c->out_inv_alpha,
-                                           g.final_k, audio, pre_tanh, (long long)T_max * c->spf, L.pv,
+                                           g.final_k, audio, pre_tanh, (long long)T_max * c->spf, c->spf, L.pv,
                                            L.tc128 + (size_t)xl * (S + 1), L.ntiles128[xl], cs);
               });
     }
@@ -1011,13 +1031,13 @@ void enqueue_decode(codec_state_t* s, Launcher& L, const int32_t* codes, int32_t
 
 codec_status decode_impl(codec_state_t* s, const int32_t* codes, const int32_t* n_frames,
                          const int32_t* ids, int32_t B, int32_t T_max, float* audio, float* pre_tanh,
-                         cudaStream_t cs)
+                         cudaStream_t cs, const int32_t* skip = nullptr)
 {
     if (!s || !codes || !n_frames || !audio) return CODEC_ERR_NULL;
     s->last_launches = 0;
     Launcher L;
     int rows0 = 0;
-    codec_status pst = plan_call(s, n_frames, ids, B, T_max, cs, L, rows0);
+    codec_status pst = plan_call(s, n_frames, ids, B, T_max, cs, L, rows0, skip);
     if (pst != CODEC_OK || rows0 == 0) return pst;
 
     // Replay a captured graph of this call's launch sequence when one exists
@@ -1034,6 +1054,7 @@ codec_status decode_impl(codec_state_t* s, const int32_t* codes, const int32_t* 
         key.push_back((long long)(uintptr_t)codes);
         key.push_back((long long)(uintptr_t)audio);
         key.push_back((long long)(uintptr_t)pre_tanh);
+        key.push_back(skip ? 1 : 0);
         for (int n : L.n_h) key.push_back(n);
         GraphEntry* ge = nullptr;
         for (GraphEntry& e : s->graphs)
@@ -1133,6 +1154,58 @@ codec_status codec_embed_chunk(codec_state_t* s, const int32_t* codes, const int
                                const int32_t* ids, int32_t B, int32_t T_max, float* emb, void* stream)
 {
     return embed_impl(s, codes, n_frames, ids, B, T_max, emb, (cudaStream_t)stream);
+}
+
+codec_status codec_decode_recompute(codec_state_t* s, const int32_t* codes, const int32_t* n_ctx,
+                                    const int32_t* n_new, const int32_t* ids, int32_t B, int32_t T_max,
+                                    float* audio, float* pre_tanh, void* stream)
+{
+    if (!s || !codes || !n_ctx || !n_new || !audio) return CODEC_ERR_NULL;
+    const codec_config& g = s->c->cfg;
+    if (B < 1 || T_max < 1) return CODEC_ERR_ARG;
+    if (B > s->n_slots) return CODEC_ERR_CAPACITY;
+    std::vector<int32_t> n_frames(B), reset_ids;
+    long long total = 0;
+    for (int b = 0; b < B; b++) {
+        if (n_ctx[b] < 0 || n_new[b] < 0 || (long long)n_ctx[b] + n_new[b] > T_max) return CODEC_ERR_ARG;
+        if (n_ctx[b] + n_new[b] > g.max_chunk_frames) return CODEC_ERR_CAPACITY;
+        // an entry with no new frames is left alone: no reset, no decode
+        n_frames[b] = n_new[b] > 0 ? n_ctx[b] + n_new[b] : 0;
+        total += n_frames[b];
+    }
+    if (total > g.max_batch_frames) return CODEC_ERR_CAPACITY;
+    // the remaining argument errors (ids) are the decode's own; check them
+    // before the reset enqueues anything
+    {
+        std::vector<char> seen(s->n_slots, 0);
+        for (int b = 0; b < B; b++) {
+            const int id = ids ? ids[b] : b;
+            if (id < 0 || id >= s->n_slots || seen[id]) return CODEC_ERR_ARG;
+            seen[id] = 1;
+            if (n_frames[b] > 0) reset_ids.push_back(id);
+        }
+    }
+    if (reset_ids.empty()) return CODEC_OK;
+    const codec_status rst = codec_state_reset(s, reset_ids.data(), (int32_t)reset_ids.size(), stream);
+    if (rst != CODEC_OK) return rst;
+    return decode_impl(s, codes, n_frames.data(), ids, B, T_max, audio, pre_tanh, (cudaStream_t)stream, n_ctx);
+}
+
+int32_t codec_chunk_frames(const codec_chunk_schedule* sch, int32_t index, int64_t frames_delivered)
+{
+    if (!sch || index < 0 || frames_delivered < 0 || sch->first < 1 || sch->steady < 1) return 0;
+    switch (sch->kind) {
+    case CODEC_SCHEDULE_FIXED:
+        return index == 0 ? sch->first : sch->steady;
+    case CODEC_SCHEDULE_RAMP:
+        if (sch->n_ramp < 0 || sch->n_ramp > 8) return 0;
+        return index < sch->n_ramp ? std::max(1, sch->ramp[index]) : sch->steady;
+    case CODEC_SCHEDULE_ADAPTIVE:
+        if (index == 0) return std::min(sch->first, sch->steady);
+        return (int32_t)std::min<int64_t>(sch->steady, std::max<int64_t>(1, frames_delivered));
+    default:
+        return 0;
+    }
 }
 
 codec_status codec_decode_chunk_host(codec_state_t* s, const int32_t* codes_host, const int32_t* n_frames,

@@ -46,6 +46,8 @@ struct PlanView {
     const int* slot;        // [B] state slot of batch entry b
     const long long* pos0;  // [B] frames the stream had decoded before this call
     const int* bidx;        // [B] row of b in the caller's codes / audio arrays
+    const int* skip;        // [B] leading frames of b whose audio is not written (recompute
+                            // mode's left context), or null for none
 };
 
 // Implicit-GEMM launch descriptor: out rows t of segment b are

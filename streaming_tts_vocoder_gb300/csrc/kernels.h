@@ -34,7 +34,7 @@ cudaError_t launch_swa(const float* q, float* o, const float* kring, const float
 
 cudaError_t launch_final_conv(const float* x, Layout xl, int C, const float* w, const float* bias,
                               const float* alpha, const float* inv_alpha, int k, float* audio,
-                              float* pre_tanh, long long audio_ld, PlanView plan, const int* tcum,
+                              float* pre_tanh, long long audio_ld, int spf, PlanView plan, const int* tcum,
                               int n_row_tiles, cudaStream_t s);
 
 // Sets the kernels' shared-memory carve-outs; called once per codec.

@@ -336,7 +336,7 @@ __global__ void __launch_bounds__(kFinalTile) final_conv_kernel(
     const float* __restrict__ x, Layout xl, int C, const float* __restrict__ w,
     const float* __restrict__ bias, const float* __restrict__ alpha,
     const float* __restrict__ inv_alpha, int k, float* __restrict__ audio,
-    float* __restrict__ pre_tanh, long long audio_ld, PlanView plan, const int* __restrict__ bidx,
+    float* __restrict__ pre_tanh, long long audio_ld, int spf, PlanView plan, const int* __restrict__ bidx,
     const int* __restrict__ tcum)
 {
     pdl_wait();
@@ -388,10 +388,13 @@ __global__ void __launch_bounds__(kFinalTile) final_conv_kernel(
     }
     __syncthreads();
     const int m = threadIdx.x;
-    if (m < nrows) {
+    // the first skip[b] frames' samples (recompute mode's left context) are
+    // computed but not written; the rest land from the start of the row
+    const long long drop = plan.skip ? (long long)__ldg(plan.skip + b) * spf : 0;
+    if (m < nrows && t0 + m >= drop) {
         float acc = __ldg(bias);
         for (int j = 0; j < k; j++) acc += sp[(m + j) * k + j];
-        const long long idx = (long long)__ldg(bidx + b) * audio_ld + t0 + m;
+        const long long idx = (long long)__ldg(bidx + b) * audio_ld + t0 + m - drop;
         audio[idx] = tanhf(acc);
         if (pre_tanh) pre_tanh[idx] = acc;
     }
@@ -399,7 +402,7 @@ __global__ void __launch_bounds__(kFinalTile) final_conv_kernel(
 
 cudaError_t launch_final_conv(const float* x, Layout xl, int C, const float* w, const float* bias,
                               const float* alpha, const float* inv_alpha, int k, float* audio,
-                              float* pre_tanh, long long audio_ld, PlanView plan, const int* tcum,
+                              float* pre_tanh, long long audio_ld, int spf, PlanView plan, const int* tcum,
                               int n_row_tiles, cudaStream_t s)
 {
     if (n_row_tiles <= 0) return cudaSuccess;
@@ -409,10 +412,10 @@ cudaError_t launch_final_conv(const float* x, Layout xl, int C, const float* w, 
     if (smem > (size_t)kFinalMaxSmem) return cudaErrorInvalidValue;
     if (KP == 8)
         launch_pdl(final_conv_kernel<8>, dim3(n_row_tiles), dim3(kFinalTile), smem, s, x, xl, C, w, bias, alpha,
-                   inv_alpha, k, audio, pre_tanh, audio_ld, plan, plan.bidx, tcum);
+                   inv_alpha, k, audio, pre_tanh, audio_ld, spf, plan, plan.bidx, tcum);
     else
         launch_pdl(final_conv_kernel<16>, dim3(n_row_tiles), dim3(kFinalTile), smem, s, x, xl, C, w, bias, alpha,
-                   inv_alpha, k, audio, pre_tanh, audio_ld, plan, plan.bidx, tcum);
+                   inv_alpha, k, audio, pre_tanh, audio_ld, spf, plan, plan.bidx, tcum);
     return cudaGetLastError();
 }
 

@@ -44,35 +44,29 @@ constexpr int kMaxDevices = 64;
 DeviceScratch g_dev[kMaxDevices];
 std::mutex g_mu;
 
-}  // namespace
-
-extern "C" codec_status codec_conv1d_noalloc(const float* x, int32_t T, int32_t Cin, const float* w,
-                                             const float* bias, const float* alpha, int32_t Cout, int32_t k,
-                                             int32_t dilation, float* y, void* stream)
+// The array's device address on the current device (looked up, with the
+// GEMM's kernel attributes set, on the first call on that device).
+codec_status device_scratch(DeviceScratch* out)
 {
-    if (!x || !w || !y) return CODEC_ERR_NULL;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return CODEC_ERR_NO_DEVICE;
-    DeviceScratch ds;
-    {
-        std::lock_guard<std::mutex> lock(g_mu);
-        if (!g_dev[dev].base) {
-            void* p = nullptr;
-            if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return CODEC_ERR_CUDA;
-            int sms = 0;
-            if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return CODEC_ERR_CUDA;
-            // the GEMM's shared-memory size and register split, as codec_create sets them
-            if (tc_configure() != cudaSuccess) return CODEC_ERR_CUDA;
-            g_dev[dev].base = static_cast<unsigned char*>(p);
-            g_dev[dev].sms = sms;
-        }
-        ds = g_dev[dev];
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_dev[dev].base) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return CODEC_ERR_CUDA;
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return CODEC_ERR_CUDA;
+        // the GEMM's shared-memory size and register split, as codec_create sets them
+        if (tc_configure() != cudaSuccess) return CODEC_ERR_CUDA;
+        g_dev[dev].base = static_cast<unsigned char*>(p);
+        g_dev[dev].sms = sms;
     }
-    // refuse what does not fit before anything is enqueued
-    if (T < 1 || k < 1 || dilation < 1) return CODEC_ERR_ARG;
-    const long long rows = (long long)(k - 1) * dilation + T;
-    if (rows * (long long)Cin > (long long)kPlaneElems || (long long)Cout * Cin * k > (long long)kPlaneElems)
-        return CODEC_ERR_CAPACITY;
+    *out = g_dev[dev];
+    return CODEC_OK;
+}
+
+TcOpScratch op_scratch(const DeviceScratch& ds)
+{
     TcOpScratch sc;
     sc.words = reinterpret_cast<int*>(ds.base);
     sc.a_hi = ds.base + kWordsBytes;
@@ -82,11 +76,49 @@ extern "C" codec_status codec_conv1d_noalloc(const float* x, int32_t T, int32_t 
     sc.a_elems = kPlaneElems;
     sc.b_elems = kPlaneElems;
     sc.err = reinterpret_cast<int*>(ds.base + kFlagOffset);
-    const int r = run_tc_conv1d(sc, x, T, Cin, w, bias, alpha, Cout, k, dilation, y, ds.sms, (cudaStream_t)stream);
+    return sc;
+}
+
+}  // namespace
+
+extern "C" codec_status codec_conv1d_noalloc(const float* x, int32_t T, int32_t Cin, const float* w,
+                                             const float* bias, const float* alpha, int32_t Cout, int32_t k,
+                                             int32_t dilation, float* y, void* stream)
+{
+    if (!x || !w || !y) return CODEC_ERR_NULL;
+    DeviceScratch ds;
+    const codec_status dst = device_scratch(&ds);
+    if (dst != CODEC_OK) return dst;
+    const TcOpScratch sc = op_scratch(ds);
+    // argument errors first, then sizes beyond the array: nothing is enqueued
+    switch (check_tc_conv1d(sc, T, Cin, alpha != nullptr, Cout, k, dilation)) {
+    case OP_OK: break;
+    case OP_BAD_ARG: return CODEC_ERR_ARG;
+    default: return CODEC_ERR_CAPACITY;
+    }
+    cudaStream_t cs = (cudaStream_t)stream;
+    // the timeout flag describes this call only
+    if (cudaMemsetAsync(sc.err, 0, sizeof(int), cs) != cudaSuccess) return CODEC_ERR_CUDA;
+    const int r = run_tc_conv1d(sc, x, T, Cin, w, bias, alpha, Cout, k, dilation, y, ds.sms, cs);
     switch (r) {
     case OP_OK: return CODEC_OK;
     case OP_BAD_ARG: return CODEC_ERR_ARG;
     case OP_TOO_BIG: return CODEC_ERR_CAPACITY;
     default: return CODEC_ERR_CUDA;
     }
+}
+
+extern "C" codec_status codec_conv1d_noalloc_status(int32_t* timed_out, void* stream)
+{
+    if (!timed_out) return CODEC_ERR_NULL;
+    *timed_out = 0;
+    DeviceScratch ds;
+    const codec_status dst = device_scratch(&ds);
+    if (dst != CODEC_OK) return dst;
+    const TcOpScratch sc = op_scratch(ds);
+    int flag = 0;
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return CODEC_ERR_CUDA;
+    if (cudaMemcpy(&flag, sc.err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return CODEC_ERR_CUDA;
+    *timed_out = flag ? 1 : 0;
+    return CODEC_OK;
 }

@@ -61,14 +61,15 @@ namespace codec {
 namespace {
 
 constexpr int kBM = 128;
-constexpr int kBK = 32;              // fp16 per k-block: 64-byte rows, 64-byte swizzle
+constexpr int kBK = 32;              // fp16 per k-block (hi or lo): 64 bytes; the three-pass layout
+                                     // puts a k-block's hi and lo in one 128-byte row
 constexpr int kThreads = 384;        // 3 warpgroups
 constexpr int kEpiWarps = 8;
 constexpr int kMaxBN = 256;          // 2 buffers x 256 columns = 512
 constexpr int kEpiCols = 128;        // columns one epilogue thread sums
 constexpr int kMaxBufs = 4;          // TMEM chunk buffers
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kSpinLimit = 1u << 25;
+constexpr uint32_t kSpinLimit = kDefaultWaitPolls;   // drains of work already in flight
 constexpr int kSmemBudget = 227 * 1024;   // the opt-in maximum per CTA
 constexpr int kStageOutBytes = kEpiWarps * 32 * 32 * 4;   // one 32 x 32 fp32 block per epilogue warp
 constexpr uint32_t kAPlaneBytes = kBM * kBK * 2;   // 8 KB: one M-tile, one plane
@@ -98,6 +99,8 @@ struct TcParams {
     float unscale;
     const float* unscale_dev;   // when set, the accumulator scale is read from here
     int* err;
+    uint32_t wait_polls;        // polls before a wait gives up
+    int unarrived_wait;         // verification: the epilogue's first wait targets a barrier nobody arrives on
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p)
@@ -135,13 +138,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
 }
 
 // Wait for the phase of the given parity; false if it did not complete
-// within the poll limit or another role of the CTA gave up first.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag)
+// within `polls` polls or another role of the CTA gave up first.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, uint32_t polls)
 {
     for (uint32_t i = 0;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (i >= kSpinLimit) {
+        if (i >= polls) {
             *abort_flag = 1;
             return false;
         }
@@ -374,7 +377,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     uint64_t* tfull = bars + 2 * p.stages;
     uint64_t* tempty = tfull + kMaxBufs;
     uint64_t* drain = tempty + kMaxBufs;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* unarrived = drain + 1;    // verification only: initialised, never arrived on
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(unarrived + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -392,6 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
             mbar_init(&tempty[i], kEpiWarps);
         }
         mbar_init(drain, 1);
+        mbar_init(unarrived, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -437,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
                 int j = kb_lo / p.cin_blocks, cb = kb_lo - j * p.cin_blocks;
                 int row0 = (int)(in0 - a.shift[j]), row1 = (int)(in1 - a.shift[j]);
                 for (int kb = kb_lo; kb < kb_hi; kb++) {
-                    if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag)) { ok = false; break; }
+                    if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.wait_polls)) { ok = false; break; }
                     const int c0 = cb * kBoxK;
                     mbar_expect_tx(&full[s], p.tx_bytes);
                     tma_load_2d(st, &ma, &full[s], c0, row0);
@@ -479,13 +484,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
                 const int sp = tile % p.n_splits;
                 const int kb_lo = sp * p.cps * p.chunk_kb, kb_hi = min(p.nkb, kb_lo + p.cps * p.chunk_kb);
                 for (int kb0 = kb_lo; kb0 < kb_hi && ok; kb0 += p.chunk_kb) {
-                    if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag)) { ok = false; break; }
+                    if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, p.wait_polls)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t d0 = tmem_base + (uint32_t)acc * p.buf_cols;
                     const uint32_t d1 = d0 + p.mt_cols;
                     const int kb1 = min(p.nkb, kb0 + p.chunk_kb);
                     for (int kb = kb0; kb < kb1; kb++) {
-                        if (!mbar_wait(&full[s], ph, abort_flag)) { ok = false; break; }
+                        if (!mbar_wait(&full[s], ph, abort_flag, p.wait_polls)) { ok = false; break; }
                         tc_fence_after();
                         // descriptors of the stage's boxes: one base plus constant
                         // steps; in three-pass mode the lo part of a row sits 64
@@ -580,7 +585,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
                 const uint32_t aph = (uint32_t)(chunk_it / p.nbuf) & 1u;
                 // one lane polls, the warp follows its verdict (tcgen05.ld needs a converged warp)
                 int w_ok = 1;
-                if (lane == 0) w_ok = mbar_wait(&tfull[acc], aph, abort_flag) ? 1 : 0;
+                uint64_t* wbar = (p.unarrived_wait && chunk_it == 0) ? unarrived : &tfull[acc];
+                if (lane == 0) w_ok = mbar_wait(wbar, aph, abort_flag, p.wait_polls) ? 1 : 0;
                 w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
                 if (!w_ok) { ok = false; break; }
                 tc_fence_after();
@@ -968,7 +974,7 @@ cudaError_t launch_tc_prep(const float* x, const float* alpha, const float* inv_
 namespace {
 
 cudaError_t tc_gemm_core(const GemmArgs& a, const TcWeights& w, const float* unscale_dev, PlanView plan,
-                         int n_row_tiles, const void* a_planes, long long a_rows, int* err,
+                         int n_row_tiles, const void* a_planes, long long a_rows, int* err, TcWaitLimit wl,
                          int num_sms, cudaStream_t s, float* ws, size_t ws_floats, int* launches)
 {
     if (n_row_tiles <= 0) return cudaSuccess;
@@ -997,7 +1003,7 @@ cudaError_t tc_gemm_core(const GemmArgs& a, const TcWeights& w, const float* uns
     const uint32_t row = w.passes == 3 ? 128u : 64u;
     p.stage_bytes = (uint32_t)p.mtiles * kBM * row + round1024((uint32_t)w.BN * row);
     p.tx_bytes = (uint32_t)p.mtiles * kBM * row + (uint32_t)w.BN * row;
-    const int extra = 1024 + 512 + kStageOutBytes;
+    const int extra = 1024 + 512 + kStageOutBytes;   // alignment slack, barriers and flags, the epilogue's staging
     p.stages = std::min(8, (kSmemBudget - extra) / (int)p.stage_bytes);
     if (p.stages < 2) return cudaErrorInvalidValue;
     p.idesc = idesc_f16(kBM, w.BN);
@@ -1044,6 +1050,8 @@ cudaError_t tc_gemm_core(const GemmArgs& a, const TcWeights& w, const float* uns
     p.unscale = w.unscale;
     p.unscale_dev = unscale_dev;
     p.err = err;
+    p.wait_polls = wl.polls;
+    p.unarrived_wait = wl.unarrived_wait;
     const size_t smem = (size_t)p.stages * p.stage_bytes + extra;
     const int tiles = p.n_mgroups * w.n_tiles * p.n_splits;
     const int grid = std::min(tiles, num_sms > 0 ? num_sms : 152);
@@ -1065,7 +1073,7 @@ cudaError_t tc_gemm_core(const GemmArgs& a, const TcWeights& w, const float* uns
 cudaError_t launch_tc_gemm(const GemmArgs& a, const TcWeights& w, PlanView plan, int n_row_tiles,
                            const TcScratch* scratch, long long a_rows, int num_sms, cudaStream_t s, int* launches)
 {
-    return tc_gemm_core(a, w, nullptr, plan, n_row_tiles, scratch->a_hi, a_rows, scratch->err,
+    return tc_gemm_core(a, w, nullptr, plan, n_row_tiles, scratch->a_hi, a_rows, scratch->err, scratch->wait,
                         num_sms, s, scratch->ws, scratch->ws_floats, launches);
 }
 
@@ -1130,17 +1138,27 @@ __global__ void op_wpack_kernel(const float* __restrict__ w, int Cout, int Cin, 
 
 }  // namespace
 
-int run_tc_conv1d(const TcOpScratch& sc, const float* x, int T, int Cin, const float* w,
-                                const float* bias, const float* alpha, int Cout, int k, int dil, float* y,
-                                int num_sms, cudaStream_t s)
+int check_tc_conv1d(const TcOpScratch& sc, int T, int Cin, bool has_alpha, int Cout, int k, int dil)
 {
     if (T < 1 || k < 1 || k > kMaxTaps || dil < 1 || !tc_eligible(Cin, Cout)) return OP_BAD_ARG;
-    if (alpha && Cin > kOpMaxCin) return OP_BAD_ARG;
+    if (has_alpha && Cin > kOpMaxCin) return OP_BAD_ARG;
     const long long H = (long long)(k - 1) * dil;
     const long long rows = H + T;
     const long long K = (long long)k * Cin;
     if ((size_t)(rows * Cin) > sc.a_elems || (size_t)(K * Cout) > sc.b_elems) return OP_TOO_BIG;
     if (rows > (1LL << 30)) return OP_TOO_BIG;
+    return OP_OK;
+}
+
+int run_tc_conv1d(const TcOpScratch& sc, const float* x, int T, int Cin, const float* w,
+                                const float* bias, const float* alpha, int Cout, int k, int dil, float* y,
+                                int num_sms, cudaStream_t s)
+{
+    const int chk = check_tc_conv1d(sc, T, Cin, alpha != nullptr, Cout, k, dil);
+    if (chk != OP_OK) return chk;
+    const long long H = (long long)(k - 1) * dil;
+    const long long rows = H + T;
+    const long long K = (long long)k * Cin;
     int* words = sc.words;
     const float* inv_alpha = reinterpret_cast<const float*>(words + kOpInvAlpha);
     op_setup_kernel<<<(std::max(Cin, 1) + 255) / 256, 256, 0, s>>>(words, T, alpha, Cin);
@@ -1181,10 +1199,10 @@ int run_tc_conv1d(const TcOpScratch& sc, const float* x, int T, int Cin, const f
     a.tcum = words + kOpPlan + 6;
     a.bm = kBM;
     PlanView plan{1, words + kOpPlan + 2, words + kOpPlan + 4, reinterpret_cast<const long long*>(words + kOpPlan),
-                  words + kOpPlan + 5};
+                  words + kOpPlan + 5, nullptr};
     const int n_row_tiles = (T + kBM - 1) / kBM;
     if (tc_gemm_core(a, tw, reinterpret_cast<const float*>(words) + kOpUnscale, plan, n_row_tiles, sc.a_hi,
-                     rows, sc.err, num_sms, s, nullptr, 0, nullptr) != cudaSuccess)
+                     rows, sc.err, sc.wait, num_sms, s, nullptr, 0, nullptr) != cudaSuccess)
         return OP_CUDA;
     return OP_OK;
 }

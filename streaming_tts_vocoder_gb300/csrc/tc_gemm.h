@@ -25,7 +25,19 @@ struct TcWeights {
 // words for its one-segment plan, weight scale and 1/alpha.
 constexpr int kOpMaxCin = 4096;
 constexpr int kOpWords = 16 + kOpMaxCin;
+// Bounded waits of the GEMM kernel: every mbarrier wait gives up after
+// `polls` polls (the CTA then raises the error flag, drains its copies and
+// MMAs, frees TMEM and returns).  unarrived_wait != 0 is for verifying that
+// path: the epilogue's first wait of each CTA then targets a barrier no role
+// ever arrives on, so it runs out after `polls` polls on any input.
+constexpr uint32_t kDefaultWaitPolls = 1u << 25;
+struct TcWaitLimit {
+    uint32_t polls = kDefaultWaitPolls;
+    int unarrived_wait = 0;
+};
+
 struct TcOpScratch {
+    TcWaitLimit wait;
     void* a_hi = nullptr;     // 2 a_elems fp16 from here on: a_lo == a_hi + a_elems
     void* a_lo = nullptr;
     size_t a_elems = 0;
@@ -40,6 +52,7 @@ struct TcOpScratch {
 // hi and lo), big enough for the widest input of any contraction, plus the
 // sticky flag a kernel sets when one of its bounded waits expires.
 struct TcScratch {
+    TcWaitLimit wait;
     void* a_hi = nullptr;     // 2 elems fp16 from here on (a_lo == a_hi + elems): the three-pass
     void* a_lo = nullptr;     // layout interleaves hi and lo over all of it, the one-pass mode uses hi
     size_t elems = 0;
@@ -71,6 +84,9 @@ cudaError_t launch_tc_gemm(const GemmArgs& a, const TcWeights& w, PlanView plan,
 // (history rows first), w [Cout][Cin][k], y [T][Cout], all device fp32;
 // alpha and bias may be null.  Returns one of OP_*.
 enum { OP_OK = 0, OP_BAD_ARG = 1, OP_TOO_BIG = 2, OP_CUDA = 3 };
+// The argument and capacity checks of run_tc_conv1d alone (enqueues nothing):
+// OP_BAD_ARG for an unsupported shape, then OP_TOO_BIG for one beyond sc.
+int check_tc_conv1d(const TcOpScratch& sc, int T, int Cin, bool has_alpha, int Cout, int k, int dil);
 int run_tc_conv1d(const TcOpScratch& sc, const float* x, int T, int Cin, const float* w, const float* bias,
                   const float* alpha, int Cout, int k, int dil, float* y, int num_sms, cudaStream_t s);
 

@@ -24,6 +24,18 @@ def assert_close(got, want, what="", rel=TOL_REL, mx=TOL_MAX):
     return r, m
 
 
+def assert_close_pre_tanh(got, want, what=""):
+    """The final conv's output before tanh, against the oracle's.  Most samples
+    of a random-weight decoder saturate the tanh (|audio| > 0.999), so the
+    waveform comparison alone cannot see errors there; this one can.  Same
+    relative L2 bound as the waveform; the waveform's max-abs bound of 1e-2
+    is stated for a signal of unit scale, so here it scales with the rms of
+    the pre-tanh signal (tens on these decoders)."""
+    w = np.asarray(want, np.float64)
+    scale = max(1.0, float(np.sqrt(np.mean(w * w)))) if w.size else 1.0
+    return assert_close(got, want, what + " (pre-tanh)", rel=TOL_REL, mx=TOL_MAX * scale)
+
+
 def bits_equal(a, b):
     a = np.ascontiguousarray(a, np.float32)
     b = np.ascontiguousarray(b, np.float32)

@@ -21,6 +21,7 @@ def lib():
 def test_exports_every_declared_function(lib):
     names = C.header_functions()
     assert "codec_decode_chunk" in names and "codec_create" in names and "codec_state_reset" in names
+    assert "codec_conv1d_noalloc" in names and "codec_state_conv1d" in names
     raw = ctypes.CDLL(str(C.LIB_PATH))
     missing = [n for n in names if not hasattr(raw, n)]
     assert not missing, missing

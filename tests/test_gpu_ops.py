@@ -5,7 +5,7 @@ M-tile with N up to 256, several N-tiles), ragged row counts and Snake on the
 input.
 
 Tolerance: the operands are split into fp16 hi + lo (about 2^-22 relative
-each) and the products are summed in fp32 in chunks of 8 MMA k-steps, so one
+each) and the products are summed in fp32 in chunks of 16 MMA k-steps, so one
 conv lands within a few 1e-7 of the float64-accumulated oracle; 2e-5
 relative L2 leaves two orders of margin while still catching a dropped cross
 term (about 2^-11 = 5e-4)."""
@@ -70,3 +70,32 @@ def test_tc_conv_argument_errors(state):
     with pytest.raises(C.CodecError) as e:
         state.conv1d(big, torch.zeros(64, 64, 1, device="cuda"), torch.zeros(200000, 64, device="cuda"))
     assert e.value.status == 5
+
+
+def test_bounded_wait_runs_out_reports_and_recovers(state):
+    """Every wait of the tensor-core GEMM is bounded.  With the verification
+    switch, each CTA's first epilogue wait targets a barrier nothing arrives
+    on, so it gives up after the given polls: the kernel must stop cleanly
+    (drain its copies and MMAs, free TMEM), the state must report the timeout,
+    and after a reset of all slots the same conv must give its normal bits."""
+    rng = np.random.default_rng(5)
+    k, dil, Cin, Cout, T = 3, 1, 96, 96, 257
+    x = torch.from_numpy((rng.standard_normal(((k - 1) * dil + T, Cin)) * 2).astype(np.float32)).cuda()
+    w = torch.from_numpy((rng.standard_normal((Cout, Cin, k)) / np.sqrt(Cin * k)).astype(np.float32)).cuda()
+    y0 = torch.full((T, Cout), float("nan"), device="cuda")
+    state.conv1d(x, w, y0, dilation=dil)
+    state.reset()
+    assert state.query(0)[1] == 0
+    try:
+        state.set_wait_limit(polls=1000, unarrived_wait=True)
+        y1 = torch.zeros(T, Cout, device="cuda")
+        state.conv1d(x, w, y1, dilation=dil)
+        assert state.query(0)[1] & C.STREAM_ERR_KERNEL_TIMEOUT
+    finally:
+        state.set_wait_limit()
+    state.reset()
+    assert state.query(0)[1] == 0
+    y2 = torch.full((T, Cout), float("nan"), device="cuda")
+    state.conv1d(x, w, y2, dilation=dil)
+    torch.cuda.synchronize()
+    assert np.array_equal(y2.cpu().numpy().view(np.uint32), y0.cpu().numpy().view(np.uint32))

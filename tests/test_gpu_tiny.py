@@ -9,7 +9,7 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_helpers import assert_close, bits_equal, decode_batch, decode_stream_chunks
+from gpu_helpers import assert_close, assert_close_pre_tanh, bits_equal, decode_batch, decode_stream_chunks
 from oracle.oracle import OracleModel
 from streaming_tts_vocoder_gb300 import codec as C
 from streaming_tts_vocoder_gb300.synthetic import (make_codes, make_weights, pack_blob,
@@ -43,7 +43,7 @@ def test_full_sequence_8_frames(tiny, precision):
     (a,), (pt,) = decode_batch(st, [(0, codes)], pre_tanh=True)
     assert a.size == 8 * 1920
     assert_close(a, ref, "audio")
-    assert_close(pt, ref_pt, "pre-tanh")
+    assert_close_pre_tanh(pt, ref_pt, "8 frames")
     assert st.query(0) == (8, 0)
 
 
@@ -74,11 +74,14 @@ def test_chunked_equals_full(tiny, precision, splits):
     cfg, blob, om = tiny
     codes = make_codes(cfg, 12, 5)
     st = make_state(cfg, blob, precision, chunk=12)
-    full = decode_batch(st, [(0, codes)])[0]
+    (full,), (full_pt,) = decode_batch(st, [(0, codes)], pre_tanh=True)
     st.reset()
-    chunked = decode_stream_chunks(st, 0, codes, splits)
+    chunked, chunked_pt = decode_stream_chunks(st, 0, codes, splits, pre_tanh=True)
     assert bits_equal(chunked, full)
-    assert_close(chunked, om.decode_full(codes), "chunked vs oracle")
+    assert bits_equal(chunked_pt, full_pt)
+    ref, ref_pt = om.decode_full(codes, pre_tanh=True)
+    assert_close(chunked, ref, "chunked vs oracle")
+    assert_close_pre_tanh(chunked_pt, ref_pt, "chunked vs oracle")
     assert st.query(0) == (12, 0)
 
 
@@ -89,14 +92,17 @@ def test_first_audio_then_single_frames(tiny, precision):
     cfg, blob, om = tiny
     codes = make_codes(cfg, 25, 3)
     st = make_state(cfg, blob, precision, chunk=25)
-    first = decode_batch(st, [(0, codes[:, :1])])[0]
+    (first,), (first_pt,) = decode_batch(st, [(0, codes[:, :1])], pre_tanh=True)
     assert first.size == 1920
-    rest = decode_stream_chunks(st, 0, codes[:, 1:], [1] * 24)
+    rest, rest_pt = decode_stream_chunks(st, 0, codes[:, 1:], [1] * 24, pre_tanh=True)
     chunked = np.concatenate([first, rest])
+    chunked_pt = np.concatenate([first_pt, rest_pt])
     st.reset()
     full = decode_batch(st, [(0, codes)])[0]
     assert bits_equal(chunked, full)
-    assert_close(chunked, om.decode_full(codes), "single-frame calls vs oracle")
+    ref, ref_pt = om.decode_full(codes, pre_tanh=True)
+    assert_close(chunked, ref, "single-frame calls vs oracle")
+    assert_close_pre_tanh(chunked_pt, ref_pt, "single-frame calls vs oracle")
 
 
 @pytest.mark.parametrize("precision", PRECISIONS)
@@ -108,14 +114,19 @@ def test_64_staggered_streams(tiny, precision):
     st = make_state(cfg, blob, precision, streams=S, chunk=25, batch=S * 25)
     codes = [make_codes(cfg, F, 1000 + s) for s in range(S)]
     out = [[] for _ in range(S)]
+    out_pt = [[] for _ in range(S)]
     for tick in staggered_schedule(S, F, 25):
         entries = [(s, codes[s][:, a:a + n]) for s, a, n in tick]
-        for (s, _), a in zip(entries, decode_batch(st, entries, T_max=25)):
+        audio, pts = decode_batch(st, entries, T_max=25, pre_tanh=True)
+        for (s, _), a, p in zip(entries, audio, pts):
             out[s].append(a)
+            out_pt[s].append(p)
     for s in range(S):
         got = np.concatenate(out[s])
         assert got.size == F * 1920
-        assert_close(got, om.decode_full(codes[s]), f"stream {s}")
+        ref, ref_pt = om.decode_full(codes[s], pre_tanh=True)
+        assert_close(got, ref, f"stream {s}")
+        assert_close_pre_tanh(np.concatenate(out_pt[s]), ref_pt, f"stream {s}")
         assert st.query(s) == (F, 0)
 
 
@@ -128,16 +139,21 @@ def test_long_form_8_streams(tiny, precision):
     st = make_state(cfg, blob, precision, streams=S, chunk=F, batch=S * F)
     codes = [make_codes(cfg, F, 77 + s) for s in range(S)]
     out = [[] for _ in range(S)]
+    out_pt = [[] for _ in range(S)]
     for c in range(F // 25):
         entries = [(s, codes[s][:, c * 25:(c + 1) * 25]) for s in range(S)]
-        for s, a in enumerate(decode_batch(st, entries)):
-            out[s].append(a)
+        audio, pts = decode_batch(st, entries, pre_tanh=True)
+        for s in range(S):
+            out[s].append(audio[s])
+            out_pt[s].append(pts[s])
     st.reset()
     full = decode_batch(st, [(s, codes[s]) for s in range(S)])
     for s in range(S):
         got = np.concatenate(out[s])
         assert bits_equal(got, full[s]), f"stream {s}: chunked != full"
-        assert_close(got, om.decode_full(codes[s]), f"stream {s}")
+        ref, ref_pt = om.decode_full(codes[s], pre_tanh=True)
+        assert_close(got, ref, f"stream {s}")
+        assert_close_pre_tanh(np.concatenate(out_pt[s]), ref_pt, f"stream {s}")
 
 
 @pytest.mark.parametrize("precision", PRECISIONS)
@@ -147,11 +163,13 @@ def test_bad_code_is_sticky_and_reset_clears(tiny, precision):
     codes = make_codes(cfg, 4, 0)
     bad = codes.copy()
     bad[1, 2] = cfg.V
-    good_a, bad_a = decode_batch(st, [(0, codes), (1, bad)])
+    (good_a, bad_a), (_, bad_pt) = decode_batch(st, [(0, codes), (1, bad)], pre_tanh=True)
     assert st.query(0) == (4, 0)
     assert st.query(1) == (4, C.STREAM_ERR_BAD_CODE)
     s = om.stream()
-    assert_close(bad_a, s.decode(bad), "bad-code stream vs oracle (zeroed frame)")
+    ref, ref_pt = s.decode(bad, pre_tanh=True)
+    assert_close(bad_a, ref, "bad-code stream vs oracle (zeroed frame)")
+    assert_close_pre_tanh(bad_pt, ref_pt, "bad-code stream vs oracle (zeroed frame)")
     decode_batch(st, [(1, codes)])
     assert st.query(1) == (8, C.STREAM_ERR_BAD_CODE)
     st.reset([1])
@@ -212,3 +230,25 @@ def test_argument_errors_enqueue_nothing(tiny):
     assert st.query(0) == (0, 0) and st.query(1) == (0, 0)
     st.decode(codes, [0, 0], audio)                   # nothing to do
     assert st.last_launches == 0
+
+
+def test_kernel_timeout_is_reported_and_reset_recovers(tiny):
+    """A decode whose tensor-core GEMMs give up on a bounded wait (each CTA's
+    first epilogue wait is pointed at a barrier nothing arrives on) reports
+    CODEC_STREAM_ERR_KERNEL_TIMEOUT; a reset of all slots clears it and the
+    next decode has its normal bits."""
+    cfg, blob, om = tiny
+    st = make_state(cfg, blob, C.PRECISION_FP16X3, chunk=8)
+    codes = make_codes(cfg, 8, 0)
+    good = decode_batch(st, [(0, codes)])[0]
+    st.reset()
+    try:
+        st.set_wait_limit(polls=1000, unarrived_wait=True)
+        decode_batch(st, [(0, codes)])
+        frames, bits = st.query(0)
+        assert frames == 8 and bits & C.STREAM_ERR_KERNEL_TIMEOUT
+    finally:
+        st.set_wait_limit()
+    st.reset()
+    assert st.query(0) == (0, 0)
+    assert bits_equal(decode_batch(st, [(0, codes)])[0], good)
