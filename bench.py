@@ -63,12 +63,16 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--decoder", choices=["qwen3", "tiny"], default="qwen3")
     ap.add_argument("--precision", choices=["fp32", "fp16x3", "fp16"], default="fp16x3")
+    ap.add_argument("--weights", choices=["fp32", "q8"], default="fp32",
+                    help="q8: create the codec from the int8-per-32 weight file (codec_create_q8)")
     ap.add_argument("--streams", type=int, default=64)
     ap.add_argument("--frames", type=int, default=250)
     ap.add_argument("--chunk", type=int, default=25)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true", help="skip the cpu_baseline oracle timing")
     ap.add_argument("--first-audio-runs", type=int, default=100)
+    ap.add_argument("--no-streaming", action="store_true",
+                    help="skip the streaming-schedule section (TTFA, gaps, carried vs recompute)")
     ap.add_argument("--schedule", action="store_true",
                     help="latency of streaming chunk schedules (time to first audio, per-chunk latency, "
                          "playback gaps) for carried-state and recompute decoding, instead of the throughput line")
@@ -125,6 +129,7 @@ def config_dict(args, precision):
         "chunk_frames": args.chunk,
         "stagger": f"stream s starts at frame s mod {args.chunk}",
         "precision": precision,
+        "weights": getattr(args, "weights", "fp32"),
         "samples_per_frame": 1920,
         "l2": "inputs larger than L2: each tick writes and reads GBs of activations",
         "parallelism": "replicas (one independent decoder per GPU, no collective)",
@@ -202,6 +207,15 @@ def kernel_source_digest(files):
     return h.hexdigest()
 
 
+def weight_bytes(cfg, precision):
+    """Bytes of the non-codebook weights as the kernels store them: fp32 or
+    the fp16 hi + lo planes (4 bytes per weight), or the hi plane alone
+    (single-pass fp16, 2 bytes) for the tensor-core contractions."""
+    from streaming_tts_vocoder_gb300.synthetic import weight_manifest
+    n = sum(t.size for t in weight_manifest(cfg) if not t.name.startswith("cb."))
+    return n * (2 if precision == "fp16" else 4)
+
+
 def oracle_sample(cfg, blob, frames, seed=1000):
     """Time the CPU oracle decoding `frames` frames of one stream."""
     from oracle import oracle as O
@@ -262,7 +276,12 @@ def run_ours(args):
     prec = {"fp16x3": C.PRECISION_FP16X3, "fp16": C.PRECISION_FP16, "fp32": C.PRECISION_FP32}[args.precision]
     blob = pack_blob(cfg, make_weights(cfg, 0))
     S, F, CH = args.streams, args.frames, args.chunk
-    cod = C.Codec(cfg, blob, max_streams=S, max_chunk_frames=CH, max_batch_frames=S * CH, precision=prec)
+    if args.weights == "q8":
+        from streaming_tts_vocoder_gb300.weights_q8 import pack_q8
+        cod = C.Codec(cfg, q8=pack_q8(cfg, blob), max_streams=S, max_chunk_frames=CH, max_batch_frames=S * CH,
+                      precision=prec)
+    else:
+        cod = C.Codec(cfg, blob, max_streams=S, max_chunk_frames=CH, max_batch_frames=S * CH, precision=prec)
     st = cod.state()
     spf = cod.samples_per_frame
 
@@ -358,6 +377,20 @@ def run_ours(args):
                 wall_us.append(1e6 * (t1 - t0))
         fa = {"device_us_median": statistics.median(dev_us), "wall_us_median": statistics.median(wall_us),
               "runs": len(dev_us), "launches": st.last_launches}
+        # a one-frame call must read every weight once: its roof is the weight bytes at the copy bandwidth
+        # (4 bytes per weight in every mode: fp32, or the fp16 hi + lo planes; 2 in single-pass fp16)
+        pk_fa, pk_fa_src = peaks()
+        wbytes = weight_bytes(cfg, args.precision)
+        fa_gbs = wbytes / (fa["device_us_median"] * 1e-6) / 1e9
+        fa["roofline"] = {"bound": "hbm", "achieved": fa_gbs, "peak": pk_fa["hbm_gbs"], "unit": "GB/s",
+                          "frac": fa_gbs / pk_fa["hbm_gbs"], "traffic": None,
+                          "algorithmic_bytes": wbytes,
+                          "note": f"every non-codebook weight read once ({pk_fa_src} copy bandwidth)",
+                          "floor_us": wbytes / (pk_fa["hbm_gbs"] * 1e9) * 1e6}
+
+    streaming = None
+    if rank == 0 and not args.no_streaming:
+        streaming = streaming_schedules(cfg, blob, prec, stream)
 
     # roofline of the dominant kernel
     pk, pk_src = peaks()
@@ -407,7 +440,7 @@ def run_ours(args):
             "data": "synthetic (uniform codes, random N(0,1/fan_in) weights)",
             "config": config_dict(args, args.precision),
             "roofline": roof, "kernels": kernels, "gpu_launches": gpu_launches,
-            "e2e": e2e, "first_audio": fa, "clocks": clk, "cpu_baseline": cpu,
+            "e2e": e2e, "first_audio": fa, "streaming": streaming, "clocks": clk, "cpu_baseline": cpu,
             "frames_per_s": world * args.steps * S * F / (ms / 1e3),
         }
         print(json.dumps(line), flush=True)
@@ -665,75 +698,106 @@ def playback_gaps(lats_ms, frames, frame_ms):
     return gaps
 
 
-SCHEDULES = {
-    # frames per call, repeated until the stream's frames are used up
-    "1_then_25": [1] + [25] * 100,
-    "ramp_4_4_8_16_25": [4, 4, 8, 16] + [25] * 100,
-    "doubling_1_2_4_8": [1, 2, 4, 8] + [8] * 400,
-    "fixed_25": [25] * 100,
-}
+def streaming_schedules(cfg, blob, prec, stream, frames=250, ctx=72, producer_ms=8.0, reps=3):
+    """Streaming latency of one stream under the orchestrator's chunk
+    schedules (the library's codec_chunk_frames: 1 then 25, the ramp 4, 4, 8,
+    16, 25, adaptive doubling from 1), in two decode modes: carried (the
+    decoder keeps its conv histories and K/V window across calls) and
+    recompute (codec_decode_recompute: each call re-decodes up to `ctx` frames
+    of left context from an empty slot and keeps only the new audio).
+
+    Each call's device latency is measured with CUDA events; the timeline is
+    then laid out on the host for two producers: codes all available up front
+    (the decode cost alone), and frames arriving every producer_ms (a talker at
+    real-time factor producer_ms / 80 ms; the pages measure the whole server
+    pipeline at 0.08-0.10).  A chunk's decode starts when its last frame has
+    arrived and the previous decode is done.  Reported per schedule and mode:
+    TTFA (first chunk ready), inter-chunk gap (time between consecutive chunks
+    becoming ready; p95), playback stall total when playback starts on the
+    first chunk, and the uninterrupted-playback latency max_i(ready_i - audio
+    before chunk i), the earliest start that never stalls."""
+    import torch
+    from streaming_tts_vocoder_gb300 import codec as C
+    cod = C.Codec(cfg, blob, max_streams=1, max_chunk_frames=ctx + 25, precision=prec)
+    st = cod.state()
+    dev = torch.device("cuda")
+    codes = make_codes(cfg, frames, 1000)
+    spf = cod.samples_per_frame
+    frame_ms = 1e3 / FRAME_RATE_HZ
+    scheds = {
+        "1_then_25": C.chunk_schedule(C.SCHEDULE_FIXED, first=1, steady=25),
+        "ramp_4_4_8_16_25": C.chunk_schedule(C.SCHEDULE_RAMP, steady=25, ramp=(4, 4, 8, 16)),
+        "adaptive_from_1": C.chunk_schedule(C.SCHEDULE_ADAPTIVE, first=1, steady=25),
+    }
+    T_max = ctx + 25
+    codes_d = torch.zeros(1, cfg.Q, T_max, dtype=torch.int32, device=dev)
+    audio = torch.empty(1, T_max * spf, device=dev)
+    out = {}
+    for name, sch in scheds.items():
+        sizes = C.schedule_chunks(sch, frames)
+        for mode in ("carried", "recompute"):
+            for _ in range(reps):                # earlier passes warm the graph cache; keep the last
+                st.reset([0], stream=stream)
+                torch.cuda.synchronize()
+                t, lats = 0, []
+                for n in sizes:
+                    lo = max(0, t - ctx) if mode == "recompute" else t
+                    seg = np.zeros((cfg.Q, T_max), np.int32)
+                    seg[:, : t + n - lo] = codes[:, lo:t + n]
+                    codes_d.copy_(torch.from_numpy(seg).reshape(1, cfg.Q, T_max))
+                    torch.cuda.synchronize()
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    if mode == "recompute":
+                        st.decode_recompute(codes_d, [t - lo], [n], audio, stream_ids=[0], stream=stream)
+                    else:
+                        st.decode(codes_d, [n], audio, stream_ids=[0], stream=stream)
+                    e1.record(stream)
+                    e1.synchronize()
+                    lats.append(e0.elapsed_time(e1))
+                    t += n
+            entry = {"chunks": len(sizes), "decode_ms_total": float(sum(lats)),
+                     "chunk_latency_ms_p50": float(np.percentile(lats, 50)),
+                     "chunk_latency_ms_p95": float(np.percentile(lats, 95))}
+            for prod, pms in (("up_front", 0.0), (f"producer_{pms_label(producer_ms)}", producer_ms)):
+                entry[prod] = stream_timeline(lats, sizes, frame_ms, pms)
+            out[f"{name}/{mode}"] = entry
+    st.close()
+    cod.close()
+    return {"decoder": cfg.name, "frames": frames, "frame_ms": frame_ms, "recompute_context_frames": ctx,
+            "producer_ms_per_frame": producer_ms, "schedules": out}
+
+
+def pms_label(ms):
+    return f"{ms:g}ms_per_frame"
+
+
+def stream_timeline(lats_ms, frames, frame_ms, producer_ms):
+    """Ready times of chunks decoded in order (decode i starts when its last
+    frame has arrived and decode i - 1 is done) and the playback metrics."""
+    ready, t_free, arrived = [], 0.0, 0
+    for lat, n in zip(lats_ms, frames):
+        arrived += n
+        start = max(arrived * producer_ms, t_free)
+        t_free = start + lat
+        ready.append(t_free)
+    before = np.concatenate([[0.0], np.cumsum(np.asarray(frames, float) * frame_ms)[:-1]])
+    gaps = np.diff(ready) if len(ready) > 1 else np.zeros(0)
+    stalls = playback_gaps(list(np.diff(np.concatenate([[0.0], ready]))), frames, frame_ms)
+    return {"ttfa_ms": float(ready[0]),
+            "inter_chunk_gap_ms_p95": float(np.percentile(gaps, 95)) if gaps.size else 0.0,
+            "playback_stall_ms_total": float(sum(stalls)),
+            "uninterrupted_playback_ms": float(np.max(np.asarray(ready) - before))}
 
 
 def run_schedule(args):
-    """Streaming latency of one stream under a chunk schedule, codes all
-    available up front (the decode cost alone).  carried: the decoder keeps
-    its conv histories and K/V window across calls.  recompute: every call
-    re-decodes up to 72 frames of left context from an empty state and keeps
-    only the new frames' audio (the server mode the pages describe).  A call
-    of n frames gives n x 80 ms of audio; playback stalls when the next chunk
-    is ready after the audio before it ran out."""
     import torch
     from streaming_tts_vocoder_gb300 import codec as C
     cfg = qwen3_config() if args.decoder == "qwen3" else tiny_config()
     blob = pack_blob(cfg, make_weights(cfg, 0))
     prec = {"fp16x3": C.PRECISION_FP16X3, "fp16": C.PRECISION_FP16, "fp32": C.PRECISION_FP32}[args.precision]
-    ctx = 72
-    F = 250
-    cod = C.Codec(cfg, blob, max_streams=1, max_chunk_frames=ctx + 25, precision=prec)
-    st = cod.state()
-    dev = torch.device("cuda")
-    stream = torch.cuda.current_stream()
-    codes = make_codes(cfg, F, 1000)
-    spf = cod.samples_per_frame
-    frame_ms = 1e3 / FRAME_RATE_HZ
-    out = {"metric": "streaming chunk latency, one stream", "decoder": args.decoder, "precision": args.precision,
-           "frames": F, "frame_ms": frame_ms, "context_frames_recompute": ctx, "schedules": {}}
-    for name, sched in SCHEDULES.items():
-        for mode in ("carried", "recompute"):
-            lat_runs = []
-            for rep in range(3):                 # first pass warms the graph cache; keep the last
-                st.reset([0], stream=stream)
-                torch.cuda.synchronize()
-                t, lats, sizes = 0, [], []
-                for n in sched:
-                    if t >= F:
-                        break
-                    n = min(n, F - t)
-                    lo = max(0, t - ctx) if mode == "recompute" else t
-                    seg = codes[:, lo:t + n]
-                    c = torch.from_numpy(np.ascontiguousarray(seg)).reshape(1, cfg.Q, seg.shape[1]).to(dev)
-                    a = torch.empty(1, seg.shape[1] * spf, device=dev)
-                    if mode == "recompute":
-                        st.reset([0], stream=stream)
-                    torch.cuda.synchronize()
-                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                    e0.record(stream)
-                    st.decode(c, [seg.shape[1]], a, stream_ids=[0], stream=stream)
-                    e1.record(stream)
-                    e1.synchronize()
-                    lats.append(e0.elapsed_time(e1))
-                    sizes.append(n)
-                    t += n
-                lat_runs.append((lats, sizes))
-            lats, sizes = lat_runs[-1]
-            gaps = playback_gaps(lats, sizes, frame_ms)
-            out["schedules"][f"{name}/{mode}"] = {
-                "ttfa_ms": lats[0], "calls": len(lats),
-                "chunk_latency_ms_p50": float(np.percentile(lats, 50)),
-                "chunk_latency_ms_p95": float(np.percentile(lats, 95)),
-                "playback_gap_ms_total": float(sum(gaps)),
-                "playback_gap_ms_p95": float(np.percentile(gaps, 95)) if gaps else 0.0,
-                "decode_ms_total": float(sum(lats)), "audio_ms": float(sum(sizes) * frame_ms)}
+    out = {"metric": "streaming chunk latency, one stream", "precision": args.precision}
+    out.update(streaming_schedules(cfg, blob, prec, torch.cuda.current_stream()))
     print(json.dumps(out))
     return 0
 

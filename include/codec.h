@@ -133,6 +133,28 @@ CODEC_API int64_t codec_weight_floats(const codec_config* cfg);
 CODEC_API codec_status codec_create(const codec_config* cfg, const float* weights, int64_t n_floats,
                           codec_t** out);
 
+/*
+ * The weight blob in the blixt/phonon "Weights" storage format: every tensor
+ * of 16,384 values or more as int8 with one f16 scale per 32 values along the
+ * rows of its converted layout (scale = max |value| / 127 of the f16-rounded
+ * values, round half to even), every other tensor as f16.  Layout, tensor by
+ * tensor in blob order, each part starting on a 4-byte boundary:
+ *   quantised: int8 q [R][L], then f16 scale [R][ceil(L / 32)], value (r, c) =
+ *              q[r][c] * scale[r][c / 32];
+ *   other:     f16 values in the blob's own layout.
+ * Converted rows: codebooks and linears [out][in]; convolutions [out][tap][in];
+ * transposed convolutions [out][phase][tap][in] with kernel index phase +
+ * tap * stride.  About a quarter of the fp32 blob's size.
+ * codec_q8_bytes: the file's size for cfg (-1 if cfg is invalid).
+ * codec_create_q8: as codec_create, from such a file (host memory, copied):
+ * a kernel expands it on the device to the fp32 blob (int8 x f16 is exact in
+ * fp32), from which the codec is built; the decode then runs on exactly the
+ * dequantised weights, in cfg.precision.  Errors as codec_create
+ * (CODEC_ERR_WEIGHTS for a wrong size).
+ */
+CODEC_API int64_t codec_q8_bytes(const codec_config* cfg);
+CODEC_API codec_status codec_create_q8(const codec_config* cfg, const void* q8, int64_t n_bytes, codec_t** out);
+
 /* Free the weights.  All states created from it must be destroyed first and
  * their GPU work finished. */
 CODEC_API void codec_destroy(codec_t* codec);

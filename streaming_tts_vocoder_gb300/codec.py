@@ -135,6 +135,8 @@ def _lib():
         sig = {
             "codec_weight_floats": (i64, [cfgp]),
             "codec_create": (i32, [cfgp, ctypes.POINTER(ctypes.c_float), i64, ctypes.POINTER(_P)]),
+            "codec_q8_bytes": (i64, [cfgp]),
+            "codec_create_q8": (i32, [cfgp, _P, i64, ctypes.POINTER(_P)]),
             "codec_destroy": (None, [_P]),
             "codec_samples_per_frame": (i32, [_P]),
             "codec_state_create": (i32, [_P, i32, ctypes.POINTER(_P)]),
@@ -215,6 +217,10 @@ def config_c(cfg, max_streams=1, max_chunk_frames=97, max_batch_frames=None,
 
 def weight_floats(cfg_c: CodecConfigC) -> int:
     return _lib().codec_weight_floats(ctypes.byref(cfg_c))
+
+
+def q8_bytes(cfg_c: CodecConfigC) -> int:
+    return _lib().codec_q8_bytes(ctypes.byref(cfg_c))
 
 
 def _check(status: int, what: str):
@@ -389,13 +395,20 @@ class Stft(_Streamed):
 class Codec:
     """codec_create / codec_destroy: the weights on the current CUDA device."""
 
-    def __init__(self, cfg, blob: np.ndarray, **capacity):
+    def __init__(self, cfg, blob: np.ndarray = None, q8: bytes = None, **capacity):
+        """blob: the fp32 weight blob (codec_create), or q8: the same weights in
+        the int8-per-32 storage format (codec_create_q8; see weights_q8.py)."""
         self.cfg = cfg
         self.cfg_c = config_c(cfg, **capacity)
-        blob = np.ascontiguousarray(blob, dtype=np.float32)
         h = ctypes.c_void_p()
-        _check(_lib().codec_create(ctypes.byref(self.cfg_c), blob.ctypes.data_as(ctypes.POINTER(ctypes.c_float)),
-                                   blob.size, ctypes.byref(h)), "codec_create")
+        if q8 is not None:
+            buf = np.frombuffer(q8, dtype=np.uint8)
+            _check(_lib().codec_create_q8(ctypes.byref(self.cfg_c), buf.ctypes.data_as(ctypes.c_void_p), buf.size,
+                                          ctypes.byref(h)), "codec_create_q8")
+        else:
+            blob = np.ascontiguousarray(blob, dtype=np.float32)
+            _check(_lib().codec_create(ctypes.byref(self.cfg_c), blob.ctypes.data_as(ctypes.POINTER(ctypes.c_float)),
+                                       blob.size, ctypes.byref(h)), "codec_create")
         self._h = h
         self.samples_per_frame = _lib().codec_samples_per_frame(h)
 

@@ -72,3 +72,17 @@ def test_playback_gaps():
     # 115 ms while the second plays until 110 + 2 x 80 = 270 ms: no gap
     assert bench.playback_gaps([10.0, 100.0, 5.0], [1, 2, 1], 80.0) == [20.0, 0.0]
     assert bench.playback_gaps([1.0], [25], 80.0) == []
+
+
+def test_stream_timeline_reproduces_the_one_then_25_cliff():
+    """A producer at 8 ms per 80 ms frame: the 25-frame chunk after a 1-frame
+    first chunk is ready long after the first frame's audio ran out (the
+    cliff the vllm-omni page describes); with all codes up front it is not."""
+    import bench
+    lat = [2.0, 3.0, 2.5]
+    r = bench.stream_timeline(lat, [1, 25, 25], 80.0, 8.0)
+    assert r["ttfa_ms"] == 8.0 + 2.0
+    assert r["uninterrupted_playback_ms"] == 26 * 8.0 + 3.0 - 80.0
+    assert r["playback_stall_ms_total"] == 26 * 8.0 + 3.0 - (10.0 + 80.0)
+    u = bench.stream_timeline(lat, [1, 25, 25], 80.0, 0.0)
+    assert u["ttfa_ms"] == 2.0 and u["playback_stall_ms_total"] == 0.0 and u["uninterrupted_playback_ms"] == 2.0
