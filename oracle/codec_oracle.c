@@ -29,6 +29,17 @@
  * sequence whatever the chunking, and chunked decoding equals a full decode
  * bit for bit.
  *
+ * Latent-input variant (blixt/phonon "Weights" and "Speed" item 7: the
+ * codec's latents are denormalised, projected by a 1x1 convolution without
+ * bias and upsampled x16 by a depthwise transposed convolution; the codec
+ * transformer then runs at the upsampled rate, 200 Hz, with a 251-position
+ * window): in place of the codebook sum and the pre-conv, latent frames
+ * [n][L] go through z = x sigma + mu, p = Wp z, and a causal depthwise
+ * ConvTranspose1d (kernel 2 s, stride s = tf_up, its own taps per channel),
+ * giving n s rows of d channels; the transformer's positions and window count
+ * those rows.  The oracle computes the three steps one after the other, as
+ * written; the GPU folds the projection into the upsampling weights.
+ *
  * Loops parallelise over output rows with OpenMP; within a row, the sum over
  * (tap, input channel) runs in ascending order for every output channel, with
  * the output channels as the innermost (vectorisable) loop.  That order is
@@ -58,6 +69,8 @@ typedef struct oc_config {
     int32_t dil[4];
     int32_t final_k;
     float rms_eps;
+    int32_t latent_dim;   /* 0: RVQ code input; L > 0: latent frames of L channels */
+    int32_t tf_up;        /* latent input: depthwise upsampling stride before the transformer */
 } oc_config;
 
 /* ------------------------------------------------------------------ ops -- */
@@ -175,6 +188,28 @@ static void convt_core(const float* a, int T, int Cin, const float* wt, const fl
                 y[(size_t)m * Cout + co] = (float)(acc[co] + (double)b[co]);
         }
         free(acc);
+    }
+}
+
+/*
+ * Causal depthwise ConvTranspose1d, kernel 2s, stride s: a holds 1 + T rows
+ * of C channels, the first being the previous chunk's last input row; each
+ * channel has its own taps u[c][0 .. 2s-1] (PyTorch ConvTranspose1d with
+ * groups = C, weight [C][1][2s]):
+ *   y[n s + p][c] = b[c] + u[c][p + s] a[n-1][c] + u[c][p] a[n][c].
+ */
+static void dwconvt_core(const float* a, int T, int C, const float* u, const float* b, int s, float* y)
+{
+    #pragma omp parallel for schedule(static)
+    for (int64_t m = 0; m < (int64_t)T * s; m++) {
+        const int n = (int)(m / s), p = (int)(m % s);
+        const float* prev = a + (size_t)n * C;
+        const float* cur = a + (size_t)(n + 1) * C;
+        for (int c = 0; c < C; c++) {
+            double v = (double)u[(size_t)c * 2 * s + p + s] * (double)prev[c];
+            v += (double)u[(size_t)c * 2 * s + p] * (double)cur[c];
+            y[(size_t)m * C + c] = (float)(v + (double)b[c]);
+        }
     }
 }
 
@@ -345,6 +380,12 @@ OC_EXPORT void oc_op_causal_conv_t(const float* x, int T, int Cin, const float* 
     free(wt);
 }
 
+/* x: [1 + T][C] (history row first); u: [C][1][2s]. */
+OC_EXPORT void oc_op_dw_conv_t(const float* x, int T, int C, const float* u, const float* b, int s, float* y)
+{
+    dwconvt_core(x, T, C, u, b, s, y);
+}
+
 /* w: [Cout][Cin]. */
 OC_EXPORT void oc_op_linear(const float* x, int T, int Cin, const float* w, int Cout,
                             const float* res, float* y)
@@ -396,6 +437,8 @@ typedef struct oc_model {
     float* blob;              /* private copy of the caller's blob */
     const float* cb[64];
     oc_conv pre;
+    const float *lat_mu, *lat_sigma, *lat_up_u, *lat_up_b;   /* latent input */
+    float* lat_proj;          /* [L][d] transposed */
     oc_layer* layer;
     const float* tf_norm;
     oc_conv up[4];            /* ConvT: k = up_k, dil unused */
@@ -407,6 +450,7 @@ typedef struct oc_model {
 typedef struct oc_state {
     const oc_model* m;
     float* h_pre;             /* [pre_k-1][E] */
+    float* h_lat;             /* latent input: [1][d], the last projected row */
     float** kh;               /* per layer [window-1][d] */
     float** vh;
     float* h_up[4];           /* [1][Cin] */
@@ -419,9 +463,11 @@ typedef struct oc_state {
 
 static int cfg_ok(const oc_config* c)
 {
-    if (c->Q < 1 || c->Q > 64 || c->V < 1 || c->E < 1 || c->pre_k < 1 || c->d < 1) return 0;
+    if (c->latent_dim == 0 && (c->Q < 1 || c->Q > 64 || c->V < 1 || c->E < 1 || c->pre_k < 1)) return 0;
+    if (c->d < 1) return 0;
     if (c->heads < 1 || c->d % c->heads || c->ffn < 1 || c->layers < 0 || c->window < 1) return 0;
-    if (c->n_up < 1 || c->n_up > 4 || c->up_s < 1 || c->up_k != 2 * c->up_s) return 0;
+    if (c->latent_dim < 0 || (c->latent_dim > 0 && c->tf_up < 1)) return 0;
+    if (c->n_up < (c->latent_dim > 0 ? 0 : 1) || c->n_up > 4 || c->up_s < 1 || c->up_k != 2 * c->up_s) return 0;
     if (c->n_stages < 1 || c->n_stages > 8 || c->n_rb < 1 || c->n_rb > 4) return 0;
     if (c->n_dil < 1 || c->n_dil > 4 || c->final_k < 1) return 0;
     return 1;
@@ -429,8 +475,11 @@ static int cfg_ok(const oc_config* c)
 
 static int64_t model_blob_floats(const oc_config* c)
 {
-    int64_t n = (int64_t)c->Q * c->V * c->E;
-    n += (int64_t)c->d * c->E * c->pre_k + c->d;
+    int64_t n;
+    if (c->latent_dim > 0)   /* mu, sigma, projection [d][L], depthwise taps [d][1][2 s], bias [d] */
+        n = 2 * (int64_t)c->latent_dim + (int64_t)c->d * c->latent_dim + (int64_t)c->d * 2 * c->tf_up + c->d;
+    else
+        n = (int64_t)c->Q * c->V * c->E + (int64_t)c->d * c->E * c->pre_k + c->d;
     n += (int64_t)c->layers * (2 * c->d + 4 * (int64_t)c->d * c->d + 2 * (int64_t)c->ffn * c->d);
     n += c->d;
     int cin = c->d;
@@ -461,8 +510,14 @@ OC_EXPORT oc_model* oc_model_create(const oc_config* cfg, const float* blob, int
     memcpy(m->blob, blob, sizeof(float) * (size_t)n_floats);
     const float* p = m->blob;
 #define TAKE(n) (p += (n), p - (n))
-    for (int q = 0; q < c->Q; q++) m->cb[q] = TAKE((int64_t)c->V * c->E);
-    {
+    if (c->latent_dim > 0) {
+        m->lat_mu = TAKE(c->latent_dim);
+        m->lat_sigma = TAKE(c->latent_dim);
+        m->lat_proj = linear_w_t(TAKE((int64_t)c->d * c->latent_dim), c->d, c->latent_dim);
+        m->lat_up_u = TAKE((int64_t)c->d * 2 * c->tf_up);
+        m->lat_up_b = TAKE(c->d);
+    } else {
+        for (int q = 0; q < c->Q; q++) m->cb[q] = TAKE((int64_t)c->V * c->E);
         const float* w = TAKE((int64_t)c->d * c->E * c->pre_k);
         m->pre.wt = conv_w_t(w, c->d, c->E, c->pre_k);
         m->pre.b = TAKE(c->d);
@@ -521,6 +576,7 @@ OC_EXPORT void oc_model_destroy(oc_model* m)
     if (!m) return;
     const oc_config* c = &m->cfg;
     free(m->pre.wt);
+    free(m->lat_proj);
     for (int l = 0; l < c->layers; l++) {
         oc_layer* L = &m->layer[l];
         free(L->wq); free(L->wk); free(L->wv); free(L->wo); free(L->w1); free(L->w2);
@@ -537,7 +593,7 @@ OC_EXPORT void oc_model_destroy(oc_model* m)
 
 static int64_t samples_per_frame(const oc_config* c)
 {
-    int64_t r = 1;
+    int64_t r = c->latent_dim > 0 ? c->tf_up : 1;
     for (int u = 0; u < c->n_up; u++) r *= c->up_s;
     for (int s = 0; s < c->n_stages; s++) r *= c->strides[s];
     return r;
@@ -551,6 +607,7 @@ OC_EXPORT oc_state* oc_state_create(const oc_model* m)
     oc_state* st = (oc_state*)calloc(1, sizeof(oc_state));
     st->m = m;
     st->h_pre = (float*)calloc((size_t)(c->pre_k - 1) * c->E + 1, sizeof(float));
+    st->h_lat = (float*)calloc((size_t)c->d, sizeof(float));
     st->kh = (float**)calloc((size_t)(c->layers + 1), sizeof(float*));
     st->vh = (float**)calloc((size_t)(c->layers + 1), sizeof(float*));
     for (int l = 0; l < c->layers; l++) {
@@ -574,6 +631,7 @@ OC_EXPORT void oc_state_reset(oc_state* st)
     const oc_model* m = st->m;
     const oc_config* c = &m->cfg;
     memset(st->h_pre, 0, sizeof(float) * (size_t)(c->pre_k - 1) * c->E);
+    memset(st->h_lat, 0, sizeof(float) * (size_t)c->d);
     for (int l = 0; l < c->layers; l++) {
         memset(st->kh[l], 0, sizeof(float) * (size_t)(c->window - 1) * c->d);
         memset(st->vh[l], 0, sizeof(float) * (size_t)(c->window - 1) * c->d);
@@ -594,6 +652,7 @@ OC_EXPORT void oc_state_destroy(oc_state* st)
     if (!st) return;
     const oc_config* c = &st->m->cfg;
     free(st->h_pre);
+    free(st->h_lat);
     for (int l = 0; l < c->layers; l++) { free(st->kh[l]); free(st->vh[l]); }
     free(st->kh); free(st->vh);
     for (int u = 0; u < c->n_up; u++) free(st->h_up[u]);
@@ -638,26 +697,17 @@ static void convt_step(const oc_conv* cv, float* hist, const float* x, int64_t n
 }
 
 /*
- * Decode n frames continuing the stream: codes [Q][ld] (columns 0..n-1 used),
- * audio [n * samples_per_frame].  pre_tanh, if not NULL, receives the final
- * conv output before tanh.  Returns the stream's sticky error bits.
+ * The decoder after its front end: h holds `rows` transformer rows [rows][d]
+ * (one per frame for code input, tf_up per frame for latent input), `seen`
+ * the transformer positions the stream had before them.  Runs the
+ * transformer, the latent ConvTs, the stages and the final Snake-conv-tanh,
+ * writing rows * (remaining upsampling) samples.  Takes ownership of h.
  */
-OC_EXPORT uint32_t oc_decode(oc_state* st, const int32_t* codes, int64_t ld, int n, float* audio,
-                             float* pre_tanh)
+static void decode_body(oc_state* st, float* h, int n, int64_t seen, float* audio, float* pre_tanh)
 {
     const oc_model* m = st->m;
     const oc_config* c = &m->cfg;
-    if (n <= 0) return st->err;
     const int d = c->d;
-
-    /* RVQ embedding sum */
-    float* e = (float*)malloc(sizeof(float) * (size_t)n * c->E);
-    st->err |= rvq_core(m->cb, c->Q, c->V, c->E, codes, ld, n, e);
-
-    /* causal pre-conv */
-    float* h = (float*)malloc(sizeof(float) * (size_t)n * d);
-    conv_step(&m->pre, st->h_pre, e, n, NULL, h);
-    free(e);
 
     /* transformer */
     const int W = c->window, Hk = W - 1;
@@ -667,7 +717,6 @@ OC_EXPORT uint32_t oc_decode(oc_state* st, const int32_t* codes, int64_t ld, int
     float* v = (float*)malloc(sizeof(float) * (size_t)n * d);
     float* o = (float*)malloc(sizeof(float) * (size_t)n * d);
     float* f = (float*)malloc(sizeof(float) * (size_t)n * c->ffn);
-    const int64_t seen = st->frames;   /* positions before the chunk */
     const int first = (seen >= Hk) ? 0 : (int)(Hk - seen);
     for (int l = 0; l < c->layers; l++) {
         const oc_layer* L = &m->layer[l];
@@ -744,6 +793,60 @@ OC_EXPORT uint32_t oc_decode(oc_state* st, const int32_t* codes, int64_t ld, int
         audio[i] = (float)tanh((double)y[i]);
     }
     free(y);
+}
+
+/*
+ * Decode n frames continuing the stream: codes [Q][ld] (columns 0..n-1 used),
+ * audio [n * samples_per_frame].  pre_tanh, if not NULL, receives the final
+ * conv output before tanh.  Returns the stream's sticky error bits.
+ */
+OC_EXPORT uint32_t oc_decode(oc_state* st, const int32_t* codes, int64_t ld, int n, float* audio,
+                             float* pre_tanh)
+{
+    const oc_model* m = st->m;
+    const oc_config* c = &m->cfg;
+    if (n <= 0 || c->latent_dim > 0) return st->err;
+
+    /* RVQ embedding sum */
+    float* e = (float*)malloc(sizeof(float) * (size_t)n * c->E);
+    st->err |= rvq_core(m->cb, c->Q, c->V, c->E, codes, ld, n, e);
+
+    /* causal pre-conv */
+    float* h = (float*)malloc(sizeof(float) * (size_t)n * c->d);
+    conv_step(&m->pre, st->h_pre, e, n, NULL, h);
+    free(e);
+
+    decode_body(st, h, n, st->frames, audio, pre_tanh);
+    st->frames += n;
+    return st->err;
+}
+
+/*
+ * Latent-input decoder: n frames of latents [n][L] continuing the stream.
+ *   z = x sigma + mu (per channel), p = Wp z (1x1, no bias), then the causal
+ *   depthwise ConvTranspose1d (stride s = tf_up) with the last projected row of
+ *   the previous chunk as its history: n s rows for the transformer.
+ */
+OC_EXPORT uint32_t oc_decode_latents(oc_state* st, const float* x, int n, float* audio, float* pre_tanh)
+{
+    const oc_model* m = st->m;
+    const oc_config* c = &m->cfg;
+    if (n <= 0 || c->latent_dim <= 0) return st->err;
+    const int L = c->latent_dim, d = c->d, s = c->tf_up;
+    float* z = (float*)malloc(sizeof(float) * (size_t)n * L);
+    for (int64_t i = 0; i < (int64_t)n * L; i++) {
+        const int l = (int)(i % L);
+        z[i] = (float)((double)x[i] * (double)m->lat_sigma[l] + (double)m->lat_mu[l]);
+    }
+    float* pr = (float*)malloc(sizeof(float) * (size_t)n * d);
+    linear_core(z, n, L, m->lat_proj, d, NULL, pr);
+    free(z);
+    float* ext = with_history(st->h_lat, 1, pr, n, d);
+    free(pr);
+    float* h = (float*)malloc(sizeof(float) * (size_t)n * s * d);
+    dwconvt_core(ext, n, d, m->lat_up_u, m->lat_up_b, s, h);
+    free(ext);
+    decode_body(st, h, n * s, st->frames * s, audio, pre_tanh);
     st->frames += n;
     return st->err;
 }

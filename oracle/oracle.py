@@ -44,6 +44,7 @@ class OcConfig(ctypes.Structure):
         ("n_rb", ctypes.c_int32), ("rb_k", ctypes.c_int32 * 4),
         ("n_dil", ctypes.c_int32), ("dil", ctypes.c_int32 * 4),
         ("final_k", ctypes.c_int32), ("rms_eps", ctypes.c_float),
+        ("latent_dim", ctypes.c_int32), ("tf_up", ctypes.c_int32),
     ]
 
 
@@ -66,6 +67,8 @@ def oc_config(cfg) -> OcConfig:
         c.dil[i] = dl
     c.final_k = cfg.final_k
     c.rms_eps = cfg.rms_eps
+    c.latent_dim = cfg.latent_dim
+    c.tf_up = cfg.tf_up
     return c
 
 
@@ -83,6 +86,8 @@ def lib():
             "oc_op_snake": (None, [_F, i64, i32, _F, _F]),
             "oc_op_causal_conv": (None, [_F, i32, i32, _F, _F, i32, i32, i32, _F, _F, _F]),
             "oc_op_causal_conv_t": (None, [_F, i32, i32, _F, _F, i32, i32, _F, _F]),
+            "oc_op_dw_conv_t": (None, [_F, i32, i32, _F, _F, i32, _F]),
+            "oc_decode_latents": (u32, [_V, _F, i32, _F, _F]),
             "oc_op_linear": (None, [_F, i32, i32, _F, i32, _F, _F]),
             "oc_op_rms_norm": (None, [_F, i32, i32, _F, f32, _F]),
             "oc_op_gelu": (None, [_F, i64, _F]),
@@ -147,6 +152,18 @@ def causal_conv_t(x_ext, w, b, stride, alpha=None):
     y = np.empty((T * stride, Cout), np.float32)
     a = None if alpha is None else _c(alpha)
     lib().oc_op_causal_conv_t(_f(x_ext), T, Cin, _f(w), _f(b), Cout, stride, _f(a), _f(y))
+    return y
+
+
+def dw_conv_t(x_ext, u, b, stride):
+    """Causal depthwise transposed conv: x_ext [1 + T][C] (history row first),
+    u [C][1][2*stride] -> [T*stride][C]."""
+    x_ext, u, b = _c(x_ext), _c(u), _c(b)
+    C = x_ext.shape[1]
+    T = x_ext.shape[0] - 1
+    assert u.shape == (C, 1, 2 * stride)
+    y = np.empty((T * stride, C), np.float32)
+    lib().oc_op_dw_conv_t(_f(x_ext), T, C, _f(u), _f(b), stride, _f(y))
     return y
 
 
@@ -222,6 +239,9 @@ class OracleModel:
         s = self.stream()
         return s.decode(codes, pre_tanh=pre_tanh)
 
+    def decode_latents_full(self, latents, pre_tanh=False):
+        return self.stream().decode_latents(latents, pre_tanh=pre_tanh)
+
 
 class OracleStream:
     """One stream's carried state (conv histories, last W-1 keys/values)."""
@@ -245,6 +265,17 @@ class OracleStream:
     @property
     def error(self) -> int:
         return lib().oc_state_error(self._s)
+
+    def decode_latents(self, latents, pre_tanh=False):
+        """latents [n][L] -> audio [n * samples_per_frame] (latent-input decoder)."""
+        x = _c(latents)
+        n = x.shape[0]
+        spf = self.model.samples_per_frame
+        audio = np.empty(n * spf, np.float32)
+        pt = np.empty(n * spf, np.float32) if pre_tanh else None
+        if n:
+            lib().oc_decode_latents(self._s, _f(x), n, _f(audio), _f(pt))
+        return (audio, pt) if pre_tanh else audio
 
     def decode(self, codes, pre_tanh=False):
         """codes [Q][n] -> audio [n * samples_per_frame] (and pre-tanh values)."""

@@ -26,6 +26,17 @@ Blob order (all fp32, PyTorch layouts):
   st.{s}.w, st.{s}.b    [C_s][C_{s+1}][2*stride], [C_{s+1}]
   st.{s}.rb.{j}.{i}.alpha / .w / .b   [C][C][k_j] resblock j, dilation i
   out.alpha, out.w, out.b             [C_4], [1][C_4][final_k], [1]
+
+Latent-input variant (latent_dim L > 0; blixt/phonon "Weights": the codec's
+latent projection, 1x1 without bias, and its depthwise x16 upsampling; the
+codec transformer at the upsampled 200 Hz rate, "Speed" item 7), in place of
+cb.* and pre.*:
+
+  lat.mu, lat.sigma     [L], [L]             denormalisation z = x sigma + mu
+  lat.proj              [d][L]               1x1 projection, no bias
+  lat.up.w, lat.up.b    [d][1][2 tf_up], [d] depthwise ConvTranspose1d (groups = d)
+
+and no latent ConvTs after the transformer (up_channels empty, C_0 = d).
 """
 from __future__ import annotations
 
@@ -59,10 +70,12 @@ class CodecConfig:
     rms_eps: float = 1e-5
     up_k: int = 4
     up_s: int = 2
+    latent_dim: int = 0    # 0: RVQ codes in; L > 0: latent frames of L channels in
+    tf_up: int = 1         # latent input: depthwise upsampling stride before the transformer
 
     @property
     def samples_per_frame(self) -> int:
-        n = 1
+        n = self.tf_up if self.latent_dim else 1
         for _ in self.up_channels:
             n *= self.up_s
         for s in self.strides:
@@ -71,7 +84,13 @@ class CodecConfig:
 
     @property
     def stage_in_channels(self) -> tuple:
-        return (self.up_channels[-1],) + tuple(self.channels[:-1])
+        c0 = self.up_channels[-1] if self.up_channels else self.d
+        return (c0,) + tuple(self.channels[:-1])
+
+    @property
+    def rows_per_frame_tf(self) -> int:
+        """Transformer rows (positions) per frame."""
+        return self.tf_up if self.latent_dim else 1
 
     def replace(self, **kw) -> "CodecConfig":
         return dataclasses.replace(self, **kw)
@@ -96,7 +115,30 @@ def qwen3_config() -> CodecConfig:
         rb_kernels=(3, 7, 11), dilations=(1, 3, 5), final_k=7)
 
 
-CONFIGS = {"tiny": tiny_config, "qwen3": qwen3_config}
+def mimi_config() -> CodecConfig:
+    """Latent-input, Mimi-style decoder (the blixt/phonon codec outline): 32
+    latent channels at 12.5 Hz, denormalised, projected 1x1 to d = 512 and
+    upsampled x16 by a depthwise transposed conv to 200 Hz; 8 transformer
+    layers (8 heads, FFN 2048) with a 251-position window at 200 Hz; stages
+    x5, x4, x3, x2 (200 Hz -> 24 kHz), channels 512 -> 256 -> 128 -> 64 -> 32,
+    one resblock k = 3 with dilations 1, 3, 5 each; final conv k = 7."""
+    return CodecConfig(
+        name="mimi", Q=0, V=0, E=0, pre_k=0, d=512, heads=8, ffn=2048, layers=8, window=251,
+        up_channels=(), strides=(5, 4, 3, 2), channels=(256, 128, 64, 32), rb_kernels=(3,),
+        dilations=(1, 3, 5), final_k=7, latent_dim=32, tf_up=16)
+
+
+def tiny_mimi_config() -> CodecConfig:
+    """The latent-input variant at oracle-check size: L = 16, d = 64, one
+    layer, window 24 (1.5 frames at 16 rows per frame), stages 5, 4, 3, 2 with
+    channels 64 -> 32 -> 16 -> 8 -> 4."""
+    return CodecConfig(
+        name="tiny_mimi", Q=0, V=0, E=0, pre_k=0, d=64, heads=4, ffn=128, layers=1, window=24,
+        up_channels=(), strides=(5, 4, 3, 2), channels=(32, 16, 8, 4), rb_kernels=(3,),
+        dilations=(1, 3, 5), final_k=7, latent_dim=16, tf_up=16)
+
+
+CONFIGS = {"tiny": tiny_config, "qwen3": qwen3_config, "mimi": mimi_config, "tiny_mimi": tiny_mimi_config}
 
 
 @dataclass(frozen=True)
@@ -121,10 +163,18 @@ def weight_manifest(cfg: CodecConfig) -> list:
     def normal(name, shape, fan_in):
         m.append(TensorSpec(name, tuple(shape), "normal", float(fan_in) ** -0.5))
 
-    for q in range(cfg.Q):
-        normal(f"cb.{q}", (cfg.V, cfg.E), cfg.Q)          # sum of Q rows has unit variance
-    normal("pre.w", (cfg.d, cfg.E, cfg.pre_k), cfg.E * cfg.pre_k)
-    normal("pre.b", (cfg.d,), cfg.E * cfg.pre_k)
+    if cfg.latent_dim:
+        L = cfg.latent_dim
+        m.append(TensorSpec("lat.mu", (L,), "normal", 0.1))
+        m.append(TensorSpec("lat.sigma", (L,), "uniform"))
+        normal("lat.proj", (cfg.d, L), L)
+        normal("lat.up.w", (cfg.d, 1, 2 * cfg.tf_up), 2)     # two taps reach each output
+        normal("lat.up.b", (cfg.d,), 2)
+    else:
+        for q in range(cfg.Q):
+            normal(f"cb.{q}", (cfg.V, cfg.E), cfg.Q)          # sum of Q rows has unit variance
+        normal("pre.w", (cfg.d, cfg.E, cfg.pre_k), cfg.E * cfg.pre_k)
+        normal("pre.b", (cfg.d,), cfg.E * cfg.pre_k)
     for l in range(cfg.layers):
         m.append(TensorSpec(f"tf.{l}.n1", (cfg.d,), "gain"))
         for w in ("wq", "wk", "wv", "wo"):
@@ -184,6 +234,13 @@ def pack_blob(cfg: CodecConfig, weights: dict) -> np.ndarray:
             raise ValueError(f"{t.name}: shape {a.shape} != {t.shape}")
         parts.append(a.reshape(-1))
     return np.ascontiguousarray(np.concatenate(parts))
+
+
+def make_latents(cfg: CodecConfig, frames: int, seed: int = 0) -> np.ndarray:
+    """Latent frames float32 [frames][L], standard normal from PCG64(seed)
+    (the normalised latents a flow head would emit)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    return np.ascontiguousarray(rng.standard_normal((frames, cfg.latent_dim)), dtype=np.float32)
 
 
 def make_codes(cfg: CodecConfig, frames: int, seed: int = 0) -> np.ndarray:

@@ -91,6 +91,26 @@ def decode(cfg, W, codes, dtype=torch.float64, taps=None):
     h = causal_conv(e, _t(W["pre.w"], dtype), _t(W["pre.b"], dtype)).t()   # [T][d]
     if taps is not None:
         taps["pre"] = h
+    return _body(cfg, W, h, dtype, taps)
+
+
+def decode_latents(cfg, W, latents, dtype=torch.float64, taps=None):
+    """Latent-input variant, full sequence from an empty state: latents [T][L]
+    -> audio [T*spf].  Denormalise, project 1x1, then the library's grouped
+    (depthwise) conv_transpose1d with the right k - s outputs trimmed."""
+    x = _t(latents, dtype)
+    z = x * _t(W["lat.sigma"], dtype) + _t(W["lat.mu"], dtype)
+    p = _linear(z, _t(W["lat.proj"], dtype))                  # [T][d]
+    T, s = p.shape[0], cfg.tf_up
+    y = F.conv_transpose1d(p.t()[None], _t(W["lat.up.w"], dtype), _t(W["lat.up.b"], dtype), stride=s,
+                           groups=cfg.d)[0]
+    h = y[:, : T * s].t()                                       # [T s][d]
+    if taps is not None:
+        taps["front"] = h
+    return _body(cfg, W, h, dtype, taps)
+
+
+def _body(cfg, W, h, dtype, taps):
     for l in range(cfg.layers):
         p = f"tf.{l}."
         u = rms_norm(h, _t(W[p + "n1"], dtype), cfg.rms_eps)
