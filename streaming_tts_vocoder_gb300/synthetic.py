@@ -292,3 +292,106 @@ def make_f0(frames: int, seed: int, voiced_fraction: float = 0.7) -> np.ndarray:
     f = np.clip(200.0 + np.cumsum(rng.normal(0.0, 8.0, frames)), 80.0, 400.0)
     f[rng.random(frames) >= voiced_fraction] = 0.0
     return f.astype(np.float32)
+
+
+# ------------------------------------------------------------------ Vocos --
+# A Vocos-style generator in front of the streaming iSTFT head (vox: "F5 ->
+# Vocos -> iSTFT"): mel frames -> causal embedding conv -> LayerNorm -> L
+# ConvNeXt blocks (causal depthwise conv, LayerNorm, pointwise MLP with GELU,
+# layer scale, residual) -> LayerNorm -> linear head to n_fft / 2 + 1
+# log-magnitudes and as many phases -> iSTFT.  Shapes follow the public
+# 24 kHz mel model (100 mels, width 512, MLP 1536, 8 blocks, n_fft 1024, hop
+# 256); nothing here holds its arithmetic.
+
+@dataclass(frozen=True)
+class VocosConfig:
+    name: str
+    n_mels: int
+    d: int
+    ffn: int
+    layers: int
+    k: int          # embedding and depthwise kernels
+    n_fft: int
+    hop: int
+    ln_eps: float = 1e-6
+    mag_clip: float = 100.0
+
+    @property
+    def n_bins(self) -> int:
+        return self.n_fft // 2 + 1
+
+
+def vocos_config() -> VocosConfig:
+    return VocosConfig(name="vocos", n_mels=100, d=512, ffn=1536, layers=8, k=7, n_fft=1024, hop=256)
+
+
+def tiny_vocos_config() -> VocosConfig:
+    return VocosConfig(name="tiny_vocos", n_mels=32, d=64, ffn=192, layers=2, k=7, n_fft=64, hop=16)
+
+
+def vocos_manifest(cfg: VocosConfig) -> list:
+    """Tensor list in blob order:
+      embed.w [d][n_mels][k], embed.b [d], norm.g, norm.b [d];
+      per block l: dw.w [d][1][k], dw.b [d], ln.g, ln.b [d], pw1.w [ffn][d], pw1.b [ffn],
+                   pw2.w [d][ffn], pw2.b [d], gamma [d];
+      final.g, final.b [d]; head.w [n_fft + 2][d], head.b [n_fft + 2]."""
+    m = []
+
+    def normal(name, shape, fan_in):
+        m.append(TensorSpec(name, tuple(shape), "normal", float(fan_in) ** -0.5))
+
+    normal("embed.w", (cfg.d, cfg.n_mels, cfg.k), cfg.n_mels * cfg.k)
+    normal("embed.b", (cfg.d,), cfg.n_mels * cfg.k)
+    m.append(TensorSpec("norm.g", (cfg.d,), "gain"))
+    m.append(TensorSpec("norm.b", (cfg.d,), "normal", 0.1))
+    for l in range(cfg.layers):
+        normal(f"blk.{l}.dw.w", (cfg.d, 1, cfg.k), cfg.k)
+        normal(f"blk.{l}.dw.b", (cfg.d,), cfg.k)
+        m.append(TensorSpec(f"blk.{l}.ln.g", (cfg.d,), "gain"))
+        m.append(TensorSpec(f"blk.{l}.ln.b", (cfg.d,), "normal", 0.1))
+        normal(f"blk.{l}.pw1.w", (cfg.ffn, cfg.d), cfg.d)
+        normal(f"blk.{l}.pw1.b", (cfg.ffn,), cfg.d)
+        normal(f"blk.{l}.pw2.w", (cfg.d, cfg.ffn), cfg.ffn)
+        normal(f"blk.{l}.pw2.b", (cfg.d,), cfg.ffn)
+        m.append(TensorSpec(f"blk.{l}.gamma", (cfg.d,), "scale", 1.0 / cfg.layers))
+    m.append(TensorSpec("final.g", (cfg.d,), "gain"))
+    m.append(TensorSpec("final.b", (cfg.d,), "normal", 0.1))
+    normal("head.w", (cfg.n_fft + 2, cfg.d), cfg.d)
+    normal("head.b", (cfg.n_fft + 2,), cfg.d)
+    return m
+
+
+def make_vocos_weights(cfg: VocosConfig, seed: int = 0) -> dict:
+    """Seeded weights in blob order from PCG64(seed); layer scales start at
+    1 / layers (times 1 + 0.1 N(0, 1), so that folding them into the second
+    MLP layer is exercised with distinct values)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    out = {}
+    for t in vocos_manifest(cfg):
+        if t.init == "normal":
+            a = rng.standard_normal(t.shape) * t.std
+        elif t.init == "gain":
+            a = 1.0 + 0.1 * rng.standard_normal(t.shape)
+        elif t.init == "scale":
+            a = t.std * (1.0 + 0.1 * rng.standard_normal(t.shape))
+        else:
+            raise ValueError(t.init)
+        out[t.name] = np.ascontiguousarray(a, dtype=np.float32)
+    return out
+
+
+def pack_vocos_blob(cfg: VocosConfig, weights: dict) -> np.ndarray:
+    parts = []
+    for t in vocos_manifest(cfg):
+        a = np.asarray(weights[t.name], dtype=np.float32)
+        if a.shape != t.shape:
+            raise ValueError(f"{t.name}: shape {a.shape} != {t.shape}")
+        parts.append(a.reshape(-1))
+    return np.ascontiguousarray(np.concatenate(parts))
+
+
+def make_mels(cfg: VocosConfig, frames: int, seed: int = 0) -> np.ndarray:
+    """Log-mel frames float32 [frames][n_mels], N(-5, 2) from PCG64(seed) (the
+    range of natural-log mel magnitudes)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    return np.ascontiguousarray(rng.normal(-5.0, 2.0, (frames, cfg.n_mels)), dtype=np.float32)
