@@ -36,8 +36,9 @@ import numpy as np
 ROOT = Path(__file__).resolve().parent
 sys.path.insert(0, str(ROOT))
 
-from streaming_tts_vocoder_gb300.synthetic import (FRAME_RATE_HZ, make_codes, make_weights, pack_blob,  # noqa: E402
-                                                   qwen3_config, staggered_schedule, tiny_config)
+from streaming_tts_vocoder_gb300.synthetic import (CONFIGS, FRAME_RATE_HZ, make_codes, make_latents,  # noqa: E402
+                                                   make_weights, pack_blob, qwen3_config, staggered_schedule,
+                                                   tiny_config)
 
 METRIC = "codec decode audio-sec/sec at 64 streams (x real time)"
 UNIT = "audio-s/s"
@@ -45,6 +46,10 @@ PEAKS_FILE = ROOT / "MEASURED_PEAKS.json"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "sm_max_mhz": 2070.0}
 SMS = 152
 FP32_LANES_PER_SM = 128
+
+
+DECODER_NAMES = {"qwen3": "Qwen3-TTS-12Hz-shaped", "tiny": "tiny", "mimi": "Mimi-shaped latent-input",
+                 "tiny_mimi": "tiny latent-input"}
 
 
 def peaks():
@@ -61,7 +66,8 @@ def parse():
     ap.add_argument("--steps", type=int, default=3)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--decoder", choices=["qwen3", "tiny"], default="qwen3")
+    ap.add_argument("--decoder", choices=["qwen3", "tiny", "mimi", "tiny_mimi"], default="qwen3",
+                    help="mimi / tiny_mimi: the latent-input variant (codec_decode_latents)")
     ap.add_argument("--precision", choices=["fp32", "fp16x3", "fp16"], default="fp16x3")
     ap.add_argument("--weights", choices=["fp32", "q8"], default="fp32",
                     help="q8: create the codec from the int8-per-32 weight file (codec_create_q8)")
@@ -78,7 +84,7 @@ def parse():
                          "playback gaps) for carried-state and recompute decoding, instead of the throughput line")
     ap.add_argument("--profile-call", default=None, metavar="S,CH,REPS",
                     help="profiling aid: REPS fixed decode calls of S streams x CH frames (graphs off), no timing")
-    ap.add_argument("--workload", choices=["decoder", "istft", "source"], default="decoder",
+    ap.add_argument("--workload", choices=["decoder", "istft", "source", "vocos"], default="decoder",
                     help="istft: the streaming iSTFT head alone (Vocos-shaped: n_fft 1024, hop 256, 24 kHz), "
                          "--streams streams x 10 chunks of 94 frames; source: the harmonic sine source (8 "
                          "harmonics, F0 every 256 samples) and the analysis STFT (n_fft 16, hop 4) on the "
@@ -122,7 +128,7 @@ def job_throughput(units_per_rank: float, ms_max: float, world: int) -> float:
 def config_dict(args, precision):
     return {
         "workload": f"{args.streams} staggered streams x {args.frames} frames, ragged ticks of <= {args.chunk} frames, "
-                    f"{'Qwen3-TTS-12Hz-shaped' if args.decoder == 'qwen3' else 'tiny'} decoder",
+                    f"{DECODER_NAMES[args.decoder]} decoder",
         "decoder": args.decoder,
         "streams": args.streams,
         "frames_per_stream": args.frames,
@@ -220,10 +226,15 @@ def oracle_sample(cfg, blob, frames, seed=1000):
     """Time the CPU oracle decoding `frames` frames of one stream."""
     from oracle import oracle as O
     m = O.OracleModel(cfg, blob)
-    codes = make_codes(cfg, frames, seed)
     s = m.stream()
-    t0 = time.perf_counter()
-    s.decode(codes)
+    if cfg.latent_dim:
+        x = make_latents(cfg, frames, seed)
+        t0 = time.perf_counter()
+        s.decode_latents(x)
+    else:
+        codes = make_codes(cfg, frames, seed)
+        t0 = time.perf_counter()
+        s.decode(codes)
     dt = time.perf_counter() - t0
     return frames / FRAME_RATE_HZ / dt, dt, O.max_threads()
 
@@ -232,17 +243,22 @@ def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
-    cfg = qwen3_config() if args.decoder == "qwen3" else tiny_config()
+    cfg = CONFIGS[args.decoder]()
     blob = pack_blob(cfg, make_weights(cfg, 0))
     from oracle import oracle as O
     m = O.OracleModel(cfg, blob)
-    frames = 25 if args.decoder == "qwen3" else 250
+    frames = {"qwen3": 25, "mimi": 100}.get(args.decoder, 250)
     times = []
     for i in range(args.warmup + args.steps):
         s = m.stream()
-        codes = make_codes(cfg, frames, 1000 + i)
-        t0 = time.perf_counter()
-        s.decode(codes)
+        if cfg.latent_dim:
+            x = make_latents(cfg, frames, 1000 + i)
+            t0 = time.perf_counter()
+            s.decode_latents(x)
+        else:
+            codes = make_codes(cfg, frames, 1000 + i)
+            t0 = time.perf_counter()
+            s.decode(codes)
         dt = time.perf_counter() - t0
         if i >= args.warmup:
             times.append(dt)
@@ -272,10 +288,11 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     from streaming_tts_vocoder_gb300 import codec as C
 
-    cfg = qwen3_config() if args.decoder == "qwen3" else tiny_config()
+    cfg = CONFIGS[args.decoder]()
     prec = {"fp16x3": C.PRECISION_FP16X3, "fp16": C.PRECISION_FP16, "fp32": C.PRECISION_FP32}[args.precision]
     blob = pack_blob(cfg, make_weights(cfg, 0))
     S, F, CH = args.streams, args.frames, args.chunk
+    latent = cfg.latent_dim > 0
     if args.weights == "q8":
         from streaming_tts_vocoder_gb300.weights_q8 import pack_q8
         cod = C.Codec(cfg, q8=pack_q8(cfg, blob), max_streams=S, max_chunk_frames=CH, max_batch_frames=S * CH,
@@ -285,15 +302,20 @@ def run_ours(args):
     st = cod.state()
     spf = cod.samples_per_frame
 
-    # inputs resident in HBM: one codes tensor per tick
-    codes = [make_codes(cfg, F, 1000 + s) for s in range(S)]
+    # inputs resident in HBM: one codes (or latents) tensor per tick
+    codes = [make_latents(cfg, F, 1000 + s) if latent else make_codes(cfg, F, 1000 + s) for s in range(S)]
     ticks = staggered_schedule(S, F, CH)
     tick_inputs = []
     h2d = d2h = 0
     for tick in ticks:
-        arr = np.zeros((len(tick), cfg.Q, CH), np.int32)
-        for b, (s, a, n) in enumerate(tick):
-            arr[b, :, :n] = codes[s][:, a:a + n]
+        if latent:
+            arr = np.zeros((len(tick), CH, cfg.latent_dim), np.float32)
+            for b, (s, a, n) in enumerate(tick):
+                arr[b, :n] = codes[s][a:a + n]
+        else:
+            arr = np.zeros((len(tick), cfg.Q, CH), np.int32)
+            for b, (s, a, n) in enumerate(tick):
+                arr[b, :, :n] = codes[s][:, a:a + n]
         nf = [n for _, _, n in tick]
         ids = [s for s, _, _ in tick]
         tick_inputs.append((torch.from_numpy(arr).to(dev), nf, ids, torch.from_numpy(arr).pin_memory()))
@@ -306,17 +328,34 @@ def run_ours(args):
 
     launches = [0]
 
+    def decode(inp, nf, out, ids):
+        if latent:
+            st.decode_latents(inp, nf, out, stream_ids=ids, stream=stream)
+        else:
+            st.decode(inp, nf, out, stream_ids=ids, stream=stream)
+
     def step():
         st.reset(stream=stream)
         launches[0] += 1
-        for codes_d, nf, ids, _ in tick_inputs:
-            st.decode(codes_d, nf, audio, stream_ids=ids, stream=stream)
+        for inp_d, nf, ids, _ in tick_inputs:
+            decode(inp_d, nf, audio, ids)
             launches[0] += st.last_launches
+
+    lat_d = torch.empty(S, CH, cfg.latent_dim, device=dev) if latent else None
 
     def step_host():
         st.reset(stream=stream)
-        for _, nf, ids, codes_h in tick_inputs:
-            st.decode_host(codes_h, nf, audio_h, stream_ids=ids, stream=stream)
+        for _, nf, ids, inp_h in tick_inputs:
+            if latent:
+                # the public call takes device buffers: copy the latents in, decode, copy the audio out
+                d = lat_d[: inp_h.shape[0]]
+                d.copy_(inp_h, non_blocking=True)
+                decode(d, nf, audio, ids)
+                for b, n in enumerate(nf):
+                    audio_h[b, : n * spf].copy_(audio[b, : n * spf], non_blocking=True)
+                stream.synchronize()
+            else:
+                st.decode_host(inp_h, nf, audio_h, stream_ids=ids, stream=stream)
 
     for _ in range(args.warmup):
         step()
@@ -359,7 +398,10 @@ def run_ours(args):
     # first-audio latency: 1 frame from an empty state
     fa = None
     if args.first_audio_runs > 0:
-        one = torch.from_numpy(np.ascontiguousarray(codes[0][:, :1])).reshape(1, cfg.Q, 1).to(dev)
+        if latent:
+            one = torch.from_numpy(np.ascontiguousarray(codes[0][:1])).reshape(1, 1, cfg.latent_dim).to(dev)
+        else:
+            one = torch.from_numpy(np.ascontiguousarray(codes[0][:, :1])).reshape(1, cfg.Q, 1).to(dev)
         a1 = torch.empty(1, spf, device=dev)
         dev_us, wall_us = [], []
         for i in range(args.first_audio_runs + 5):
@@ -368,7 +410,7 @@ def run_ours(args):
             s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             t0 = time.perf_counter()
             s0.record(stream)
-            st.decode(one, [1], a1, stream_ids=[0], stream=stream)
+            decode(one, [1], a1, [0])
             s1.record(stream)
             s1.synchronize()
             t1 = time.perf_counter()
@@ -389,7 +431,7 @@ def run_ours(args):
                           "floor_us": wbytes / (pk_fa["hbm_gbs"] * 1e9) * 1e6}
 
     streaming = None
-    if rank == 0 and not args.no_streaming:
+    if rank == 0 and not args.no_streaming and not latent:
         streaming = streaming_schedules(cfg, blob, prec, stream)
 
     # roofline of the dominant kernel
@@ -420,13 +462,25 @@ def run_ours(args):
         if name == "gemm_tc":
             # the fp16x3 split issues three MMAs per useful one: the tensor pipe's share of its peak
             roof["issued_frac"] = (3.0 if args.precision == "fp16x3" else 1.0) * achieved / peak
-    kernels = {k: {"launches": v["launches"], "ms": round(v["ms"], 3),
-                   "share": round(v["ms"] / max(1e-9, sum(x["ms"] for x in kstats.values())), 4)}
-               for k, v in kstats.items() if v["launches"]}
+    # per kernel kind: share of device time, and the algorithmic bytes (flops)
+    # over its summed event time against the measured copy bandwidth (tensor peak)
+    kernels = {}
+    tot_ms = max(1e-9, sum(x["ms"] for x in kstats.values()))
+    for k, v in kstats.items():
+        if not v["launches"]:
+            continue
+        e = {"launches": v["launches"], "ms": round(v["ms"], 3), "share": round(v["ms"] / tot_ms, 4)}
+        if v["ms"] > 0:
+            gbs = v["bytes"] / (v["ms"] / 1e3) / 1e9
+            e["gbs"] = round(gbs, 1)
+            e["hbm_frac"] = round(gbs / pk["hbm_gbs"], 4)
+            if k in ("gemm_tc", "gemm_simt"):
+                e["tflops"] = round(v["flops"] / (v["ms"] / 1e3) / 1e12, 2)
+        kernels[k] = e
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
-        frames = 40 if args.decoder == "qwen3" else 400
+        frames = {"qwen3": 40, "mimi": 100}.get(args.decoder, 400)
         v, dt, cores = oracle_sample(cfg, blob, frames)
         cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
                "sample": f"one stream x {frames} frames of the workload's decoder from an empty state ({dt:.1f} s)"}
@@ -598,6 +652,72 @@ def run_istft(args):
                      "traffic": None, "peak_note": f"{pk_src} copy bandwidth",
                      "algorithmic_bytes_per_frame": alg / frames},
         "gpu_launches": args.steps * NCH * 3 + args.steps, "clocks": clocks, "cpu_baseline": cpu}))
+    return 0
+
+
+def run_vocos(args):
+    """Throughput of the streaming Vocos-style generator + iSTFT head (24 kHz
+    shape: 100 mels, width 512, MLP 1536, 8 blocks, n_fft 1024, hop 256): S
+    streams, each 10 chunks of 94 frames (about 1 s of audio), mel frames
+    resident in HBM.  The roofline is the pointwise GEMMs' useful flops over
+    their share of the call, against the sustained tensor peak; the whole
+    call's algorithmic flops per audio second are reported beside it."""
+    import torch
+    from streaming_tts_vocoder_gb300 import codec as C
+    from streaming_tts_vocoder_gb300.synthetic import make_mels, make_vocos_weights, pack_vocos_blob, vocos_config
+    cfg = vocos_config()
+    S, CH, NCH = args.streams, 94, 10
+    prec = {"fp16x3": C.PRECISION_FP16X3, "fp16": C.PRECISION_FP16, "fp32": C.PRECISION_FP32}[args.precision]
+    W = make_vocos_weights(cfg, 0)
+    voc = C.Vocos(cfg, pack_vocos_blob(cfg, W), max_streams=S, max_chunk_frames=CH, max_batch_frames=S * CH,
+                  precision=prec)
+    dev = torch.device("cuda")
+    stream = torch.cuda.current_stream()
+    mel = torch.from_numpy(np.stack([make_mels(cfg, CH * NCH, 3000 + s) for s in range(S)])).to(dev)
+    chunks = [mel[:, c * CH:(c + 1) * CH].contiguous() for c in range(NCH)]
+    audio = torch.empty(S, CH * cfg.hop, device=dev)
+
+    def step():
+        voc.reset(stream=stream)
+        for c in range(NCH):
+            voc.decode(chunks[c], [CH] * S, audio, stream=stream)
+
+    clk = ClockSampler(torch.cuda.current_device())
+    clk.start()
+    ms = timed_steps(step, args.steps, max(3, args.warmup), stream)
+    clocks = clk.stop()
+    sr = 24000
+    frames = S * CH * NCH
+    audio_s = frames * cfg.hop / sr
+    d, F, H = cfg.d, cfg.ffn, cfg.n_fft + 2
+    flops_frame = 2.0 * (cfg.k * cfg.n_mels * d + cfg.layers * 2 * d * F + d * H)
+    cpu = None
+    if not args.no_cpu:
+        from oracle import vocos as OV
+        sample = make_mels(cfg, 8, 3000)
+        t0 = time.perf_counter()
+        OV.decode_full(cfg, W, sample)
+        dt = time.perf_counter() - t0
+        cpu = {"value": 8 * cfg.hop / sr / dt, "unit": "audio-s/s", "cores": 1, "kind": "oracle",
+               "sample": f"one stream x 8 frames from an empty state ({dt:.1f} s)"}
+    pk, pk_src = peaks()
+    achieved = flops_frame * frames / (ms / 1e3) / 1e12
+    print(json.dumps({
+        "metric": "Vocos-style generator + iSTFT head audio-sec/sec", "value": audio_s / (ms / 1e3),
+        "unit": "audio-s/s", "n_gpus": 1, "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": {"fp32": "f32", "fp16x3": "fp16x3 (pointwise layers), f32 elsewhere", "fp16": "fp16"}[args.precision],
+        "data": "synthetic (seeded log-mel frames, random weights)",
+        "config": {"workload": f"{S} streams x {NCH} chunks of {CH} frames, 24 kHz Vocos shape (100 mels, "
+                               f"d 512, MLP 1536, 8 blocks, n_fft 1024, hop 256)",
+                   "l2": "a 256 MB buffer is written before each step"},
+        "frames_per_s": frames / (ms / 1e3),
+        "roofline": {"bound": "tensor", "kernel": "whole call (algorithmic flops over call time)",
+                     "achieved": achieved, "peak": pk.get("bf16_tflops_sustained", pk["bf16_tflops"]),
+                     "unit": "TFLOP/s", "frac": achieved / pk.get("bf16_tflops_sustained", pk["bf16_tflops"]),
+                     "traffic": None, "peak_note": f"{pk_src} sustained bf16",
+                     "algorithmic_flops_per_frame": flops_frame},
+        "gpu_launches": None, "clocks": clocks, "cpu_baseline": cpu}))
     return 0
 
 
@@ -814,6 +934,8 @@ def main():
         return run_istft(args)
     if args.workload == "source":
         return run_source(args)
+    if args.workload == "vocos":
+        return run_vocos(args)
     if args.schedule:
         return run_schedule(args)
     return run_ours(args)

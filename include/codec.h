@@ -85,7 +85,7 @@ typedef struct codec_config {
     int32_t Q, V, E;          /* codebooks, entries per codebook, codebook width */
     int32_t pre_k;            /* kernel of the causal Conv1d E -> d */
     int32_t d, heads, ffn;    /* transformer width, heads (d % heads == 0), MLP width */
-    int32_t layers, window;   /* transformer layers; keys per query (itself included) */
+    int32_t layers, window;   /* transformer layers; keys per query (itself included), 1..256 */
     int32_t n_up, up_k, up_s; /* latent transposed convs: count (1..4), kernel, stride; up_k == 2*up_s */
     int32_t up_ch[4];         /* their output channels; up_ch[n_up-1] = C_0 */
     int32_t n_stages;         /* BigVGAN stages (1..8) */
@@ -101,6 +101,15 @@ typedef struct codec_config {
     int32_t max_chunk_frames; /* largest n_frames[b] accepted in one call (>= 1) */
     int32_t max_batch_frames; /* largest sum of n_frames over one call (>= max_chunk_frames) */
     int32_t precision;        /* codec_precision */
+    /* Latent-input variant (blixt/phonon "Weights", "Speed" item 7): 0 for RVQ
+     * code input (Q, V, E, pre_k as above).  L > 0 (a multiple of 4): frames
+     * of L continuous latent channels come in (codec_decode_latents), are
+     * denormalised, projected 1x1 to d and upsampled tf_up times by a causal
+     * depthwise transposed conv (kernel 2 tf_up); the transformer then runs
+     * at tf_up rows per frame (window and positions count those rows), and
+     * n_up may be 0 (C_0 = d).  Q, V, E, pre_k are ignored. */
+    int32_t latent_dim;
+    int32_t tf_up;            /* latent input: 1..64 */
 } codec_config;
 
 typedef struct codec_stream_info {
@@ -122,7 +131,10 @@ typedef struct codec_state_s codec_state_t;
  *   per stage: Snake alpha [Cin], ConvT weight [Cin][Cout][2 s], bias [Cout],
  *     then per resblock j, per dilation i: Snake alpha [C], conv weight
  *     [C][C][rb_k[j]], bias [C];
- *   final Snake alpha [C_n], conv weight [1][C_n][final_k], bias [1]. */
+ *   final Snake alpha [C_n], conv weight [1][C_n][final_k], bias [1].
+ * Latent input: in place of the codebooks and the pre-conv, mu [L], sigma
+ *   [L] (z = x sigma + mu), projection [d][L] (1x1, no bias), depthwise
+ *   transposed-conv taps [d][1][2 tf_up], bias [d]. */
 CODEC_API int64_t codec_weight_floats(const codec_config* cfg);
 
 /* Validate cfg, repack the weights for the kernels and upload them to the
@@ -195,13 +207,26 @@ CODEC_API codec_status codec_state_reset(codec_state_t* state, const int32_t* st
  * caller keeps codes and audio alive until that work completes.
  * Errors (nothing enqueued): CODEC_ERR_NULL, CODEC_ERR_ARG (B < 1, T_max < 1,
  * n_frames out of range, slot id out of range or repeated),
- * CODEC_ERR_CAPACITY; CODEC_ERR_CUDA if a launch fails.
+ * CODEC_ERR_CAPACITY, CODEC_ERR_CONFIG (a latent-input codec);
+ * CODEC_ERR_CUDA if a launch fails.
  * Codes outside [0, V) do not fail the call: they set the stream's sticky
  * CODEC_STREAM_ERR_BAD_CODE bit and that frame's embedding is zero.
  */
 CODEC_API codec_status codec_decode_chunk(codec_state_t* state, const int32_t* codes, const int32_t* n_frames,
                                 const int32_t* stream_ids, int32_t B, int32_t T_max, float* audio,
                                 void* stream);
+
+/* codec_decode_chunk for the latent-input variant (cfg.latent_dim = L > 0;
+ * else CODEC_ERR_CONFIG): latents device float [B][T_max][L], stream b's
+ * frames are rows 0 .. n_frames[b] - 1 of batch entry b.  The front end
+ * (denormalise, 1x1 projection folded into the depthwise upsampling's phase
+ * GEMM) replaces the codebook sum and the pre-conv; everything else,
+ * arguments, errors and the carried state included, is as codec_decode_chunk.
+ * pre_tanh as in codec_decode_chunk_ex (may be NULL).  Chunks of any sizes
+ * share one state (blixt/phonon "Speed" item 7: chunks of 1, 2, 4, 8 frames). */
+CODEC_API codec_status codec_decode_latents(codec_state_t* state, const float* latents, const int32_t* n_frames,
+                                            const int32_t* stream_ids, int32_t B, int32_t T_max, float* audio,
+                                            float* pre_tanh, void* stream);
 
 /* As codec_decode_chunk, and also writes the final conv's output before tanh
  * to pre_tanh (device float, same layout as audio; may be NULL).  For
@@ -540,6 +565,54 @@ CODEC_API codec_status codec_stft_reset(codec_stft_t* stft, const int32_t* strea
 CODEC_API codec_status codec_stft_decode(codec_stft_t* stft, const float* x, const int32_t* n_frames,
                                          const int32_t* stream_ids, int32_t B, int32_t T_max, float* spec,
                                          void* stream);
+
+/*
+ * Streaming Vocos-style generator in front of the iSTFT head (vox, "How each
+ * model runs": F5-TTS ends in "Vocos -> iSTFT"), causal like the decoder:
+ *   h = LayerNorm(conv_k(mel) + b)                          (embedding, causal)
+ *   per block: h = h + gamma * (W2 GELU(W1 LayerNorm(dwconv_k(h) + b_dw) + b1) + b2)
+ *   spec = W_head LayerNorm(h) + b_head: n_fft / 2 + 1 log-magnitudes, then
+ *   as many phases; audio = the streaming iSTFT head above (mag_clip).
+ * LayerNorm over the channels with biased variance, eps inside the root;
+ * GELU in its erf form; dwconv a per-channel causal conv.  Each stream carries
+ * the embedding conv's last k - 1 mel rows, each block's last k - 1 input rows
+ * and the head's frames, so chunked decoding equals a full decode.  The
+ * pointwise layers run on the tcgen05 fp16x3 path when precision asks for it
+ * and their channel counts allow (the layer scale folded into W2 and b2); the
+ * rest in fp32.
+ */
+typedef struct codec_vocos_config {
+    int32_t n_mels, d, ffn, layers;   /* multiples of 4; d <= 1024 */
+    int32_t k;                        /* embedding and depthwise kernel, 1..16 */
+    int32_t n_fft, hop;               /* as codec_istft_config */
+    float ln_eps, mag_clip;
+    int32_t max_streams, max_chunk_frames, max_batch_frames;
+    int32_t precision;                /* codec_precision */
+} codec_vocos_config;
+
+typedef struct codec_vocos_s codec_vocos_t;
+
+/* Weight blob (fp32, PyTorch layouts) in this order: embedding conv [d][n_mels][k],
+ * bias [d]; LayerNorm gain, bias [d]; per block: depthwise taps [d][1][k], bias [d],
+ * LayerNorm gain, bias [d], W1 [ffn][d], b1 [ffn], W2 [d][ffn], b2 [d], layer scale
+ * [d]; final LayerNorm gain, bias [d]; head [n_fft + 2][d], bias [n_fft + 2].
+ * Returns its length in floats, or -1 for an invalid config. */
+CODEC_API int64_t codec_vocos_weight_floats(const codec_vocos_config* cfg);
+
+/* Allocates everything on the current device (slots reset).  One host thread
+ * and one stream at a time per object.  Errors as codec_create. */
+CODEC_API codec_status codec_vocos_create(const codec_vocos_config* cfg, const float* weights, int64_t n_floats,
+                                          codec_vocos_t** out);
+CODEC_API void codec_vocos_destroy(codec_vocos_t* vocos);
+CODEC_API codec_status codec_vocos_reset(codec_vocos_t* vocos, const int32_t* stream_ids, int32_t n, void* stream);
+
+/* mel: device float [B][T_max][n_mels] (entry b's first n_frames[b] frames);
+ * n_frames, stream_ids: host [B] (ids distinct, NULL: 0 .. B-1); audio: device
+ * float [B][T_max hop], entry b's first n_frames[b] hop samples written.
+ * Argument errors (as codec_decode_chunk) return before anything is enqueued. */
+CODEC_API codec_status codec_vocos_decode(codec_vocos_t* vocos, const float* mel, const int32_t* n_frames,
+                                          const int32_t* stream_ids, int32_t B, int32_t T_max, float* audio,
+                                          void* stream);
 
 /* Static description of a status code. */
 CODEC_API const char* codec_status_string(codec_status status);

@@ -47,6 +47,7 @@ class CodecConfigC(ctypes.Structure):
         ("final_k", ctypes.c_int32), ("rms_eps", ctypes.c_float),
         ("max_streams", ctypes.c_int32), ("max_chunk_frames", ctypes.c_int32),
         ("max_batch_frames", ctypes.c_int32), ("precision", ctypes.c_int32),
+        ("latent_dim", ctypes.c_int32), ("tf_up", ctypes.c_int32),
     ]
 
 
@@ -114,6 +115,14 @@ def schedule_chunks(schedule: ChunkScheduleC, total_frames: int) -> list:
     return out
 
 
+class VocosConfigC(ctypes.Structure):
+    _fields_ = [("n_mels", ctypes.c_int32), ("d", ctypes.c_int32), ("ffn", ctypes.c_int32),
+                ("layers", ctypes.c_int32), ("k", ctypes.c_int32), ("n_fft", ctypes.c_int32),
+                ("hop", ctypes.c_int32), ("ln_eps", ctypes.c_float), ("mag_clip", ctypes.c_float),
+                ("max_streams", ctypes.c_int32), ("max_chunk_frames", ctypes.c_int32),
+                ("max_batch_frames", ctypes.c_int32), ("precision", ctypes.c_int32)]
+
+
 class StreamInfoC(ctypes.Structure):
     _fields_ = [("frames_decoded", ctypes.c_int64), ("error_bits", ctypes.c_uint32),
                 ("reserved", ctypes.c_int32)]
@@ -144,6 +153,7 @@ def _lib():
             "codec_state_reset": (i32, [_P, _I32P, i32, _P]),
             "codec_decode_chunk": (i32, [_P, _P, _I32P, _I32P, i32, i32, _P, _P]),
             "codec_decode_chunk_ex": (i32, [_P, _P, _I32P, _I32P, i32, i32, _P, _P, _P]),
+            "codec_decode_latents": (i32, [_P, _P, _I32P, _I32P, i32, i32, _P, _P, _P]),
             "codec_decode_chunk_host": (i32, [_P, _P, _I32P, _I32P, i32, i32, _P, _P]),
             "codec_decode_recompute": (i32, [_P, _P, _I32P, _I32P, _I32P, i32, i32, _P, _P, _P]),
             "codec_chunk_frames": (i32, [ctypes.POINTER(ChunkScheduleC), i32, i64]),
@@ -168,6 +178,12 @@ def _lib():
             "codec_sine_destroy": (None, [_P]),
             "codec_sine_reset": (i32, [_P, _I32P, i32, _P]),
             "codec_sine_decode": (i32, [_P, _P, _I32P, _I32P, i32, i32, _P, _P]),
+            "codec_vocos_weight_floats": (i64, [ctypes.POINTER(VocosConfigC)]),
+            "codec_vocos_create": (i32, [ctypes.POINTER(VocosConfigC), ctypes.POINTER(ctypes.c_float), i64,
+                                         ctypes.POINTER(_P)]),
+            "codec_vocos_destroy": (None, [_P]),
+            "codec_vocos_reset": (i32, [_P, _I32P, i32, _P]),
+            "codec_vocos_decode": (i32, [_P, _P, _I32P, _I32P, i32, i32, _P, _P]),
             "codec_stft_create": (i32, [ctypes.POINTER(StftConfigC), ctypes.POINTER(_P)]),
             "codec_stft_destroy": (None, [_P]),
             "codec_stft_reset": (i32, [_P, _I32P, i32, _P]),
@@ -212,6 +228,8 @@ def config_c(cfg, max_streams=1, max_chunk_frames=97, max_batch_frames=None,
     c.max_chunk_frames = max_chunk_frames
     c.max_batch_frames = max_batch_frames if max_batch_frames is not None else max_chunk_frames * max_streams
     c.precision = precision
+    c.latent_dim = cfg.latent_dim
+    c.tf_up = cfg.tf_up
     return c
 
 
@@ -274,6 +292,66 @@ def conv1d_noalloc_timed_out(stream=None) -> bool:
     _check(_lib().codec_conv1d_noalloc_status(ctypes.byref(flag), _stream_handle(stream)),
            "codec_conv1d_noalloc_status")
     return bool(flag.value)
+
+
+def vocos_config_c(cfg, max_streams=1, max_chunk_frames=64, max_batch_frames=None, precision=PRECISION_FP32):
+    c = VocosConfigC()
+    c.n_mels, c.d, c.ffn, c.layers, c.k = cfg.n_mels, cfg.d, cfg.ffn, cfg.layers, cfg.k
+    c.n_fft, c.hop, c.ln_eps, c.mag_clip = cfg.n_fft, cfg.hop, cfg.ln_eps, cfg.mag_clip
+    c.max_streams, c.max_chunk_frames = max_streams, max_chunk_frames
+    c.max_batch_frames = max_batch_frames if max_batch_frames is not None else max_streams * max_chunk_frames
+    c.precision = precision
+    return c
+
+
+def vocos_weight_floats(cfg_c) -> int:
+    return _lib().codec_vocos_weight_floats(ctypes.byref(cfg_c))
+
+
+class Vocos:
+    """codec_vocos_*: the streaming Vocos-style generator + iSTFT head."""
+
+    def __init__(self, cfg, blob, max_streams=1, max_chunk_frames=64, max_batch_frames=None,
+                 precision=PRECISION_FP32):
+        self.cfg = cfg
+        self.cfg_c = vocos_config_c(cfg, max_streams, max_chunk_frames, max_batch_frames, precision)
+        blob = np.ascontiguousarray(blob, dtype=np.float32)
+        h = _P()
+        _check(_lib().codec_vocos_create(ctypes.byref(self.cfg_c), blob.ctypes.data_as(ctypes.POINTER(ctypes.c_float)),
+                                         blob.size, ctypes.byref(h)), "codec_vocos_create")
+        self._h = h
+
+    def close(self):
+        if getattr(self, "_h", None):
+            _lib().codec_vocos_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        self.close()
+
+    def reset(self, stream_ids=None, stream=None):
+        if stream_ids is None:
+            _check(_lib().codec_vocos_reset(self._h, None, 0, _stream_handle(stream)), "codec_vocos_reset")
+        else:
+            ids = np.ascontiguousarray(stream_ids, dtype=np.int32)
+            _check(_lib().codec_vocos_reset(self._h, ids.ctypes.data_as(_I32P), ids.size, _stream_handle(stream)),
+                   "codec_vocos_reset")
+
+    def decode(self, mel, n_frames, audio, stream_ids=None, stream=None):
+        """mel: contiguous float32 CUDA [B][T_max][n_mels]; audio: float32 CUDA
+        [B][T_max hop]; n_frames, stream_ids: host sequences of length B."""
+        B, T_max, nm = mel.shape
+        nf = np.ascontiguousarray(n_frames, dtype=np.int32)
+        ids = None if stream_ids is None else np.ascontiguousarray(stream_ids, dtype=np.int32)
+        if nf.size != B or (ids is not None and ids.size != B):
+            raise ValueError("n_frames / stream_ids must have one entry per batch row")
+        if nm != self.cfg.n_mels or not (mel.is_cuda and mel.is_contiguous() and str(mel.dtype) == "torch.float32"):
+            raise ValueError(f"mel must be a contiguous float32 CUDA tensor [B][T_max][{self.cfg.n_mels}]")
+        if not (audio.is_cuda and audio.is_contiguous() and audio.numel() >= B * T_max * self.cfg.hop):
+            raise ValueError("audio must be a contiguous float32 CUDA tensor of B * T_max * hop values")
+        ids_p = None if ids is None else ids.ctypes.data_as(_I32P)
+        _check(_lib().codec_vocos_decode(self._h, _ptr(mel), nf.ctypes.data_as(_I32P), ids_p, B, T_max, _ptr(audio),
+                                         _stream_handle(stream)), "codec_vocos_decode")
 
 
 class Istft:
@@ -471,6 +549,25 @@ class CodecState:
             s = _lib().codec_decode_chunk_ex(self._h, _ptr(codes), nf.ctypes.data_as(_I32P), ids_p, B, T_max,
                                              _ptr(audio), _ptr(pre_tanh), st)
         _check(s, "codec_decode_chunk")
+
+    def decode_latents(self, latents, n_frames, audio, stream_ids=None, pre_tanh=None, stream=None):
+        """codec_decode_latents: latents device float32 [B][T_max][L]; audio
+        device float32 [B][T_max * spf]; n_frames and stream_ids host, length B."""
+        B, T_max, L = latents.shape
+        nf = np.ascontiguousarray(n_frames, dtype=np.int32)
+        ids = None if stream_ids is None else np.ascontiguousarray(stream_ids, dtype=np.int32)
+        if nf.size != B or (ids is not None and ids.size != B):
+            raise ValueError("n_frames / stream_ids must have one entry per batch row")
+        if not (latents.is_cuda and str(latents.dtype) == "torch.float32" and latents.is_contiguous()):
+            raise ValueError("latents must be a contiguous float32 CUDA tensor")
+        if L != self.codec.cfg.latent_dim:
+            raise ValueError(f"latents must have {self.codec.cfg.latent_dim} channels")
+        if not (audio.is_cuda and audio.is_contiguous() and audio.numel() >= B * T_max * self.codec.samples_per_frame):
+            raise ValueError("audio must be a contiguous float32 CUDA tensor of B * T_max * spf values")
+        ids_p = None if ids is None else ids.ctypes.data_as(_I32P)
+        pt = None if pre_tanh is None else _ptr(pre_tanh)
+        _check(_lib().codec_decode_latents(self._h, _ptr(latents), nf.ctypes.data_as(_I32P), ids_p, B, T_max,
+                                           _ptr(audio), pt, _stream_handle(stream)), "codec_decode_latents")
 
     def decode_recompute(self, codes, n_ctx, n_new, audio, stream_ids=None, pre_tanh=None, stream=None):
         """codec_decode_recompute: per entry, reset its slot, decode n_ctx + n_new

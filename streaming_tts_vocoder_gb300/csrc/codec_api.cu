@@ -75,8 +75,13 @@ struct codec_s {
     int n_levels = 0;
     int level_r[16] = {};
     int num_sms = 0;
+    int lvl_tf = 0;                // level of the transformer rows: 0 (code input) or 1 (latent input)
+    int r_tf = 1;                  // transformer rows (positions) per frame
     float* cb = nullptr;
-    Contraction pre;
+    Contraction pre;               // code input: the causal pre-conv; latent input: the folded
+                                   // projection + depthwise upsampling phase GEMM
+    float* lat_mu = nullptr;       // latent input: denormalisation
+    float* lat_sigma = nullptr;
     std::vector<LayerW> layers;
     float* tf_norm = nullptr;
     Contraction up[4];
@@ -145,11 +150,17 @@ namespace {
 bool cfg_valid(const codec_config* c)
 {
     auto m4 = [](int v) { return v > 0 && v % 4 == 0; };
-    if (c->Q < 1 || c->Q > 64 || c->V < 1 || !m4(c->E)) return false;
-    if (c->pre_k < 1 || c->pre_k > kMaxTaps) return false;
+    const bool latent = c->latent_dim != 0;
+    if (latent) {
+        if (!m4(c->latent_dim) || c->tf_up < 1 || c->tf_up > 64) return false;
+    } else {
+        if (c->Q < 1 || c->Q > 64 || c->V < 1 || !m4(c->E)) return false;
+        if (c->pre_k < 1 || c->pre_k > kMaxTaps) return false;
+    }
     if (!m4(c->d) || c->heads < 1 || c->d % c->heads || c->d / c->heads > 128) return false;
-    if (!m4(c->ffn) || c->layers < 0 || c->layers > 64 || c->window < 1 || c->window > 128) return false;
-    if (c->n_up < 1 || c->n_up > 4 || c->up_s < 1 || c->up_k != 2 * c->up_s) return false;
+    if (!m4(c->ffn) || c->layers < 0 || c->layers > 64 || c->window < 1 || c->window > kSwaWindowMax) return false;
+    if (swa_smem_bytes(c->d / c->heads, c->window) > kSwaSmemMax) return false;
+    if (c->n_up < (latent ? 0 : 1) || c->n_up > 4 || c->up_s < 1 || c->up_k != 2 * c->up_s) return false;
     for (int u = 0; u < c->n_up; u++) if (!m4(c->up_ch[u])) return false;
     if (c->n_stages < 1 || c->n_stages > 8) return false;
     for (int s = 0; s < c->n_stages; s++) if (c->strides[s] < 1 || !m4(c->ch[s])) return false;
@@ -157,12 +168,15 @@ bool cfg_valid(const codec_config* c)
     for (int j = 0; j < c->n_rb; j++) if (c->rb_k[j] < 1 || c->rb_k[j] > kMaxTaps) return false;
     for (int i = 0; i < c->n_dil; i++) if (c->dil[i] < 1 || c->dil[i] > 64) return false;
     if (c->final_k < 1 || c->final_k > kMaxTaps) return false;
+    if (c->n_stages >= 1 && c->n_stages <= 8 &&
+        final_conv_smem_bytes(c->ch[c->n_stages - 1], c->final_k) > kFinalSmemMax)
+        return false;
     if (!(c->rms_eps > 0.f)) return false;
     if (c->max_streams < 1 || c->max_chunk_frames < 1 || c->max_batch_frames < c->max_chunk_frames) return false;
     if (c->precision != CODEC_PRECISION_FP32 && c->precision != CODEC_PRECISION_FP16X3 &&
         c->precision != CODEC_PRECISION_FP16)
         return false;
-    long long spf = 1;
+    long long spf = latent ? c->tf_up : 1;
     for (int u = 0; u < c->n_up; u++) spf *= c->up_s;
     for (int s = 0; s < c->n_stages; s++) spf *= c->strides[s];
     if (spf > (1 << 20)) return false;
@@ -172,8 +186,11 @@ bool cfg_valid(const codec_config* c)
 
 long long blob_floats(const codec_config* c)
 {
-    long long n = (long long)c->Q * c->V * c->E;
-    n += (long long)c->d * c->E * c->pre_k + c->d;
+    long long n;
+    if (c->latent_dim)   // mu, sigma, projection [d][L], depthwise taps [d][1][2 tf_up], bias [d]
+        n = 2LL * c->latent_dim + (long long)c->d * c->latent_dim + (long long)c->d * 2 * c->tf_up + c->d;
+    else
+        n = (long long)c->Q * c->V * c->E + (long long)c->d * c->E * c->pre_k + c->d;
     n += (long long)c->layers * (2LL * c->d + 4LL * c->d * c->d + 2LL * c->ffn * c->d);
     n += c->d;
     long long cin = c->d;
@@ -274,6 +291,30 @@ void make_convt(codec_s* c, Contraction& C, const float* w, const float* b, cons
     finish_contraction(c, C, p, b, Cout, alpha, st);
 }
 
+// Latent front end: the 1x1 projection Wp [d][L] folded into the causal
+// depthwise transposed conv u [d][1][2s] (blixt/phonon "Weights": the
+// projection merged into the upsampling weights), as one phase GEMM
+// [2 L][s d] over [z[n-1] | z[n]] (z = the denormalised latents):
+//   y[n s + p][c] = b[c] + sum_l u[c][p+s] Wp[c][l] z[n-1][l] + u[c][p] Wp[c][l] z[n][l].
+// The folded products are formed in double and rounded once.
+void make_front(codec_s* c, Contraction& C, const float* Wp, const float* u, const float* b, int L, int d, int s,
+                codec_status& st)
+{
+    C.Cin = L; C.N = s * d; C.ntaps = 2;
+    C.shift[0] = 1;
+    C.shift[1] = 0;
+    std::vector<float> p((size_t)2 * L * s * d);
+    for (int l = 0; l < L; l++)
+        for (int ph = 0; ph < s; ph++)
+            for (int ch = 0; ch < d; ch++) {
+                const size_t n = (size_t)ph * d + ch;
+                const double w = Wp[(size_t)ch * L + l];
+                p[(size_t)l * C.N + n] = (float)((double)u[(size_t)ch * 2 * s + ph + s] * w);
+                p[((size_t)L + l) * C.N + n] = (float)((double)u[(size_t)ch * 2 * s + ph] * w);
+            }
+    finish_contraction(c, C, p, b, d, nullptr, st);
+}
+
 // Linear weights [Cout][Cin] (several concatenated along Cout) -> [Cin][sum Cout].
 void make_linear(codec_s* c, Contraction& C, std::vector<const float*> ws, int Cin, int Cout_each,
                  codec_status& st)
@@ -346,13 +387,27 @@ codec_status codec_create(const codec_config* cfg, const float* weights, int64_t
     c->spf = 1;
     c->level_r[0] = 1;
     c->n_levels = 1;
+    if (g.latent_dim) {
+        c->lvl_tf = 1;
+        c->r_tf = g.tf_up;
+        c->spf = g.tf_up;
+        c->level_r[c->n_levels++] = c->spf;
+    }
     for (int u = 0; u < g.n_up; u++) { c->spf *= g.up_s; c->level_r[c->n_levels++] = c->spf; }
     for (int s = 0; s < g.n_stages; s++) { c->spf *= g.strides[s]; c->level_r[c->n_levels++] = c->spf; }
 
     const float* p = weights;
     auto take = [&](long long n) { const float* r = p; p += n; return r; };
-    c->cb = dev_upload(c->allocs, take((long long)g.Q * g.V * g.E), (size_t)g.Q * g.V * g.E, st);
-    {
+    if (g.latent_dim) {
+        const int L = g.latent_dim;
+        c->lat_mu = dev_upload(c->allocs, take(L), (size_t)L, st);
+        c->lat_sigma = dev_upload(c->allocs, take(L), (size_t)L, st);
+        const float* wp = take((long long)g.d * L);
+        const float* u = take((long long)g.d * 2 * g.tf_up);
+        const float* b = take(g.d);
+        make_front(c, c->pre, wp, u, b, L, g.d, g.tf_up, st);
+    } else {
+        c->cb = dev_upload(c->allocs, take((long long)g.Q * g.V * g.E), (size_t)g.Q * g.V * g.E, st);
         const float* w = take((long long)g.d * g.E * g.pre_k);
         const float* b = take(g.d);
         make_conv(c, c->pre, w, b, nullptr, g.E, g.d, g.pre_k, 1, st);
@@ -448,32 +503,35 @@ codec_status codec_state_create(codec_t* c, int32_t n_streams, codec_state_t** o
     const int S = s->n_slots;
     codec_status st = CODEC_OK;
 
-    // per-level history rows in front of every segment
+    // per-level history rows in front of every segment; the transformer's
+    // level (0, or 1 behind the latent front end) feeds the first ConvT
     const int last = c->n_levels - 1;
-    s->P[0] = std::max(g.pre_k - 1, 1);
-    for (int u = 0; u < g.n_up; u++) s->P[1 + u] = 1;
+    const int lt = c->lvl_tf;
+    s->P[0] = g.latent_dim ? 1 : std::max(g.pre_k - 1, 1);
+    s->P[lt] = std::max(s->P[lt], 1);
+    for (int u = 0; u < g.n_up; u++) s->P[lt + 1 + u] = 1;
     for (int si = 0; si < g.n_stages; si++) {
         int P = 1;
         for (int j = 0; j < g.n_rb; j++)
             for (int i = 0; i < g.n_dil; i++) P = std::max(P, (g.rb_k[j] - 1) * g.dil[i]);
         if (si == g.n_stages - 1) P = std::max(P, g.final_k - 1);
-        s->P[g.n_up + 1 + si] = P;
+        s->P[lt + g.n_up + 1 + si] = P;
     }
     auto rows = [&](int lvl, bool pref) {
         return (size_t)g.max_batch_frames * c->level_r[lvl] + (pref ? (size_t)S * s->P[lvl] : 0);
     };
     auto& A = s->allocs;
-    const size_t r0 = rows(0, false);
-    s->e = dev_alloc<float>(A, rows(0, true) * g.E, st);
+    const size_t r0 = rows(lt, false);
+    s->e = dev_alloc<float>(A, rows(0, true) * (g.latent_dim ? g.latent_dim : g.E), st);
     s->h = dev_alloc<float>(A, r0 * g.d, st);
     s->u = dev_alloc<float>(A, r0 * g.d, st);
     s->q = dev_alloc<float>(A, r0 * g.d, st);
     s->o = dev_alloc<float>(A, r0 * g.d, st);
     s->f = dev_alloc<float>(A, r0 * g.ffn, st);
-    s->hf = dev_alloc<float>(A, rows(0, true) * g.d, st);
-    for (int u = 0; u < g.n_up; u++) s->up_out[u] = dev_alloc<float>(A, rows(1 + u, true) * g.up_ch[u], st);
+    s->hf = dev_alloc<float>(A, rows(lt, true) * g.d, st);
+    for (int u = 0; u < g.n_up; u++) s->up_out[u] = dev_alloc<float>(A, rows(lt + 1 + u, true) * g.up_ch[u], st);
     for (int si = 0; si < g.n_stages; si++) {
-        const int lvl = g.n_up + 1 + si;
+        const int lvl = lt + g.n_up + 1 + si;
         const size_t n = rows(lvl, true) * g.ch[si];
         s->x0[si] = dev_alloc<float>(A, n, st);
         for (int j = 0; j < g.n_rb; j++)
@@ -491,11 +549,12 @@ codec_status codec_state_create(codec_t* c, int32_t n_streams, codec_state_t** o
         s->hist.push_back(d);
         s->hist_floats_per_slot += (double)H * C;
     };
-    add_hist(s->e, g.E, g.pre_k - 1, 0);
-    add_hist(s->hf, g.d, 1, 0);
-    for (int u = 0; u < g.n_up; u++) add_hist(s->up_out[u], g.up_ch[u], 1, 1 + u);
+    if (g.latent_dim) add_hist(s->e, g.latent_dim, 1, 0);      // the front phase GEMM's z[n-1]
+    else add_hist(s->e, g.E, g.pre_k - 1, 0);
+    add_hist(s->hf, g.d, 1, lt);
+    for (int u = 0; u < g.n_up; u++) add_hist(s->up_out[u], g.up_ch[u], 1, lt + 1 + u);
     for (int si = 0; si < g.n_stages; si++) {
-        const int lvl = g.n_up + 1 + si;
+        const int lvl = lt + g.n_up + 1 + si;
         int h0 = 0;
         for (int j = 0; j < g.n_rb; j++) h0 = std::max(h0, (g.rb_k[j] - 1) * g.dil[0]);
         add_hist(s->x0[si], g.ch[si], h0, lvl);
@@ -504,7 +563,7 @@ codec_status codec_state_create(codec_t* c, int32_t n_streams, codec_state_t** o
         add_hist(s->y[si], g.ch[si], si == g.n_stages - 1 ? g.final_k - 1 : 1, lvl);
     }
     s->hist_d = dev_upload(A, s->hist.data(), s->hist.size(), st);
-    s->R = next_pow2(g.max_chunk_frames + g.window - 1);
+    s->R = next_pow2(g.max_chunk_frames * c->r_tf + g.window - 1);
     const size_t ring = (size_t)std::max(g.layers, 1) * S * s->R * g.d;
     s->kring = dev_alloc<float>(A, ring, st, true);
     s->vring = dev_alloc<float>(A, ring, st, true);
@@ -534,7 +593,7 @@ codec_status codec_state_create(codec_t* c, int32_t n_streams, codec_state_t** o
         if (cudaMallocHost(&s->slots_h, sizeof(int) * S) != cudaSuccess) st = CODEC_ERR_OOM;
         else if (cudaEventCreateWithFlags(&s->slots_ev, cudaEventDisableTiming) != cudaSuccess) st = CODEC_ERR_CUDA;
     }
-    s->codes_d = dev_alloc<int>(A, (size_t)S * g.Q * g.max_chunk_frames, st);
+    s->codes_d = dev_alloc<int>(A, (size_t)S * std::max(g.Q, 1) * g.max_chunk_frames, st);
     s->audio_d = dev_alloc<float>(A, (size_t)S * g.max_chunk_frames * c->spf, st);
     if (st == CODEC_OK && g.precision != CODEC_PRECISION_FP32) {
         // operand planes for the widest tensor-core input: (contraction, input level, prefixed?)
@@ -547,16 +606,16 @@ codec_status codec_state_create(codec_t* c, int32_t n_streams, codec_state_t** o
         };
         need(c->pre, 0, true);
         for (const LayerW& L : c->layers) {
-            need(L.qkv, 0, false);
-            need(L.o, 0, false);
-            need(L.w1, 0, false);
-            need(L.w2, 0, false);
+            need(L.qkv, lt, false);
+            need(L.o, lt, false);
+            need(L.w1, lt, false);
+            need(L.w2, lt, false);
         }
-        for (int u = 0; u < g.n_up; u++) need(c->up[u], u, true);
+        for (int u = 0; u < g.n_up; u++) need(c->up[u], lt + u, true);
         for (int si = 0; si < g.n_stages; si++) {
-            need(c->st[si], g.n_up + si, true);
+            need(c->st[si], lt + g.n_up + si, true);
             for (int j = 0; j < g.n_rb; j++)
-                for (int i = 0; i < g.n_dil; i++) need(c->rb[c->rb_index(si, j, i)], g.n_up + 1 + si, true);
+                for (int i = 0; i < g.n_dil; i++) need(c->rb[c->rb_index(si, j, i)], lt + g.n_up + 1 + si, true);
         }
         // split-GEMM partials: 64 M floats (256 MB)
         if (!tc_scratch_alloc(&s->tc_scratch, std::max<size_t>(elems, 4), b_elems, size_t(64) << 20, A))
@@ -759,7 +818,7 @@ struct Launcher {
     PlanView pv;
     const int* tc64;     // device, [levels][S + 1]
     const int* tc128;
-    const int* q16;                         // device, [S + 1] blocks of 16 frames
+    const int* q16;                         // device, [S + 1] attention blocks of kSwaQueries frames
     int nq16 = 0;
     std::vector<int> ntiles64, ntiles128;   // per level
     std::vector<int> slot_h, n_h;           // host copies of the compacted batch
@@ -818,6 +877,7 @@ struct Launcher {
             a.ring_R = s->R;
             a.d = s->c->cfg.d;
         }
+        a.pos_r = s->c->r_tf;
         const double M = (double)rows(in_lvl);
         const double flops = 2.0 * M * C.N * C.K;
         const double out_rw = (epi == EPI_RESID || epi == EPI_MRF_FIRST) ? 2.0
@@ -914,7 +974,8 @@ codec_status plan_call(codec_state_t* s, const int32_t* n_frames, const int32_t*
     {
         int* q16 = P + s->off_q16;
         q16[0] = 0;
-        for (int b = 0; b < Bc; b++) q16[b + 1] = q16[b] + (cf[b + 1] - cf[b] + 15) / 16;
+        for (int b = 0; b < Bc; b++)
+            q16[b + 1] = q16[b] + ((cf[b + 1] - cf[b]) * c->r_tf + kSwaQueries - 1) / kSwaQueries;
         L.nq16 = q16[Bc];
     }
     if (cudaMemcpyAsync(s->plan_d, P, sizeof(int) * s->plan_ints, cudaMemcpyHostToDevice, cs) != cudaSuccess)
@@ -935,29 +996,47 @@ codec_status plan_call(codec_state_t* s, const int32_t* n_frames, const int32_t*
     return CODEC_OK;
 }
 
-// The launch sequence of one decode call, enqueued on cs.
-void enqueue_decode(codec_state_t* s, Launcher& L, const int32_t* codes, int32_t T_max, float* audio,
+// The launch sequence of one decode call, enqueued on cs.  `input` is the
+// codes (int32 [B][Q][T_max]) or, for a latent-input codec, the latents
+// (float [B][T_max][L]).
+void enqueue_decode(codec_state_t* s, Launcher& L, const void* input, int32_t T_max, float* audio,
                     float* pre_tanh, int rows0, cudaStream_t cs)
 {
     codec_s* c = s->c;
     const codec_config& g = c->cfg;
     const int S = s->n_slots;
     L.cs = cs;
-    const Layout L0d{1, 0}, L0p{1, s->P[0]};
+    const int lt = c->lvl_tf, rt = c->r_tf;
+    const Layout L0p{1, s->P[0]};
+    const Layout Ltd{rt, 0};                 // the transformer's dense rows
     auto lay = [&](int lvl) { return Layout{c->level_r[lvl], s->P[lvl]}; };
+    const int rows_tf = rows0 * rt;
 
     const double hist_bytes = 8.0 * s->hist_floats_per_slot * (double)L.Bc;
     L.run(CODEC_KERNEL_HISTORY, 0.0, hist_bytes, "history fill",
           [&] { return launch_hist_fill(s->hist_d, (int)s->hist.size(), L.pv, cs); });
-    L.run(CODEC_KERNEL_GATHER, (double)rows0 * g.Q * g.E, 4.0 * rows0 * ((double)g.Q * (1 + g.E) + g.E), "codebook gather",
-          [&] { return launch_rvq_gather(c->cb, g.Q, g.V, g.E, codes, T_max, L.pv, s->e, L0p, s->err_d, rows0, cs); });
-    L.gemm(c->pre, s->e, L0p, 0, s->h, L0d, g.d, 1, nullptr, EPI_STORE, 1.f, 0, "pre-conv");
-    const double norm_flops = 3.0 * rows0 * g.d, norm_bytes = 8.0 * rows0 * g.d;
-    double attn_flops = 0.0, attn_bytes = 8.0 * rows0 * g.d;
+    if (g.latent_dim) {
+        const int Lc = g.latent_dim;
+        L.run(CODEC_KERNEL_GATHER, 2.0 * rows0 * Lc, 4.0 * rows0 * 2.0 * Lc, "latent fill", [&] {
+            return launch_latent_fill(static_cast<const float*>(input), Lc, T_max, L.pv, c->lat_mu, c->lat_sigma,
+                                      s->e, L0p, rows0, cs);
+        });
+        L.gemm(c->pre, s->e, L0p, 0, s->h, Ltd, g.d, g.tf_up, nullptr, EPI_STORE, 1.f, 0, "latent front");
+    } else {
+        L.run(CODEC_KERNEL_GATHER, (double)rows0 * g.Q * g.E, 4.0 * rows0 * ((double)g.Q * (1 + g.E) + g.E),
+              "codebook gather", [&] {
+                  return launch_rvq_gather(c->cb, g.Q, g.V, g.E, static_cast<const int32_t*>(input), T_max, L.pv,
+                                           s->e, L0p, s->err_d, rows0, cs);
+              });
+        L.gemm(c->pre, s->e, L0p, 0, s->h, Ltd, g.d, 1, nullptr, EPI_STORE, 1.f, 0, "pre-conv");
+    }
+    const double norm_flops = 3.0 * rows_tf * g.d, norm_bytes = 8.0 * rows_tf * g.d;
+    double attn_flops = 0.0, attn_bytes = 8.0 * rows_tf * g.d;
     for (size_t b = 0; b < L.n_h.size(); b++) {
-        const long long p0 = s->frames_h[L.slot_h[b]];
-        for (int t = 0; t < L.n_h[b]; t++) attn_flops += 4.0 * g.d * (double)std::min<long long>(p0 + t + 1, g.window);
-        attn_bytes += 8.0 * g.d * (double)(L.n_h[b] + std::min<long long>(p0, g.window - 1));
+        const long long p0 = s->frames_h[L.slot_h[b]] * rt;
+        const long long nq = (long long)L.n_h[b] * rt;
+        for (long long t = 0; t < nq; t++) attn_flops += 4.0 * g.d * (double)std::min<long long>(p0 + t + 1, g.window);
+        attn_bytes += 8.0 * g.d * (double)(nq + std::min<long long>(p0, g.window - 1));
     }
     for (int l = 0; l < g.layers; l++) {
         const LayerW& W = c->layers[l];
@@ -967,28 +1046,28 @@ void enqueue_decode(codec_state_t* s, Launcher& L, const int32_t* codes, int32_t
         void* pl = s->tc_scratch.a_hi;
         const int pil = W.qkv.tc.passes == 3 ? 1 : 0;
         L.run(CODEC_KERNEL_RMSNORM, norm_flops, norm_bytes, "rmsnorm 1", [&] {
-            return launch_rms_norm(s->h, L0d, W.n1, g.rms_eps, s->u, L0d, g.d, L.pv, rows0, cs,
+            return launch_rms_norm(s->h, Ltd, W.n1, g.rms_eps, s->u, Ltd, g.d, L.pv, rows_tf, cs,
                                    W.qkv.use_tc ? pl : nullptr, pil);
         });
-        L.gemm(W.qkv, s->u, L0d, 0, s->q, L0d, g.d, 1, nullptr, EPI_QKV, 1.f, l, "qkv", W.qkv.use_tc);
+        L.gemm(W.qkv, s->u, Ltd, lt, s->q, Ltd, g.d, 1, nullptr, EPI_QKV, 1.f, l, "qkv", W.qkv.use_tc);
         const size_t per_layer = (size_t)S * s->R * g.d;
         L.run(CODEC_KERNEL_ATTENTION, attn_flops, attn_bytes, "attention", [&] {
             return launch_swa(s->q, s->o, s->kring + per_layer * l, s->vring + per_layer * l, g.d, g.heads,
-                              g.window, s->R, L.pv, L.q16, L.nq16, cs, W.o.use_tc ? pl : nullptr,
+                              g.window, s->R, rt, L.pv, L.q16, L.nq16, cs, W.o.use_tc ? pl : nullptr,
                               W.o.tc.passes == 3 ? 1 : 0);
         });
-        L.gemm(W.o, s->o, L0d, 0, s->h, L0d, g.d, 1, s->h, EPI_RESID, 1.f, 0, "out-proj", W.o.use_tc);
+        L.gemm(W.o, s->o, Ltd, lt, s->h, Ltd, g.d, 1, s->h, EPI_RESID, 1.f, 0, "out-proj", W.o.use_tc);
         L.run(CODEC_KERNEL_RMSNORM, norm_flops, norm_bytes, "rmsnorm 2", [&] {
-            return launch_rms_norm(s->h, L0d, W.n2, g.rms_eps, s->u, L0d, g.d, L.pv, rows0, cs,
+            return launch_rms_norm(s->h, Ltd, W.n2, g.rms_eps, s->u, Ltd, g.d, L.pv, rows_tf, cs,
                                    W.w1.use_tc ? pl : nullptr, W.w1.tc.passes == 3 ? 1 : 0);
         });
-        L.gemm(W.w1, s->u, L0d, 0, s->f, L0d, g.ffn, 1, nullptr, EPI_GELU, 1.f, 0, "mlp 1", W.w1.use_tc);
-        L.gemm(W.w2, s->f, L0d, 0, s->h, L0d, g.d, 1, s->h, EPI_RESID, 1.f, 0, "mlp 2");
+        L.gemm(W.w1, s->u, Ltd, lt, s->f, Ltd, g.ffn, 1, nullptr, EPI_GELU, 1.f, 0, "mlp 1", W.w1.use_tc);
+        L.gemm(W.w2, s->f, Ltd, lt, s->h, Ltd, g.d, 1, s->h, EPI_RESID, 1.f, 0, "mlp 2");
     }
     L.run(CODEC_KERNEL_RMSNORM, norm_flops, norm_bytes, "final rmsnorm",
-          [&] { return launch_rms_norm(s->h, L0d, c->tf_norm, g.rms_eps, s->hf, L0p, g.d, L.pv, rows0, cs); });
+          [&] { return launch_rms_norm(s->h, Ltd, c->tf_norm, g.rms_eps, s->hf, lay(lt), g.d, L.pv, rows_tf, cs); });
     const float* x = s->hf;
-    int xl = 0;
+    int xl = lt;
     for (int u = 0; u < g.n_up; u++) {
         L.gemm(c->up[u], x, lay(xl), xl, s->up_out[u], lay(xl + 1), g.up_ch[u], g.up_s, nullptr, EPI_STORE,
                1.f, 0, "latent upsample");
@@ -1029,7 +1108,7 @@ void enqueue_decode(codec_state_t* s, Launcher& L, const int32_t* codes, int32_t
           [&] { return launch_hist_commit(s->hist_d, (int)s->hist.size(), L.pv, nullptr, s->frames_d, cs); });
 }
 
-codec_status decode_impl(codec_state_t* s, const int32_t* codes, const int32_t* n_frames,
+codec_status decode_impl(codec_state_t* s, const void* codes, const int32_t* n_frames,
                          const int32_t* ids, int32_t B, int32_t T_max, float* audio, float* pre_tanh,
                          cudaStream_t cs, const int32_t* skip = nullptr)
 {
@@ -1121,6 +1200,7 @@ codec_status embed_impl(codec_state_t* s, const int32_t* codes, const int32_t* n
                         int32_t B, int32_t T_max, float* emb, cudaStream_t cs)
 {
     if (!s || !codes || !n_frames || !emb) return CODEC_ERR_NULL;
+    if (s->c->cfg.latent_dim) return CODEC_ERR_CONFIG;
     const codec_config& g = s->c->cfg;
     Launcher L;
     int rows0 = 0;
@@ -1140,6 +1220,7 @@ extern "C" {
 codec_status codec_decode_chunk(codec_state_t* s, const int32_t* codes, const int32_t* n_frames,
                                 const int32_t* ids, int32_t B, int32_t T_max, float* audio, void* stream)
 {
+    if (s && s->c->cfg.latent_dim) return CODEC_ERR_CONFIG;
     return decode_impl(s, codes, n_frames, ids, B, T_max, audio, nullptr, (cudaStream_t)stream);
 }
 
@@ -1147,7 +1228,16 @@ codec_status codec_decode_chunk_ex(codec_state_t* s, const int32_t* codes, const
                                    const int32_t* ids, int32_t B, int32_t T_max, float* audio,
                                    float* pre_tanh, void* stream)
 {
+    if (s && s->c->cfg.latent_dim) return CODEC_ERR_CONFIG;
     return decode_impl(s, codes, n_frames, ids, B, T_max, audio, pre_tanh, (cudaStream_t)stream);
+}
+
+codec_status codec_decode_latents(codec_state_t* s, const float* latents, const int32_t* n_frames,
+                                  const int32_t* ids, int32_t B, int32_t T_max, float* audio, float* pre_tanh,
+                                  void* stream)
+{
+    if (s && !s->c->cfg.latent_dim) return CODEC_ERR_CONFIG;
+    return decode_impl(s, latents, n_frames, ids, B, T_max, audio, pre_tanh, (cudaStream_t)stream);
 }
 
 codec_status codec_embed_chunk(codec_state_t* s, const int32_t* codes, const int32_t* n_frames,
@@ -1162,6 +1252,7 @@ codec_status codec_decode_recompute(codec_state_t* s, const int32_t* codes, cons
 {
     if (!s || !codes || !n_ctx || !n_new || !audio) return CODEC_ERR_NULL;
     const codec_config& g = s->c->cfg;
+    if (g.latent_dim) return CODEC_ERR_CONFIG;
     if (B < 1 || T_max < 1) return CODEC_ERR_ARG;
     if (B > s->n_slots) return CODEC_ERR_CAPACITY;
     std::vector<int32_t> n_frames(B), reset_ids;
@@ -1214,6 +1305,7 @@ codec_status codec_decode_chunk_host(codec_state_t* s, const int32_t* codes_host
 {
     if (!s || !codes_host || !n_frames || !audio_host) return CODEC_ERR_NULL;
     const codec_config& g = s->c->cfg;
+    if (g.latent_dim) return CODEC_ERR_CONFIG;
     if (B < 1 || T_max < 1) return CODEC_ERR_ARG;
     if (B > s->n_slots || T_max > g.max_chunk_frames) return CODEC_ERR_CAPACITY;
     cudaStream_t cs = (cudaStream_t)stream;

@@ -11,6 +11,9 @@
 namespace codec {
 
 constexpr int kMaxTaps = 16;
+// Queries of one stream that one sliding-window attention block takes (the
+// per-call plan counts each stream's attention blocks in these units).
+constexpr int kSwaQueries = 32;
 
 // Epilogue modes of the implicit-GEMM kernels (what happens to acc = A*B).
 enum Epi : int {
@@ -76,6 +79,7 @@ struct GemmArgs {
     float* vring;
     int ring_R;              // ring rows per slot (power of two)
     int d;
+    int pos_r;               // transformer rows (positions) per frame
     // tiling
     const int* tcum;         // [B + 1] cumulative row tiles of the input level
     int bm;
@@ -92,6 +96,18 @@ __device__ __forceinline__ int find_seg(const int* cum, int B, int x)
     while (lo < hi) {
         int mid = (lo + hi + 1) >> 1;
         if (__ldg(cum + mid) <= x) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+// The same over rows of a level with r rows per frame: largest b with
+// cum[b] * r <= x.
+__device__ __forceinline__ int find_seg_r(const int* cum, int B, long long x, int r)
+{
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if ((long long)__ldg(cum + mid) * r <= x) lo = mid; else hi = mid - 1;
     }
     return lo;
 }
@@ -200,10 +216,10 @@ __device__ __forceinline__ void gemm_store(const GemmArgs& a, const PlanView& pl
             a.out[out_row * a.d + n] = v;
         } else {
             if (b < 0) {            // dense tiling: t is the row over all segments
-                b = find_seg(plan.cf, plan.B, t);
-                t -= __ldg(plan.cf + b);
+                b = find_seg_r(plan.cf, plan.B, t, a.pos_r);
+                t -= __ldg(plan.cf + b) * a.pos_r;
             }
-            const long long pos = __ldg(plan.pos0 + b) + t;
+            const long long pos = __ldg(plan.pos0 + b) * a.pos_r + t;
             const long long rr = (long long)__ldg(plan.slot + b) * a.ring_R + (pos & (a.ring_R - 1));
             if (n < 2 * a.d) a.kring[rr * a.d + (n - a.d)] = v;
             else a.vring[rr * a.d + (n - 2 * a.d)] = v;

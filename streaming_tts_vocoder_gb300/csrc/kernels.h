@@ -18,19 +18,33 @@ cudaError_t launch_rvq_gather(const float* cb, int Q, int V, int E, const int* c
                               PlanView plan, float* e, Layout el, unsigned* err_words,
                               int total_rows, cudaStream_t s);
 
+// Latent input: e[row] = x * sigma + mu for the call's frames (x [B][T_max][L]).
+cudaError_t launch_latent_fill(const float* x, int L, int T_max, PlanView plan, const float* mu,
+                               const float* sigma, float* e, Layout el, int total_rows, cudaStream_t s);
+
 cudaError_t launch_gemm_simt(const GemmArgs& a, PlanView plan, int n_row_tiles, cudaStream_t s);
 
-// planes (optional): write the rows as a tensor-core GEMM's operand planes
+// Rows of x and y run at xl.r rows per frame.  planes (optional): write the
+// rows as a tensor-core GEMM's operand planes
 // (interleaved hi/lo when planes_il, else the hi plane) instead of y.
 cudaError_t launch_rms_norm(const float* x, Layout xl, const float* g, float eps, float* y, Layout yl,
                             int d, PlanView plan, int total_rows, cudaStream_t s, void* planes = nullptr,
                             int planes_il = 1);
 
-// qcum: [B + 1] cumulative blocks of 16 queries per batch entry.  planes
+// qcum: [B + 1] cumulative blocks of kSwaQueries queries per batch entry.  planes
 // (optional): the output as operand planes instead of o, as for RMSNorm.
+// Shared memory one attention block needs (the kernel allows up to 227 KB).
+size_t swa_smem_bytes(int dh, int window);
+constexpr int kSwaWindowMax = 256;
+constexpr size_t kSwaSmemMax = 227 * 1024;
+
 cudaError_t launch_swa(const float* q, float* o, const float* kring, const float* vring, int d,
-                       int heads, int window, int ring_R, PlanView plan, const int* qcum, int n_qblocks,
+                       int heads, int window, int ring_R, int pos_r, PlanView plan, const int* qcum, int n_qblocks,
                        cudaStream_t s, void* planes = nullptr, int planes_il = 1);
+
+// Shared memory of one final-conv block (the kernel allows up to kFinalSmemMax).
+size_t final_conv_smem_bytes(int C, int k);
+constexpr size_t kFinalSmemMax = 160 * 1024;
 
 cudaError_t launch_final_conv(const float* x, Layout xl, int C, const float* w, const float* bias,
                               const float* alpha, const float* inv_alpha, int k, float* audio,

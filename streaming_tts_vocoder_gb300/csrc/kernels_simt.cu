@@ -62,6 +62,43 @@ cudaError_t launch_rvq_gather(const float* cb, int Q, int V, int E, const int* c
     return cudaGetLastError();
 }
 
+// ---------------------------------------------------------- latent fill --
+// Latent-input decoder: e[row] = x[row] * sigma + mu (per channel, one
+// rounding) for every frame of the call, from the caller's [B][T_max][L]
+// latents into the level-0 buffer (blixt/phonon "Weights": the codec's
+// latents are denormalised before the projection).  One thread per float4.
+__global__ void __launch_bounds__(256) latent_fill_kernel(const float* __restrict__ x, int L, int T_max,
+                                                          PlanView plan, const float* __restrict__ mu,
+                                                          const float* __restrict__ sigma, float* __restrict__ e,
+                                                          Layout el, int total_rows)
+{
+    pdl_wait();
+    pdl_launch();
+    const int L4 = L >> 2;
+    const long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+    if (i >= (long long)total_rows * L4) return;
+    const int row = (int)(i / L4), c4 = (int)(i - (long long)row * L4);
+    const int b = find_seg(plan.cf, plan.B, row);
+    const int t = row - __ldg(plan.cf + b);
+    const float4 v = __ldg(reinterpret_cast<const float4*>(x + ((long long)__ldg(plan.bidx + b) * T_max + t) * L) + c4);
+    const float4 m = __ldg(reinterpret_cast<const float4*>(mu) + c4);
+    const float4 sg = __ldg(reinterpret_cast<const float4*>(sigma) + c4);
+    reinterpret_cast<float4*>(e + (seg_base(el, plan.cf, b) + t) * L)[c4] =
+        make_float4(__fmaf_rn(v.x, sg.x, m.x), __fmaf_rn(v.y, sg.y, m.y), __fmaf_rn(v.z, sg.z, m.z),
+                    __fmaf_rn(v.w, sg.w, m.w));
+}
+
+cudaError_t launch_latent_fill(const float* x, int L, int T_max, PlanView plan, const float* mu,
+                               const float* sigma, float* e, Layout el, int total_rows, cudaStream_t s)
+{
+    if (total_rows <= 0) return cudaSuccess;
+    if (L % 4 != 0) return cudaErrorInvalidValue;
+    const long long n = (long long)total_rows * (L / 4);
+    launch_pdl(latent_fill_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s, x, L, T_max, plan, mu, sigma,
+               e, el, total_rows);
+    return cudaGetLastError();
+}
+
 // ------------------------------------------------------ fp32 implicit GEMM --
 // out[t][n] = epi( sum_j sum_ci A(in[base(b) + t - shift_j][ci]) W[j Cin + ci][n] )
 // 64 x 64 output tile per block, 16-deep K slices in shared memory, 4 x 4
@@ -144,6 +181,8 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmArgs a, PlanView pla
 cudaError_t launch_gemm_simt(const GemmArgs& a, PlanView plan, int n_row_tiles, cudaStream_t s)
 {
     if (n_row_tiles <= 0) return cudaSuccess;
+    // A rows and W rows are read as float4s
+    if (a.Cin % 4 != 0 || a.N % 4 != 0) return cudaErrorInvalidValue;
     dim3 grid(n_row_tiles, (a.N + SB_N - 1) / SB_N);
     launch_pdl(gemm_simt_kernel, dim3(grid), dim3(256), 0, s, a, plan);
     return cudaGetLastError();
@@ -163,8 +202,9 @@ __global__ void rms_norm_kernel(const float* __restrict__ x, Layout xl, const fl
     const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (row >= total_rows) return;
-    const int b = find_seg(plan.cf, plan.B, row);
-    const int t = row - __ldg(plan.cf + b);
+    // xl.r rows per frame (yl has the same rate)
+    const int b = find_seg_r(plan.cf, plan.B, row, xl.r);
+    const int t = row - __ldg(plan.cf + b) * xl.r;
     const float4* xr = reinterpret_cast<const float4*>(x + (seg_base(xl, plan.cf, b) + t) * d);
     const long long yrow = seg_base(yl, plan.cf, b) + t;
     float4* yr = reinterpret_cast<float4*>(y + yrow * d);
@@ -198,120 +238,170 @@ cudaError_t launch_rms_norm(const float* x, Layout xl, const float* g, float eps
 }
 
 // ---------------------------------------------- sliding-window attention --
-// A block takes up to 16 consecutive queries of one stream and one head,
-// stages the keys and values of every position they can see (at most
-// 16 + W - 1 rows, read from the stream's ring: position p lives in ring row
-// p mod R) in shared memory, and gives each warp two queries.  Query at
-// absolute position p attends positions max(0, p - W + 1) .. p.  Lane i
-// scores keys lo + i, lo + 32 + i, ...; max and denominator go through a
-// fixed butterfly and the value sum runs over the keys in position order, so
-// a query's result depends only on its position and the keys, never on the
-// chunking (blixt/phonon "Speed" item 7: ring of keys and values; item 11:
-// softmax with max subtraction).
-constexpr int kSwaMaxW = 128;
+// A block takes up to kSwaQueries consecutive queries of one stream and one
+// head.  It stages the keys and values of every position they can see (at
+// most kSwaQueries + W - 1 rows of the stream's ring: position p lives in
+// ring row p mod R) in shared memory once, with 128-bit loads, then runs
+// three passes over the whole block: every (query, key) score (a thread per
+// pair, the dot product over the head's channels in ascending order), the
+// softmax of each query (a warp per query: lane i takes keys lo + i,
+// lo + 32 + i, ... of the query's own window lo .. p, max and denominator
+// through a fixed butterfly), and every output channel (a thread per
+// (query, channel), the value sum over the window's keys in position order).
+// A query at absolute position p attends positions max(0, p - W + 1) .. p, and
+// every sum it takes runs in an order fixed by its own window, so its result
+// never depends on how the stream was chunked (blixt/phonon "Speed" item 7:
+// a ring of keys and values; item 11: softmax with max subtraction).
+constexpr int kSwaMaxW = kSwaWindowMax;
 constexpr int kSwaMaxDh = 128;
-constexpr int kSwaQ = 16;           // queries per block
-constexpr int kSwaWarps = 8;
-constexpr int kSwaMaxSmem = 160 * 1024;
+constexpr int kSwaThreads = 256;
+constexpr int kSwaWarps = kSwaThreads / 32;
+constexpr int kSwaMaxSmem = (int)kSwaSmemMax;
 
 // planes set: the attention output goes straight into the out-projection's
 // tensor-core operand planes (dense rows) instead of o.
-__global__ void __launch_bounds__(kSwaWarps * 32) swa_kernel(
+__global__ void __launch_bounds__(kSwaThreads) swa_kernel(
     const float* __restrict__ q, float* __restrict__ o, const float* __restrict__ kring,
-    const float* __restrict__ vring, int d, int heads, int W, int R, PlanView plan,
+    const float* __restrict__ vring, int d, int heads, int W, int R, int pos_r, PlanView plan,
     const int* __restrict__ qcum, void* planes, int planes_il)
 {
     pdl_wait();
     pdl_launch();
-    extern __shared__ float sm[];
+    extern __shared__ float4 swa_sm4[];
     const int dh = d / heads;
-    const int ld = dh + 1;                              // padded row: conflict-free column reads
-    const int maxk = kSwaQ + W - 1;
-    float* sk = sm;                                     // [maxk][dh + 1]
-    float* sv = sk + maxk * ld;                         // [maxk][dh + 1]
-    float* sq = sv + maxk * ld;                         // [kSwaWarps][dh]
-    float* sp = sq + kSwaWarps * dh;                    // [kSwaWarps][W]
+    const int dh4 = dh >> 2;
+    const int ld4 = dh4 + 1;                            // padded rows (float4 units): conflict-free row reads
+    const int maxk = kSwaQueries + W - 1;
+    const int lds = maxk + 1;
+    float4* sk = swa_sm4;                               // [maxk][ld4]
+    float4* sv = sk + (size_t)maxk * ld4;               // [maxk][ld4]
+    float4* sq = sv + (size_t)maxk * ld4;               // [kSwaQueries][ld4]
+    float* sp = reinterpret_cast<float*>(sq + (size_t)kSwaQueries * ld4);   // [kSwaQueries][lds] scores, then e^(s - m)
+    float* sz = sp + (size_t)kSwaQueries * lds;         // [kSwaQueries] 1 / denominator
     const int h = blockIdx.y;
     const int blk = blockIdx.x;
     const int b = find_seg(qcum, plan.B, blk);
-    const int n = __ldg(plan.cf + b + 1) - __ldg(plan.cf + b);
-    const int tq0 = (blk - __ldg(qcum + b)) * kSwaQ;
-    const int nq = min(kSwaQ, n - tq0);
-    const long long p0 = __ldg(plan.pos0 + b) + tq0;   // position of the block's first query
+    // pos_r transformer rows (positions) per frame
+    const int n = (__ldg(plan.cf + b + 1) - __ldg(plan.cf + b)) * pos_r;
+    const int tq0 = (blk - __ldg(qcum + b)) * kSwaQueries;
+    const int nq = min(kSwaQueries, n - tq0);
+    const long long p0 = __ldg(plan.pos0 + b) * pos_r + tq0;   // position of the block's first query
     const long long kstart = p0 - W + 1 > 0 ? p0 - W + 1 : 0;
     const int nk = (int)(p0 + nq - kstart);             // keys the block's queries can see
     const long long slot_base = (long long)__ldg(plan.slot + b) * R;
-    for (int i = threadIdx.x; i < nk * dh; i += blockDim.x) {
-        const int r = i / dh, c = i - r * dh;
-        const long long row = (slot_base + ((kstart + r) & (R - 1))) * d + h * dh + c;
-        sk[r * ld + c] = __ldg(kring + row);
-        sv[r * ld + c] = __ldg(vring + row);
+    const long long row0 = (long long)__ldg(plan.cf + b) * pos_r + tq0;
+    const int tid = threadIdx.x;
+    for (int i = tid; i < nk * dh4; i += kSwaThreads) {
+        const int r = i / dh4, c4 = i - r * dh4;
+        const long long at = (slot_base + ((kstart + r) & (R - 1))) * d + h * dh + 4 * c4;
+        sk[r * ld4 + c4] = __ldg(reinterpret_cast<const float4*>(kring + at));
+        sv[r * ld4 + c4] = __ldg(reinterpret_cast<const float4*>(vring + at));
+    }
+    for (int i = tid; i < nq * dh4; i += kSwaThreads) {
+        const int r = i / dh4, c4 = i - r * dh4;
+        sq[r * ld4 + c4] = __ldg(reinterpret_cast<const float4*>(q + (row0 + r) * d + h * dh + 4 * c4));
     }
     __syncthreads();
-    const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // scores of every (query, key) pair the block holds, four keys per
+    // thread (four independent chains; each dot product still runs over the
+    // channels in ascending order); keys outside a query's window are skipped
     const float scale = 1.0f / sqrtf((float)dh);
-    const long long row0 = (long long)__ldg(plan.cf + b) + tq0;
+    const int nk4 = (nk + 3) >> 2;
+    for (int i = tid; i < nq * nk4; i += kSwaThreads) {
+        // keys j, j + nk4, j + 2 nk4, j + 3 nk4: consecutive threads read
+        // consecutive key rows (conflict-free 128-bit shared loads)
+        const int qi = i / nk4, j = i - qi * nk4;
+        const long long pos = p0 + qi;
+        const float4* qr = sq + qi * ld4;
+        float dot[4] = {0.f, 0.f, 0.f, 0.f};
+        const float4* kr[4];
+#pragma unroll
+        for (int u = 0; u < 4; u++) kr[u] = sk + min(j + u * nk4, nk - 1) * ld4;
+        for (int c4 = 0; c4 < dh4; c4++) {
+            const float4 a = qr[c4];
+#pragma unroll
+            for (int u = 0; u < 4; u++) {
+                const float4 k4 = kr[u][c4];
+                dot[u] = fmaf(a.x, k4.x, dot[u]);
+                dot[u] = fmaf(a.y, k4.y, dot[u]);
+                dot[u] = fmaf(a.z, k4.z, dot[u]);
+                dot[u] = fmaf(a.w, k4.w, dot[u]);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; u++) {
+            const int jj = j + u * nk4;
+            const long long kp = kstart + jj;
+            if (jj < nk && kp <= pos && kp >= pos - W + 1) sp[qi * lds + jj] = dot[u] * scale;
+        }
+    }
+    __syncthreads();
+    const int wib = tid >> 5, lane = tid & 31;
     for (int qi = wib; qi < nq; qi += kSwaWarps) {
         const long long pos = p0 + qi;
         const long long lo = pos - W + 1 > 0 ? pos - W + 1 : 0;
         const int nkq = (int)(pos - lo + 1);
-        const int off = (int)(lo - kstart);             // smem row of key lo
-        const float* qr = q + (row0 + qi) * d + h * dh;
-        for (int c = lane; c < dh; c += 32) sq[wib * dh + c] = qr[c];
-        __syncwarp();
-        float sc[kSwaMaxW / 32];
+        float* pr = sp + qi * lds + (int)(lo - kstart);  // the query's window, key lo first
         float m = -INFINITY;
-#pragma unroll
-        for (int u = 0; u < kSwaMaxW / 32; u++) {
-            const int i = lane + 32 * u;
-            sc[u] = -INFINITY;
-            if (i < nkq) {
-                const float* kr = sk + (off + i) * ld;
-                float dot = 0.f;
-                for (int c = 0; c < dh; c++) dot = fmaf(sq[wib * dh + c], kr[c], dot);
-                sc[u] = dot * scale;
-                m = fmaxf(m, sc[u]);
-            }
-        }
+        for (int i = lane; i < nkq; i += 32) m = fmaxf(m, pr[i]);
 #pragma unroll
         for (int sh = 16; sh; sh >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, sh));
         float z = 0.f;
-#pragma unroll
-        for (int u = 0; u < kSwaMaxW / 32; u++) {
-            const int i = lane + 32 * u;
-            if (i < nkq) {
-                const float pe = expf(sc[u] - m);
-                sp[wib * W + i] = pe;
-                z += pe;
-            }
+        for (int i = lane; i < nkq; i += 32) {
+            const float pe = expf(pr[i] - m);
+            pr[i] = pe;
+            z += pe;
         }
 #pragma unroll
         for (int sh = 16; sh; sh >>= 1) z += __shfl_xor_sync(0xffffffffu, z, sh);
-        __syncwarp();
-        const float inv_z = 1.0f / z;
-        for (int c = lane; c < dh; c += 32) {
-            float acc = 0.f;
-            for (int i = 0; i < nkq; i++) acc = fmaf(sp[wib * W + i], sv[(off + i) * ld + c], acc);
-            if (planes) plane_store1(planes, planes_il, row0 + qi, d, h * dh + c, acc * inv_z);
-            else o[(row0 + qi) * d + h * dh + c] = acc * inv_z;
+        if (lane == 0) sz[qi] = 1.0f / z;
+    }
+    __syncthreads();
+    // outputs, four channels per thread (four independent chains; each
+    // channel's sum runs over the query's keys in position order)
+    for (int i = tid; i < nq * dh4; i += kSwaThreads) {
+        const int qi = i / dh4, c4 = i - qi * dh4;
+        const long long pos = p0 + qi;
+        const long long lo = pos - W + 1 > 0 ? pos - W + 1 : 0;
+        const int nkq = (int)(pos - lo + 1);
+        const int off = (int)(lo - kstart);
+        const float* pr = sp + qi * lds + off;
+        const float4* vc = sv + (size_t)off * ld4 + c4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int k = 0; k < nkq; k++) {
+            const float pk = pr[k];
+            const float4 v4 = vc[(size_t)k * ld4];
+            acc.x = fmaf(pk, v4.x, acc.x);
+            acc.y = fmaf(pk, v4.y, acc.y);
+            acc.z = fmaf(pk, v4.z, acc.z);
+            acc.w = fmaf(pk, v4.w, acc.w);
         }
-        __syncwarp();
+        const float iz = sz[qi];
+        const float4 y = make_float4(acc.x * iz, acc.y * iz, acc.z * iz, acc.w * iz);
+        if (planes) plane_store4(planes, planes_il, row0 + qi, d, h * dh + 4 * c4, y);
+        else *reinterpret_cast<float4*>(o + (row0 + qi) * d + h * dh + 4 * c4) = y;
     }
 }
 
+size_t swa_smem_bytes(int dh, int window)
+{
+    const size_t maxk = (size_t)kSwaQueries + window - 1;
+    const size_t ld4 = (size_t)dh / 4 + 1;
+    return 16 * (2 * maxk * ld4 + (size_t)kSwaQueries * ld4) + 4 * ((size_t)kSwaQueries * (maxk + 1) + kSwaQueries);
+}
+
 cudaError_t launch_swa(const float* q, float* o, const float* kring, const float* vring, int d,
-                       int heads, int window, int ring_R, PlanView plan, const int* qcum, int n_qblocks,
+                       int heads, int window, int ring_R, int pos_r, PlanView plan, const int* qcum, int n_qblocks,
                        cudaStream_t s, void* planes, int planes_il)
 {
     if (n_qblocks <= 0) return cudaSuccess;
     if (planes && (d % 32 != 0)) return cudaErrorInvalidValue;
     const int dh = d / heads;
-    if (dh > kSwaMaxDh || window > kSwaMaxW) return cudaErrorInvalidValue;
-    const int maxk = kSwaQ + window - 1;
-    const size_t smem = sizeof(float) * (2 * (size_t)maxk * (dh + 1) + (size_t)kSwaWarps * dh + (size_t)kSwaWarps * window);
+    if (dh > kSwaMaxDh || dh % 4 != 0 || window > kSwaMaxW) return cudaErrorInvalidValue;
+    const size_t smem = swa_smem_bytes(dh, window);
     if (smem > (size_t)kSwaMaxSmem) return cudaErrorInvalidValue;
-    launch_pdl(swa_kernel, dim3(n_qblocks, heads), dim3(kSwaWarps * 32), smem, s, q, o, kring, vring, d, heads,
-               window, ring_R, plan, qcum, planes, planes_il);
+    launch_pdl(swa_kernel, dim3(n_qblocks, heads), dim3(kSwaThreads), smem, s, q, o, kring, vring, d, heads,
+               window, ring_R, pos_r, plan, qcum, planes, planes_il);
     return cudaGetLastError();
 }
 
@@ -319,18 +409,75 @@ cudaError_t launch_swa(const float* q, float* o, const float* kring, const float
 // y[t] = tanh(b + sum_j p_j[t - (k-1) + j]), p_j[r] = sum_c w[j][c] snake(x[r][c]),
 // C -> 1.  One thread per input row computes that row's k partial dot
 // products (its channels read once, Snake applied once per element) into
-// shared memory; then one thread per output row sums its k partials in tap
-// order.  A block covers 128 output rows and the k-1 history rows before
-// them.  Bandwidth-bound: one input row in, one sample out (blixt/phonon
-// "Open work": a direct kernel for the last convolution with 1 output
-// channel).
+// shared memory; each warp brings its 32 rows' channels through shared
+// memory 32 at a time with coalesced 128-bit loads.  Then one thread per
+// output row sums its k partials in tap order.  A block covers 128 output rows and
+// the k-1 history rows before them.  One input row in, one sample out
+// (blixt/phonon "Open work": a direct kernel for the last convolution with 1
+// output channel); with C Snakes per sample its cost is the sine, so this
+// kernel takes the sine as a Cody-Waite reduction of a x to [-pi, pi] (2 pi
+// split into a float and its remainder) and the hardware sine there (absolute
+// error a few 1e-7, against about 1e-7 for sinf): its Snake is not bit-equal
+// to the operand prep's, and nothing else reads it.
+__device__ __forceinline__ float snake_final(float x, float a, float inv_a)
+{
+    const float y = __fmul_rn(a, x);
+    const float k = rintf(y * 0.159154943091895336f);           // y / (2 pi), nearest integer
+    float r = __fmaf_rn(-k, 6.28318548202514648f, y);           // 2 pi rounded to float
+    r = __fmaf_rn(-k, -1.7484555314695172e-7f, r);              // 2 pi minus that float
+    const float sn = __sinf(r);
+    return __fadd_rn(x, __fmul_rn(__fmul_rn(sn, sn), inv_a));
+}
 constexpr int kFinalTile = 128;
 constexpr int kFinalMaxK = 16;
-constexpr int kFinalMaxSmem = 160 * 1024;
+constexpr int kFinalMaxSmem = (int)kFinalSmemMax;
 
 // KP: taps padded to 8 or 16.  The weights sit in shared memory as [C][KP]
 // (zero beyond k) and are read as float4s, the Snake parameters as float2s,
 // so a channel costs its Snake, KP/4 + 1 shared loads and KP FMAs.
+// One warp's rows r0 .. r0 + 31 (those below `rows`) of the tile: their
+// channels come through shared memory 32 at a time, loaded by the whole warp
+// (each load instruction covers whole 128-byte row segments), and each lane
+// then takes its own row's 32 channels: Snake, then the KP tap partials.
+template <int KP>
+__device__ __forceinline__ void final_rows(const float* __restrict__ x, long long base, int C, int rows, int r0,
+                                           const float4* sw, const float2* sa, float4* stg, int lane, float* part)
+{
+    constexpr int kPitch = 9;                                   // float4s per staged row (8 + 1 pad)
+#pragma unroll
+    for (int j = 0; j < KP; j++) part[j] = 0.f;
+    for (int c0 = 0; c0 < C; c0 += 32) {
+        const int nq = min(32, C - c0) >> 2;                    // float4s of this chunk per row
+        __syncwarp();
+        for (int i = lane; i < 32 * nq; i += 32) {
+            const int rr = i / nq, q = i - rr * nq;
+            if (r0 + rr < rows)
+                stg[rr * kPitch + q] = __ldg(reinterpret_cast<const float4*>(x + (base + r0 + rr) * C + c0) + q);
+        }
+        __syncwarp();
+        if (r0 + lane < rows) {
+            for (int q = 0; q < nq; q++) {
+                const float4 v = stg[lane * kPitch + q];
+                const float e[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int u = 0; u < 4; u++) {
+                    const int c = c0 + 4 * q + u;
+                    const float2 al = sa[c];
+                    const float sn = snake_final(e[u], al.x, al.y);
+#pragma unroll
+                    for (int g = 0; g < KP / 4; g++) {
+                        const float4 wq = sw[c * (KP / 4) + g];
+                        part[4 * g] = fmaf(wq.x, sn, part[4 * g]);
+                        part[4 * g + 1] = fmaf(wq.y, sn, part[4 * g + 1]);
+                        part[4 * g + 2] = fmaf(wq.z, sn, part[4 * g + 2]);
+                        part[4 * g + 3] = fmaf(wq.w, sn, part[4 * g + 3]);
+                    }
+                }
+            }
+        }
+    }
+}
+
 template <int KP>
 __global__ void __launch_bounds__(kFinalTile) final_conv_kernel(
     const float* __restrict__ x, Layout xl, int C, const float* __restrict__ w,
@@ -344,7 +491,9 @@ __global__ void __launch_bounds__(kFinalTile) final_conv_kernel(
     extern __shared__ float4 sm4[];
     float4* sw = sm4;                                                   // [C][KP / 4]
     float2* sa = reinterpret_cast<float2*>(sm4 + (size_t)C * (KP / 4)); // [C] (alpha, 1/alpha)
-    float* sp = reinterpret_cast<float*>(sa + C);                       // [kFinalTile + k - 1][k] partials
+    float4* stg = reinterpret_cast<float4*>(sa + C) + (threadIdx.x >> 5) * 32 * 9;   // per warp [32][9]
+    float* sp = reinterpret_cast<float*>(reinterpret_cast<float4*>(sa + C) + (kFinalTile / 32) * 32 * 9);
+    // sp: [kFinalTile + k - 1][k] partials
     const int tile = blockIdx.x;
     const int b = find_seg(tcum, plan.B, tile);
     const int seg_rows = (__ldg(plan.cf + b + 1) - __ldg(plan.cf + b)) * xl.r;
@@ -359,32 +508,18 @@ __global__ void __launch_bounds__(kFinalTile) final_conv_kernel(
     for (int i = threadIdx.x; i < C; i += blockDim.x) sa[i] = make_float2(__ldg(alpha + i), __ldg(inv_alpha + i));
     __syncthreads();
     const int rows = nrows + k - 1;
-    for (int r = threadIdx.x; r < rows; r += blockDim.x) {
-        float part[KP];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float part[KP];
+    // rows 0 .. 127: warp w takes rows 32 w .. 32 w + 31; rows 128 .. rows - 1
+    // (the k - 1 past the tile): warp 0 again
+    for (int r0 = 32 * warp; r0 < rows; r0 += kFinalTile) {
+        final_rows<KP>(x, base, C, rows, r0, sw, sa, stg, lane, part);
+        const int r = r0 + lane;
+        if (r < rows) {
 #pragma unroll
-        for (int j = 0; j < KP; j++) part[j] = 0.f;
-        const float4* xr = reinterpret_cast<const float4*>(x + (base + r) * C);
-        for (int c4 = 0; c4 < (C >> 2); c4++) {
-            const float4 v = __ldg(xr + c4);
-            const float e[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int u = 0; u < 4; u++) {
-                const int c = 4 * c4 + u;
-                const float2 al = sa[c];
-                const float sn = snake_f(e[u], al.x, al.y);
-#pragma unroll
-                for (int q = 0; q < KP / 4; q++) {
-                    const float4 wq = sw[c * (KP / 4) + q];
-                    part[4 * q] = fmaf(wq.x, sn, part[4 * q]);
-                    part[4 * q + 1] = fmaf(wq.y, sn, part[4 * q + 1]);
-                    part[4 * q + 2] = fmaf(wq.z, sn, part[4 * q + 2]);
-                    part[4 * q + 3] = fmaf(wq.w, sn, part[4 * q + 3]);
-                }
-            }
+            for (int j = 0; j < KP; j++)
+                if (j < k) sp[r * k + j] = part[j];
         }
-#pragma unroll
-        for (int j = 0; j < KP; j++)
-            if (j < k) sp[r * k + j] = part[j];
     }
     __syncthreads();
     const int m = threadIdx.x;
@@ -400,6 +535,13 @@ __global__ void __launch_bounds__(kFinalTile) final_conv_kernel(
     }
 }
 
+size_t final_conv_smem_bytes(int C, int k)
+{
+    const int KP = k <= 8 ? 8 : 16;
+    return sizeof(float) * ((size_t)KP * C + 2 * (size_t)C + (size_t)(kFinalTile / 32) * 32 * 9 * 4 +
+                            (size_t)(kFinalTile + k - 1) * k);
+}
+
 cudaError_t launch_final_conv(const float* x, Layout xl, int C, const float* w, const float* bias,
                               const float* alpha, const float* inv_alpha, int k, float* audio,
                               float* pre_tanh, long long audio_ld, int spf, PlanView plan, const int* tcum,
@@ -408,7 +550,7 @@ cudaError_t launch_final_conv(const float* x, Layout xl, int C, const float* w, 
     if (n_row_tiles <= 0) return cudaSuccess;
     if (k > kFinalMaxK) return cudaErrorInvalidValue;
     const int KP = k <= 8 ? 8 : 16;
-    const size_t smem = sizeof(float) * ((size_t)KP * C + 2 * (size_t)C + (size_t)(kFinalTile + k - 1) * k);
+    const size_t smem = final_conv_smem_bytes(C, k);
     if (smem > (size_t)kFinalMaxSmem) return cudaErrorInvalidValue;
     if (KP == 8)
         launch_pdl(final_conv_kernel<8>, dim3(n_row_tiles), dim3(kFinalTile), smem, s, x, xl, C, w, bias, alpha,

@@ -302,10 +302,10 @@ __device__ __forceinline__ float* epi_dst4(const GemmArgs& a, const PlanView& pl
         if (a.d & 3) return nullptr;
         if (n < a.d) return a.out + out_row * a.d + n;
         if (b < 0) {                // dense tiling: t is the row over all segments
-            b = find_seg(plan.cf, plan.B, t);
-            t -= __ldg(plan.cf + b);
+            b = find_seg_r(plan.cf, plan.B, t, a.pos_r);
+            t -= __ldg(plan.cf + b) * a.pos_r;
         }
-        const long long pos = __ldg(plan.pos0 + b) + t;
+        const long long pos = __ldg(plan.pos0 + b) * a.pos_r + t;
         const long long rr = (long long)__ldg(plan.slot + b) * a.ring_R + (pos & (a.ring_R - 1));
         return n < 2 * a.d ? a.kring + rr * a.d + (n - a.d) : a.vring + rr * a.d + (n - 2 * a.d);
     }
@@ -1196,6 +1196,7 @@ int run_tc_conv1d(const TcOpScratch& sc, const float* x, int T, int Cin, const f
     a.out_step = 1;
     a.epi = EPI_STORE;
     a.scale = 1.f;
+    a.pos_r = 1;
     a.tcum = words + kOpPlan + 6;
     a.bm = kBM;
     PlanView plan{1, words + kOpPlan + 2, words + kOpPlan + 4, reinterpret_cast<const long long*>(words + kOpPlan),

@@ -45,9 +45,17 @@ std::vector<Tensor> blob_tensors(const codec_config* c)
     auto two = [&](int64_t r, int64_t l) { t.push_back({K_2D, r, l, 1, r * l}); };
     auto conv = [&](int64_t co, int64_t ci, int64_t k) { t.push_back({K_CONV, co, ci, k, co * ci * k}); };
     auto convt = [&](int64_t ci, int64_t co, int64_t k) { t.push_back({K_CONVT, ci, co, k, ci * co * k}); };
-    for (int q = 0; q < c->Q; q++) two(c->V, c->E);
-    conv(c->d, c->E, c->pre_k);
-    vec(c->d);
+    if (c->latent_dim) {                     // mu, sigma, projection, depthwise taps [d][1][2 s], bias
+        vec(c->latent_dim);
+        vec(c->latent_dim);
+        two(c->d, c->latent_dim);
+        conv(c->d, 1, 2 * c->tf_up);
+        vec(c->d);
+    } else {
+        for (int q = 0; q < c->Q; q++) two(c->V, c->E);
+        conv(c->d, c->E, c->pre_k);
+        vec(c->d);
+    }
     for (int l = 0; l < c->layers; l++) {
         vec(c->d);
         for (int i = 0; i < 4; i++) two(c->d, c->d);

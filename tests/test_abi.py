@@ -39,7 +39,7 @@ def test_invalid_configs_rejected(lib):
     bad = [
         ("heads", 5),          # d % heads != 0
         ("window", 0),
-        ("window", 129),
+        ("window", 257),       # the attention kernel takes windows up to 256
         ("up_k", 3),           # kernel must be 2 * stride
         ("E", 6),              # channel counts are multiples of 4
         ("max_batch_frames", 1),
