@@ -302,37 +302,56 @@ __global__ void __launch_bounds__(kSwaThreads) swa_kernel(
         sq[r * ld4 + c4] = __ldg(reinterpret_cast<const float4*>(q + (row0 + r) * d + h * dh + 4 * c4));
     }
     __syncthreads();
-    // scores of every (query, key) pair the block holds, four keys per
-    // thread (four independent chains; each dot product still runs over the
-    // channels in ascending order); keys outside a query's window are skipped
+    // scores of every (query, key) pair the block holds, in register tiles of
+    // 4 queries x 4 keys per thread (8 shared loads per 64 FMAs); each dot
+    // product still runs over the channels in ascending order.  A thread's keys
+    // are j, j + nk4, j + 2 nk4, j + 3 nk4, so consecutive threads read
+    // consecutive key rows (conflict-free 128-bit loads); keys outside a
+    // query's window are skipped
     const float scale = 1.0f / sqrtf((float)dh);
     const int nk4 = (nk + 3) >> 2;
-    for (int i = tid; i < nq * nk4; i += kSwaThreads) {
-        // keys j, j + nk4, j + 2 nk4, j + 3 nk4: consecutive threads read
-        // consecutive key rows (conflict-free 128-bit shared loads)
-        const int qi = i / nk4, j = i - qi * nk4;
-        const long long pos = p0 + qi;
-        const float4* qr = sq + qi * ld4;
-        float dot[4] = {0.f, 0.f, 0.f, 0.f};
+    const int nq4 = (nq + 3) >> 2;
+    for (int i = tid; i < nq4 * nk4; i += kSwaThreads) {
+        const int qg = i / nk4, j = i - qg * nk4;
         const float4* kr[4];
-#pragma unroll
-        for (int u = 0; u < 4; u++) kr[u] = sk + min(j + u * nk4, nk - 1) * ld4;
-        for (int c4 = 0; c4 < dh4; c4++) {
-            const float4 a = qr[c4];
-#pragma unroll
-            for (int u = 0; u < 4; u++) {
-                const float4 k4 = kr[u][c4];
-                dot[u] = fmaf(a.x, k4.x, dot[u]);
-                dot[u] = fmaf(a.y, k4.y, dot[u]);
-                dot[u] = fmaf(a.z, k4.z, dot[u]);
-                dot[u] = fmaf(a.w, k4.w, dot[u]);
-            }
-        }
+        const float4* qr[4];
 #pragma unroll
         for (int u = 0; u < 4; u++) {
-            const int jj = j + u * nk4;
-            const long long kp = kstart + jj;
-            if (jj < nk && kp <= pos && kp >= pos - W + 1) sp[qi * lds + jj] = dot[u] * scale;
+            kr[u] = sk + min(j + u * nk4, nk - 1) * ld4;
+            qr[u] = sq + min(4 * qg + u, nq - 1) * ld4;
+        }
+        float dot[4][4];
+#pragma unroll
+        for (int a = 0; a < 4; a++)
+#pragma unroll
+            for (int u = 0; u < 4; u++) dot[a][u] = 0.f;
+        for (int c4 = 0; c4 < dh4; c4++) {
+            float4 k4[4], q4[4];
+#pragma unroll
+            for (int u = 0; u < 4; u++) {
+                k4[u] = kr[u][c4];
+                q4[u] = qr[u][c4];
+            }
+#pragma unroll
+            for (int a = 0; a < 4; a++)
+#pragma unroll
+                for (int u = 0; u < 4; u++) {
+                    dot[a][u] = fmaf(q4[a].x, k4[u].x, dot[a][u]);
+                    dot[a][u] = fmaf(q4[a].y, k4[u].y, dot[a][u]);
+                    dot[a][u] = fmaf(q4[a].z, k4[u].z, dot[a][u]);
+                    dot[a][u] = fmaf(q4[a].w, k4[u].w, dot[a][u]);
+                }
+        }
+#pragma unroll
+        for (int a = 0; a < 4; a++) {
+            const int qi = 4 * qg + a;
+            const long long pos = p0 + qi;
+#pragma unroll
+            for (int u = 0; u < 4; u++) {
+                const int jj = j + u * nk4;
+                const long long kp = kstart + jj;
+                if (qi < nq && jj < nk && kp <= pos && kp >= pos - W + 1) sp[qi * lds + jj] = dot[a][u] * scale;
+            }
         }
     }
     __syncthreads();
@@ -357,29 +376,46 @@ __global__ void __launch_bounds__(kSwaThreads) swa_kernel(
         if (lane == 0) sz[qi] = 1.0f / z;
     }
     __syncthreads();
-    // outputs, four channels per thread (four independent chains; each
+    // outputs, eight channels per thread (eight independent chains; each
     // channel's sum runs over the query's keys in position order)
-    for (int i = tid; i < nq * dh4; i += kSwaThreads) {
-        const int qi = i / dh4, c4 = i - qi * dh4;
+    // a thread's float4 columns are c4 and c4 + dh4 / 2: consecutive threads
+    // read consecutive 16-byte columns (conflict-free)
+    const int per = (dh4 & 1) ? 1 : 2;                  // float4s per thread
+    const int groups = dh4 / per;
+    for (int i = tid; i < nq * groups; i += kSwaThreads) {
+        const int qi = i / groups, c4 = i - qi * groups;
         const long long pos = p0 + qi;
         const long long lo = pos - W + 1 > 0 ? pos - W + 1 : 0;
         const int nkq = (int)(pos - lo + 1);
         const int off = (int)(lo - kstart);
         const float* pr = sp + qi * lds + off;
         const float4* vc = sv + (size_t)off * ld4 + c4;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int k = 0; k < nkq; k++) {
-            const float pk = pr[k];
-            const float4 v4 = vc[(size_t)k * ld4];
-            acc.x = fmaf(pk, v4.x, acc.x);
-            acc.y = fmaf(pk, v4.y, acc.y);
-            acc.z = fmaf(pk, v4.z, acc.z);
-            acc.w = fmaf(pk, v4.w, acc.w);
+        float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f), acc1 = acc0;
+        if (per == 2) {
+            for (int k = 0; k < nkq; k++) {
+                const float pk = pr[k];
+                const float4 v0 = vc[(size_t)k * ld4], v1 = vc[(size_t)k * ld4 + groups];
+                acc0.x = fmaf(pk, v0.x, acc0.x); acc0.y = fmaf(pk, v0.y, acc0.y);
+                acc0.z = fmaf(pk, v0.z, acc0.z); acc0.w = fmaf(pk, v0.w, acc0.w);
+                acc1.x = fmaf(pk, v1.x, acc1.x); acc1.y = fmaf(pk, v1.y, acc1.y);
+                acc1.z = fmaf(pk, v1.z, acc1.z); acc1.w = fmaf(pk, v1.w, acc1.w);
+            }
+        } else {
+            for (int k = 0; k < nkq; k++) {
+                const float pk = pr[k];
+                const float4 v0 = vc[(size_t)k * ld4];
+                acc0.x = fmaf(pk, v0.x, acc0.x); acc0.y = fmaf(pk, v0.y, acc0.y);
+                acc0.z = fmaf(pk, v0.z, acc0.z); acc0.w = fmaf(pk, v0.w, acc0.w);
+            }
         }
         const float iz = sz[qi];
-        const float4 y = make_float4(acc.x * iz, acc.y * iz, acc.z * iz, acc.w * iz);
-        if (planes) plane_store4(planes, planes_il, row0 + qi, d, h * dh + 4 * c4, y);
-        else *reinterpret_cast<float4*>(o + (row0 + qi) * d + h * dh + 4 * c4) = y;
+        for (int e = 0; e < per; e++) {
+            const float4 a = e ? acc1 : acc0;
+            const float4 y = make_float4(a.x * iz, a.y * iz, a.z * iz, a.w * iz);
+            const int ch = h * dh + 4 * (c4 + e * groups);
+            if (planes) plane_store4(planes, planes_il, row0 + qi, d, ch, y);
+            else *reinterpret_cast<float4*>(o + (row0 + qi) * d + ch) = y;
+        }
     }
 }
 
