@@ -397,7 +397,11 @@ CODEC_API int32_t codec_state_last_launches(const codec_state_t* state);
  * sums the event intervals per kernel kind and stops recording.  Each
  * record also carries the algorithmic work of its launch: useful
  * floating-point operations (2 per multiply-add) and the bytes the operation
- * must move at minimum (inputs read once, outputs written once). */
+ * must move at minimum (inputs read once, outputs written once).  While
+ * recording, a call runs the resblocks of each multi-receptive-field block one
+ * after the other on the caller's stream (otherwise resblocks 1 and 2 run
+ * concurrently with resblock 0 on internal streams), so that no two recorded
+ * launches overlap; the results are the same either way. */
 typedef enum codec_kernel_kind {
     CODEC_KERNEL_GATHER = 0,
     CODEC_KERNEL_GEMM_SIMT = 1,

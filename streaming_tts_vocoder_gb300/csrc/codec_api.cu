@@ -113,6 +113,14 @@ struct codec_state_s {
     float* rbuf[8][4][4] = {};
     float* y[8] = {};
     TcScratch tc_scratch;
+    // Resblock chains 1 and 2 of an MRF run their convs before the last one on
+    // side streams, each with its own operand planes and split-K partials
+    // (chain 0 uses tc_scratch on the caller's stream).
+    static constexpr int kChains = 3;
+    TcScratch tc_chain[kChains - 1];
+    cudaStream_t side[kChains - 1] = {};
+    cudaEvent_t fork_ev = nullptr;
+    cudaEvent_t done_ev[kChains - 1] = {};
     // plan: device copy and a ring of page-locked host staging copies
     int plan_ints = 0;
     int off_pos0 = 0, off_cf = 0, off_slot = 0, off_bidx = 0, off_tc64 = 0, off_tc128 = 0, off_q16 = 0, off_skip = 0;
@@ -620,6 +628,28 @@ codec_status codec_state_create(codec_t* c, int32_t n_streams, codec_state_t** o
         // split-GEMM partials: 64 M floats (256 MB)
         if (!tc_scratch_alloc(&s->tc_scratch, std::max<size_t>(elems, 4), b_elems, size_t(64) << 20, A))
             st = CODEC_ERR_OOM;
+        // the side chains' planes, sized for the stages' inputs, and partials
+        if (st == CODEC_OK && g.n_rb > 1) {
+            size_t st_elems = 4;
+            for (int si = 0; si < g.n_stages; si++)
+                for (int j = 1; j < g.n_rb; j++)
+                    for (int i = 0; i < g.n_dil; i++) {
+                        const Contraction& C = c->rb[c->rb_index(si, j, i)];
+                        if (C.use_tc) st_elems = std::max(st_elems, rows(lt + g.n_up + 1 + si, true) * (size_t)C.Cin);
+                    }
+            for (int j = 0; j < std::min(g.n_rb, (int)codec_state_s::kChains) - 1 && st == CODEC_OK; j++) {
+                if (!tc_scratch_alloc(&s->tc_chain[j], st_elems, 1, size_t(64) << 20, A)) st = CODEC_ERR_OOM;
+                s->tc_chain[j].err = s->tc_scratch.err;      // one timeout flag for the state
+            }
+        }
+    }
+    if (st == CODEC_OK && g.n_rb > 1) {
+        for (int j = 0; j < codec_state_s::kChains - 1 && st == CODEC_OK; j++)
+            if (cudaStreamCreateWithFlags(&s->side[j], cudaStreamNonBlocking) != cudaSuccess ||
+                cudaEventCreateWithFlags(&s->done_ev[j], cudaEventDisableTiming) != cudaSuccess)
+                st = CODEC_ERR_CUDA;
+        if (st == CODEC_OK && cudaEventCreateWithFlags(&s->fork_ev, cudaEventDisableTiming) != cudaSuccess)
+            st = CODEC_ERR_CUDA;
     }
     if (st == CODEC_OK && cudaDeviceSynchronize() != cudaSuccess) st = CODEC_ERR_CUDA;
     if (st != CODEC_OK) {
@@ -630,6 +660,11 @@ codec_status codec_state_create(codec_t* c, int32_t n_streams, codec_state_t** o
         if (s->slots_h) cudaFreeHost(s->slots_h);
         if (s->slots_ev) cudaEventDestroy(s->slots_ev);
         if (s->cap_stream) cudaStreamDestroy(s->cap_stream);
+        for (int j = 0; j < codec_state_s::kChains - 1; j++) {
+            if (s->side[j]) cudaStreamDestroy(s->side[j]);
+            if (s->done_ev[j]) cudaEventDestroy(s->done_ev[j]);
+        }
+        if (s->fork_ev) cudaEventDestroy(s->fork_ev);
         free_all(A);
         delete s;
         return st;
@@ -651,6 +686,11 @@ void codec_state_destroy(codec_state_t* s)
     for (cudaEvent_t e : s->prof_ev) cudaEventDestroy(e);
     for (GraphEntry& e : s->graphs) cudaGraphExecDestroy(e.exec);
     if (s->cap_stream) cudaStreamDestroy(s->cap_stream);
+    for (int j = 0; j < codec_state_s::kChains - 1; j++) {
+        if (s->side[j]) cudaStreamDestroy(s->side[j]);
+        if (s->done_ev[j]) cudaEventDestroy(s->done_ev[j]);
+    }
+    if (s->fork_ev) cudaEventDestroy(s->fork_ev);
     free_all(s->allocs);
     delete s;
 }
@@ -681,6 +721,7 @@ codec_status codec_state_set_wait_limit(codec_state_t* s, uint32_t polls, int32_
     s->seen.clear();
     s->tc_scratch.wait = wl;
     s->tc_scratch.op.wait = wl;
+    for (TcScratch& t : s->tc_chain) t.wait = wl;
     return CODEC_OK;
 }
 
@@ -815,6 +856,7 @@ namespace {
 struct Launcher {
     codec_state_s* s;
     cudaStream_t cs;
+    TcScratch* scr = nullptr;               // operand planes and partials of the current chain
     PlanView pv;
     const int* tc64;     // device, [levels][S + 1]
     const int* tc128;
@@ -891,14 +933,14 @@ struct Launcher {
             a.dense = (il.P == 0 && ol.P == 0 && C.ntaps == 1 && out_step == 1) ? 1 : 0;
             const int n_row_tiles = a.dense ? (int)((rows(in_lvl) + 127) / 128) : ntiles128[in_lvl];
             const long long arows = il.P ? rows_pref(in_lvl, il) : rows(in_lvl);
+            TcScratch* sc = scr ? scr : &s->tc_scratch;
             if (!from_producer)
                 run(CODEC_KERNEL_OPERAND_PREP, 0.0, 8.0 * (double)arows * C.Cin, what, [&] {
-                    return launch_tc_prep(in, C.alpha, C.inv_alpha, arows, C.Cin, &s->tc_scratch, C.tc.passes == 3,
-                                          cs);
+                    return launch_tc_prep(in, C.alpha, C.inv_alpha, arows, C.Cin, sc, C.tc.passes == 3, cs);
                 });
             int extra = 0;
             run(CODEC_KERNEL_GEMM_TC, flops, bytes, what, [&] {
-                return launch_tc_gemm(a, C.tc, pv, n_row_tiles, &s->tc_scratch, arows, s->c->num_sms, cs, &extra);
+                return launch_tc_gemm(a, C.tc, pv, n_row_tiles, sc, arows, s->c->num_sms, cs, &extra);
             });
             launches += extra > 1 ? extra - 1 : 0;   // the split reduction, timed with its GEMM
         } else {
@@ -1079,17 +1121,44 @@ void enqueue_decode(codec_state_t* s, Launcher& L, const void* input, int32_t T_
         const int C = g.ch[si];
         L.gemm(c->st[si], x, lay(xl), xl, s->x0[si], lay(lvl), C, g.strides[si], nullptr, EPI_STORE, 1.f, 0,
                "stage upsample");
+        // The resblocks of an MRF are independent until their sum: every conv but
+        // the last of resblock j > 0 runs on side stream j - 1 with its own
+        // scratch, concurrently with resblock 0 on cs; the last convs then add
+        // into y in resblock order on cs, so the sum's order (and its bits) is
+        // that of a serial run.
+        // (serial while per-launch timing is on: concurrent launches would
+        // overlap each other's event intervals)
+        const bool fork = g.n_rb > 1 && s->side[0] != nullptr && !s->prof_on;
+        if (fork && L.err == cudaSuccess) {
+            if (cudaEventRecord(s->fork_ev, cs) != cudaSuccess) L.err = cudaErrorUnknown;
+            for (int j = 1; j < g.n_rb && L.err == cudaSuccess; j++)
+                if (cudaStreamWaitEvent(s->side[j - 1], s->fork_ev, 0) != cudaSuccess) L.err = cudaErrorUnknown;
+        }
+        float* last_in[4] = {};
         for (int j = 0; j < g.n_rb; j++) {
+            const bool on_side = fork && j > 0;
+            L.cs = on_side ? s->side[j - 1] : cs;
+            L.scr = on_side ? &s->tc_chain[j - 1] : nullptr;
             const float* rin = s->x0[si];
-            for (int ii = 0; ii < g.n_dil; ii++) {
-                const bool last_d = ii == g.n_dil - 1;
-                float* out = last_d ? s->y[si] : s->rbuf[si][j][ii + 1];
-                int epi = EPI_RESID;
-                if (last_d && g.n_rb > 1) epi = j == 0 ? EPI_MRF_FIRST : (j == g.n_rb - 1 ? EPI_MRF_LAST : EPI_MRF_ADD);
-                L.gemm(c->rb[c->rb_index(si, j, ii)], rin, lay(lvl), lvl, out, lay(lvl), C, 1, rin, epi,
+            for (int ii = 0; ii < g.n_dil - 1; ii++) {
+                float* out = s->rbuf[si][j][ii + 1];
+                L.gemm(c->rb[c->rb_index(si, j, ii)], rin, lay(lvl), lvl, out, lay(lvl), C, 1, rin, EPI_RESID,
                        1.0f / (float)g.n_rb, 0, "resblock conv");
                 rin = out;
             }
+            last_in[j] = const_cast<float*>(rin);
+            if (on_side && L.err == cudaSuccess && cudaEventRecord(s->done_ev[j - 1], L.cs) != cudaSuccess)
+                L.err = cudaErrorUnknown;
+        }
+        L.cs = cs;
+        L.scr = nullptr;
+        for (int j = 0; j < g.n_rb; j++) {
+            if (fork && j > 0 && L.err == cudaSuccess && cudaStreamWaitEvent(cs, s->done_ev[j - 1], 0) != cudaSuccess)
+                L.err = cudaErrorUnknown;
+            int epi = EPI_RESID;
+            if (g.n_rb > 1) epi = j == 0 ? EPI_MRF_FIRST : (j == g.n_rb - 1 ? EPI_MRF_LAST : EPI_MRF_ADD);
+            L.gemm(c->rb[c->rb_index(si, j, g.n_dil - 1)], last_in[j], lay(lvl), lvl, s->y[si], lay(lvl), C, 1,
+                   last_in[j], epi, 1.0f / (float)g.n_rb, 0, "resblock conv");
         }
         x = s->y[si];
         xl = lvl;

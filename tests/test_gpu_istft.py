@@ -17,7 +17,9 @@ pytestmark = pytest.mark.gpu
 
 # (n_fft, hop): Vocos at 24 kHz, Kokoro's iSTFTNet (the Core AI note: stride 5, 11 bins), HiFT-sized,
 # and a non-power-of-two size with two frames per sample
-CONFIGS = [(1024, 256), (20, 5), (16, 4), (48, 24)]
+# powers of two with even log2 (radix-4 stages only) and odd log2 (one radix-2
+# stage first: 32, 512), and sizes that take the direct DFT (20, 48)
+CONFIGS = [(1024, 256), (20, 5), (16, 4), (48, 24), (32, 8), (512, 128)]
 # the oracle is float64; the kernels sum in float32 (FFT, overlap-add): errors are rounding-sized
 REL_L2, MAX_ABS_REL = 1e-5, 1e-4
 

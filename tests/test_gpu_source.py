@@ -75,7 +75,7 @@ def test_sine_ragged_vs_oracle_and_chunking(upp, fs, H):
     assert np.array_equal(np.concatenate(parts), full)
 
 
-@pytest.mark.parametrize("n_fft,hop", [(1024, 256), (20, 5), (16, 4), (48, 24)])
+@pytest.mark.parametrize("n_fft,hop", [(1024, 256), (20, 5), (16, 4), (48, 24), (32, 8), (512, 128)])
 def test_stft_ragged_vs_oracle_and_chunking(n_fft, hop):
     S, F, chunk = 5, 40, 11
     st = C.Stft(n_fft, hop, max_streams=S, max_chunk_frames=chunk)
