@@ -411,7 +411,8 @@ typedef enum codec_kernel_kind {
     CODEC_KERNEL_ATTENTION = 5,
     CODEC_KERNEL_FINAL_CONV = 6,
     CODEC_KERNEL_HISTORY = 7,
-    CODEC_KERNEL_KINDS = 8
+    CODEC_KERNEL_MRF_SUM = 8,   /* the MRF average of a small call's separately written resblocks */
+    CODEC_KERNEL_KINDS = 9
 } codec_kernel_kind;
 
 typedef struct codec_kernel_stats {

@@ -52,7 +52,7 @@ class CodecConfigC(ctypes.Structure):
 
 
 KERNEL_KINDS = ["gather", "gemm_simt", "gemm_tc", "operand_prep", "rmsnorm", "attention", "final_conv",
-                "history"]
+                "history", "mrf_sum"]
 
 
 class KernelStatsC(ctypes.Structure):

@@ -112,6 +112,9 @@ struct codec_state_s {
     float* x0[8] = {};
     float* rbuf[8][4][4] = {};
     float* y[8] = {};
+    // small calls: resblocks 1 and 2's own outputs before the MRF sum
+    static constexpr int kMrfSmallFrames = 8;
+    float* ymrf[8][4] = {};
     TcScratch tc_scratch;
     // Resblock chains 1 and 2 of an MRF run their convs before the last one on
     // side streams, each with its own operand planes and split-K partials
@@ -644,6 +647,12 @@ codec_status codec_state_create(codec_t* c, int32_t n_streams, codec_state_t** o
         }
     }
     if (st == CODEC_OK && g.n_rb > 1) {
+        for (int si = 0; si < g.n_stages; si++) {
+            const int lvl = lt + g.n_up + 1 + si;
+            const size_t n = ((size_t)codec_state_s::kMrfSmallFrames * c->level_r[lvl] +
+                              (size_t)std::min(S, codec_state_s::kMrfSmallFrames) * s->P[lvl]) * g.ch[si];
+            for (int j = 1; j < g.n_rb; j++) s->ymrf[si][j] = dev_alloc<float>(A, n, st);
+        }
         for (int j = 0; j < codec_state_s::kChains - 1 && st == CODEC_OK; j++)
             if (cudaStreamCreateWithFlags(&s->side[j], cudaStreamNonBlocking) != cudaSuccess ||
                 cudaEventCreateWithFlags(&s->done_ev[j], cudaEventDisableTiming) != cudaSuccess)
@@ -1134,6 +1143,10 @@ void enqueue_decode(codec_state_t* s, Launcher& L, const void* input, int32_t T_
             for (int j = 1; j < g.n_rb && L.err == cudaSuccess; j++)
                 if (cudaStreamWaitEvent(s->side[j - 1], s->fork_ev, 0) != cudaSuccess) L.err = cudaErrorUnknown;
         }
+        // a small call (first audio) also runs each resblock's last conv on its
+        // own stream into its own buffer, and one kernel forms the MRF sum
+        // with the same additions in the same order
+        const bool split_mrf = fork && L.frames <= codec_state_s::kMrfSmallFrames && s->ymrf[si][1] != nullptr;
         float* last_in[4] = {};
         for (int j = 0; j < g.n_rb; j++) {
             const bool on_side = fork && j > 0;
@@ -1147,12 +1160,27 @@ void enqueue_decode(codec_state_t* s, Launcher& L, const void* input, int32_t T_
                 rin = out;
             }
             last_in[j] = const_cast<float*>(rin);
+            if (split_mrf) {
+                float* out = j == 0 ? s->y[si] : s->ymrf[si][j];
+                L.gemm(c->rb[c->rb_index(si, j, g.n_dil - 1)], rin, lay(lvl), lvl, out, lay(lvl), C, 1, rin,
+                       EPI_RESID, 1.0f / (float)g.n_rb, 0, "resblock conv");
+            }
             if (on_side && L.err == cudaSuccess && cudaEventRecord(s->done_ev[j - 1], L.cs) != cudaSuccess)
                 L.err = cudaErrorUnknown;
         }
         L.cs = cs;
         L.scr = nullptr;
-        for (int j = 0; j < g.n_rb; j++) {
+        if (split_mrf) {
+            for (int j = 1; j < g.n_rb; j++)
+                if (L.err == cudaSuccess && cudaStreamWaitEvent(cs, s->done_ev[j - 1], 0) != cudaSuccess)
+                    L.err = cudaErrorUnknown;
+            const double R = (double)L.rows(lvl);
+            L.run(CODEC_KERNEL_MRF_SUM, R * C * g.n_rb, 4.0 * R * C * (g.n_rb + 1), "MRF sum", [&] {
+                return launch_mrf_sum(s->y[si], s->ymrf[si][1], g.n_rb > 2 ? s->ymrf[si][2] : nullptr, lay(lvl), C,
+                                      1.0f / (float)g.n_rb, L.pv, L.rows(lvl), cs);
+            });
+        }
+        for (int j = 0; j < g.n_rb && !split_mrf; j++) {
             if (fork && j > 0 && L.err == cudaSuccess && cudaStreamWaitEvent(cs, s->done_ev[j - 1], 0) != cudaSuccess)
                 L.err = cudaErrorUnknown;
             int epi = EPI_RESID;

@@ -51,6 +51,11 @@ cudaError_t launch_final_conv(const float* x, Layout xl, int C, const float* w, 
                               float* pre_tanh, long long audio_ld, int spf, PlanView plan, const int* tcum,
                               int n_row_tiles, cudaStream_t s);
 
+// y = ((y + y1) + y2) * scale over the chunk rows of a prefixed level (y2 may
+// be null), the multi-receptive-field average of separately written resblocks.
+cudaError_t launch_mrf_sum(float* y, const float* y1, const float* y2, Layout l, int C, float scale, PlanView plan,
+                           long long total_rows, cudaStream_t s);
+
 // Sets the kernels' shared-memory carve-outs; called once per codec.
 cudaError_t configure_simt_kernels();
 

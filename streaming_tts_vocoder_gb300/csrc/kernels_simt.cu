@@ -254,7 +254,7 @@ cudaError_t launch_rms_norm(const float* x, Layout xl, const float* g, float eps
 // a ring of keys and values; item 11: softmax with max subtraction).
 constexpr int kSwaMaxW = kSwaWindowMax;
 constexpr int kSwaMaxDh = 128;
-constexpr int kSwaThreads = 256;
+constexpr int kSwaThreads = 512;
 constexpr int kSwaWarps = kSwaThreads / 32;
 constexpr int kSwaMaxSmem = (int)kSwaSmemMax;
 
@@ -594,6 +594,48 @@ cudaError_t launch_final_conv(const float* x, Layout xl, int C, const float* w, 
     else
         launch_pdl(final_conv_kernel<16>, dim3(n_row_tiles), dim3(kFinalTile), smem, s, x, xl, C, w, bias, alpha,
                    inv_alpha, k, audio, pre_tanh, audio_ld, spf, plan, plan.bidx, tcum);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------ MRF sum --
+// y = ((y + y1) + y2) * scale (y2 may be null: (y + y1) * scale), rounded at
+// each step, over the chunk rows of every segment of a prefixed level: the
+// multi-receptive-field average of resblocks whose last convs wrote separate
+// buffers, in the same order and with the same roundings as the chained MRF
+// epilogues (first, add, last) of the GEMM.
+__global__ void __launch_bounds__(256) mrf_sum_kernel(float* __restrict__ y, const float* __restrict__ y1,
+                                                      const float* __restrict__ y2, Layout l, int C, float scale,
+                                                      PlanView plan, long long total_rows)
+{
+    pdl_wait();
+    pdl_launch();
+    const int C4 = C >> 2;
+    const long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+    if (i >= total_rows * C4) return;
+    const long long row = i / C4;
+    const int c4 = (int)(i - row * C4);
+    const int b = find_seg_r(plan.cf, plan.B, row, l.r);
+    const long long t = row - (long long)__ldg(plan.cf + b) * l.r;
+    const long long at = (seg_base(l, plan.cf, b) + t) * C4 + c4;
+    float4 v = reinterpret_cast<float4*>(y)[at];
+    const float4 a = reinterpret_cast<const float4*>(y1)[at];
+    v = make_float4(__fadd_rn(v.x, a.x), __fadd_rn(v.y, a.y), __fadd_rn(v.z, a.z), __fadd_rn(v.w, a.w));
+    if (y2) {
+        const float4 e = reinterpret_cast<const float4*>(y2)[at];
+        v = make_float4(__fadd_rn(v.x, e.x), __fadd_rn(v.y, e.y), __fadd_rn(v.z, e.z), __fadd_rn(v.w, e.w));
+    }
+    reinterpret_cast<float4*>(y)[at] =
+        make_float4(__fmul_rn(v.x, scale), __fmul_rn(v.y, scale), __fmul_rn(v.z, scale), __fmul_rn(v.w, scale));
+}
+
+cudaError_t launch_mrf_sum(float* y, const float* y1, const float* y2, Layout l, int C, float scale, PlanView plan,
+                           long long total_rows, cudaStream_t s)
+{
+    if (total_rows <= 0) return cudaSuccess;
+    if (C % 4 != 0) return cudaErrorInvalidValue;
+    const long long n = total_rows * (C / 4);
+    launch_pdl(mrf_sum_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s, y, y1, y2, l, C, scale, plan,
+               total_rows);
     return cudaGetLastError();
 }
 
