@@ -552,9 +552,13 @@ def layer_labels(cfg):
     names += ["final rmsnorm"] + [f"latent up {u}" for u in range(len(cfg.up_channels))]
     for s in range(len(cfg.strides)):
         names.append(f"stage {s} convT")
+        # each resblock's convs but the last, resblock by resblock; then the
+        # last convs, which add into the MRF sum in resblock order
         for k in cfg.rb_kernels:
-            for d in cfg.dilations:
+            for d in cfg.dilations[:-1]:
                 names.append(f"stage {s} rb k{k} d{d}")
+        for k in cfg.rb_kernels:
+            names.append(f"stage {s} rb k{k} d{cfg.dilations[-1]}")
     return names + ["final conv", "history commit"]
 
 
