@@ -451,37 +451,46 @@ cudaError_t launch_swa(const float* q, float* o, const float* kring, const float
 // the k-1 history rows before them.  One input row in, one sample out
 // (blixt/phonon "Open work": a direct kernel for the last convolution with 1
 // output channel); with C Snakes per sample its cost is the sine, so this
-// kernel takes the sine as a Cody-Waite reduction of a x to [-pi, pi] (2 pi
-// split into a float and its remainder) and the hardware sine there (absolute
-// error a few 1e-7, against about 1e-7 for sinf): its Snake is not bit-equal
-// to the operand prep's, and nothing else reads it.
-__device__ __forceinline__ float snake_final(float x, float a, float inv_a)
-{
-    const float y = __fmul_rn(a, x);
-    const float k = rintf(y * 0.159154943091895336f);           // y / (2 pi), nearest integer
-    float r = __fmaf_rn(-k, 6.28318548202514648f, y);           // 2 pi rounded to float
-    r = __fmaf_rn(-k, -1.7484555314695172e-7f, r);              // 2 pi minus that float
-    const float sn = __sinf(r);
-    return __fadd_rn(x, __fmul_rn(__fmul_rn(sn, sn), inv_a));
-}
+// kernel takes it as a Cody-Waite reduction of a x to [-pi, pi] (2 pi split
+// into a float and its remainder) and the hardware sine there (absolute error
+// a few 1e-7, against about 1e-7 for sinf), and forms x + sin^2 / a with one
+// fused multiply-add; nothing else reads this Snake.
 constexpr int kFinalTile = 128;
+constexpr int kFinalWarps = kFinalTile / 32 + 1;   // four for the tile's rows, one for the k - 1 before them
 constexpr int kFinalMaxK = 16;
 constexpr int kFinalMaxSmem = (int)kFinalSmemMax;
 
+// The Snake of two channels' values at once, in packed fp32 operations (each
+// half rounds as the scalar operation would).
+__device__ __forceinline__ float2 snake_final2(float2 x, float2 a, float2 inv_a)
+{
+    const float2 y = __fmul2_rn(a, x);
+    const float2 t = __fmul2_rn(y, make_float2(0.159154943091895336f, 0.159154943091895336f));
+    const float2 nk = make_float2(-rintf(t.x), -rintf(t.y));     // -(y / (2 pi)), nearest integer
+    float2 r = __ffma2_rn(nk, make_float2(6.28318548202514648f, 6.28318548202514648f), y);   // 2 pi as a float
+    r = __ffma2_rn(nk, make_float2(-1.7484555314695172e-7f, -1.7484555314695172e-7f), r);   // and the rest
+    const float2 sn = make_float2(__sinf(r.x), __sinf(r.y));
+    return __ffma2_rn(__fmul2_rn(sn, sn), inv_a, x);
+}
+
 // KP: taps padded to 8 or 16.  The weights sit in shared memory as [C][KP]
-// (zero beyond k) and are read as float4s, the Snake parameters as float2s,
-// so a channel costs its Snake, KP/4 + 1 shared loads and KP FMAs.
+// (zero beyond k) and are read as float4s, the Snake parameters of a channel
+// pair as one float4 (a_c, a_c+1, 1/a_c, 1/a_c+1).  Snake runs on channel
+// pairs and the tap partials on tap pairs in packed fp32 (one instruction per
+// two roundings, each the one the scalar code makes), so a channel costs half
+// a Snake, KP/2 packed FMAs and KP/4 + 1/2 shared loads.
 // One warp's rows r0 .. r0 + 31 (those below `rows`) of the tile: their
 // channels come through shared memory 32 at a time, loaded by the whole warp
 // (each load instruction covers whole 128-byte row segments), and each lane
-// then takes its own row's 32 channels: Snake, then the KP tap partials.
+// then takes its own row's 32 channels: Snake, then the KP tap partials in
+// channel order.
 template <int KP>
 __device__ __forceinline__ void final_rows(const float* __restrict__ x, long long base, int C, int rows, int r0,
-                                           const float4* sw, const float2* sa, float4* stg, int lane, float* part)
+                                           const float4* sw, const float4* sa, float4* stg, int lane, float2* part)
 {
     constexpr int kPitch = 9;                                   // float4s per staged row (8 + 1 pad)
 #pragma unroll
-    for (int j = 0; j < KP; j++) part[j] = 0.f;
+    for (int j = 0; j < KP / 2; j++) part[j] = make_float2(0.f, 0.f);
     for (int c0 = 0; c0 < C; c0 += 32) {
         const int nq = min(32, C - c0) >> 2;                    // float4s of this chunk per row
         __syncwarp();
@@ -494,19 +503,19 @@ __device__ __forceinline__ void final_rows(const float* __restrict__ x, long lon
         if (r0 + lane < rows) {
             for (int q = 0; q < nq; q++) {
                 const float4 v = stg[lane * kPitch + q];
-                const float e[4] = {v.x, v.y, v.z, v.w};
+                const int cb = c0 + 4 * q;
+                const float4 p0 = sa[cb >> 1], p1 = sa[(cb >> 1) + 1];
+                const float2 s01 = snake_final2(make_float2(v.x, v.y), make_float2(p0.x, p0.y), make_float2(p0.z, p0.w));
+                const float2 s23 = snake_final2(make_float2(v.z, v.w), make_float2(p1.x, p1.y), make_float2(p1.z, p1.w));
+                const float sn[4] = {s01.x, s01.y, s23.x, s23.y};
 #pragma unroll
                 for (int u = 0; u < 4; u++) {
-                    const int c = c0 + 4 * q + u;
-                    const float2 al = sa[c];
-                    const float sn = snake_final(e[u], al.x, al.y);
+                    const float2 s2 = make_float2(sn[u], sn[u]);
 #pragma unroll
                     for (int g = 0; g < KP / 4; g++) {
-                        const float4 wq = sw[c * (KP / 4) + g];
-                        part[4 * g] = fmaf(wq.x, sn, part[4 * g]);
-                        part[4 * g + 1] = fmaf(wq.y, sn, part[4 * g + 1]);
-                        part[4 * g + 2] = fmaf(wq.z, sn, part[4 * g + 2]);
-                        part[4 * g + 3] = fmaf(wq.w, sn, part[4 * g + 3]);
+                        const float4 wq = sw[(cb + u) * (KP / 4) + g];
+                        part[2 * g] = __ffma2_rn(make_float2(wq.x, wq.y), s2, part[2 * g]);
+                        part[2 * g + 1] = __ffma2_rn(make_float2(wq.z, wq.w), s2, part[2 * g + 1]);
                     }
                 }
             }
@@ -515,7 +524,7 @@ __device__ __forceinline__ void final_rows(const float* __restrict__ x, long lon
 }
 
 template <int KP>
-__global__ void __launch_bounds__(kFinalTile) final_conv_kernel(
+__global__ void __launch_bounds__(kFinalWarps * 32) final_conv_kernel(
     const float* __restrict__ x, Layout xl, int C, const float* __restrict__ w,
     const float* __restrict__ bias, const float* __restrict__ alpha,
     const float* __restrict__ inv_alpha, int k, float* __restrict__ audio,
@@ -526,9 +535,9 @@ __global__ void __launch_bounds__(kFinalTile) final_conv_kernel(
     pdl_launch();
     extern __shared__ float4 sm4[];
     float4* sw = sm4;                                                   // [C][KP / 4]
-    float2* sa = reinterpret_cast<float2*>(sm4 + (size_t)C * (KP / 4)); // [C] (alpha, 1/alpha)
-    float4* stg = reinterpret_cast<float4*>(sa + C) + (threadIdx.x >> 5) * 32 * 9;   // per warp [32][9]
-    float* sp = reinterpret_cast<float*>(reinterpret_cast<float4*>(sa + C) + (kFinalTile / 32) * 32 * 9);
+    float4* sa = sm4 + (size_t)C * (KP / 4);                            // [C / 2] channel-pair Snake parameters
+    float4* stg = sa + C / 2 + (threadIdx.x >> 5) * 32 * 9;             // per warp [32][9]
+    float* sp = reinterpret_cast<float*>(sa + C / 2 + kFinalWarps * 32 * 9);
     // sp: [kFinalTile + k - 1][k] partials
     const int tile = blockIdx.x;
     const int b = find_seg(tcum, plan.B, tile);
@@ -541,20 +550,23 @@ __global__ void __launch_bounds__(kFinalTile) final_conv_kernel(
         const int c = i / KP, j = i - c * KP;
         swf[i] = j < k ? __ldg(w + (size_t)j * C + c) : 0.f;
     }
-    for (int i = threadIdx.x; i < C; i += blockDim.x) sa[i] = make_float2(__ldg(alpha + i), __ldg(inv_alpha + i));
+    for (int i = threadIdx.x; i < C / 2; i += blockDim.x)
+        sa[i] = make_float4(__ldg(alpha + 2 * i), __ldg(alpha + 2 * i + 1), __ldg(inv_alpha + 2 * i),
+                            __ldg(inv_alpha + 2 * i + 1));
     __syncthreads();
     const int rows = nrows + k - 1;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    float part[KP];
-    // rows 0 .. 127: warp w takes rows 32 w .. 32 w + 31; rows 128 .. rows - 1
-    // (the k - 1 past the tile): warp 0 again
-    for (int r0 = 32 * warp; r0 < rows; r0 += kFinalTile) {
+    float2 part[KP / 2];
+    // warp w takes rows 32 w .. 32 w + 31: the tile's k - 1 history rows and
+    // its first rows, ..., the last warp the tile's last k - 1 rows (all at once,
+    // not a second pass of one warp)
+    for (int r0 = 32 * warp; r0 < rows; r0 += 32 * kFinalWarps) {
         final_rows<KP>(x, base, C, rows, r0, sw, sa, stg, lane, part);
         const int r = r0 + lane;
         if (r < rows) {
 #pragma unroll
             for (int j = 0; j < KP; j++)
-                if (j < k) sp[r * k + j] = part[j];
+                if (j < k) sp[r * k + j] = (j & 1) ? part[j >> 1].y : part[j >> 1].x;
         }
     }
     __syncthreads();
@@ -574,7 +586,7 @@ __global__ void __launch_bounds__(kFinalTile) final_conv_kernel(
 size_t final_conv_smem_bytes(int C, int k)
 {
     const int KP = k <= 8 ? 8 : 16;
-    return sizeof(float) * ((size_t)KP * C + 2 * (size_t)C + (size_t)(kFinalTile / 32) * 32 * 9 * 4 +
+    return sizeof(float) * ((size_t)KP * C + 2 * (size_t)C + (size_t)kFinalWarps * 32 * 9 * 4 +
                             (size_t)(kFinalTile + k - 1) * k);
 }
 
@@ -584,15 +596,15 @@ cudaError_t launch_final_conv(const float* x, Layout xl, int C, const float* w, 
                               int n_row_tiles, cudaStream_t s)
 {
     if (n_row_tiles <= 0) return cudaSuccess;
-    if (k > kFinalMaxK) return cudaErrorInvalidValue;
+    if (k > kFinalMaxK || C % 4 != 0) return cudaErrorInvalidValue;
     const int KP = k <= 8 ? 8 : 16;
     const size_t smem = final_conv_smem_bytes(C, k);
     if (smem > (size_t)kFinalMaxSmem) return cudaErrorInvalidValue;
     if (KP == 8)
-        launch_pdl(final_conv_kernel<8>, dim3(n_row_tiles), dim3(kFinalTile), smem, s, x, xl, C, w, bias, alpha,
+        launch_pdl(final_conv_kernel<8>, dim3(n_row_tiles), dim3(kFinalWarps * 32), smem, s, x, xl, C, w, bias, alpha,
                    inv_alpha, k, audio, pre_tanh, audio_ld, spf, plan, plan.bidx, tcum);
     else
-        launch_pdl(final_conv_kernel<16>, dim3(n_row_tiles), dim3(kFinalTile), smem, s, x, xl, C, w, bias, alpha,
+        launch_pdl(final_conv_kernel<16>, dim3(n_row_tiles), dim3(kFinalWarps * 32), smem, s, x, xl, C, w, bias, alpha,
                    inv_alpha, k, audio, pre_tanh, audio_ld, spf, plan, plan.bidx, tcum);
     return cudaGetLastError();
 }
