@@ -526,17 +526,22 @@ def run_profile_call(args):
     S, CH, REPS = (int(v) for v in args.profile_call.split(","))
     import torch
     from streaming_tts_vocoder_gb300 import codec as C
-    cfg = qwen3_config() if args.decoder == "qwen3" else tiny_config()
+    cfg = CONFIGS[args.decoder]()
+    latent = bool(cfg.latent_dim)
     blob = pack_blob(cfg, make_weights(cfg, 0))
     prec = {"fp16x3": C.PRECISION_FP16X3, "fp16": C.PRECISION_FP16, "fp32": C.PRECISION_FP32}[args.precision]
     cod = C.Codec(cfg, blob, max_streams=S, max_chunk_frames=CH, max_batch_frames=S * CH, precision=prec)
     st = cod.state()
     st.set_graphs(False)
     dev = torch.device("cuda")
-    codes = torch.from_numpy(np.stack([make_codes(cfg, CH, 1000 + s) for s in range(S)])).to(dev)
+    mk = make_latents if latent else make_codes
+    inp = torch.from_numpy(np.stack([mk(cfg, CH, 1000 + s) for s in range(S)])).to(dev)
     audio = torch.empty(S, CH * cod.samples_per_frame, device=dev)
     for _ in range(REPS):
-        st.decode(codes, [CH] * S, audio)
+        if latent:
+            st.decode_latents(inp, [CH] * S, audio)
+        else:
+            st.decode(inp, [CH] * S, audio)
     torch.cuda.synchronize()
     print(json.dumps({"profile_call": [S, CH, REPS], "mean_abs": float(audio.abs().mean())}))
     return 0

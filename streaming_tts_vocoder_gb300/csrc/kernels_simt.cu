@@ -237,6 +237,21 @@ cudaError_t launch_rms_norm(const float* x, Layout xl, const float* g, float eps
     return cudaGetLastError();
 }
 
+// 16-byte global -> shared copy that bypasses the registers (both addresses
+// 16-byte aligned), and its group commit / wait.
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(smem)),
+                 "l"(gmem)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait()
+{
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // ---------------------------------------------- sliding-window attention --
 // A block takes up to kSwaQueries consecutive queries of one stream and one
 // head.  It stages the keys and values of every position they can see (at
@@ -291,16 +306,26 @@ __global__ void __launch_bounds__(kSwaThreads) swa_kernel(
     const long long slot_base = (long long)__ldg(plan.slot + b) * R;
     const long long row0 = (long long)__ldg(plan.cf + b) * pos_r + tq0;
     const int tid = threadIdx.x;
+    // staging by asynchronous 16-byte copies, every one of a thread's in
+    // flight at once: keys and queries (group 0), then values (group 1),
+    // which land while the scores and the softmax run
     for (int i = tid; i < nk * dh4; i += kSwaThreads) {
         const int r = i / dh4, c4 = i - r * dh4;
         const long long at = (slot_base + ((kstart + r) & (R - 1))) * d + h * dh + 4 * c4;
-        sk[r * ld4 + c4] = __ldg(reinterpret_cast<const float4*>(kring + at));
-        sv[r * ld4 + c4] = __ldg(reinterpret_cast<const float4*>(vring + at));
+        cp_async16(sk + r * ld4 + c4, kring + at);
     }
     for (int i = tid; i < nq * dh4; i += kSwaThreads) {
         const int r = i / dh4, c4 = i - r * dh4;
-        sq[r * ld4 + c4] = __ldg(reinterpret_cast<const float4*>(q + (row0 + r) * d + h * dh + 4 * c4));
+        cp_async16(sq + r * ld4 + c4, q + (row0 + r) * d + h * dh + 4 * c4);
     }
+    cp_async_commit();
+    for (int i = tid; i < nk * dh4; i += kSwaThreads) {
+        const int r = i / dh4, c4 = i - r * dh4;
+        const long long at = (slot_base + ((kstart + r) & (R - 1))) * d + h * dh + 4 * c4;
+        cp_async16(sv + r * ld4 + c4, vring + at);
+    }
+    cp_async_commit();
+    cp_async_wait<1>();
     __syncthreads();
     // scores of every (query, key) pair the block holds, in register tiles of
     // 4 queries x 4 keys per thread (8 shared loads per 64 FMAs); each dot
@@ -375,6 +400,7 @@ __global__ void __launch_bounds__(kSwaThreads) swa_kernel(
         for (int sh = 16; sh; sh >>= 1) z += __shfl_xor_sync(0xffffffffu, z, sh);
         if (lane == 0) sz[qi] = 1.0f / z;
     }
+    cp_async_wait<0>();
     __syncthreads();
     // outputs, eight channels per thread (eight independent chains; each
     // channel's sum runs over the query's keys in position order)
