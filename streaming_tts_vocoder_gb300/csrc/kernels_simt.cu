@@ -275,7 +275,7 @@ constexpr int kSwaMaxSmem = (int)kSwaSmemMax;
 
 // planes set: the attention output goes straight into the out-projection's
 // tensor-core operand planes (dense rows) instead of o.
-__global__ void __launch_bounds__(kSwaThreads) swa_kernel(
+__global__ void __launch_bounds__(kSwaThreads, 2) swa_kernel(
     const float* __restrict__ q, float* __restrict__ o, const float* __restrict__ kring,
     const float* __restrict__ vring, int d, int heads, int W, int R, int pos_r, PlanView plan,
     const int* __restrict__ qcum, void* planes, int planes_il)
@@ -402,45 +402,62 @@ __global__ void __launch_bounds__(kSwaThreads) swa_kernel(
     }
     cp_async_wait<0>();
     __syncthreads();
-    // outputs, eight channels per thread (eight independent chains; each
-    // channel's sum runs over the query's keys in position order)
-    // a thread's float4 columns are c4 and c4 + dh4 / 2: consecutive threads
-    // read consecutive 16-byte columns (conflict-free)
-    const int per = (dh4 & 1) ? 1 : 2;                  // float4s per thread
-    const int groups = dh4 / per;
-    for (int i = tid; i < nq * groups; i += kSwaThreads) {
-        const int qi = i / groups, c4 = i - qi * groups;
-        const long long pos = p0 + qi;
+    // outputs: a thread takes two consecutive queries and one float4 column
+    // (consecutive threads read consecutive 16-byte columns: conflict-free),
+    // so each value row it loads serves both queries.  Their windows differ
+    // by one key at each end: the first query's is union keys 0 .. n0 - 1,
+    // the second's d1 .. n0 (d1 = 0 while both windows start at position 0);
+    // each channel's sum runs over its own query's keys in position order.
+    const int npair = (nq + 1) >> 1;
+    for (int i = tid; i < npair * dh4; i += kSwaThreads) {
+        const int qp = i / dh4, c4 = i - qp * dh4;
+        const int qa = 2 * qp;
+        const bool two = qa + 1 < nq;
+        const long long pos = p0 + qa;
         const long long lo = pos - W + 1 > 0 ? pos - W + 1 : 0;
-        const int nkq = (int)(pos - lo + 1);
+        const int n0 = (int)(pos - lo + 1);
+        const int d1 = pos + 1 - W + 1 > 0 ? 1 : 0;      // the second window's first key in the union
         const int off = (int)(lo - kstart);
-        const float* pr = sp + qi * lds + off;
+        const float* pa = sp + qa * lds + off;
+        const float* pb = sp + (qa + 1) * lds + off + d1;  // pb[k - d1]: the second query's key k of the union
         const float4* vc = sv + (size_t)off * ld4 + c4;
         float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f), acc1 = acc0;
-        if (per == 2) {
-            for (int k = 0; k < nkq; k++) {
-                const float pk = pr[k];
-                const float4 v0 = vc[(size_t)k * ld4], v1 = vc[(size_t)k * ld4 + groups];
-                acc0.x = fmaf(pk, v0.x, acc0.x); acc0.y = fmaf(pk, v0.y, acc0.y);
-                acc0.z = fmaf(pk, v0.z, acc0.z); acc0.w = fmaf(pk, v0.w, acc0.w);
-                acc1.x = fmaf(pk, v1.x, acc1.x); acc1.y = fmaf(pk, v1.y, acc1.y);
-                acc1.z = fmaf(pk, v1.z, acc1.z); acc1.w = fmaf(pk, v1.w, acc1.w);
+        int k = 0;
+        if (d1) {
+            const float pk = pa[0];
+            const float4 v = vc[0];
+            acc0.x = fmaf(pk, v.x, acc0.x); acc0.y = fmaf(pk, v.y, acc0.y);
+            acc0.z = fmaf(pk, v.z, acc0.z); acc0.w = fmaf(pk, v.w, acc0.w);
+            k = 1;
+        }
+        if (two) {
+            for (; k < n0; k++) {
+                const float4 v = vc[(size_t)k * ld4];
+                const float pk = pa[k], qk = pb[k - d1];
+                acc0.x = fmaf(pk, v.x, acc0.x); acc0.y = fmaf(pk, v.y, acc0.y);
+                acc0.z = fmaf(pk, v.z, acc0.z); acc0.w = fmaf(pk, v.w, acc0.w);
+                acc1.x = fmaf(qk, v.x, acc1.x); acc1.y = fmaf(qk, v.y, acc1.y);
+                acc1.z = fmaf(qk, v.z, acc1.z); acc1.w = fmaf(qk, v.w, acc1.w);
             }
+            const float4 v = vc[(size_t)n0 * ld4];
+            const float qk = pb[n0 - d1];
+            acc1.x = fmaf(qk, v.x, acc1.x); acc1.y = fmaf(qk, v.y, acc1.y);
+            acc1.z = fmaf(qk, v.z, acc1.z); acc1.w = fmaf(qk, v.w, acc1.w);
         } else {
-            for (int k = 0; k < nkq; k++) {
-                const float pk = pr[k];
-                const float4 v0 = vc[(size_t)k * ld4];
-                acc0.x = fmaf(pk, v0.x, acc0.x); acc0.y = fmaf(pk, v0.y, acc0.y);
-                acc0.z = fmaf(pk, v0.z, acc0.z); acc0.w = fmaf(pk, v0.w, acc0.w);
+            for (; k < n0; k++) {
+                const float4 v = vc[(size_t)k * ld4];
+                const float pk = pa[k];
+                acc0.x = fmaf(pk, v.x, acc0.x); acc0.y = fmaf(pk, v.y, acc0.y);
+                acc0.z = fmaf(pk, v.z, acc0.z); acc0.w = fmaf(pk, v.w, acc0.w);
             }
         }
-        const float iz = sz[qi];
-        for (int e = 0; e < per; e++) {
-            const float4 a = e ? acc1 : acc0;
-            const float4 y = make_float4(a.x * iz, a.y * iz, a.z * iz, a.w * iz);
-            const int ch = h * dh + 4 * (c4 + e * groups);
-            if (planes) plane_store4(planes, planes_il, row0 + qi, d, ch, y);
-            else *reinterpret_cast<float4*>(o + (row0 + qi) * d + ch) = y;
+        const int ch = h * dh + 4 * c4;
+        for (int e = 0; e < (two ? 2 : 1); e++) {
+            const float4 acc = e ? acc1 : acc0;
+            const float iz = sz[qa + e];
+            const float4 y = make_float4(acc.x * iz, acc.y * iz, acc.z * iz, acc.w * iz);
+            if (planes) plane_store4(planes, planes_il, row0 + qa + e, d, ch, y);
+            else *reinterpret_cast<float4*>(o + (row0 + qa + e) * d + ch) = y;
         }
     }
 }
