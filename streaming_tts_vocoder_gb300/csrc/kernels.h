@@ -18,9 +18,10 @@ cudaError_t launch_rvq_gather(const float* cb, int Q, int V, int E, const int* c
                               PlanView plan, float* e, Layout el, unsigned* err_words,
                               int total_rows, cudaStream_t s);
 
-// Latent input: e[row] = x * sigma + mu for the call's frames (x [B][T_max][L]).
+// Latent input: e[row] = x * sigma + mu for the call's frames (x [B][T_max][L]);
+// rows of e are ldo floats apart (0: L).
 cudaError_t launch_latent_fill(const float* x, int L, int T_max, PlanView plan, const float* mu,
-                               const float* sigma, float* e, Layout el, int total_rows, cudaStream_t s);
+                               const float* sigma, float* e, Layout el, int total_rows, cudaStream_t s, int ldo = 0);
 
 cudaError_t launch_gemm_simt(const GemmArgs& a, PlanView plan, int n_row_tiles, cudaStream_t s);
 

@@ -65,12 +65,13 @@ cudaError_t launch_rvq_gather(const float* cb, int Q, int V, int E, const int* c
 // ---------------------------------------------------------- latent fill --
 // Latent-input decoder: e[row] = x[row] * sigma + mu (per channel, one
 // rounding) for every frame of the call, from the caller's [B][T_max][L]
-// latents into the level-0 buffer (blixt/phonon "Weights": the codec's
-// latents are denormalised before the projection).  One thread per float4.
+// latents into the level-0 buffer, whose rows are ldo >= L floats apart
+// (blixt/phonon "Weights": the codec's latents are denormalised before the
+// projection).  One thread per float4.
 __global__ void __launch_bounds__(256) latent_fill_kernel(const float* __restrict__ x, int L, int T_max,
                                                           PlanView plan, const float* __restrict__ mu,
                                                           const float* __restrict__ sigma, float* __restrict__ e,
-                                                          Layout el, int total_rows)
+                                                          Layout el, int total_rows, int ldo)
 {
     pdl_wait();
     pdl_launch();
@@ -83,19 +84,20 @@ __global__ void __launch_bounds__(256) latent_fill_kernel(const float* __restric
     const float4 v = __ldg(reinterpret_cast<const float4*>(x + ((long long)__ldg(plan.bidx + b) * T_max + t) * L) + c4);
     const float4 m = __ldg(reinterpret_cast<const float4*>(mu) + c4);
     const float4 sg = __ldg(reinterpret_cast<const float4*>(sigma) + c4);
-    reinterpret_cast<float4*>(e + (seg_base(el, plan.cf, b) + t) * L)[c4] =
+    reinterpret_cast<float4*>(e + (seg_base(el, plan.cf, b) + t) * ldo)[c4] =
         make_float4(__fmaf_rn(v.x, sg.x, m.x), __fmaf_rn(v.y, sg.y, m.y), __fmaf_rn(v.z, sg.z, m.z),
                     __fmaf_rn(v.w, sg.w, m.w));
 }
 
 cudaError_t launch_latent_fill(const float* x, int L, int T_max, PlanView plan, const float* mu,
-                               const float* sigma, float* e, Layout el, int total_rows, cudaStream_t s)
+                               const float* sigma, float* e, Layout el, int total_rows, cudaStream_t s, int ldo)
 {
     if (total_rows <= 0) return cudaSuccess;
-    if (L % 4 != 0) return cudaErrorInvalidValue;
+    if (ldo <= 0) ldo = L;
+    if (L % 4 != 0 || ldo % 4 != 0 || ldo < L) return cudaErrorInvalidValue;
     const long long n = (long long)total_rows * (L / 4);
     launch_pdl(latent_fill_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s, x, L, T_max, plan, mu, sigma,
-               e, el, total_rows);
+               e, el, total_rows, ldo);
     return cudaGetLastError();
 }
 

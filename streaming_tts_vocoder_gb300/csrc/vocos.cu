@@ -55,15 +55,21 @@ struct VBlock {
 // LayerNorm over the d channels of each row (biased variance, eps inside the
 // root), optionally after a causal depthwise conv of k taps over the rows of
 // a prefixed buffer:  y[c] = b_dw[c] + sum_j w[j][c] x[row - (k - 1) + j][c].
-// A warp per row; lane l takes channels l, l + 32, ... in ascending order, and
-// the sums over the row go through a fixed butterfly, so a row's result does
-// not depend on the batch it came in.
+// A warp per row; lane l takes the four-channel groups l, l + 32, ... (128-bit
+// loads and stores), each row sum runs over a lane's channels in ascending
+// order and then through a fixed butterfly, so a row's result does not depend
+// on the batch it came in.  KT: the tap count when fixed at compile time
+// (every load of a row's taps then in flight at once), 0 for the runtime k;
+// PG: the groups per lane the registers hold (d <= 128 PG).  planes set: the
+// result goes straight into the next linear's tensor-core operand planes
+// (layout planes_il), split as the prep kernel would, instead of y.
+template <int KT, int PG>
 __global__ void __launch_bounds__(256) vocos_ln_kernel(const float* __restrict__ x, Layout xl,
                                                        const float* __restrict__ dw_w,
                                                        const float* __restrict__ dw_b, int k,
                                                        const float* __restrict__ g, const float* __restrict__ b,
                                                        float eps, int d, float* __restrict__ y, Layout yl,
-                                                       PlanView plan, int total_rows)
+                                                       PlanView plan, int total_rows, void* planes, int planes_il)
 {
     pdl_wait();
     pdl_launch();
@@ -73,24 +79,42 @@ __global__ void __launch_bounds__(256) vocos_ln_kernel(const float* __restrict__
     const int seg = find_seg(plan.cf, plan.B, row);
     const int t = row - __ldg(plan.cf + seg);
     const long long xr = seg_base(xl, plan.cf, seg) + t;
-    constexpr int kMaxPer = 32;          // d <= 1024
-    float v[kMaxPer];
+    const int d4 = d >> 2;
+    auto f4 = [](const float* p, int i) { return reinterpret_cast<const float4*>(p)[i]; };
+    auto fma4 = [](float4 w, float4 v, float4 a) {
+        return make_float4(fmaf(w.x, v.x, a.x), fmaf(w.y, v.y, a.y), fmaf(w.z, v.z, a.z), fmaf(w.w, v.w, a.w));
+    };
+    float4 v[PG];
     float s = 0.f;
 #pragma unroll
-    for (int i = 0; i < kMaxPer; i++) {
-        const int c = lane + 32 * i;
-        v[i] = 0.f;
-        if (c < d) {
-            float a;
-            if (dw_w) {
-                a = __ldg(dw_b + c);
+    for (int i = 0; i < PG; i++) {
+        const int c4 = lane + 32 * i;
+        v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (c4 < d4) {
+            float4 a;
+            if (dw_w && KT > 0) {
+                float4 xs[KT > 0 ? KT : 1], ws[KT > 0 ? KT : 1];
+#pragma unroll
+                for (int j = 0; j < KT; j++) {
+                    xs[j] = f4(x + (xr - (KT - 1) + j) * d, c4);
+                    ws[j] = __ldg(reinterpret_cast<const float4*>(dw_w + (size_t)j * d) + c4);
+                }
+                a = __ldg(reinterpret_cast<const float4*>(dw_b) + c4);
+#pragma unroll
+                for (int j = 0; j < KT; j++) a = fma4(ws[j], xs[j], a);
+            } else if (dw_w) {
+                a = __ldg(reinterpret_cast<const float4*>(dw_b) + c4);
                 for (int j = 0; j < k; j++)
-                    a = fmaf(__ldg(dw_w + (size_t)j * d + c), x[(xr - (k - 1) + j) * d + c], a);
+                    a = fma4(__ldg(reinterpret_cast<const float4*>(dw_w + (size_t)j * d) + c4),
+                             f4(x + (xr - (k - 1) + j) * d, c4), a);
             } else {
-                a = x[xr * d + c];
+                a = f4(x + xr * d, c4);
             }
             v[i] = a;
-            s += a;
+            s += a.x;
+            s += a.y;
+            s += a.z;
+            s += a.w;
         }
     }
 #pragma unroll
@@ -98,11 +122,13 @@ __global__ void __launch_bounds__(256) vocos_ln_kernel(const float* __restrict__
     const float mean = s / (float)d;
     float q = 0.f;
 #pragma unroll
-    for (int i = 0; i < kMaxPer; i++) {
-        const int c = lane + 32 * i;
-        if (c < d) {
-            const float e = v[i] - mean;
-            q = fmaf(e, e, q);
+    for (int i = 0; i < PG; i++) {
+        if (lane + 32 * i < d4) {
+            const float ex = v[i].x - mean, ey = v[i].y - mean, ez = v[i].z - mean, ew = v[i].w - mean;
+            q = fmaf(ex, ex, q);
+            q = fmaf(ey, ey, q);
+            q = fmaf(ez, ez, q);
+            q = fmaf(ew, ew, q);
         }
     }
 #pragma unroll
@@ -110,9 +136,17 @@ __global__ void __launch_bounds__(256) vocos_ln_kernel(const float* __restrict__
     const float r = rsqrtf(q / (float)d + eps);
     const long long yr = seg_base(yl, plan.cf, seg) + t;
 #pragma unroll
-    for (int i = 0; i < kMaxPer; i++) {
-        const int c = lane + 32 * i;
-        if (c < d) y[yr * d + c] = fmaf((v[i] - mean) * r, __ldg(g + c), __ldg(b + c));
+    for (int i = 0; i < PG; i++) {
+        const int c4 = lane + 32 * i;
+        if (c4 < d4) {
+            const float4 gg = __ldg(reinterpret_cast<const float4*>(g) + c4);
+            const float4 bb = __ldg(reinterpret_cast<const float4*>(b) + c4);
+            const float4 o =
+                make_float4(fmaf((v[i].x - mean) * r, gg.x, bb.x), fmaf((v[i].y - mean) * r, gg.y, bb.y),
+                            fmaf((v[i].z - mean) * r, gg.z, bb.z), fmaf((v[i].w - mean) * r, gg.w, bb.w));
+            if (planes) plane_store4(planes, planes_il, yr, d, 4 * c4, o);
+            else reinterpret_cast<float4*>(y + yr * d)[c4] = o;
+        }
     }
 }
 
@@ -139,13 +173,15 @@ struct codec_vocos_s {
     int num_sms = 0;
     int P = 0;                       // history rows in front of each segment (k - 1, at least 1)
     VContraction embed, head;        // head: N padded to Hp = n_fft + 2 rounded up to 16 (zero columns)
+    int Mp = 0;                      // mel channels padded to a multiple of 32 (zero channels): the
+                                     // embedding conv's input width, so that it runs on the tensor cores
     int Hp = 0;
     float *norm_g = nullptr, *norm_b = nullptr, *final_g = nullptr, *final_b = nullptr;
     std::vector<VBlock> blocks;
     float* zeros = nullptr;          // [n_mels] / ones: the mel copy's identity affine
     float* ones = nullptr;
     // activations
-    float* mel = nullptr;            // prefixed [rows][n_mels]
+    float* mel = nullptr;            // prefixed [rows][Mp], channels n_mels .. Mp - 1 zero
     std::vector<float*> xb;          // block inputs x_0 .. x_L, prefixed [rows][d]
     float* emb = nullptr;            // dense [rows][d]
     float* u = nullptr;              // dense [rows][d]
@@ -290,16 +326,19 @@ codec_status codec_vocos_create(const codec_vocos_config* cfg, const float* weig
 
     const float* p = weights;
     auto take = [&](long long n) { const float* r = p; p += n; return r; };
-    {   // embedding conv [d][n_mels][k] -> [k n_mels][d], tap j reads row t - (k - 1 - j)
+    {   // embedding conv [d][n_mels][k] -> [k Mp][d] (zero rows for the pad
+        // channels, which add exact zeros), tap j reads row t - (k - 1 - j)
         const float* w = take((long long)d * g.n_mels * k);
         const float* b = take(d);
+        s->Mp = (g.n_mels + 31) / 32 * 32;
+        const int Mp = s->Mp;
         VContraction& C = s->embed;
-        C.Cin = g.n_mels; C.N = d; C.ntaps = k;
+        C.Cin = Mp; C.N = d; C.ntaps = k;
         for (int j = 0; j < k; j++) C.shift[j] = k - 1 - j;
-        std::vector<float> wkn((size_t)k * g.n_mels * d);
+        std::vector<float> wkn((size_t)k * Mp * d, 0.f);
         for (int co = 0; co < d; co++)
             for (int ci = 0; ci < g.n_mels; ci++)
-                for (int j = 0; j < k; j++) wkn[((size_t)j * g.n_mels + ci) * d + co] = w[((size_t)co * g.n_mels + ci) * k + j];
+                for (int j = 0; j < k; j++) wkn[((size_t)j * Mp + ci) * d + co] = w[((size_t)co * g.n_mels + ci) * k + j];
         vfinish(s, C, wkn, b, st);
     }
     s->norm_g = vupload(s, take(d), d, st);
@@ -346,7 +385,7 @@ codec_status codec_vocos_create(const codec_vocos_config* cfg, const float* weig
     }
     // activations: chunk rows of every stream plus P history rows per stream
     const size_t R = (size_t)g.max_batch_frames, RP = R + (size_t)S * s->P;
-    s->mel = valloc<float>(s, RP * g.n_mels, st);
+    s->mel = valloc<float>(s, RP * s->Mp, st, true);
     s->xb.resize(g.layers + 1);
     for (int l = 0; l <= g.layers; l++) s->xb[l] = valloc<float>(s, RP * d, st);
     s->emb = valloc<float>(s, R * d, st);
@@ -362,7 +401,7 @@ codec_status codec_vocos_create(const codec_vocos_config* cfg, const float* weig
         h.state = valloc<float>(s, (size_t)S * (k - 1) * C, st, true);
         s->hist.push_back(h);
     };
-    add_hist(s->mel, g.n_mels);
+    add_hist(s->mel, s->Mp);
     for (int l = 0; l < g.layers; l++) add_hist(s->xb[l], d);
     if (!s->hist.empty()) s->hist_d = vupload(s, s->hist.data(), s->hist.size(), st);
     s->frames_d = valloc<long long>(s, S, st, true);
@@ -519,8 +558,9 @@ codec_status codec_vocos_decode(codec_vocos_t* s, const float* mel, const int32_
         if (e != cudaSuccess && err == cudaSuccess) err = e;
         return err == cudaSuccess;
     };
+    // from_producer: the LayerNorm before the linear already wrote its operand planes
     auto gemm = [&](const VContraction& C, const float* in, Layout il, float* out, Layout ol, const float* res,
-                    int epi) {
+                    int epi, bool from_producer = false) {
         if (err != cudaSuccess) return;
         GemmArgs a{};
         a.in = in; a.in_l = il; a.Cin = C.Cin; a.ntaps = C.ntaps;
@@ -535,7 +575,7 @@ codec_status codec_vocos_decode(codec_vocos_t* s, const float* mel, const int32_
             a.dense = (il.P == 0 && ol.P == 0 && C.ntaps == 1) ? 1 : 0;
             const int tiles = a.dense ? (rows + 127) / 128 : n128;
             const long long arows = rows + (long long)Bc * il.P;
-            ok(launch_tc_prep(in, nullptr, nullptr, arows, C.Cin, &s->tc, C.tc.passes == 3, cs));
+            if (!from_producer) ok(launch_tc_prep(in, nullptr, nullptr, arows, C.Cin, &s->tc, C.tc.passes == 3, cs));
             int extra = 0;
             ok(launch_tc_gemm(a, C.tc, pv, tiles, &s->tc, arows, s->num_sms, cs, &extra));
             launches += extra > 1 ? extra - 1 : 0;
@@ -545,26 +585,39 @@ codec_status codec_vocos_decode(codec_vocos_t* s, const float* mel, const int32_
             ok(launch_gemm_simt(a, pv, n64, cs));
         }
     };
+    // to: the linear that reads y next; when it runs on the tensor cores the
+    // LayerNorm writes its operand planes instead of y (returns true)
     auto ln = [&](const float* x, Layout xl, const float* dw, const float* dwb, const float* gg, const float* bb,
-                  float* y, Layout yl) {
-        if (err != cudaSuccess) return;
-        launch_pdl(vocos_ln_kernel, dim3((rows + 7) / 8), dim3(256), 0, cs, x, xl, dw, dwb, g.k, gg, bb, g.ln_eps, d,
-                   y, yl, pv, rows);
+                  float* y, Layout yl, const VContraction* to = nullptr) {
+        if (err != cudaSuccess) return false;
+        void* pl = (to && to->use_tc && yl.P == 0) ? s->tc.a_hi : nullptr;
+        const int il = to && to->tc.passes == 3 ? 1 : 0;
+        const dim3 grid((rows + 7) / 8), blk(256);
+        if (d <= 512 && dw && g.k == 7)
+            launch_pdl(vocos_ln_kernel<7, 4>, grid, blk, 0, cs, x, xl, dw, dwb, g.k, gg, bb, g.ln_eps, d, y, yl, pv,
+                       rows, pl, il);
+        else if (d <= 512)
+            launch_pdl(vocos_ln_kernel<0, 4>, grid, blk, 0, cs, x, xl, dw, dwb, g.k, gg, bb, g.ln_eps, d, y, yl, pv,
+                       rows, pl, il);
+        else
+            launch_pdl(vocos_ln_kernel<0, 8>, grid, blk, 0, cs, x, xl, dw, dwb, g.k, gg, bb, g.ln_eps, d, y, yl, pv,
+                       rows, pl, il);
         ok(cudaGetLastError());
+        return pl != nullptr;
     };
 
     if (!s->hist.empty()) ok(launch_hist_fill(s->hist_d, (int)s->hist.size(), pv, cs));
-    ok(launch_latent_fill(mel, g.n_mels, T_max, pv, s->zeros, s->ones, s->mel, Lp, rows, cs));
+    ok(launch_latent_fill(mel, g.n_mels, T_max, pv, s->zeros, s->ones, s->mel, Lp, rows, cs, s->Mp));
     gemm(s->embed, s->mel, Lp, s->emb, Ld, nullptr, EPI_STORE);
     ln(s->emb, Ld, nullptr, nullptr, s->norm_g, s->norm_b, s->xb[0], Lp);
     for (int l = 0; l < g.layers; l++) {
         const VBlock& Bk = s->blocks[l];
-        ln(s->xb[l], Lp, Bk.dw_w, Bk.dw_b, Bk.ln_g, Bk.ln_b, s->u, Ld);
-        gemm(Bk.pw1, s->u, Ld, s->f, Ld, nullptr, EPI_GELU);
+        const bool p1 = ln(s->xb[l], Lp, Bk.dw_w, Bk.dw_b, Bk.ln_g, Bk.ln_b, s->u, Ld, &Bk.pw1);
+        gemm(Bk.pw1, s->u, Ld, s->f, Ld, nullptr, EPI_GELU, p1);
         gemm(Bk.pw2, s->f, Ld, s->xb[l + 1], Lp, s->xb[l], EPI_RESID);
     }
-    ln(s->xb[g.layers], Lp, nullptr, nullptr, s->final_g, s->final_b, s->u, Ld);
-    gemm(s->head, s->u, Ld, s->spec, Ld, nullptr, EPI_STORE);
+    const bool ph = ln(s->xb[g.layers], Lp, nullptr, nullptr, s->final_g, s->final_b, s->u, Ld, &s->head);
+    gemm(s->head, s->u, Ld, s->spec, Ld, nullptr, EPI_STORE, ph);
     if (err == cudaSuccess) {
         launch_pdl(vocos_scatter_kernel, dim3(rows), dim3(256), 0, cs, (const float*)s->spec, s->Hp, H, T_max, pv,
                    rows, s->spec_b);
