@@ -903,6 +903,12 @@ struct Launcher {
     }
 
     long long rows(int lvl) const { return frames * s->c->level_r[lvl]; }
+    int max_frames() const
+    {
+        int m = 0;
+        for (int n : n_h) m = std::max(m, n);
+        return m;
+    }
     long long rows_pref(int lvl, Layout l) const { return frames * s->c->level_r[lvl] + (long long)Bc * l.P; }
 
     // from_producer: the operand planes are already in plane block 0, written
@@ -1077,7 +1083,7 @@ void enqueue_decode(codec_state_t* s, Launcher& L, const void* input, int32_t T_
         L.run(CODEC_KERNEL_GATHER, (double)rows0 * g.Q * g.E, 4.0 * rows0 * ((double)g.Q * (1 + g.E) + g.E),
               "codebook gather", [&] {
                   return launch_rvq_gather(c->cb, g.Q, g.V, g.E, static_cast<const int32_t*>(input), T_max, L.pv,
-                                           s->e, L0p, s->err_d, rows0, cs);
+                                           s->e, L0p, s->err_d, L.max_frames(), cs);
               });
         L.gemm(c->pre, s->e, L0p, 0, s->h, Ltd, g.d, 1, nullptr, EPI_STORE, 1.f, 0, "pre-conv");
     }
@@ -1305,7 +1311,10 @@ codec_status embed_impl(codec_state_t* s, const int32_t* codes, const int32_t* n
     if (pst != CODEC_OK || rows0 == 0) return pst;
     L.run(CODEC_KERNEL_GATHER, (double)rows0 * g.Q * g.E, 4.0 * rows0 * ((double)g.Q * (1 + g.E) + g.E),
           "codebook gather",
-          [&] { return launch_rvq_gather(s->c->cb, g.Q, g.V, g.E, codes, T_max, L.pv, emb, Layout{1, 0}, s->err_d, rows0, cs); });
+          [&] {
+              return launch_rvq_gather(s->c->cb, g.Q, g.V, g.E, codes, T_max, L.pv, emb, Layout{1, 0}, s->err_d,
+                                       L.max_frames(), cs);
+          });
     s->last_launches = L.launches;
     return L.err == cudaSuccess ? CODEC_OK : CODEC_ERR_CUDA;
 }

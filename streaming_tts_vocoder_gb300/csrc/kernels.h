@@ -14,9 +14,10 @@ struct HistDesc {
     Layout l;
 };
 
+// max_frames: the call's longest chunk (frames of its longest batch entry).
 cudaError_t launch_rvq_gather(const float* cb, int Q, int V, int E, const int* codes, int T_max,
                               PlanView plan, float* e, Layout el, unsigned* err_words,
-                              int total_rows, cudaStream_t s);
+                              int max_frames, cudaStream_t s);
 
 // Latent input: e[row] = x * sigma + mu for the call's frames (x [B][T_max][L]);
 // rows of e are ldo floats apart (0: L).

@@ -11,9 +11,11 @@ namespace codec {
 
 // ---------------------------------------------------------------- gather --
 // e[row] = sum_q CB_q[code[q][t]] in fp32, q ascending (vllm-omni "Edge TTS
-// design", section 1.3: RVQ embedding sum).  One block per frame row, one
-// float4 of channels per thread: every load is a 128-bit load of a codebook
-// row.  A code outside [0, V) zeroes the row and sets the slot's sticky bit.
+// design", section 1.3: RVQ embedding sum).  One block per (frame t, batch
+// entry b) of a grid of the call's longest chunk x its entries (blocks past
+// an entry's frames return at once), one float4 of channels per thread:
+// every load is a 128-bit load of a codebook row.  A code outside [0, V)
+// zeroes the row and sets the slot's sticky bit.
 __global__ void __launch_bounds__(128) rvq_gather_kernel(
     const float* __restrict__ cb, int Q, int V, int E, const int* __restrict__ codes, int T_max,
     PlanView plan, const int* __restrict__ bidx, float* __restrict__ e, Layout el,
@@ -23,9 +25,8 @@ __global__ void __launch_bounds__(128) rvq_gather_kernel(
     pdl_launch();
     __shared__ int sc[64];
     __shared__ int sbad;
-    const int row = blockIdx.x;
-    const int b = find_seg(plan.cf, plan.B, row);
-    const int t = row - __ldg(plan.cf + b);
+    const int b = blockIdx.y, t = blockIdx.x;
+    if (t >= __ldg(plan.cf + b + 1) - __ldg(plan.cf + b)) return;
     if (threadIdx.x == 0) sbad = 0;
     __syncthreads();
     const int* cr = codes + ((long long)__ldg(bidx + b) * Q) * T_max + t;
@@ -54,11 +55,11 @@ __global__ void __launch_bounds__(128) rvq_gather_kernel(
 
 cudaError_t launch_rvq_gather(const float* cb, int Q, int V, int E, const int* codes, int T_max,
                               PlanView plan, float* e, Layout el, unsigned* err_words,
-                              int total_rows, cudaStream_t s)
+                              int max_frames, cudaStream_t s)
 {
-    if (total_rows <= 0) return cudaSuccess;
-    launch_pdl(rvq_gather_kernel, dim3(total_rows), dim3(128), 0, s, cb, Q, V, E, codes, T_max, plan, plan.bidx,
-               e, el, err_words);
+    if (max_frames <= 0 || plan.B <= 0) return cudaSuccess;
+    launch_pdl(rvq_gather_kernel, dim3(max_frames, plan.B), dim3(128), 0, s, cb, Q, V, E, codes, T_max, plan,
+               plan.bidx, e, el, err_words);
     return cudaGetLastError();
 }
 
@@ -194,7 +195,11 @@ cudaError_t launch_gemm_simt(const GemmArgs& a, PlanView plan, int n_row_tiles, 
 // y = x / sqrt(mean(x^2) + eps) * g, one warp per row; the row's sum of
 // squares runs lane-strided then through a fixed butterfly.
 // planes set: the normalised row goes straight into a tensor-core GEMM's
-// operand planes (row of layout yl) instead of y.
+// operand planes (row of layout yl) instead of y.  PR: float4s of the row a
+// lane keeps in registers (the whole row is loaded at once, d <= 128 PR),
+// or 0 for a loop over any width.  Rows of dense layouts (no history rows in
+// either) need no segment lookup: row r is layout row r.
+template <int PR>
 __global__ void rms_norm_kernel(const float* __restrict__ x, Layout xl, const float* __restrict__ g,
                                 float eps, float* __restrict__ y, Layout yl, int d, PlanView plan,
                                 int total_rows, void* planes, int planes_il)
@@ -204,14 +209,47 @@ __global__ void rms_norm_kernel(const float* __restrict__ x, Layout xl, const fl
     const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (row >= total_rows) return;
-    // xl.r rows per frame (yl has the same rate)
-    const int b = find_seg_r(plan.cf, plan.B, row, xl.r);
-    const int t = row - __ldg(plan.cf + b) * xl.r;
-    const float4* xr = reinterpret_cast<const float4*>(x + (seg_base(xl, plan.cf, b) + t) * d);
-    const long long yrow = seg_base(yl, plan.cf, b) + t;
+    long long xrow = row, yrow = row;
+    if (xl.P != 0 || yl.P != 0) {
+        // xl.r rows per frame (yl has the same rate)
+        const int b = find_seg_r(plan.cf, plan.B, row, xl.r);
+        const int t = row - __ldg(plan.cf + b) * xl.r;
+        xrow = seg_base(xl, plan.cf, b) + t;
+        yrow = seg_base(yl, plan.cf, b) + t;
+    }
+    const float4* xr = reinterpret_cast<const float4*>(x + xrow * d);
     float4* yr = reinterpret_cast<float4*>(y + yrow * d);
     const int d4 = d >> 2;
+    const float4* g4 = reinterpret_cast<const float4*>(g);
     float ss = 0.f;
+    if (PR > 0) {
+        float4 v[PR > 0 ? PR : 1];
+#pragma unroll
+        for (int i = 0; i < PR; i++) {
+            const int c = lane + 32 * i;
+            v[i] = c < d4 ? xr[c] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int i = 0; i < PR; i++)
+            if (lane + 32 * i < d4) {
+                ss = fmaf(v[i].x, v[i].x, ss); ss = fmaf(v[i].y, v[i].y, ss);
+                ss = fmaf(v[i].z, v[i].z, ss); ss = fmaf(v[i].w, v[i].w, ss);
+            }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        const float r = rsqrtf(ss / (float)d + eps);
+#pragma unroll
+        for (int i = 0; i < PR; i++) {
+            const int c = lane + 32 * i;
+            if (c < d4) {
+                const float4 w = __ldg(g4 + c);
+                const float4 o = make_float4(v[i].x * r * w.x, v[i].y * r * w.y, v[i].z * r * w.z, v[i].w * r * w.w);
+                if (planes) plane_store4(planes, planes_il, yrow, d, 4 * c, o);
+                else yr[c] = o;
+            }
+        }
+        return;
+    }
     for (int c = lane; c < d4; c += 32) {
         const float4 v = xr[c];
         ss = fmaf(v.x, v.x, ss); ss = fmaf(v.y, v.y, ss); ss = fmaf(v.z, v.z, ss); ss = fmaf(v.w, v.w, ss);
@@ -219,7 +257,6 @@ __global__ void rms_norm_kernel(const float* __restrict__ x, Layout xl, const fl
 #pragma unroll
     for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
     const float r = rsqrtf(ss / (float)d + eps);
-    const float4* g4 = reinterpret_cast<const float4*>(g);
     for (int c = lane; c < d4; c += 32) {
         const float4 v = xr[c], w = __ldg(g4 + c);
         const float4 o = make_float4(v.x * r * w.x, v.y * r * w.y, v.z * r * w.z, v.w * r * w.w);
@@ -234,8 +271,13 @@ cudaError_t launch_rms_norm(const float* x, Layout xl, const float* g, float eps
     if (planes && (d % 32 != 0)) return cudaErrorInvalidValue;
     if (total_rows <= 0) return cudaSuccess;
     const int threads = 256, rows_per_block = threads / 32;
-    launch_pdl(rms_norm_kernel, dim3((total_rows + rows_per_block - 1) / rows_per_block), dim3(threads), 0, s,
-               x, xl, g, eps, y, yl, d, plan, total_rows, planes, planes_il);
+    const dim3 grid((total_rows + rows_per_block - 1) / rows_per_block);
+    if (d <= 1024)
+        launch_pdl(rms_norm_kernel<8>, grid, dim3(threads), 0, s, x, xl, g, eps, y, yl, d, plan, total_rows, planes,
+                   planes_il);
+    else
+        launch_pdl(rms_norm_kernel<0>, grid, dim3(threads), 0, s, x, xl, g, eps, y, yl, d, plan, total_rows, planes,
+                   planes_il);
     return cudaGetLastError();
 }
 
