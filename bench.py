@@ -550,7 +550,7 @@ def run_profile_call(args):
 def layer_labels(cfg):
     """Names of the decoder's launches in call order (an operand prep carries
     the name of the GEMM it feeds)."""
-    names = ["history fill", "codebook gather", "pre-conv"]
+    names = ["history fill"] + (["latent fill", "latent front"] if cfg.latent_dim else ["codebook gather", "pre-conv"])
     for l in range(cfg.layers):
         names += [f"L{l} rmsnorm 1", f"L{l} qkv", f"L{l} attention", f"L{l} out-proj", f"L{l} rmsnorm 2",
                   f"L{l} mlp 1", f"L{l} mlp 2"]
@@ -573,20 +573,25 @@ def run_layer_times(args):
     S, CH = (int(v) for v in args.layer_times.split(","))
     import torch
     from streaming_tts_vocoder_gb300 import codec as C
-    cfg = qwen3_config() if args.decoder == "qwen3" else tiny_config()
+    cfg = CONFIGS[args.decoder]()
+    latent = bool(cfg.latent_dim)
     blob = pack_blob(cfg, make_weights(cfg, 0))
     prec = {"fp16x3": C.PRECISION_FP16X3, "fp16": C.PRECISION_FP16, "fp32": C.PRECISION_FP32}[args.precision]
     cod = C.Codec(cfg, blob, max_streams=S, max_chunk_frames=CH, max_batch_frames=S * CH, precision=prec)
     st = cod.state()
     st.set_graphs(False)
     dev = torch.device("cuda")
-    codes = torch.from_numpy(np.stack([make_codes(cfg, CH, 1000 + s) for s in range(S)])).to(dev)
+    mk = make_latents if latent else make_codes
+    inp = torch.from_numpy(np.stack([mk(cfg, CH, 1000 + s) for s in range(S)])).to(dev)
     audio = torch.empty(S, CH * cod.samples_per_frame, device=dev)
     for _ in range(3):
         st.reset()
         torch.cuda.synchronize()
         st.profile_begin()
-        st.decode(codes, [CH] * S, audio)
+        if latent:
+            st.decode_latents(inp, [CH] * S, audio)
+        else:
+            st.decode(inp, [CH] * S, audio)
         st.profile_end()
     names = iter(layer_labels(cfg))
     rows, cur = [], None

@@ -71,7 +71,9 @@ constexpr int kMaxBufs = 4;          // TMEM chunk buffers
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSpinLimit = kDefaultWaitPolls;   // drains of work already in flight
 constexpr int kSmemBudget = 227 * 1024;   // the opt-in maximum per CTA
-constexpr int kStageOutBytes = kEpiWarps * 32 * 32 * 4;   // one 32 x 32 fp32 block per epilogue warp
+// one 32 x 32 fp32 block per epilogue warp, then 32 ints per warp (the q/K/V
+// scatter's ring rows of the warp's 32 rows)
+constexpr int kStageOutBytes = kEpiWarps * 32 * 32 * 4 + kEpiWarps * 32 * 4;
 constexpr uint32_t kAPlaneBytes = kBM * kBK * 2;   // 8 KB: one M-tile, one plane
 constexpr int kChunkKb = 8;          // 8 k-blocks = 256 of K = 16 MMA k-steps per TMEM chunk
 
@@ -289,6 +291,18 @@ __device__ __forceinline__ void stage_put(float4* stg, int lane, const float* v)
 __device__ __forceinline__ float4 stage_get(const float4* stg, int r, int cq)
 {
     return stg[r * 8 + (cq ^ (r & 7))];
+}
+
+// Ring row (slot x ring_R + position mod ring_R) of the keys and values of
+// output row t (the projection's row; b < 0: dense tiling, t over all segments).
+__device__ __forceinline__ int qkv_ring_row(const GemmArgs& a, const PlanView& plan, int b, int t)
+{
+    if (b < 0) {
+        b = find_seg_r(plan.cf, plan.B, t, a.pos_r);
+        t -= __ldg(plan.cf + b) * a.pos_r;
+    }
+    const long long pos = __ldg(plan.pos0 + b) * a.pos_r + t;
+    return (int)((long long)__ldg(plan.slot + b) * a.ring_R + (pos & (a.ring_R - 1)));
 }
 
 // Destination of four consecutive output columns n .. n+3 of output row t
@@ -562,6 +576,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
         const int m = q * 32 + lane;
         const int cq = lane & 7;        // column quad of the transposed pass
         float4* stg = stage_out + (warp - 4) * 256;
+        int* srow = reinterpret_cast<int*>(stage_out + kEpiWarps * 256) + (warp - 4) * 32;
         const bool has_res = a.epi == EPI_RESID || a.epi == EPI_MRF_FIRST || a.epi == EPI_MRF_ADD || a.epi == EPI_MRF_LAST;
         const bool has_old = a.epi == EPI_MRF_ADD || a.epi == EPI_MRF_LAST;
         int chunk_it = 0;
@@ -633,6 +648,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
             // body is long); the slice's sums are always sum[0..31], the rest
             // move down by 32 after each slice.
             const bool vec_ok = a.epi == EPI_QKV ? (a.d & 3) == 0 : (a.out_C & 3) == 0;
+            // q/K/V scatter: each lane finds the ring row of one of the warp's 32
+            // rows once per tile (a segment search); the slices then read it
+            const bool qkv4 = a.epi == EPI_QKV && vec_ok;
+            if (qkv4) {
+                const int mr = q * 32 + lane;
+                srow[lane] = mr < tr.nrows ? qkv_ring_row(a, plan, tr.b, tr.t0 + mr) : 0;
+                __syncwarp();
+            }
 #pragma unroll 1
             for (int c = 0; c < nvalid; c += 32) {
                 stage_put(stg, lane, sum);
@@ -689,7 +712,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
                             y.z = epi_plain(a, v.z, bias4[2], unscale);
                             y.w = epi_plain(a, v.w, bias4[3], unscale);
                             const long long orow = out_base + (long long)t * a.out_step;
-                            float* dst = epi_dst4(a, plan, tr.b, t, orow, n, cnt);
+                            float* dst;
+                            if (qkv4 && n >= a.d) {
+                                const long long rr = srow[r];
+                                dst = n < 2 * a.d ? a.kring + rr * a.d + (n - a.d) : a.vring + rr * a.d + (n - 2 * a.d);
+                            } else {
+                                dst = epi_dst4(a, plan, tr.b, t, orow, n, cnt);
+                            }
                             if (dst) *reinterpret_cast<float4*>(dst) = y;
                             else epi_store_slow(a, plan, tr.b, t, orow, n, cnt, v, unscale);
                         }
