@@ -912,10 +912,11 @@ struct Launcher {
     long long rows_pref(int lvl, Layout l) const { return frames * s->c->level_r[lvl] + (long long)Bc * l.P; }
 
     // from_producer: the operand planes are already in plane block 0, written
-    // by the kernel that produced `in`; otherwise the prep kernel makes them.
+    // by the kernel that produced `in`; otherwise the prep kernel makes them
+    // (of GELU(in) when a_gelu: tensor-core path only).
     void gemm(const Contraction& C, const float* in, Layout il, int in_lvl, float* out, Layout ol,
               int out_C, int out_step, const float* res, int epi, float scale, int layer_ring,
-              const char* what, bool from_producer = false)
+              const char* what, bool from_producer = false, bool a_gelu = false)
     {
         if (err != cudaSuccess) return;
         const int S1 = s->n_slots + 1;
@@ -951,7 +952,7 @@ struct Launcher {
             TcScratch* sc = scr ? scr : &s->tc_scratch;
             if (!from_producer)
                 run(CODEC_KERNEL_OPERAND_PREP, 0.0, 8.0 * (double)arows * C.Cin, what, [&] {
-                    return launch_tc_prep(in, C.alpha, C.inv_alpha, arows, C.Cin, sc, C.tc.passes == 3, cs);
+                    return launch_tc_prep(in, C.alpha, C.inv_alpha, arows, C.Cin, sc, C.tc.passes == 3, cs, a_gelu);
                 });
             int extra = 0;
             run(CODEC_KERNEL_GEMM_TC, flops, bytes, what, [&] {
@@ -1118,8 +1119,13 @@ void enqueue_decode(codec_state_t* s, Launcher& L, const void* input, int32_t T_
             return launch_rms_norm(s->h, Ltd, W.n2, g.rms_eps, s->u, Ltd, g.d, L.pv, rows_tf, cs,
                                    W.w1.use_tc ? pl : nullptr, W.w1.tc.passes == 3 ? 1 : 0);
         });
-        L.gemm(W.w1, s->u, Ltd, lt, s->f, Ltd, g.ffn, 1, nullptr, EPI_GELU, 1.f, 0, "mlp 1", W.w1.use_tc);
-        L.gemm(W.w2, s->f, Ltd, lt, s->h, Ltd, g.d, 1, s->h, EPI_RESID, 1.f, 0, "mlp 2");
+        // on the tensor cores the GELU moves from the first linear's epilogue to
+        // the second's operand prep (the same function of the same value, so the
+        // same bits; the prep runs at full occupancy, the epilogue on 8 warps)
+        const bool gelu_prep = W.w1.use_tc && W.w2.use_tc;
+        L.gemm(W.w1, s->u, Ltd, lt, s->f, Ltd, g.ffn, 1, nullptr, gelu_prep ? EPI_STORE : EPI_GELU, 1.f, 0, "mlp 1",
+               W.w1.use_tc);
+        L.gemm(W.w2, s->f, Ltd, lt, s->h, Ltd, g.d, 1, s->h, EPI_RESID, 1.f, 0, "mlp 2", false, gelu_prep);
     }
     L.run(CODEC_KERNEL_RMSNORM, norm_flops, norm_bytes, "final rmsnorm",
           [&] { return launch_rms_norm(s->h, Ltd, c->tf_norm, g.rms_eps, s->hf, lay(lt), g.d, L.pv, rows_tf, cs); });

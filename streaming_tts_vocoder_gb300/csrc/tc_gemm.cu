@@ -799,7 +799,7 @@ __global__ void __launch_bounds__(kReduceRows * 8) tc_reduce_kernel(const GemmAr
         if (n + e < a.N) gemm_store(a, plan, tr.b, t, out_row, n + e, __fmul_rn(sum[e], us));
 }
 
-// hi = fp16(a), lo = fp16(a - hi), a = Snake(x) or x; eight consecutive
+// hi = fp16(a), lo = fp16(a - hi), a = Snake(x), GELU(x) or x; eight consecutive
 // channels (32 bytes in, 16 out per plane) per thread and one unit per
 // thread, so every load of the grid can be in flight at once.  The Snake
 // parameters are read as float4 when aligned (4 loads per thread, not 16).
@@ -808,7 +808,7 @@ __global__ void __launch_bounds__(kReduceRows * 8) tc_reduce_kernel(const GemmAr
 __global__ void __launch_bounds__(256) tc_prep_kernel(const float4* __restrict__ x, const float* __restrict__ alpha,
                                                       const float* __restrict__ inv_alpha, bool vec_alpha,
                                                       unsigned units, unsigned cin8, uint4* __restrict__ hi,
-                                                      bool interleaved)
+                                                      bool interleaved, bool gelu)
 {
     pdl_wait();
     pdl_launch();
@@ -838,6 +838,9 @@ __global__ void __launch_bounds__(256) tc_prep_kernel(const float4* __restrict__
         }
 #pragma unroll
         for (int e = 0; e < 8; e++) v[e] = snake_f(v[e], al[e], ia[e]);
+    } else if (gelu) {
+#pragma unroll
+        for (int e = 0; e < 8; e++) v[e] = gelu_f(v[e]);
     }
     uint32_t h[4], l[4];
 #pragma unroll
@@ -987,7 +990,7 @@ bool tc_scratch_alloc(TcScratch* s, size_t elems, size_t b_elems, size_t ws_floa
 }
 
 cudaError_t launch_tc_prep(const float* x, const float* alpha, const float* inv_alpha, long long rows, int Cin,
-                           TcScratch* scratch, bool with_lo, cudaStream_t s)
+                           TcScratch* scratch, bool with_lo, cudaStream_t s, bool gelu)
 {
     const long long n = rows * Cin;
     if (n <= 0) return cudaSuccess;
@@ -996,7 +999,7 @@ cudaError_t launch_tc_prep(const float* x, const float* alpha, const float* inv_
     const bool vec_alpha = alpha && ((reinterpret_cast<uintptr_t>(alpha) | reinterpret_cast<uintptr_t>(inv_alpha)) & 15) == 0;
     launch_pdl(tc_prep_kernel, dim3((units + 255) / 256), dim3(256), 0, s, reinterpret_cast<const float4*>(x),
                alpha, inv_alpha, vec_alpha, units, (unsigned)(Cin / 8), static_cast<uint4*>(scratch->a_hi),
-               with_lo);
+               with_lo, gelu);
     return cudaGetLastError();
 }
 

@@ -70,9 +70,10 @@ bool tc_pack_weights(const float* wkn, int ntaps, int Cin, int N, int passes, Tc
 bool tc_scratch_alloc(TcScratch* s, size_t elems, size_t b_elems, size_t ws_floats, std::vector<void*>& allocs);
 
 // A-operand planes of rows x Cin: hi = fp16(a), lo = fp16(a - hi) (lo only
-// when with_lo) with a = Snake(x) when alpha is given, else x.
+// when with_lo) with a = Snake(x) when alpha is given, else GELU(x) when gelu,
+// else x.
 cudaError_t launch_tc_prep(const float* x, const float* alpha, const float* inv_alpha, long long rows, int Cin,
-                           TcScratch* scratch, bool with_lo, cudaStream_t s);
+                           TcScratch* scratch, bool with_lo, cudaStream_t s, bool gelu = false);
 // The GEMM over the planes prepared by launch_tc_prep (a_rows rows); when it
 // has too few tiles for the GPU it also launches the split reduction.
 // *launches is incremented per kernel launched.

@@ -560,7 +560,7 @@ codec_status codec_vocos_decode(codec_vocos_t* s, const float* mel, const int32_
     };
     // from_producer: the LayerNorm before the linear already wrote its operand planes
     auto gemm = [&](const VContraction& C, const float* in, Layout il, float* out, Layout ol, const float* res,
-                    int epi, bool from_producer = false) {
+                    int epi, bool from_producer = false, bool a_gelu = false) {
         if (err != cudaSuccess) return;
         GemmArgs a{};
         a.in = in; a.in_l = il; a.Cin = C.Cin; a.ntaps = C.ntaps;
@@ -575,7 +575,8 @@ codec_status codec_vocos_decode(codec_vocos_t* s, const float* mel, const int32_
             a.dense = (il.P == 0 && ol.P == 0 && C.ntaps == 1) ? 1 : 0;
             const int tiles = a.dense ? (rows + 127) / 128 : n128;
             const long long arows = rows + (long long)Bc * il.P;
-            if (!from_producer) ok(launch_tc_prep(in, nullptr, nullptr, arows, C.Cin, &s->tc, C.tc.passes == 3, cs));
+            if (!from_producer)
+                ok(launch_tc_prep(in, nullptr, nullptr, arows, C.Cin, &s->tc, C.tc.passes == 3, cs, a_gelu));
             int extra = 0;
             ok(launch_tc_gemm(a, C.tc, pv, tiles, &s->tc, arows, s->num_sms, cs, &extra));
             launches += extra > 1 ? extra - 1 : 0;
@@ -613,8 +614,10 @@ codec_status codec_vocos_decode(codec_vocos_t* s, const float* mel, const int32_
     for (int l = 0; l < g.layers; l++) {
         const VBlock& Bk = s->blocks[l];
         const bool p1 = ln(s->xb[l], Lp, Bk.dw_w, Bk.dw_b, Bk.ln_g, Bk.ln_b, s->u, Ld, &Bk.pw1);
-        gemm(Bk.pw1, s->u, Ld, s->f, Ld, nullptr, EPI_GELU, p1);
-        gemm(Bk.pw2, s->f, Ld, s->xb[l + 1], Lp, s->xb[l], EPI_RESID);
+        // the GELU in the second linear's operand prep on the tensor cores (same bits)
+        const bool gp = Bk.pw1.use_tc && Bk.pw2.use_tc;
+        gemm(Bk.pw1, s->u, Ld, s->f, Ld, nullptr, gp ? EPI_STORE : EPI_GELU, p1);
+        gemm(Bk.pw2, s->f, Ld, s->xb[l + 1], Lp, s->xb[l], EPI_RESID, false, gp);
     }
     const bool ph = ln(s->xb[g.layers], Lp, nullptr, nullptr, s->final_g, s->final_b, s->u, Ld, &s->head);
     gemm(s->head, s->u, Ld, s->spec, Ld, nullptr, EPI_STORE, ph);
