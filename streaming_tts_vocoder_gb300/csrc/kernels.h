@@ -37,6 +37,14 @@ cudaError_t launch_rms_norm(const float* x, Layout xl, const float* g, float eps
 // (optional): the output as operand planes instead of o, as for RMSNorm.
 // Shared memory one attention block needs (the kernel allows up to 227 KB).
 size_t swa_smem_bytes(int dh, int window);
+// The tensor-core variant for long windows (head width 64, window >= 128);
+// launch_swa takes it where eligible.
+size_t swa_mma_smem_bytes(int window);
+bool swa_mma_eligible(int dh, int window);
+cudaError_t configure_swa_mma();
+cudaError_t launch_swa_mma(const float* q, float* o, const float* kring, const float* vring, int d, int heads,
+                           int window, int ring_R, int pos_r, PlanView plan, const int* qcum, int n_qblocks,
+                           cudaStream_t s, void* planes, int planes_il);
 constexpr int kSwaWindowMax = 256;
 constexpr size_t kSwaSmemMax = 227 * 1024;
 

@@ -222,7 +222,7 @@ __global__ void rms_norm_kernel(const float* __restrict__ x, Layout xl, const fl
     const int d4 = d >> 2;
     const float4* g4 = reinterpret_cast<const float4*>(g);
     float ss = 0.f;
-    if (PR > 0) {
+    if constexpr (PR > 0) {
         float4 v[PR > 0 ? PR : 1];
 #pragma unroll
         for (int i = 0; i < PR; i++) {
@@ -248,20 +248,20 @@ __global__ void rms_norm_kernel(const float* __restrict__ x, Layout xl, const fl
                 else yr[c] = o;
             }
         }
-        return;
-    }
-    for (int c = lane; c < d4; c += 32) {
-        const float4 v = xr[c];
-        ss = fmaf(v.x, v.x, ss); ss = fmaf(v.y, v.y, ss); ss = fmaf(v.z, v.z, ss); ss = fmaf(v.w, v.w, ss);
-    }
+    } else {
+        for (int c = lane; c < d4; c += 32) {
+            const float4 v = xr[c];
+            ss = fmaf(v.x, v.x, ss); ss = fmaf(v.y, v.y, ss); ss = fmaf(v.z, v.z, ss); ss = fmaf(v.w, v.w, ss);
+        }
 #pragma unroll
-    for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    const float r = rsqrtf(ss / (float)d + eps);
-    for (int c = lane; c < d4; c += 32) {
-        const float4 v = xr[c], w = __ldg(g4 + c);
-        const float4 o = make_float4(v.x * r * w.x, v.y * r * w.y, v.z * r * w.z, v.w * r * w.w);
-        if (planes) plane_store4(planes, planes_il, yrow, d, 4 * c, o);
-        else yr[c] = o;
+        for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        const float r = rsqrtf(ss / (float)d + eps);
+        for (int c = lane; c < d4; c += 32) {
+            const float4 v = xr[c], w = __ldg(g4 + c);
+            const float4 o = make_float4(v.x * r * w.x, v.y * r * w.y, v.z * r * w.z, v.w * r * w.w);
+            if (planes) plane_store4(planes, planes_il, yrow, d, 4 * c, o);
+            else yr[c] = o;
+        }
     }
 }
 
@@ -521,6 +521,9 @@ cudaError_t launch_swa(const float* q, float* o, const float* kring, const float
     if (planes && (d % 32 != 0)) return cudaErrorInvalidValue;
     const int dh = d / heads;
     if (dh > kSwaMaxDh || dh % 4 != 0 || window > kSwaMaxW) return cudaErrorInvalidValue;
+    if (swa_mma_eligible(dh, window))
+        return launch_swa_mma(q, o, kring, vring, d, heads, window, ring_R, pos_r, plan, qcum, n_qblocks, s, planes,
+                              planes_il);
     const size_t smem = swa_smem_bytes(dh, window);
     if (smem > (size_t)kSwaMaxSmem) return cudaErrorInvalidValue;
     launch_pdl(swa_kernel, dim3(n_qblocks, heads), dim3(kSwaThreads), smem, s, q, o, kring, vring, d, heads,
@@ -816,6 +819,8 @@ cudaError_t launch_state_reset(const HistDesc* d, int nd, const int* slots, int 
 cudaError_t configure_simt_kernels()
 {
     cudaError_t e = cudaFuncSetAttribute(swa_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSwaMaxSmem);
+    if (e != cudaSuccess) return e;
+    e = configure_swa_mma();
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(final_conv_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kFinalMaxSmem);
     if (e != cudaSuccess) return e;
