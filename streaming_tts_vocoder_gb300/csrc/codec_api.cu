@@ -1112,7 +1112,7 @@ void enqueue_decode(codec_state_t* s, Launcher& L, const void* input, int32_t T_
         L.run(CODEC_KERNEL_ATTENTION, attn_flops, attn_bytes, "attention", [&] {
             return launch_swa(s->q, s->o, s->kring + per_layer * l, s->vring + per_layer * l, g.d, g.heads,
                               g.window, s->R, rt, L.pv, L.q16, L.nq16, cs, W.o.use_tc ? pl : nullptr,
-                              W.o.tc.passes == 3 ? 1 : 0);
+                              W.o.tc.passes == 3 ? 1 : 0, g.precision != CODEC_PRECISION_FP32);
         });
         L.gemm(W.o, s->o, Ltd, lt, s->h, Ltd, g.d, 1, s->h, EPI_RESID, 1.f, 0, "out-proj", W.o.use_tc);
         L.run(CODEC_KERNEL_RMSNORM, norm_flops, norm_bytes, "rmsnorm 2", [&] {

@@ -48,9 +48,11 @@ cudaError_t launch_swa_mma(const float* q, float* o, const float* kring, const f
 constexpr int kSwaWindowMax = 256;
 constexpr size_t kSwaSmemMax = 227 * 1024;
 
+// tensor_cores: take the tensor-core variant where it is eligible (the fp32
+// precision mode keeps every product on the CUDA cores).
 cudaError_t launch_swa(const float* q, float* o, const float* kring, const float* vring, int d,
                        int heads, int window, int ring_R, int pos_r, PlanView plan, const int* qcum, int n_qblocks,
-                       cudaStream_t s, void* planes = nullptr, int planes_il = 1);
+                       cudaStream_t s, void* planes = nullptr, int planes_il = 1, bool tensor_cores = false);
 
 // Shared memory of one final-conv block (the kernel allows up to kFinalSmemMax).
 size_t final_conv_smem_bytes(int C, int k);

@@ -515,13 +515,13 @@ size_t swa_smem_bytes(int dh, int window)
 
 cudaError_t launch_swa(const float* q, float* o, const float* kring, const float* vring, int d,
                        int heads, int window, int ring_R, int pos_r, PlanView plan, const int* qcum, int n_qblocks,
-                       cudaStream_t s, void* planes, int planes_il)
+                       cudaStream_t s, void* planes, int planes_il, bool tensor_cores)
 {
     if (n_qblocks <= 0) return cudaSuccess;
     if (planes && (d % 32 != 0)) return cudaErrorInvalidValue;
     const int dh = d / heads;
     if (dh > kSwaMaxDh || dh % 4 != 0 || window > kSwaMaxW) return cudaErrorInvalidValue;
-    if (swa_mma_eligible(dh, window))
+    if (tensor_cores && swa_mma_eligible(dh, window))
         return launch_swa_mma(q, o, kring, vring, d, heads, window, ring_R, pos_r, plan, qcum, n_qblocks, s, planes,
                               planes_il);
     const size_t smem = swa_smem_bytes(dh, window);

@@ -118,6 +118,29 @@ def test_mimi_shaped_decoder_window_251_ring_512():
     assert bits_equal(a, b)
 
 
+@pytest.mark.parametrize("precision", [C.PRECISION_FP32, C.PRECISION_FP16X3])
+def test_long_window_head_64_attention_path(precision):
+    """A small latent decoder with 64-wide heads and a 150-position window:
+    in the tensor-core modes its attention takes the warp-MMA kernel for long
+    windows (keys staged from a 16-aligned position), in fp32 the CUDA-core
+    one.  20 frames (320 positions) against the oracle, and every chunking,
+    ragged ones included, equal to a full GPU decode bit for bit."""
+    import dataclasses
+    cfg = dataclasses.replace(tiny_mimi_config(), name="tiny_mimi_h64", d=128, heads=2, ffn=256, window=150)
+    blob = pack_blob(cfg, make_weights(cfg, 0))
+    cod = C.Codec(cfg, blob, max_streams=2, max_chunk_frames=20, max_batch_frames=40, precision=precision)
+    st = cod.state()
+    x = make_latents(cfg, 20, 9)
+    (full,), (full_pt,) = decode_lat(st, [(0, x)])
+    ref, ref_pt = OracleModel(cfg, blob).decode_latents_full(x, pre_tanh=True)
+    assert_close(full, ref, "20 frames")
+    assert_close_pre_tanh(full_pt, ref_pt, "20 frames")
+    for splits in ([1, 2, 4, 8, 5], [3] * 6 + [2], [13, 7]):
+        st.reset()
+        a, p = chunked(st, 1, x, splits)
+        assert bits_equal(a, full) and bits_equal(p, full_pt), splits
+
+
 def test_latent_variant_call_errors(tiny_mimi):
     cfg, blob, om = tiny_mimi
     cod = C.Codec(cfg, blob, max_streams=1, max_chunk_frames=4, precision=C.PRECISION_FP32)
