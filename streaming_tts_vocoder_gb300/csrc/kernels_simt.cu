@@ -300,13 +300,16 @@ __device__ __forceinline__ void cp_async_wait()
 // A block takes up to kSwaQueries consecutive queries of one stream and one
 // head.  It stages the keys and values of every position they can see (at
 // most kSwaQueries + W - 1 rows of the stream's ring: position p lives in
-// ring row p mod R) in shared memory once, with 128-bit loads, then runs
-// three passes over the whole block: every (query, key) score (a thread per
-// pair, the dot product over the head's channels in ascending order), the
-// softmax of each query (a warp per query: lane i takes keys lo + i,
-// lo + 32 + i, ... of the query's own window lo .. p, max and denominator
-// through a fixed butterfly), and every output channel (a thread per
-// (query, channel), the value sum over the window's keys in position order).
+// ring row p mod R) in shared memory once, by asynchronous 16-byte copies,
+// then runs three passes over the whole block: every (query, key) score (a
+// thread per 4 x 4 tile of pairs, each dot product over the head's channels
+// in ascending order), the softmax of each query (a warp per query: lane i
+// takes keys lo + i, lo + 32 + i, ... of the query's own window lo .. p, max
+// and denominator through a fixed butterfly), and every output channel (a
+// thread per pair of queries and four channels, each value sum over its
+// query's window keys in position order).  This is the CUDA-core kernel;
+// long windows with 64-wide heads take the tensor-core one in the
+// tensor-core precision modes (attention_mma.cu).
 // A query at absolute position p attends positions max(0, p - W + 1) .. p, and
 // every sum it takes runs in an order fixed by its own window, so its result
 // never depends on how the stream was chunked (blixt/phonon "Speed" item 7:
