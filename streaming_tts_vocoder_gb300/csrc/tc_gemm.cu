@@ -80,6 +80,7 @@ constexpr int kChunkKb = 8;          // 8 k-blocks = 256 of K = 16 MMA k-steps p
 struct TcParams {
     int n_row_tiles;
     int mtiles;         // M-tiles per CTA tile: 2 when BN <= 128, else 1
+    int issuers;        // MMA-issuing threads: one per M-tile
     int n_mgroups;      // ceil(n_row_tiles / mtiles)
     int n_tiles_n;
     int BN;
@@ -401,15 +402,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     constexpr uint32_t kABox = kBM * kRow;                    // one M-tile's A box
     constexpr int kBoxK = kPasses == 3 ? 2 * kBK : kBK;       // box width in elements
     if (threadIdx.x == 0) {
+        // every MMA-issuing thread commits once per stage, chunk and drain
         for (int s = 0; s < p.stages; s++) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], p.issuers);
         }
         for (int i = 0; i < p.nbuf; i++) {
-            mbar_init(&tfull[i], 1);
+            mbar_init(&tfull[i], p.issuers);
             mbar_init(&tempty[i], kEpiWarps);
         }
-        mbar_init(drain, 1);
+        mbar_init(drain, p.issuers);
         mbar_init(unarrived, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -483,12 +485,17 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
                 const int last = q + ((it - 1 - q) / p.stages) * p.stages;
                 mbar_drain(&full[q], (uint32_t)(last / p.stages) & 1u);
             }
-        } else if (warp == 1 && lane == 0) {
+        } else if ((warp == 1 || (warp == 2 && p.issuers == 2)) && lane == 0) {
             // --------------------------------------------------- MMA issue --
             // The k-loop of a tile is cut into chunks of chunk_kb k-blocks; each
             // chunk accumulates from zero into one of the TMEM buffers, which
             // the epilogue folds into rounded fp32 sums while the next chunk
-            // runs.  Indices by increments, as in the producer.
+            // runs.  Indices by increments, as in the producer.  Two M-tiles
+            // get an issuing thread each (warp 1: M-tile 0, warp 2: M-tile 1):
+            // for narrow tiles one thread's issue loop, not the tensor pipe,
+            // set the pace.  An accumulator gets its MMAs in one fixed order
+            // from one thread.
+            const int mi = warp - 1;
             int s = 0, acc = 0;
             uint32_t ph = 0, aph = 0;
             const uint32_t smem0 = smem_u32(smem);
@@ -500,8 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
                 for (int kb0 = kb_lo; kb0 < kb_hi && ok; kb0 += p.chunk_kb) {
                     if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, p.wait_polls)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t d0 = tmem_base + (uint32_t)acc * p.buf_cols;
-                    const uint32_t d1 = d0 + p.mt_cols;
+                    const uint32_t d0 = tmem_base + (uint32_t)acc * p.buf_cols + (uint32_t)mi * p.mt_cols;
                     const int kb1 = min(p.nkb, kb0 + p.chunk_kb);
                     for (int kb = kb0; kb < kb1; kb++) {
                         if (!mbar_wait(&full[s], ph, abort_flag, p.wait_polls)) { ok = false; break; }
@@ -509,36 +515,19 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
                         // descriptors of the stage's boxes: one base plus constant
                         // steps; in three-pass mode the lo part of a row sits 64
                         // bytes after its hi part
-                        const uint64_t a0h = kPasses == 3 ? sdesc_sw128(sa) : sdesc_sw64(sa);
-                        const uint64_t a0l = a0h + (64 >> 4);
-                        const uint64_t a1h = a0h + (kABox >> 4);
-                        const uint64_t a1l = a1h + (64 >> 4);
-                        const uint64_t bh = a0h + (((uint32_t)p.mtiles * kABox) >> 4);
+                        const uint64_t base = kPasses == 3 ? sdesc_sw128(sa) : sdesc_sw64(sa);
+                        const uint64_t ah = base + (((uint32_t)mi * kABox) >> 4);
+                        const uint64_t al = ah + (64 >> 4);
+                        const uint64_t bh = base + (((uint32_t)p.mtiles * kABox) >> 4);
                         const uint64_t bl = bh + (64 >> 4);
-                        if (p.mtiles == 2) {
 #pragma unroll
-                            for (int k = 0; k < kBK / 16; k++) {
-                                const uint64_t o = (uint64_t)((k * 32) >> 4);
-                                const uint32_t accum = (kb != kb0 || k != 0) ? 1u : 0u;
-                                mma_f16(d0, a0h + o, bh + o, p.idesc, accum);
-                                mma_f16(d1, a1h + o, bh + o, p.idesc, accum);
-                                if (kPasses == 3) {
-                                    mma_f16(d0, a0h + o, bl + o, p.idesc, 1u);
-                                    mma_f16(d1, a1h + o, bl + o, p.idesc, 1u);
-                                    mma_f16(d0, a0l + o, bh + o, p.idesc, 1u);
-                                    mma_f16(d1, a1l + o, bh + o, p.idesc, 1u);
-                                }
-                            }
-                        } else {
-#pragma unroll
-                            for (int k = 0; k < kBK / 16; k++) {
-                                const uint64_t o = (uint64_t)((k * 32) >> 4);
-                                const uint32_t accum = (kb != kb0 || k != 0) ? 1u : 0u;
-                                mma_f16(d0, a0h + o, bh + o, p.idesc, accum);
-                                if (kPasses == 3) {
-                                    mma_f16(d0, a0h + o, bl + o, p.idesc, 1u);
-                                    mma_f16(d0, a0l + o, bh + o, p.idesc, 1u);
-                                }
+                        for (int k = 0; k < kBK / 16; k++) {
+                            const uint64_t o = (uint64_t)((k * 32) >> 4);
+                            const uint32_t accum = (kb != kb0 || k != 0) ? 1u : 0u;
+                            mma_f16(d0, ah + o, bh + o, p.idesc, accum);
+                            if (kPasses == 3) {
+                                mma_f16(d0, ah + o, bl + o, p.idesc, 1u);
+                                mma_f16(d0, al + o, bh + o, p.idesc, 1u);
                             }
                         }
                         mma_commit(&empty[s]);
@@ -1031,6 +1020,7 @@ cudaError_t tc_gemm_core(const GemmArgs& a, const TcWeights& w, const float* uns
     p.cin_blocks = a.Cin / kBK;
     p.ntaps = a.ntaps;
     p.nkb = a.ntaps * p.cin_blocks;
+    p.issuers = p.mtiles;
     // operand rows in a stage: 128 bytes (a k-block's hi and lo) or 64 (hi only)
     const uint32_t row = w.passes == 3 ? 128u : 64u;
     p.stage_bytes = (uint32_t)p.mtiles * kBM * row + round1024((uint32_t)w.BN * row);
