@@ -887,11 +887,16 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer
 
 uint32_t round1024(uint32_t x) { return (x + 1023u) & ~1023u; }
 
-// N-tile: a multiple of 32 up to 256 that pads N least (ties: the wider).
+// N-tile: 32, 64, 96, 128 or 256, the one that pads N least (ties: the
+// wider).  Tiles of at most 128 columns pair two M-tiles with an MMA-issuing
+// thread each, and a 256-column MMA runs at the pipe's rate; the widths in
+// between (160 to 224) ran one M-tile from one issuing thread, which set the
+// pace below the pipe's rate.
 int pick_bn(int N)
 {
     int best = 32;
     for (int bn = 32; bn <= kMaxBN; bn += 32) {
+        if (bn > 128 && bn < kMaxBN) continue;
         const int pad = (N + bn - 1) / bn * bn, best_pad = (N + best - 1) / best * best;
         if (pad < best_pad || (pad == best_pad && bn > best)) best = bn;
     }
