@@ -81,6 +81,7 @@ struct TcParams {
     int n_row_tiles;
     int mtiles;         // M-tiles per CTA tile: 2 when BN <= 128, else 1
     int issuers;        // MMA-issuing threads: one per M-tile
+    int b_early;        // 1: B may be loaded before the grid dependency resolves
     int n_mgroups;      // ceil(n_row_tiles / mtiles)
     int n_tiles_n;
     int BN;
@@ -425,12 +426,29 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    // the set-up above touches shared memory and TMEM only; global memory
-    // written by earlier kernels is read from here on
+    const int total_tiles = p.n_mgroups * p.n_tiles_n * p.n_splits;
+    // Weights written before any kernel of the stream ran (p.b_early) do not
+    // depend on the earlier kernels: the copy thread issues the B boxes of its
+    // first tile's first stages now, while an earlier kernel may still run.
+    int b_pre = 0;
+    if (p.b_early && warp == 0 && lane == 0 && (int)blockIdx.x < total_tiles) {
+        prefetch_tensormap(&mb);
+        const int tile = blockIdx.x;
+        const int sp = tile % p.n_splits, mn = tile / p.n_splits;
+        const int n0 = (mn % p.n_tiles_n) * p.BN;
+        const int kb_lo = sp * p.cps * p.chunk_kb, kb_hi = min(p.nkb, kb_lo + p.cps * p.chunk_kb);
+        b_pre = min(p.stages, kb_hi - kb_lo);
+        uint8_t* st = smem;
+        for (int q = 0; q < b_pre; q++, st += p.stage_bytes) {
+            mbar_expect_tx(&full[q], p.tx_bytes);
+            tma_load_2d(st + p.mtiles * kABox, &mb, &full[q], (kb_lo + q) * kBoxK, n0);
+        }
+    }
+    // the set-up above touches shared memory, TMEM and the weights only;
+    // global memory written by earlier kernels is read from here on
     pdl_wait();
     pdl_launch();
     const uint32_t tmem_base = *tmem_slot;
-    const int total_tiles = p.n_mgroups * p.n_tiles_n * p.n_splits;
     const float unscale = p.unscale_dev ? *p.unscale_dev : p.unscale;
     const int wg = warp >> 2;
 
@@ -460,10 +478,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
                 for (int kb = kb_lo; kb < kb_hi; kb++) {
                     if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.wait_polls)) { ok = false; break; }
                     const int c0 = cb * kBoxK;
-                    mbar_expect_tx(&full[s], p.tx_bytes);
+                    // the first b_pre stages were armed, and their B boxes issued, above
+                    if (it >= b_pre) mbar_expect_tx(&full[s], p.tx_bytes);
                     tma_load_2d(st, &ma, &full[s], c0, row0);
                     if (p.mtiles == 2) tma_load_2d(st + kABox, &ma, &full[s], c0, row1);
-                    tma_load_2d(st + p.mtiles * kABox, &mb, &full[s], kb * kBoxK, n0);
+                    if (it >= b_pre) tma_load_2d(st + p.mtiles * kABox, &mb, &full[s], kb * kBoxK, n0);
                     it++;
                     st += p.stage_bytes;
                     if (++s == p.stages) {
@@ -950,7 +969,15 @@ bool tc_pack_weights(const float* wkn, int ntaps, int Cin, int N, int passes, Tc
     out->unscale = std::ldexp(1.0f, -e);
     out->BN = pick_bn(N);
     out->n_tiles = (N + out->BN - 1) / out->BN;
+    out->b_static = true;   // the synchronous copy above completes before any later kernel
     if (!make_map(&out->map_hi, dh, KP, (uint64_t)N, passes == 3 ? 2 * kBK : kBK, (uint32_t)out->BN)) return false;
+    out->n_alt = 0;
+    for (const int bn : {128, 64}) {
+        if (bn >= out->BN) continue;
+        if (!make_map(&out->map_alt[out->n_alt], dh, KP, (uint64_t)N, passes == 3 ? 2 * kBK : kBK, (uint32_t)bn))
+            return false;
+        out->bn_alt[out->n_alt++] = bn;
+    }
     return true;
 }
 
@@ -1011,81 +1038,100 @@ cudaError_t tc_gemm_core(const GemmArgs& a, const TcWeights& w, const float* uns
     if (!make_map(&ma, a_planes, a_inner, (uint64_t)a_rows, box_k, kBM)) return cudaErrorInvalidValue;
     TcParams p;
     p.n_row_tiles = n_row_tiles;
-    // two M-tiles share each B tile when N is narrow, unless pairing would
-    // leave SMs idle (few rows: latency matters more than B traffic).  Each
-    // M-tile's MMAs are the same either way, so the pairing never changes a
-    // result's bits.
-    {
-        const int sms = num_sms > 0 ? num_sms : 152;
-        p.mtiles = (w.BN <= 128 && ((n_row_tiles + 1) / 2) * w.n_tiles >= sms) ? 2 : 1;
-    }
-    p.n_mgroups = (n_row_tiles + p.mtiles - 1) / p.mtiles;
-    p.n_tiles_n = w.n_tiles;
-    p.BN = w.BN;
     p.cin_blocks = a.Cin / kBK;
     p.ntaps = a.ntaps;
     p.nkb = a.ntaps * p.cin_blocks;
-    p.issuers = p.mtiles;
-    // operand rows in a stage: 128 bytes (a k-block's hi and lo) or 64 (hi only)
-    const uint32_t row = w.passes == 3 ? 128u : 64u;
-    p.stage_bytes = (uint32_t)p.mtiles * kBM * row + round1024((uint32_t)w.BN * row);
-    p.tx_bytes = (uint32_t)p.mtiles * kBM * row + (uint32_t)w.BN * row;
-    const int extra = 1024 + 512 + kStageOutBytes;   // alignment slack, barriers and flags, the epilogue's staging
-    p.stages = std::min(8, (kSmemBudget - extra) / (int)p.stage_bytes);
-    if (p.stages < 2) return cudaErrorInvalidValue;
-    p.idesc = idesc_f16(kBM, w.BN);
-    p.mt_cols = (uint32_t)((w.BN + 31) / 32 * 32);
-    p.buf_cols = (uint32_t)p.mtiles * p.mt_cols;
-    p.nbuf = std::min<int>(kMaxBufs, (int)(kTmemCols / p.buf_cols));
     // a short k-loop (<= 12 k-blocks, 24 k-steps) accumulates in one chunk;
     // longer ones are cut every kChunkKb k-blocks
     p.chunk_kb = p.nkb <= 12 ? p.nkb : kChunkKb;
     p.n_chunks = (p.nkb + p.chunk_kb - 1) / p.chunk_kb;
-    // Too few tiles to fill the GPU: split the k-loop over CTAs by whole
-    // chunks.  The reduce kernel folds the chunk partials in the same order
-    // as the unsplit epilogue, so splitting never changes a result's bits.
-    p.n_splits = 1;
-    p.cps = p.n_chunks;
-    p.ws = nullptr;
-    {
+    const int sms = num_sms > 0 ? num_sms : 152;
+    // One candidate N-tile width: M-tile pairing, split count and the time of
+    // the busiest CTA in MMA cycles.
+    struct Shape {
+        int bn, n_tiles, mtiles, cps, n_splits;
+        const CUtensorMap* map;
+        double est;
+    };
+    auto shape_for = [&](int bn, const CUtensorMap* map) {
+        Shape c{bn, (a.N + bn - 1) / bn, 1, p.n_chunks, 1, map, 0.0};
+        // two M-tiles share each B tile when N is narrow, unless pairing would
+        // leave SMs idle (few rows: latency matters more than B traffic).  Each
+        // M-tile's MMAs are the same either way, so the pairing never changes a
+        // result's bits.
+        c.mtiles = (bn <= 128 && ((n_row_tiles + 1) / 2) * c.n_tiles >= sms) ? 2 : 1;
+        // Too few tiles to fill the GPU: split the k-loop over CTAs by whole
+        // chunks.  The reduce kernel folds the chunk partials in the same order
+        // as the unsplit epilogue, so splitting never changes a result's bits.
         // Pick the split count that minimises waves / splits, the time of the
         // busiest CTA in units of a whole tile's k-loop: with few tiles (a
         // one-frame call) it spreads every tile over many CTAs; with a little
         // over one wave (1600 rows of a transformer linear: 156 tiles on 152
         // SMs) it evens out the second wave.  A split pays for its partials'
         // round trip and the reduction, so it must win by more than 10 %.
-        const int sms = num_sms > 0 ? num_sms : 152;
-        const int tiles = ((n_row_tiles + p.mtiles - 1) / p.mtiles) * w.n_tiles;
+        const int tiles = ((n_row_tiles + c.mtiles - 1) / c.mtiles) * c.n_tiles;
         const size_t need = (size_t)p.n_chunks * n_row_tiles * kBM * a.N;
         if (ws && p.n_chunks >= 2 && need <= ws_floats && tiles < 4 * sms) {
             double best = (double)((tiles + sms - 1) / sms);
-            int best_cps = p.n_chunks;
             for (int ns = 2; ns <= p.n_chunks; ns++) {
                 const int cps = (p.n_chunks + ns - 1) / ns;
                 const int nsplit = (p.n_chunks + cps - 1) / cps;
                 const double t = (double)((tiles * nsplit + sms - 1) / sms) * cps / p.n_chunks;
                 if (t < best * 0.9) {
                     best = t;
-                    best_cps = cps;
+                    c.cps = cps;
                 }
             }
-            p.cps = best_cps;
-            p.n_splits = (p.n_chunks + p.cps - 1) / p.cps;
-            if (p.n_splits > 1) p.ws = ws;
+            c.n_splits = (p.n_chunks + c.cps - 1) / c.cps;
         }
-    }
+        // a 128 x bn x 16 MMA: about bn / 2 cycles, never under ~48
+        const double mma = std::max(48.0, 0.49 * bn) * c.mtiles;
+        c.est = (double)((tiles * c.n_splits + sms - 1) / sms) * c.cps * mma;
+        return c;
+    };
+    Shape sh = shape_for(w.BN, &w.map_hi);
+    // A call of one or two row tiles (a frame or two) is bound by latency: a
+    // narrower tile over the same weight planes may finish sooner (the
+    // per-element result of an MMA does not depend on the tile width, so
+    // neither do the bits); it must win by 10 %.  With more rows the
+    // partials' traffic of the extra splits was measured to cancel the gain.
+    if (n_row_tiles <= 2 && sh.n_tiles < sms)
+        for (int i = 0; i < w.n_alt; i++) {
+            const Shape c = shape_for(w.bn_alt[i], &w.map_alt[i]);
+            if (c.est < sh.est * 0.9) sh = c;
+        }
+    p.mtiles = sh.mtiles;
+    p.n_mgroups = (n_row_tiles + p.mtiles - 1) / p.mtiles;
+    p.n_tiles_n = sh.n_tiles;
+    p.BN = sh.bn;
+    p.issuers = p.mtiles;
+    p.b_early = w.b_static ? 1 : 0;
+    // operand rows in a stage: 128 bytes (a k-block's hi and lo) or 64 (hi only)
+    const uint32_t row = w.passes == 3 ? 128u : 64u;
+    p.stage_bytes = (uint32_t)p.mtiles * kBM * row + round1024((uint32_t)p.BN * row);
+    p.tx_bytes = (uint32_t)p.mtiles * kBM * row + (uint32_t)p.BN * row;
+    const int extra = 1024 + 512 + kStageOutBytes;   // alignment slack, barriers and flags, the epilogue's staging
+    p.stages = std::min(8, (kSmemBudget - extra) / (int)p.stage_bytes);
+    if (p.stages < 2) return cudaErrorInvalidValue;
+    p.idesc = idesc_f16(kBM, p.BN);
+    p.mt_cols = (uint32_t)((p.BN + 31) / 32 * 32);
+    p.buf_cols = (uint32_t)p.mtiles * p.mt_cols;
+    p.nbuf = std::min<int>(kMaxBufs, (int)(kTmemCols / p.buf_cols));
+    p.cps = sh.cps;
+    p.n_splits = sh.n_splits;
+    p.ws = p.n_splits > 1 ? ws : nullptr;
     p.unscale = w.unscale;
     p.unscale_dev = unscale_dev;
     p.err = err;
     p.wait_polls = wl.polls;
     p.unarrived_wait = wl.unarrived_wait;
     const size_t smem = (size_t)p.stages * p.stage_bytes + extra;
-    const int tiles = p.n_mgroups * w.n_tiles * p.n_splits;
-    const int grid = std::min(tiles, num_sms > 0 ? num_sms : 152);
+    const int tiles = p.n_mgroups * p.n_tiles_n * p.n_splits;
+    const int grid = std::min(tiles, sms);
     if (w.passes == 3)
-        launch_pdl(tc_gemm_kernel<3>, dim3(grid), dim3(kThreads), smem, s, ma, w.map_hi, a, plan, p);
+        launch_pdl(tc_gemm_kernel<3>, dim3(grid), dim3(kThreads), smem, s, ma, *sh.map, a, plan, p);
     else
-        launch_pdl(tc_gemm_kernel<1>, dim3(grid), dim3(kThreads), smem, s, ma, w.map_hi, a, plan, p);
+        launch_pdl(tc_gemm_kernel<1>, dim3(grid), dim3(kThreads), smem, s, ma, *sh.map, a, plan, p);
     cudaError_t e = cudaGetLastError();
     if (launches) (*launches)++;
     if (e != cudaSuccess || p.n_splits == 1) return e;

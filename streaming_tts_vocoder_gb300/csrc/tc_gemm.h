@@ -19,6 +19,17 @@ struct TcWeights {
     int BN = 0;              // N tile (multiple of 32, <= 256)
     int n_tiles = 0;
     int passes = 3;          // 3: hi*hi + hi*lo + lo*hi; 1: hi*hi only (single fp16 pass)
+    // the planes were complete before any kernel that may precede a GEMM in
+    // its stream ran (uploaded by a synchronous copy): the GEMM may load them
+    // before its grid dependency resolves
+    bool b_static = false;
+    // Narrower N tiles over the same planes (128 and/or 64 columns, when BN is
+    // wider), for calls with too few tiles to fill the GPU: a 128 x N x 16 MMA
+    // costs about N / 2 cycles above a floor near 48, so a narrow tile ends a
+    // chunk sooner and more CTAs share the work.
+    CUtensorMap map_alt[2];
+    int bn_alt[2] = {0, 0};
+    int n_alt = 0;
 };
 
 // Scratch of one standalone tensor-core conv: operand planes, and kOpWords
