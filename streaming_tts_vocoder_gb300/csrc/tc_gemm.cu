@@ -80,7 +80,10 @@ constexpr int kChunkKb = 8;          // 8 k-blocks = 256 of K = 16 MMA k-steps p
 struct TcParams {
     int n_row_tiles;
     int mtiles;         // M-tiles per CTA tile: 2 when BN <= 128, else 1
-    int issuers;        // MMA-issuing threads: one per M-tile
+    int issuers;        // MMA-issuing threads: one per M-tile, or two halves of one tile's N
+    uint32_t iss_a;     // the second issuer's offsets: its A box (bytes into the stage),
+    uint32_t iss_b;     //   its B rows (bytes into the stage's B box)
+    uint32_t iss_d;     //   and its accumulator columns
     int b_early;        // 1: B may be loaded before the grid dependency resolves
     int n_mgroups;      // ceil(n_row_tiles / mtiles)
     int n_tiles_n;
@@ -431,6 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     // depend on the earlier kernels: the copy thread issues the B boxes of its
     // first tile's first stages now, while an earlier kernel may still run.
     int b_pre = 0;
+    if (warp == 0 && lane == 0) prefetch_tensormap(&ma);   // a kernel parameter: no dependency
     if (p.b_early && warp == 0 && lane == 0 && (int)blockIdx.x < total_tiles) {
         prefetch_tensormap(&mb);
         const int tile = blockIdx.x;
@@ -513,7 +517,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
             // get an issuing thread each (warp 1: M-tile 0, warp 2: M-tile 1):
             // for narrow tiles one thread's issue loop, not the tensor pipe,
             // set the pace.  An accumulator gets its MMAs in one fixed order
-            // from one thread.
+            // from one thread.  A lone M-tile in a latency-bound call may
+            // instead be cut into two column halves, one per issuing thread
+            // (the per-element result of an MMA does not depend on its width).
             const int mi = warp - 1;
             int s = 0, acc = 0;
             uint32_t ph = 0, aph = 0;
@@ -526,7 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
                 for (int kb0 = kb_lo; kb0 < kb_hi && ok; kb0 += p.chunk_kb) {
                     if (!mbar_wait(&tempty[acc], aph ^ 1u, abort_flag, p.wait_polls)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t d0 = tmem_base + (uint32_t)acc * p.buf_cols + (uint32_t)mi * p.mt_cols;
+                    const uint32_t d0 = tmem_base + (uint32_t)acc * p.buf_cols + (uint32_t)mi * p.iss_d;
                     const int kb1 = min(p.nkb, kb0 + p.chunk_kb);
                     for (int kb = kb0; kb < kb1; kb++) {
                         if (!mbar_wait(&full[s], ph, abort_flag, p.wait_polls)) { ok = false; break; }
@@ -535,9 +541,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
                         // steps; in three-pass mode the lo part of a row sits 64
                         // bytes after its hi part
                         const uint64_t base = kPasses == 3 ? sdesc_sw128(sa) : sdesc_sw64(sa);
-                        const uint64_t ah = base + (((uint32_t)mi * kABox) >> 4);
+                        const uint64_t ah = base + (((uint32_t)mi * p.iss_a) >> 4);
                         const uint64_t al = ah + (64 >> 4);
-                        const uint64_t bh = base + (((uint32_t)p.mtiles * kABox) >> 4);
+                        const uint64_t bh = base + (((uint32_t)p.mtiles * kABox + (uint32_t)mi * p.iss_b) >> 4);
                         const uint64_t bl = bh + (64 >> 4);
 #pragma unroll
                         for (int k = 0; k < kBK / 16; k++) {
@@ -1104,7 +1110,6 @@ cudaError_t tc_gemm_core(const GemmArgs& a, const TcWeights& w, const float* uns
     p.n_mgroups = (n_row_tiles + p.mtiles - 1) / p.mtiles;
     p.n_tiles_n = sh.n_tiles;
     p.BN = sh.bn;
-    p.issuers = p.mtiles;
     p.b_early = w.b_static ? 1 : 0;
     // operand rows in a stage: 128 bytes (a k-block's hi and lo) or 64 (hi only)
     const uint32_t row = w.passes == 3 ? 128u : 64u;
@@ -1113,9 +1118,25 @@ cudaError_t tc_gemm_core(const GemmArgs& a, const TcWeights& w, const float* uns
     const int extra = 1024 + 512 + kStageOutBytes;   // alignment slack, barriers and flags, the epilogue's staging
     p.stages = std::min(8, (kSmemBudget - extra) / (int)p.stage_bytes);
     if (p.stages < 2) return cudaErrorInvalidValue;
-    p.idesc = idesc_f16(kBM, p.BN);
     p.mt_cols = (uint32_t)((p.BN + 31) / 32 * 32);
     p.buf_cols = (uint32_t)p.mtiles * p.mt_cols;
+    // Second issuing thread: the second M-tile, or (one M-tile, at most one
+    // CTA tile per SM: latency-bound) the second half of the tile's columns.
+    // Half of a 32-multiple is a 16-multiple (a valid MMA width) and starts
+    // its B rows on a whole swizzle atom.
+    p.issuers = 1;
+    p.iss_a = p.iss_b = p.iss_d = 0;
+    p.idesc = idesc_f16(kBM, p.BN);
+    if (p.mtiles == 2) {
+        p.issuers = 2;
+        p.iss_a = (uint32_t)kBM * row;
+        p.iss_d = p.mt_cols;
+    } else if (p.BN % 32 == 0 && (long long)p.n_mgroups * p.n_tiles_n * sh.n_splits <= sms) {
+        p.issuers = 2;
+        p.iss_b = (uint32_t)(p.BN / 2) * row;
+        p.iss_d = (uint32_t)(p.BN / 2);
+        p.idesc = idesc_f16(kBM, p.BN / 2);
+    }
     p.nbuf = std::min<int>(kMaxBufs, (int)(kTmemCols / p.buf_cols));
     p.cps = sh.cps;
     p.n_splits = sh.n_splits;
