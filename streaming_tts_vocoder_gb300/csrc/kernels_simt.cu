@@ -199,15 +199,28 @@ cudaError_t launch_gemm_simt(const GemmArgs& a, PlanView plan, int n_row_tiles, 
 // lane keeps in registers (the whole row is loaded at once, d <= 128 PR),
 // or 0 for a loop over any width.  Rows of dense layouts (no history rows in
 // either) need no segment lookup: row r is layout row r.
-template <int PR>
+template <int PR, bool kGainsEarly>
 __global__ void rms_norm_kernel(const float* __restrict__ x, Layout xl, const float* __restrict__ g,
                                 float eps, float* __restrict__ y, Layout yl, int d, PlanView plan,
                                 int total_rows, void* planes, int planes_il)
 {
-    pdl_wait();
-    pdl_launch();
     const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
+    const int d4 = d >> 2;
+    const float4* g4 = reinterpret_cast<const float4*>(g);
+    // the gains are weights, written before any kernel of the stream ran:
+    // with few rows (latency-bound) they are loaded before the wait for the
+    // earlier kernels; with many, the registers that takes cost occupancy
+    float4 gw[PR > 0 && kGainsEarly ? PR : 1];
+    if constexpr (PR > 0 && kGainsEarly) {
+#pragma unroll
+        for (int i = 0; i < PR; i++) {
+            const int c = lane + 32 * i;
+            gw[i] = c < d4 ? __ldg(g4 + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+    pdl_wait();
+    pdl_launch();
     if (row >= total_rows) return;
     long long xrow = row, yrow = row;
     if (xl.P != 0 || yl.P != 0) {
@@ -219,8 +232,6 @@ __global__ void rms_norm_kernel(const float* __restrict__ x, Layout xl, const fl
     }
     const float4* xr = reinterpret_cast<const float4*>(x + xrow * d);
     float4* yr = reinterpret_cast<float4*>(y + yrow * d);
-    const int d4 = d >> 2;
-    const float4* g4 = reinterpret_cast<const float4*>(g);
     float ss = 0.f;
     if constexpr (PR > 0) {
         float4 v[PR > 0 ? PR : 1];
@@ -242,7 +253,9 @@ __global__ void rms_norm_kernel(const float* __restrict__ x, Layout xl, const fl
         for (int i = 0; i < PR; i++) {
             const int c = lane + 32 * i;
             if (c < d4) {
-                const float4 w = __ldg(g4 + c);
+                float4 w;
+                if constexpr (kGainsEarly) w = gw[i];
+                else w = __ldg(g4 + c);
                 const float4 o = make_float4(v[i].x * r * w.x, v[i].y * r * w.y, v[i].z * r * w.z, v[i].w * r * w.w);
                 if (planes) plane_store4(planes, planes_il, yrow, d, 4 * c, o);
                 else yr[c] = o;
@@ -272,12 +285,15 @@ cudaError_t launch_rms_norm(const float* x, Layout xl, const float* g, float eps
     if (total_rows <= 0) return cudaSuccess;
     const int threads = 256, rows_per_block = threads / 32;
     const dim3 grid((total_rows + rows_per_block - 1) / rows_per_block);
-    if (d <= 1024)
-        launch_pdl(rms_norm_kernel<8>, grid, dim3(threads), 0, s, x, xl, g, eps, y, yl, d, plan, total_rows, planes,
-                   planes_il);
+    if (d <= 1024 && total_rows <= 2048)
+        launch_pdl(rms_norm_kernel<8, true>, grid, dim3(threads), 0, s, x, xl, g, eps, y, yl, d, plan, total_rows,
+                   planes, planes_il);
+    else if (d <= 1024)
+        launch_pdl(rms_norm_kernel<8, false>, grid, dim3(threads), 0, s, x, xl, g, eps, y, yl, d, plan, total_rows,
+                   planes, planes_il);
     else
-        launch_pdl(rms_norm_kernel<0>, grid, dim3(threads), 0, s, x, xl, g, eps, y, yl, d, plan, total_rows, planes,
-                   planes_il);
+        launch_pdl(rms_norm_kernel<0, false>, grid, dim3(threads), 0, s, x, xl, g, eps, y, yl, d, plan, total_rows,
+                   planes, planes_il);
     return cudaGetLastError();
 }
 

@@ -635,6 +635,19 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
                         if (p.n_splits == 1) {
 #pragma unroll
                             for (int i = 0; i < 32; i++) sum[c + i] = __fadd_rn(sum[c + i], __uint_as_float(r[i]));
+                        } else if (c < nvalid && mt < p.n_row_tiles && tr.nrows <= 16) {
+                            // a tile of a few rows (a frame or two): each lane
+                            // stores its own row's 16 or 32 columns, with no
+                            // transpose through shared memory
+                            if (m < tr.nrows) {
+                                float4* dst = reinterpret_cast<float4*>(wtile + (size_t)m * a.N + c);
+                                const int cnt = min(32, nvalid - c);
+#pragma unroll
+                                for (int i = 0; i < 8; i++)
+                                    if (4 * i < cnt)
+                                        dst[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                                                             __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+                            }
                         } else if (c < nvalid && mt < p.n_row_tiles) {
                             stage_put(stg, lane, reinterpret_cast<const float*>(r));
                             __syncwarp();
@@ -791,6 +804,18 @@ __global__ void __launch_bounds__(kReduceRows * 8) tc_reduce_kernel(const GemmAr
     const bool v4 = n + 4 <= a.N && (a.N & 3) == 0;
     int c = 0;
     if (v4) {
+        for (; c + 8 <= n_chunks; c += 8) {
+            float4 p[8];
+#pragma unroll
+            for (int u = 0; u < 8; u++) p[u] = __ldg(reinterpret_cast<const float4*>(src + (size_t)(c + u) * stride));
+#pragma unroll
+            for (int u = 0; u < 8; u++) {
+                sum[0] = __fadd_rn(sum[0], p[u].x);
+                sum[1] = __fadd_rn(sum[1], p[u].y);
+                sum[2] = __fadd_rn(sum[2], p[u].z);
+                sum[3] = __fadd_rn(sum[3], p[u].w);
+            }
+        }
         for (; c + 4 <= n_chunks; c += 4) {
             float4 p[4];
 #pragma unroll
