@@ -98,6 +98,7 @@ struct TcParams {
     uint32_t buf_cols;    // TMEM columns per buffer: mtiles x round32(BN) <= 256
     uint32_t mt_cols;     // TMEM column offset between the M-tiles of a buffer
     int nbuf;             // TMEM buffers (512 / buf_cols, at most kMaxBufs)
+    int epi_cols;         // columns of one M-tile an epilogue warpgroup finishes (<= kEpiCols)
     int chunk_kb;         // k-blocks accumulated in TMEM before the epilogue folds them in
     int n_chunks;         // chunks of a tile's k-loop
     int n_splits;         // CTA tiles per output tile along K (1: fold in registers)
@@ -579,13 +580,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
         asm volatile("setmaxnreg.inc.sync.aligned.u32 232;" ::: "memory");
         // ------------------------------------------------------ epilogue --
         // With two M-tiles, warpgroup 1 + g finishes M-tile g; with one, it
-        // finishes columns 128 g .. 128 g + 127.  Thread (warp w, lane l)
+        // finishes columns E g .. E g + E - 1 (E = p.epi_cols: 128, or half a
+        // narrower tile in 32-column slices).  Thread (warp w, lane l)
         // owns row 32 (w % 4) + l and keeps its <= 128 column sums in
         // registers across the chunks.
         const int g = wg - 1;
         const int my_mt = p.mtiles == 2 ? g : 0;
-        const int col0 = p.mtiles == 2 ? 0 : g * kEpiCols;
-        const int ncol = max(0, min(kEpiCols, p.BN - col0));
+        const int col0 = p.mtiles == 2 ? 0 : g * p.epi_cols;
+        const int ncol = max(0, min(p.epi_cols, p.BN - col0));
         const int q = warp & 3;
         const int m = q * 32 + lane;
         const int cq = lane & 7;        // column quad of the transposed pass
@@ -783,7 +785,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
 // Split tiles: fold the chunk partials of each output in chunk order with
 // rounded adds, exactly as the unsplit epilogue folds them in registers, then
 // apply the same per-element epilogue.  One thread per (row, 4 columns); the
-// partial loads of several chunks are in flight at once.
+// partial loads of up to 16 chunks are in flight at once.
 constexpr int kReduceRows = 32;
 __global__ void __launch_bounds__(kReduceRows * 8) tc_reduce_kernel(const GemmArgs a, const PlanView plan,
                                                                    const float* __restrict__ ws, int n_chunks,
@@ -804,6 +806,18 @@ __global__ void __launch_bounds__(kReduceRows * 8) tc_reduce_kernel(const GemmAr
     const bool v4 = n + 4 <= a.N && (a.N & 3) == 0;
     int c = 0;
     if (v4) {
+        for (; c + 16 <= n_chunks; c += 16) {
+            float4 p[16];
+#pragma unroll
+            for (int u = 0; u < 16; u++) p[u] = __ldg(reinterpret_cast<const float4*>(src + (size_t)(c + u) * stride));
+#pragma unroll
+            for (int u = 0; u < 16; u++) {
+                sum[0] = __fadd_rn(sum[0], p[u].x);
+                sum[1] = __fadd_rn(sum[1], p[u].y);
+                sum[2] = __fadd_rn(sum[2], p[u].z);
+                sum[3] = __fadd_rn(sum[3], p[u].w);
+            }
+        }
         for (; c + 8 <= n_chunks; c += 8) {
             float4 p[8];
 #pragma unroll
@@ -1145,6 +1159,10 @@ cudaError_t tc_gemm_core(const GemmArgs& a, const TcWeights& w, const float* uns
     if (p.stages < 2) return cudaErrorInvalidValue;
     p.mt_cols = (uint32_t)((p.BN + 31) / 32 * 32);
     p.buf_cols = (uint32_t)p.mtiles * p.mt_cols;
+    // Epilogue: with two M-tiles each warpgroup finishes one; with one, the
+    // two warpgroups share its columns in 32-column slices (a lone tile of
+    // at most 128 columns used to leave the second warpgroup idle).
+    p.epi_cols = (p.mtiles == 2 || p.BN > kEpiCols) ? kEpiCols : std::max(32, ((p.BN + 1) / 2 + 31) / 32 * 32);
     // Second issuing thread: the second M-tile, or (one M-tile, at most one
     // CTA tile per SM: latency-bound) the second half of the tile's columns.
     // Half of a 32-multiple is a 16-multiple (a valid MMA width) and starts
